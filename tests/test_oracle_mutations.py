@@ -1,0 +1,111 @@
+"""Planted mistakes: each test breaks one step of the oracle (on the CPU,
+through monkeypatch) and checks that at least one of the pins catches it.
+This shows the pins are strong enough to detect a dropped term, a wrong
+sign or index, or a swapped operand anywhere in the oracle."""
+import numpy as np
+import pytest
+
+import sys, os
+sys.path.insert(0, os.path.dirname(__file__))
+import test_oracle_formats as TF  # noqa: E402
+import test_oracle_forward as TW  # noqa: E402
+import test_oracle_routing as TR  # noqa: E402
+from oracle import formats as F
+from oracle import moe as M
+
+
+def _pins_forward():
+    TW.test_exact_swiglu_golden_case()
+    TW.test_forward_vs_brute_force(6, 3, 128, 64, 40)
+
+
+def _expect_caught(pin):
+    with pytest.raises(AssertionError):
+        pin()
+
+
+def test_pins_pass_unmutated():
+    _pins_forward()
+    TR.test_route_ties_lower_index_first()
+    TR.test_expand_invariants_and_roundtrip()
+
+
+def test_swapped_gate_up_is_caught(monkeypatch):
+    def bad(g):
+        I = g.shape[1] // 2
+        return F.bf16_round((M.silu_f32(g[:, I:]) * g[:, :I]).astype(np.float32))
+    monkeypatch.setattr(M, "swiglu_bf16", bad)
+    _expect_caught(_pins_forward)
+
+
+def test_dropped_token_scale_is_caught(monkeypatch):
+    monkeypatch.setattr(M, "apply_row_scale", lambda acc, s: acc)
+    _expect_caught(_pins_forward)
+
+
+def test_wrong_nibble_order_is_caught(monkeypatch):
+    def bad(packed):
+        p = np.asarray(packed, dtype=np.uint8)
+        out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+        out[..., 0::2] = p >> 4
+        out[..., 1::2] = p & 0xF
+        return out
+    monkeypatch.setattr(F, "unpack_e2m1", bad)
+    _expect_caught(_pins_forward)
+
+
+def test_e8m0_bias_off_by_one_is_caught(monkeypatch):
+    orig = F.e8m0_decode
+    monkeypatch.setattr(F, "e8m0_decode", lambda c: orig(c) * 2.0)
+    _expect_caught(TF.test_e8m0_vs_ml_dtypes)
+    _expect_caught(_pins_forward)
+
+
+def test_reversed_slot_weights_in_combine_is_caught(monkeypatch):
+    orig = M.combine
+    monkeypatch.setattr(M, "combine", lambda w, y, r: orig(w[:, ::-1].copy(), y, r))
+    _expect_caught(lambda: TW.test_forward_vs_brute_force(6, 3, 128, 64, 40))
+
+
+def test_tie_rule_reversed_is_caught(monkeypatch):
+    orig = M.route
+
+    def bad(logits, k):
+        E = logits.shape[1]
+        ids, w = orig(logits[:, ::-1].copy(), k)
+        return (E - 1 - ids).astype(np.int32), w
+    monkeypatch.setattr(M, "route", bad)
+    _expect_caught(TR.test_route_ties_lower_index_first)
+
+
+def test_round_half_up_encoder_is_caught(monkeypatch):
+    orig = F.e4m3_encode
+
+    def bad(v):
+        v = np.asarray(v, dtype=np.float64)
+        return orig(v * (1 + 2.0 ** -20))            # nudges ties upward
+    monkeypatch.setattr(F, "e4m3_encode", bad)
+    _expect_caught(TF.test_e4m3_encode_vs_torch_cast)
+
+
+def test_unstable_expansion_is_caught(monkeypatch):
+    orig = M.expand
+
+    def bad(ids, w, E):
+        rt = orig(ids, w, E)
+        for e in range(E):               # reverse token order inside experts
+            a, b = rt.offsets[e], rt.offsets[e + 1]
+            rt.token_of_row[a:b] = rt.token_of_row[a:b][::-1].copy()
+        return rt
+    monkeypatch.setattr(M, "expand", bad)
+    _expect_caught(TR.test_expand_invariants_and_roundtrip)
+
+
+def test_transposed_gemm_operand_is_caught(monkeypatch):
+    orig = M.Weights.dense
+
+    def bad(self, which, e):
+        d = orig(self, which, e)
+        return d[::-1].copy()                # output features permuted
+    monkeypatch.setattr(M.Weights, "dense", bad)
+    _expect_caught(_pins_forward)
