@@ -1,0 +1,194 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) fused MXFP4 x FP8 mixture-of-experts
+ * forward.
+ *
+ * Pages cited (title and section):
+ *   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add
+ *           MXFP4xFP8 CUTLASS MoE backend for SM90": Description (runtime
+ *           activation expansion and per-token FP8 activation quantization;
+ *           precomputed grouped GEMM work scheduling and TMA descriptor state;
+ *           folded weight-scale storage; per-token scale epilogue),
+ *           Implementation Notes, review comments (interleave preconditions
+ *           n % 16 and k % 64; K % 32 for the scale shape; zero routed tokens
+ *           must be a no-op, not an error).
+ *   [P4411] flashinfer PR #4411, "revert(moe): revert #3738 SM90 CUTLASS MoE
+ *           backend (+ dependents #4025, #4080) on release-v0.6.17":
+ *           Description (caller-owned workspace and its size query kept as
+ *           public API; a null TMA descriptor corrupts the CUDA context).
+ *   [P4793] flashinfer PR #4793, "Unify MoE CuTe DSL dispatch to be dtype
+ *           agnostic": review comments (uint8 scale tensors; quant_mode
+ *           strings "w4a4"/"w4a8"; fail fast with NotImplementedError on
+ *           unsupported architectures).
+ *   [P3614] flashinfer PR #3614, "fix: make the cutlass MoE gemm profiler
+ *           MXFP8-aware": description (never launch with a null scale-factor
+ *           buffer; fail fast with 'No valid tactics' instead of a deep
+ *           kernel assert).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless the name says host.  The
+ *     caller owns all memory; no entry point allocates device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; the return value reports only
+ *     host-side validation and launch errors.  Device-side errors (a bounded
+ *     wait that ran out) are written to a status word in the workspace and
+ *     read back with moe_read_device_status().
+ *   - No C++ exception crosses the ABI.  Invalid arguments are rejected before
+ *     any CUDA call is made.
+ *   - num_tokens == 0 returns MOE_OK and launches nothing [P3738 review
+ *     comments: an empty routed batch is a no-op].
+ */
+#ifndef PRECISION_MOE_GROUPED_GB300_MOE_H_
+#define PRECISION_MOE_GROUPED_GB300_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,        /* null pointer, negative size, bad enum   */
+  MOE_ERR_UNSUPPORTED = -2,        /* mode/shape/device this build cannot run */
+  MOE_ERR_MISALIGNED = -3,         /* pointer alignment or shape divisibility */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -4,
+  MOE_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed       */
+  MOE_ERR_DEVICE_TIMEOUT = -6      /* a device-side bounded wait ran out      */
+} moe_status;
+
+/* Quantisation modes (the pages' W4A8 / W4A16 / MXFP8 paths).  This build
+ * implements MOE_W4A8_MXFP4_FP8; the others return MOE_ERR_UNSUPPORTED. */
+typedef enum {
+  MOE_W4A8_MXFP4_FP8 = 0,    /* MXFP4 weights, runtime per-token FP8 E4M3 acts */
+  MOE_W4A16_MXFP4_BF16 = 1,  /* MXFP4 weights, bf16 activations               */
+  MOE_W8A8_MXFP8 = 2         /* MXFP8 weights and MXFP8 activations           */
+} moe_quant_mode;
+
+/* Problem shape.  Activation SwiGLU and softmax-top-k-renormalised routing
+ * are fixed.  Limits: num_tokens >= 0; 1 <= num_experts <= 1024;
+ * 1 <= top_k <= min(num_experts, 32); hidden and inter positive multiples of
+ * 128; num_tokens * top_k < 2^31. */
+typedef struct {
+  int32_t num_tokens;   /* T */
+  int32_t num_experts;  /* E */
+  int32_t top_k;        /* k */
+  int32_t hidden;       /* H */
+  int32_t inter;        /* I (w1 has 2I rows: gate rows 0..I-1, up rows I..2I-1) */
+} moe_shape;
+
+/* Optional per-call settings (moe_forward_ex); zero-initialise for defaults. */
+typedef struct {
+  int32_t tile_variant;  /* 0 auto; 1 decode tiles (<= 32 tokens per GEMM tile,
+                            deep weight pipeline); 2 prefill tiles (<= 224)   */
+  int32_t timeout_ms;    /* device bounded-wait limit, 0 = 1000 ms           */
+  int32_t reserved[6];   /* must be zero                                     */
+} moe_options;
+
+/* Byte offsets of the intermediate tensors inside the workspace, for tests
+ * and diagnostics (R = num_tokens * top_k expanded rows).  Layouts:
+ *   status      int32[4]      device status word, tile count, 2 spare
+ *   ids         int32[T,k]    routed expert of (token, slot), descending logit
+ *   weights     float[T,k]    renormalised softmax routing weights
+ *   row_of      int32[T,k]    expanded row of (token, slot)
+ *   counts      int32[E]      rows per expert
+ *   offsets     int32[E+1]    exclusive scan of counts
+ *   token_slot  int32[R]      token*top_k + slot of each expanded row
+ *   tiles       int32[4*max]  GEMM work map: (expert, first row, rows, 0)
+ *   xq          uint8[R,H]    FP8 E4M3 codes of the expanded activations
+ *   x_scale     float[R]      per-row (per-token) activation scale
+ *   h           bf16[R,I]     SwiGLU output
+ *   hq          uint8[R,I]    FP8 E4M3 codes of h
+ *   h_scale     float[R]      per-row scale of hq
+ *   y           bf16[R,H]     GEMM2 output (scaled)
+ *   x_stage, logits_stage, out_stage: device staging used by moe_forward_host */
+typedef struct {
+  uint64_t status, ids, weights, row_of, counts, offsets, chunk_counts, token_slot,
+      tiles, xq, x_scale, h, hq, h_scale, y, x_stage, logits_stage, out_stage, total;
+  int32_t max_tiles, num_chunks, reserved[6];
+} moe_ws_layout;
+
+/* Workspace bytes moe_forward needs for `shape` and `quant_mode` (host-only,
+ * pure).  Returns 0 for an invalid shape or mode.  The caller allocates it
+ * (256-byte aligned) [P4411 Description: caller-owned workspace and its size
+ * query]. */
+size_t moe_workspace_size(const moe_shape* shape, int32_t quant_mode);
+
+/* Fills `layout` with the workspace carving used by moe_forward. */
+int32_t moe_workspace_layout(const moe_shape* shape, int32_t quant_mode,
+                             moe_ws_layout* layout);
+
+/* Re-lays the expert weights from the user layout into the layout the GEMM
+ * kernels stream (bit-preserving: only rows and scale bytes move)
+ * [P3738 Description: folded weight-scale storage independent of the tile
+ * choice; review comments: interleave kernels and their n % 16, k % 64
+ * preconditions].
+ * User layout (W4A8 / W4A16), all uint8, device:
+ *   w1    [E, 2I, H/2]  E2M1 codes, two per byte, low nibble = even k
+ *   w1_sf [E, 2I, H/32] E8M0 scale per 32 consecutive k
+ *   w2    [E, H, I/2],  w2_sf [E, H, I/32]
+ * Outputs have the same byte sizes and must not alias the inputs.  Pointers
+ * must be 256-byte aligned.  Asynchronous on `stream`. */
+int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode,
+                            const void* w1, const void* w1_sf, const void* w2,
+                            const void* w2_sf, void* w1_p, void* w1_sf_p, void* w2_p,
+                            void* w2_sf_p, void* stream);
+
+/* The fused forward: routing -> expert-sorted expansion with per-token FP8
+ * quantisation -> GEMM1 (gate|up) with SwiGLU and the token scale in its
+ * epilogue -> per-row FP8 quantisation of h -> GEMM2 -> top-k weighted
+ * combine.
+ *   x              bf16  [T, H]  (16-byte aligned)
+ *   router_logits  float [T, E]  finite values
+ *   w1_p .. w2_sf_p              prepared weights (moe_prepare_weights)
+ *   out            bf16  [T, H]  written in full (16-byte aligned)
+ *   workspace      >= moe_workspace_size() bytes, 256-byte aligned
+ * [P3738 Description, Implementation Notes]. */
+int32_t moe_forward(const moe_shape* shape, int32_t quant_mode, const void* x,
+                    const float* router_logits, const void* w1_p, const void* w1_sf_p,
+                    const void* w2_p, const void* w2_sf_p, void* out, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* moe_forward with options (opts may be NULL). */
+int32_t moe_forward_ex(const moe_shape* shape, int32_t quant_mode, const void* x,
+                       const float* router_logits, const void* w1_p, const void* w1_sf_p,
+                       const void* w2_p, const void* w2_sf_p, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream, const moe_options* opts);
+
+/* End-to-end variant with HOST activations: copies x_host (bf16 [T,H]) and
+ * logits_host (float [T,E]) into the workspace's staging area, runs the
+ * forward, and copies the result back to out_host (bf16 [T,H]) -- all on
+ * `stream`.  Host buffers should be pinned for asynchronous copies; they must
+ * stay valid until the stream reaches this point. */
+int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void* x_host,
+                         const float* logits_host, const void* w1_p, const void* w1_sf_p,
+                         const void* w2_p, const void* w2_sf_p, void* out_host,
+                         void* workspace, size_t workspace_bytes, void* stream,
+                         const moe_options* opts);
+
+/* Reads the device status word of `workspace` (synchronises `stream`).
+ * *status = MOE_OK or the moe_status of the first device-side error since
+ * the workspace was last used by moe_forward (which clears it). */
+int32_t moe_read_device_status(const void* workspace, void* stream, int32_t* status);
+
+/* Exercises the bounded-wait machinery: launches one block that waits on a
+ * barrier nothing completes, with a limit of `timeout_us`; the wait gives
+ * up, writes MOE_ERR_DEVICE_TIMEOUT to the status word of `workspace` and
+ * the kernel returns normally.  For tests of the failure path. */
+int32_t moe_selftest_timeout(void* workspace, int32_t timeout_us, void* stream);
+
+/* Message describing the last error returned on the calling thread. */
+const char* moe_last_error(void);
+
+/* Static description of a status code. */
+const char* moe_status_string(int32_t status);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* PRECISION_MOE_GROUPED_GB300_MOE_H_ */

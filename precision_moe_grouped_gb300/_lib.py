@@ -1,0 +1,169 @@
+"""ctypes binding of libmoe.so (include/moe.h).
+
+Argument marshalling only: every step of the forward runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  If the
+library is not built, loading fails loudly -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_MISALIGNED = -3
+MOE_ERR_WORKSPACE_TOO_SMALL = -4
+MOE_ERR_CUDA = -5
+MOE_ERR_DEVICE_TIMEOUT = -6
+
+MOE_W4A8_MXFP4_FP8 = 0
+MOE_W4A16_MXFP4_BF16 = 1
+MOE_W8A8_MXFP8 = 2
+
+# every symbol include/moe.h declares
+EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_prepare_weights", "moe_forward",
+           "moe_forward_ex", "moe_forward_host", "moe_read_device_status",
+           "moe_selftest_timeout", "moe_last_error", "moe_status_string", "moe_version")
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32)]
+
+
+class MoeOptions(ctypes.Structure):
+    _fields_ = [("tile_variant", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 6)]
+
+
+class WsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "status", "ids", "weights", "row_of", "counts", "offsets", "chunk_counts", "token_slot",
+        "tiles", "xq", "x_scale", "h", "hq", "h_scale", "y", "x_stage", "logits_stage",
+        "out_stage", "total")] + [("max_tiles", ctypes.c_int32), ("num_chunks", ctypes.c_int32),
+                                  ("reserved", ctypes.c_int32 * 6)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"moe error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libmoe.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as "
+                           f"g; g.build()\"` first (there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    shp = ctypes.POINTER(MoeShape)
+    lib.moe_workspace_size.argtypes = [shp, i32]
+    lib.moe_workspace_size.restype = sz
+    lib.moe_workspace_layout.argtypes = [shp, i32, ctypes.POINTER(WsLayout)]
+    lib.moe_workspace_layout.restype = i32
+    lib.moe_prepare_weights.argtypes = [shp, i32] + [vp] * 9
+    lib.moe_prepare_weights.restype = i32
+    lib.moe_forward.argtypes = [shp, i32] + [vp] * 8 + [sz, vp]
+    lib.moe_forward.restype = i32
+    lib.moe_forward_ex.argtypes = [shp, i32] + [vp] * 8 + [sz, vp, ctypes.POINTER(MoeOptions)]
+    lib.moe_forward_ex.restype = i32
+    lib.moe_forward_host.argtypes = [shp, i32] + [vp] * 8 + [sz, vp, ctypes.POINTER(MoeOptions)]
+    lib.moe_forward_host.restype = i32
+    lib.moe_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+    lib.moe_read_device_status.restype = i32
+    lib.moe_selftest_timeout.argtypes = [vp, i32, vp]
+    lib.moe_selftest_timeout.restype = i32
+    for f in ("moe_last_error", "moe_version"):
+        getattr(lib, f).argtypes = []
+        getattr(lib, f).restype = ctypes.c_char_p
+    lib.moe_status_string.argtypes = [i32]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def check(rc: int) -> None:
+    if rc != MOE_OK:
+        lib = load()
+        raise MoeError(rc, (lib.moe_last_error() or b"").decode() or
+                       lib.moe_status_string(rc).decode())
+
+
+def shape(T: int, E: int, k: int, H: int, I: int) -> MoeShape:
+    return MoeShape(T, E, k, H, I)
+
+
+def options(tile_variant: int = 0, timeout_ms: int = 0) -> MoeOptions:
+    o = MoeOptions()
+    o.tile_variant, o.timeout_ms = tile_variant, timeout_ms
+    return o
+
+
+def workspace_size(s: MoeShape, mode: int = MOE_W4A8_MXFP4_FP8) -> int:
+    return int(load().moe_workspace_size(ctypes.byref(s), mode))
+
+
+def workspace_layout(s: MoeShape, mode: int = MOE_W4A8_MXFP4_FP8) -> WsLayout:
+    L = WsLayout()
+    check(load().moe_workspace_layout(ctypes.byref(s), mode, ctypes.byref(L)))
+    return L
+
+
+def _stream(stream) -> int:
+    if stream is not None:
+        return int(stream)
+    import torch
+    return int(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def prepare_weights(s: MoeShape, w1, w1_sf, w2, w2_sf, w1_p, w1_sf_p, w2_p, w2_sf_p,
+                    mode: int = MOE_W4A8_MXFP4_FP8, stream=None) -> None:
+    check(load().moe_prepare_weights(ctypes.byref(s), mode, *(_ptr(t) for t in (
+        w1, w1_sf, w2, w2_sf, w1_p, w1_sf_p, w2_p, w2_sf_p)), _stream(stream)))
+
+
+def forward(s: MoeShape, x, logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out, workspace,
+            mode: int = MOE_W4A8_MXFP4_FP8, opts: MoeOptions | None = None, stream=None) -> None:
+    lib = load()
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    args = [ctypes.byref(s), mode, _ptr(x), _ptr(logits), _ptr(w1_p), _ptr(w1_sf_p), _ptr(w2_p),
+            _ptr(w2_sf_p), _ptr(out), _ptr(workspace), nbytes, _stream(stream)]
+    if opts is None:
+        check(lib.moe_forward(*args))
+    else:
+        check(lib.moe_forward_ex(*args, ctypes.byref(opts)))
+
+
+def forward_host(s: MoeShape, x_host, logits_host, w1_p, w1_sf_p, w2_p, w2_sf_p, out_host,
+                 workspace, mode: int = MOE_W4A8_MXFP4_FP8, opts: MoeOptions | None = None,
+                 stream=None) -> None:
+    nbytes = workspace.numel() * workspace.element_size()
+    check(load().moe_forward_host(ctypes.byref(s), mode, _ptr(x_host), _ptr(logits_host),
+                                  _ptr(w1_p), _ptr(w1_sf_p), _ptr(w2_p), _ptr(w2_sf_p),
+                                  _ptr(out_host), _ptr(workspace), nbytes, _stream(stream),
+                                  ctypes.byref(opts) if opts is not None else None))
+
+
+def read_device_status(workspace, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    check(load().moe_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def selftest_timeout(workspace, timeout_us: int, stream=None) -> None:
+    check(load().moe_selftest_timeout(_ptr(workspace), timeout_us, _stream(stream)))

@@ -1,0 +1,424 @@
+// abi.cu -- the C ABI (include/moe.h): argument validation, workspace
+// carving, TMA descriptor encoding and the launch sequence of the fused MoE
+// forward.  Host code only; the kernels live in route.cu, gemm.cu, rowops.cu
+// and prepare.cu.
+//
+// Pages cited (title and section):
+//   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add
+//           MXFP4xFP8 CUTLASS MoE backend for SM90": Description (precomputed
+//           grouped GEMM work scheduling and TMA descriptor state before the
+//           GEMM launch), review comments (validate n % 16 / k % 64 and
+//           K % 32 at the API boundary with clear errors; an empty routed
+//           batch is a no-op).
+//   [P4411] flashinfer PR #4411, "revert(moe): revert #3738 SM90 CUTLASS MoE
+//           backend (+ dependents #4025, #4080) on release-v0.6.17":
+//           Description (caller-owned workspace + size query; a null TMA
+//           descriptor raised an illegal instruction that surfaced in a later
+//           op).
+//   [P3614] flashinfer PR #3614, "fix: make the cutlass MoE gemm profiler
+//           MXFP8-aware": description (never launch with a null scale buffer;
+//           fail fast at init instead of a deep kernel assert).
+//
+// Every pointer, size and alignment is checked here before the first CUDA
+// call, and no tensor map is ever encoded from a null base address.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int32_t fail(int32_t code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int32_t fail(int32_t code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+#define MOE_CUDA(call)                                                                  \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(MOE_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));        \
+  } while (0)
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int32_t check_shape(const moe_shape* s, int32_t mode) {
+  if (!s) return fail(MOE_ERR_INVALID_ARG, "shape is NULL");
+  if (mode < 0 || mode > 2) return fail(MOE_ERR_INVALID_ARG, "quant_mode %d unknown", mode);
+  if (s->num_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "num_tokens < 0");
+  if (s->num_experts < 1 || s->num_experts > 1024)
+    return fail(MOE_ERR_INVALID_ARG, "num_experts must be in [1, 1024]");
+  if (s->top_k < 1 || s->top_k > s->num_experts || s->top_k > 32)
+    return fail(MOE_ERR_INVALID_ARG, "top_k must be in [1, min(num_experts, 32)]");
+  if (s->hidden <= 0 || s->inter <= 0) return fail(MOE_ERR_INVALID_ARG, "hidden/inter <= 0");
+  if (s->hidden % 128 != 0 || s->inter % 128 != 0)
+    return fail(MOE_ERR_MISALIGNED, "hidden (%d) and inter (%d) must be multiples of 128",
+                s->hidden, s->inter);
+  if (static_cast<int64_t>(s->num_tokens) * s->top_k >= (int64_t(1) << 31))
+    return fail(MOE_ERR_INVALID_ARG, "num_tokens * top_k must be < 2^31");
+  if (static_cast<int64_t>(s->num_experts) * 2 * s->inter >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(s->num_experts) * s->hidden >= (int64_t(1) << 31))
+    return fail(MOE_ERR_INVALID_ARG, "num_experts * rows must be < 2^31");
+  return MOE_OK;
+}
+
+void compute_layout(const moe_shape* s, moe_ws_layout* L) {
+  std::memset(L, 0, sizeof(*L));
+  const int64_t T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden,
+                I = s->inter;
+  const int64_t R = T * k;
+  const int64_t chunks = (T + moe::kRouteChunk - 1) / moe::kRouteChunk;
+  const int64_t max_tiles = R / moe::kDecodeBN + (E < R ? E : R) + 1;
+  size_t off = 0;
+  auto take = [&](int64_t bytes) {
+    off = align_up(off, kAlign);
+    const size_t o = off;
+    off += static_cast<size_t>(bytes > 0 ? bytes : 0);
+    return static_cast<uint64_t>(o);
+  };
+  L->status = take(16);
+  L->ids = take(R * 4);
+  L->weights = take(R * 4);
+  L->row_of = take(R * 4);
+  L->counts = take(E * 4);
+  L->offsets = take((E + 1) * 4);
+  L->chunk_counts = take(chunks * E * 4);
+  L->token_slot = take(R * 4);
+  L->tiles = take(max_tiles * 16);
+  L->xq = take(R * H);
+  L->x_scale = take(R * 4);
+  L->h = take(R * I * 2);
+  L->hq = take(R * I);
+  L->h_scale = take(R * 4);
+  L->y = take(R * H * 2);
+  L->x_stage = take(T * H * 2);
+  L->logits_stage = take(T * E * 4);
+  L->out_stage = take(T * H * 2);
+  L->total = align_up(off, kAlign);
+  L->max_tiles = static_cast<int32_t>(max_tiles);
+  L->num_chunks = static_cast<int32_t>(chunks);
+}
+
+// ----------------------------------------------------------- device state
+struct DeviceInfo {
+  int num_sms = 0;
+  bool ok = false;
+};
+
+int32_t device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev].ok) {
+    int major = 0, minor = 0, sms = 0;
+    MOE_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    MOE_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (major != 10 || minor != 3)
+      return fail(MOE_ERR_UNSUPPORTED,
+                  "this library is built for sm_103a (GB300); device %d is sm_%d%d", dev, major,
+                  minor);
+    cache[dev].num_sms = sms;
+    cache[dev].ok = true;
+  }
+  *out = cache[dev];
+  return MOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D tensor map over a row-major [rows, cols] matrix; box = box_cols x
+// box_rows elements, 128-byte swizzle.  fp4: 16U4_ALIGN16B (each group of 16
+// packed codes lands as 16 bytes in shared memory), else uint8.
+int32_t make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, bool fp4,
+                  uint32_t box_cols, uint32_t box_rows) {
+  if (!base) return fail(MOE_ERR_INVALID_ARG, "refusing to encode a tensor map for NULL");
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {fp4 ? cols / 2 : cols};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m,
+                  fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) rows=%llu cols=%llu fp4=%d",
+                static_cast<int>(r), static_cast<unsigned long long>(rows),
+                static_cast<unsigned long long>(cols), fp4 ? 1 : 0);
+  return MOE_OK;
+}
+
+int pick_variant(const moe_shape* s, const moe_options* o) {
+  if (o && (o->tile_variant == 1 || o->tile_variant == 2)) return o->tile_variant;
+  const double rows_per_expert =
+      static_cast<double>(s->num_tokens) * s->top_k / static_cast<double>(s->num_experts);
+  return rows_per_expert <= 16.0 ? 1 : 2;
+}
+
+int32_t check_options(const moe_options* o) {
+  if (!o) return MOE_OK;
+  if (o->tile_variant < 0 || o->tile_variant > 2)
+    return fail(MOE_ERR_INVALID_ARG, "tile_variant must be 0, 1 or 2");
+  if (o->timeout_ms < 0) return fail(MOE_ERR_INVALID_ARG, "timeout_ms < 0");
+  for (int i = 0; i < 6; ++i)
+    if (o->reserved[i] != 0) return fail(MOE_ERR_INVALID_ARG, "reserved option fields must be 0");
+  return MOE_OK;
+}
+
+int32_t check_forward_args(const moe_shape* shape, int32_t mode, const void* x,
+                           const float* logits, const void* w1, const void* w1_sf,
+                           const void* w2, const void* w2_sf, const void* out, void* ws,
+                           size_t ws_bytes, const moe_options* opts) {
+  int32_t st = check_shape(shape, mode);
+  if (st != MOE_OK) return st;
+  if ((st = check_options(opts)) != MOE_OK) return st;
+  if (mode != MOE_W4A8_MXFP4_FP8)
+    return fail(MOE_ERR_UNSUPPORTED, "quant_mode %d is not implemented in this build", mode);
+  if (shape->num_tokens == 0) return MOE_OK;
+  if (!x || !logits || !w1 || !w1_sf || !w2 || !w2_sf || !out || !ws)
+    return fail(MOE_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(logits, 4))
+    return fail(MOE_ERR_MISALIGNED, "x/out must be 16-byte aligned, logits 4-byte aligned");
+  if (!aligned(w1, 256) || !aligned(w2, 256) || !aligned(w1_sf, 256) || !aligned(w2_sf, 256) ||
+      !aligned(ws, 256))
+    return fail(MOE_ERR_MISALIGNED, "weights, scales and workspace must be 256-byte aligned");
+  moe_ws_layout L;
+  compute_layout(shape, &L);
+  if (ws_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < required %llu", ws_bytes,
+                static_cast<unsigned long long>(L.total));
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, uint64_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+int32_t run_forward(const moe_shape* s, const void* x, const float* logits, const void* w1,
+                    const void* w1_sf, const void* w2, const void* w2_sf, void* out, void* ws,
+                    cudaStream_t st, const moe_options* opts) {
+  DeviceInfo dev;
+  int32_t rc = device_info(&dev);
+  if (rc != MOE_OK) return rc;
+  moe_ws_layout L;
+  compute_layout(s, &L);
+  const int T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden, I = s->inter;
+  const int R = T * k;
+  const int variant = pick_variant(s, opts);
+  const int bn = variant == 1 ? moe::kDecodeBN : moe::kPrefillBN;
+  const uint64_t timeout_ns =
+      static_cast<uint64_t>(opts && opts->timeout_ms > 0 ? opts->timeout_ms : 1000) * 1000000ull;
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* num_tiles = status + 1;
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* wts = at<float>(ws, L.weights);
+  int32_t* row_of = at<int32_t>(ws, L.row_of);
+  int32_t* chunk = at<int32_t>(ws, L.chunk_counts);
+  int4* tiles = at<int4>(ws, L.tiles);
+  uint8_t* xq = at<uint8_t>(ws, L.xq);
+  float* x_scale = at<float>(ws, L.x_scale);
+  void* h = at<void>(ws, L.h);
+  uint8_t* hq = at<uint8_t>(ws, L.hq);
+  float* h_scale = at<float>(ws, L.h_scale);
+  void* y = at<void>(ws, L.y);
+
+  CUtensorMap tm_w1, tm_x, tm_w2, tm_h;
+  if ((rc = make_tmap(&tm_w1, w1, static_cast<uint64_t>(E) * 2 * I, H, true, 128, 128)) != MOE_OK ||
+      (rc = make_tmap(&tm_x, xq, R, H, false, 128, 32)) != MOE_OK ||
+      (rc = make_tmap(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, true, 128, 128)) != MOE_OK ||
+      (rc = make_tmap(&tm_h, hq, R, I, false, 128, 32)) != MOE_OK)
+    return rc;
+
+  MOE_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, st));
+  MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts),
+                            at<int32_t>(ws, L.offsets), chunk, tiles, num_tiles, st));
+  MOE_CUDA(moe::launch_scatter_quant(x, ids, chunk, T, E, k, H, row_of,
+                                     at<int32_t>(ws, L.token_slot), xq, x_scale, st));
+  moe::GemmArgs g1{&tm_w1, &tm_x, static_cast<const uint8_t*>(w1_sf), tiles, num_tiles,
+                   x_scale, h, 2 * I, H, I, status, timeout_ns, 16384u, dev.num_sms};
+  MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
+  MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
+  moe::GemmArgs g2{&tm_w2, &tm_h, static_cast<const uint8_t*>(w2_sf), tiles, num_tiles,
+                   h_scale, y, H, I, H, status, timeout_ns, 16384u, dev.num_sms};
+  MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
+  MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_version(void) { return "precision_moe_grouped_gb300 0.1 (sm_103a)"; }
+
+const char* moe_last_error(void) { return g_last_error; }
+
+const char* moe_status_string(int32_t status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer or shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t moe_workspace_size(const moe_shape* shape, int32_t quant_mode) {
+  if (check_shape(shape, quant_mode) != MOE_OK) return 0;
+  moe_ws_layout L;
+  compute_layout(shape, &L);
+  return static_cast<size_t>(L.total);
+}
+
+int32_t moe_workspace_layout(const moe_shape* shape, int32_t quant_mode, moe_ws_layout* layout) {
+  int32_t st = check_shape(shape, quant_mode);
+  if (st != MOE_OK) return st;
+  if (!layout) return fail(MOE_ERR_INVALID_ARG, "layout is NULL");
+  compute_layout(shape, layout);
+  return MOE_OK;
+}
+
+int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode, const void* w1,
+                            const void* w1_sf, const void* w2, const void* w2_sf, void* w1_p,
+                            void* w1_sf_p, void* w2_p, void* w2_sf_p, void* stream) {
+  int32_t st = check_shape(shape, quant_mode);
+  if (st != MOE_OK) return st;
+  if (quant_mode != MOE_W4A8_MXFP4_FP8)
+    return fail(MOE_ERR_UNSUPPORTED, "quant_mode %d is not implemented in this build",
+                quant_mode);
+  const void* ins[4] = {w1, w1_sf, w2, w2_sf};
+  const void* outs[4] = {w1_p, w1_sf_p, w2_p, w2_sf_p};
+  for (int i = 0; i < 4; ++i) {
+    if (!ins[i] || !outs[i]) return fail(MOE_ERR_INVALID_ARG, "a weight pointer is NULL");
+    if (!aligned(ins[i], 256) || !aligned(outs[i], 256))
+      return fail(MOE_ERR_MISALIGNED, "weight buffers must be 256-byte aligned");
+    if (ins[i] == outs[i]) return fail(MOE_ERR_INVALID_ARG, "prepared weights must not alias");
+  }
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != MOE_OK) return st;
+  const int E = shape->num_experts, H = shape->hidden, I = shape->inter;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(moe::launch_prepare_w1(static_cast<const uint8_t*>(w1),
+                                  static_cast<const uint8_t*>(w1_sf),
+                                  static_cast<uint8_t*>(w1_p), static_cast<uint8_t*>(w1_sf_p), E,
+                                  I, H, s));
+  MOE_CUDA(cudaMemcpyAsync(w2_p, w2, static_cast<size_t>(E) * H * (I / 2),
+                           cudaMemcpyDeviceToDevice, s));
+  MOE_CUDA(moe::launch_prepare_sf_plain(static_cast<const uint8_t*>(w2_sf),
+                                        static_cast<uint8_t*>(w2_sf_p), E, H, I, s));
+  return MOE_OK;
+}
+
+int32_t moe_forward_ex(const moe_shape* shape, int32_t quant_mode, const void* x,
+                       const float* router_logits, const void* w1_p, const void* w1_sf_p,
+                       const void* w2_p, const void* w2_sf_p, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream, const moe_options* opts) {
+  int32_t st = check_forward_args(shape, quant_mode, x, router_logits, w1_p, w1_sf_p, w2_p,
+                                  w2_sf_p, out, workspace, workspace_bytes, opts);
+  if (st != MOE_OK || shape->num_tokens == 0) return st;
+  return run_forward(shape, x, router_logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out, workspace,
+                     static_cast<cudaStream_t>(stream), opts);
+}
+
+int32_t moe_forward(const moe_shape* shape, int32_t quant_mode, const void* x,
+                    const float* router_logits, const void* w1_p, const void* w1_sf_p,
+                    const void* w2_p, const void* w2_sf_p, void* out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  return moe_forward_ex(shape, quant_mode, x, router_logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out,
+                        workspace, workspace_bytes, stream, nullptr);
+}
+
+int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void* x_host,
+                         const float* logits_host, const void* w1_p, const void* w1_sf_p,
+                         const void* w2_p, const void* w2_sf_p, void* out_host,
+                         void* workspace, size_t workspace_bytes, void* stream,
+                         const moe_options* opts) {
+  int32_t st = check_shape(shape, quant_mode);
+  if (st != MOE_OK) return st;
+  if (shape->num_tokens == 0) return MOE_OK;
+  if (!x_host || !logits_host || !out_host || !workspace)
+    return fail(MOE_ERR_INVALID_ARG, "a required pointer is NULL");
+  moe_ws_layout L;
+  compute_layout(shape, &L);
+  void* xs = at<void>(workspace, L.x_stage);
+  float* ls = at<float>(workspace, L.logits_stage);
+  void* os = at<void>(workspace, L.out_stage);
+  st = check_forward_args(shape, quant_mode, xs, ls, w1_p, w1_sf_p, w2_p, w2_sf_p, os, workspace,
+                          workspace_bytes, opts);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t T = shape->num_tokens, H = shape->hidden, E = shape->num_experts;
+  MOE_CUDA(cudaMemcpyAsync(xs, x_host, T * H * 2, cudaMemcpyHostToDevice, s));
+  MOE_CUDA(cudaMemcpyAsync(ls, logits_host, T * E * 4, cudaMemcpyHostToDevice, s));
+  st = run_forward(shape, xs, ls, w1_p, w1_sf_p, w2_p, w2_sf_p, os, workspace, s, opts);
+  if (st != MOE_OK) return st;
+  MOE_CUDA(cudaMemcpyAsync(out_host, os, T * H * 2, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}
+
+int32_t moe_read_device_status(const void* workspace, void* stream, int32_t* status) {
+  if (!workspace || !status) return fail(MOE_ERR_INVALID_ARG, "NULL workspace or status");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  MOE_CUDA(cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  *status = v;
+  return MOE_OK;
+}
+
+int32_t moe_selftest_timeout(void* workspace, int32_t timeout_us, void* stream) {
+  if (!workspace || !aligned(workspace, 256))
+    return fail(MOE_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+  if (timeout_us <= 0 || timeout_us > 2000000)
+    return fail(MOE_ERR_INVALID_ARG, "timeout_us must be in (0, 2e6]");
+  DeviceInfo dev;
+  int32_t st = device_info(&dev);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, 16, s));
+  MOE_CUDA(moe::launch_timeout_selftest(static_cast<int32_t*>(workspace),
+                                        static_cast<uint64_t>(timeout_us) * 1000ull, s));
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// moe_internal.h -- launch helpers shared by the library's translation units
+// (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Device status codes written to the workspace status word (match moe_status).
+constexpr int32_t kDevTimeout = -6;
+
+// Tokens per routing chunk: the unit of the per-chunk expert histogram that
+// makes the expert-major scatter deterministic (stable in token order).
+constexpr int kRouteChunk = 32;
+
+// GEMM tiling: weights fill MMA-M = 128 (one M-tile), tokens fill MMA-N.
+constexpr int kTileM = 128;
+constexpr int kTileK = 128;          // K elements per pipeline stage
+constexpr int kDecodeBN = 32;        // max tokens per tile, decode variant
+constexpr int kPrefillBN = 224;      // max tokens per tile, prefill variant
+
+struct GemmArgs {
+  const CUtensorMap* tmap_w;   // host copy, passed by value to the kernel
+  const CUtensorMap* tmap_x;
+  const uint8_t* w_sf;         // prepared scale bytes
+  const int4* tiles;           // (expert, first row, rows, 0)
+  const int32_t* num_tiles;    // device scalar
+  const float* row_scale;      // per-row activation scale
+  void* out;                   // bf16 output
+  int32_t m_per_expert;        // 2I (GEMM1) or H (GEMM2)
+  int32_t k;                   // H (GEMM1) or I (GEMM2)
+  int32_t out_ld;              // I (GEMM1) or H (GEMM2)
+  int32_t* status;
+  uint64_t timeout_ns;
+  uint32_t a_tx_bytes;         // shared-memory bytes one weight TMA box delivers
+  int32_t num_sms;
+};
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
+                         int32_t* chunk_counts, cudaStream_t s);
+cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
+                        int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
+                        int32_t* num_tiles, cudaStream_t s);
+cudaError_t launch_scatter_quant(const void* x, const int32_t* ids, const int32_t* chunk_base,
+                                 int T, int E, int k, int H, int32_t* row_of,
+                                 int32_t* token_slot, uint8_t* xq, float* x_scale,
+                                 cudaStream_t s);
+cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_scale,
+                          cudaStream_t s);
+cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
+                           int H, void* out, cudaStream_t s);
+cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_prepare_w1(const uint8_t* w1, const uint8_t* w1_sf, uint8_t* w1_p,
+                              uint8_t* w1_sf_p, int E, int I, int H, cudaStream_t s);
+cudaError_t launch_prepare_sf_plain(const uint8_t* sf, uint8_t* sf_p, int E, int M, int K,
+                                    cudaStream_t s);
+cudaError_t launch_timeout_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace moe

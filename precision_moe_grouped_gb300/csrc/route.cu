@@ -1,0 +1,294 @@
+// route.cu -- routing, expert histogram/scan + GEMM work map, and the
+// expert-major scatter with fused per-token FP8 quantisation.
+//
+// Pages cited (title and section):
+//   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add
+//           MXFP4xFP8 CUTLASS MoE backend for SM90": Description ("runtime
+//           activation expansion and per-token FP8 quantization"; "precompute
+//           grouped GEMM work scheduling ... before the main GEMM kernel"),
+//           Implementation Notes (per-token activation scales computed while
+//           expanding routed MoE rows; precomputed work map so the GEMM hot
+//           path does no grouped tile lookup), review comments (64-bit linear
+//           work index; zero routed tokens is a no-op).
+//
+// Kernel chain: route (one warp per token; per-chunk expert histogram) ->
+// scan (one CTA: counts, offsets, per-chunk bases, GEMM tile list) ->
+// scatter_quant (one CTA per chunk: stable ranks, then FP8 codes written to
+// each of the token's k expanded rows).  Nothing returns to the host.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cfloat>
+#include <climits>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+// ---------------------------------------------------------------- routing
+// One warp per token.  Lane l holds logits of experts l, l+32, ... (NV per
+// lane).  k rounds of a warp argmax pick the experts in descending logit
+// order, equal logits resolved toward the lower expert index.  Weights are
+// the softmax over the k selected logits (renormalised top-k softmax).
+template <int NV>
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T,
+                                                    int E, int k, int32_t* __restrict__ ids,
+                                                    float* __restrict__ wts,
+                                                    int32_t* __restrict__ chunk_counts) {
+  extern __shared__ int32_t hist[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int t0 = blockIdx.x * kRouteChunk;
+  for (int tt = warp; tt < kRouteChunk; tt += nwarps) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    const float* row = logits + static_cast<size_t>(t) * E;
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? row[e] : -FLT_MAX;
+    }
+    uint32_t taken = 0;
+    float my_v = 0.f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      float best = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
+          best = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ob > best || (ob == best && oi < bi)) {
+          best = ob;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_v = best;
+        my_id = bi;
+      }
+    }
+    const float lmax = __shfl_sync(0xffffffffu, my_v, 0);
+    float ex = lane < k ? expf(my_v - lmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+      ids[static_cast<size_t>(t) * k + lane] = my_id;
+      wts[static_cast<size_t>(t) * k + lane] = ex / sum;
+      atomicAdd(&hist[my_id], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    chunk_counts[static_cast<size_t>(blockIdx.x) * E + i] = hist[i];
+}
+
+// Exclusive scan of one int per thread over a block of up to 1024 threads.
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_sums[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    int s = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += y;
+    }
+    warp_sums[lane] = s;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int base = warp > 0 ? warp_sums[warp - 1] : 0;
+  *total = warp_sums[((blockDim.x + 31) >> 5) - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+// One CTA (blockDim >= E): per-expert counts, offsets, per-chunk bases
+// (stable ranks start there), and the GEMM tile list.  A tile is a run of
+// at most `bn` consecutive rows of one expert; an expert with c rows gets
+// ceil(c / tsz) tiles of tsz = roundup16(ceil(c / ceil(c / bn))) rows, so
+// its tiles are balanced and every MMA-N is a multiple of 16.
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ chunk_counts,
+                                                    int num_chunks, int E, int bn,
+                                                    int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ chunk_base,
+                                                    int4* __restrict__ tiles,
+                                                    int32_t* __restrict__ num_tiles) {
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E)
+    for (int ch = 0; ch < num_chunks; ++ch) c += chunk_counts[static_cast<size_t>(ch) * E + e];
+  int total_rows;
+  const int off = block_exclusive_scan(e < E ? c : 0, &total_rows);
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = off;
+    int run = off;
+    for (int ch = 0; ch < num_chunks; ++ch) {
+      const size_t i = static_cast<size_t>(ch) * E + e;
+      const int cc = chunk_counts[i];
+      chunk_base[i] = run;
+      run += cc;
+    }
+  }
+  if (e == 0) offsets[E] = total_rows;
+  int nt = 0, tsz = 0;
+  if (e < E && c > 0) {
+    const int n0 = (c + bn - 1) / bn;
+    tsz = (((c + n0 - 1) / n0) + 15) & ~15;
+    nt = (c + tsz - 1) / tsz;
+  }
+  int total_tiles;
+  const int toff = block_exclusive_scan(nt, &total_tiles);
+  for (int i = 0; i < nt; ++i) {
+    const int r0 = i * tsz;
+    tiles[toff + i] = make_int4(e, off + r0, min(tsz, c - r0), 0);
+  }
+  if (e == 0) *num_tiles = total_tiles;
+}
+
+// One CTA per chunk of kRouteChunk tokens.  Warp 0 walks the chunk's tokens
+// in order and hands out rows from the chunk's per-expert bases (a token's k
+// experts are distinct, so the k lanes never collide), which makes each
+// expert's rows ascend in token order.  Then every warp quantises tokens:
+// amax -> s = amax/448, inv = 448/amax (IEEE divisions) -> E4M3 codes of
+// x*inv (round to nearest even, satfinite), written to all k rows.
+__global__ void __launch_bounds__(256) scatter_quant_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids,
+    const int32_t* __restrict__ chunk_base, int T, int E, int k, int H,
+    int32_t* __restrict__ row_of, int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq,
+    float* __restrict__ x_scale) {
+  extern __shared__ int32_t sm[];
+  int32_t* base = sm;               // [E]
+  int32_t* rows = sm + E;           // [kRouteChunk * k]
+  const int t0 = blockIdx.x * kRouteChunk;
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    base[i] = chunk_base[static_cast<size_t>(blockIdx.x) * E + i];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  if (warp == 0) {
+    for (int tt = 0; tt < kRouteChunk; ++tt) {
+      const int t = t0 + tt;
+      if (t >= T) break;
+      if (lane < k) {
+        const size_t ts = static_cast<size_t>(t) * k + lane;
+        const int e = ids[ts];
+        const int r = base[e];
+        base[e] = r + 1;
+        rows[tt * k + lane] = r;
+        row_of[ts] = r;
+        token_slot[r] = static_cast<int32_t>(ts);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  const int nvec = H / 16;  // 16 elements (two 16-byte loads) per lane step
+  for (int tt = warp; tt < kRouteChunk; tt += nwarps) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    float amax = 0.f;
+    for (int i = lane; i < nvec; i += 32) {
+      uint4 q[2] = {__ldg(xr + 2 * i), __ldg(xr + 2 * i + 1)};
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 f = __bfloat1622float2(b[j]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const bool nz = amax > 0.f;
+    const float s = nz ? amax / 448.0f : 1.0f;
+    const float inv = nz ? 448.0f / amax : 0.0f;
+    for (int i = lane; i < nvec; i += 32) {
+      uint4 out = make_uint4(0, 0, 0, 0);
+      if (nz) {
+        uint4 q[2] = {__ldg(xr + 2 * i), __ldg(xr + 2 * i + 1)};
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f0 = __bfloat1622float2(b[2 * j]);
+          const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
+          const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv)), __NV_SATFINITE, __NV_E4M3);
+          const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)), __NV_SATFINITE, __NV_E4M3);
+          w[j] = (lo & 0xFFFFu) | (hi << 16);
+        }
+        out = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      for (int j = 0; j < k; ++j) {
+        uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(rows[tt * k + j]) * H);
+        dst[i] = out;
+      }
+    }
+    if (lane < k) x_scale[rows[tt * k + lane]] = s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
+                         int32_t* chunk_counts, cudaStream_t s) {
+  const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
+  const size_t smem = static_cast<size_t>(E) * sizeof(int32_t);
+  const int nv = (E + 31) / 32;
+  if (nv <= 1) route_kernel<1><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else if (nv <= 2) route_kernel<2><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else if (nv <= 4) route_kernel<4><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else if (nv <= 8) route_kernel<8><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else if (nv <= 16) route_kernel<16><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else route_kernel<32><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
+                        int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
+                        int32_t* num_tiles, cudaStream_t s) {
+  const int threads = ((E + 31) / 32) * 32;
+  scan_kernel<<<1, threads, 0, s>>>(chunk_counts, num_chunks, E, bn, counts, offsets, chunk_base,
+                                    tiles, num_tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_quant(const void* x, const int32_t* ids, const int32_t* chunk_base,
+                                 int T, int E, int k, int H, int32_t* row_of,
+                                 int32_t* token_slot, uint8_t* xq, float* x_scale,
+                                 cudaStream_t s) {
+  const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
+  const size_t smem = static_cast<size_t>(E + kRouteChunk * k) * sizeof(int32_t);
+  scatter_quant_kernel<<<chunks, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(x), ids,
+                                                 chunk_base, T, E, k, H, row_of, token_slot, xq,
+                                                 x_scale);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

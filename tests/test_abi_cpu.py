@@ -1,0 +1,123 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+function include/moe.h declares; host-only entry points (workspace size and
+layout) and argument validation work without a GPU (validation returns
+before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import precision_moe_grouped_gb300 as P
+from precision_moe_grouped_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        from precision_moe_grouped_gb300 import build
+        try:
+            build.build()
+        except (RuntimeError, FileNotFoundError) as e:  # no nvcc on this machine
+            pytest.skip(f"cannot build libmoe.so here: {e}")
+    return P.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    decl = declared_functions()
+    assert len(decl) >= 10
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert set(decl) == set(L.EXPORTS)
+    assert b"sm_103a" in lib.moe_version()
+
+
+def _shape(T=16, E=8, k=2, H=256, I=128):
+    return P.shape(T, E, k, H, I)
+
+
+def test_workspace_size_and_layout(lib):
+    s = _shape(4096, 256, 8, 7168, 2048)
+    n = P.workspace_size(s)
+    lay = P.workspace_layout(s)
+    assert n == lay.total and n % 256 == 0
+    R = 4096 * 8
+    offs = [("status", 16), ("ids", R * 4), ("weights", R * 4), ("row_of", R * 4),
+            ("counts", 256 * 4), ("offsets", 257 * 4), ("chunk_counts", 128 * 256 * 4),
+            ("token_slot", R * 4), ("tiles", lay.max_tiles * 16), ("xq", R * 7168),
+            ("x_scale", R * 4), ("h", R * 2048 * 2), ("hq", R * 2048), ("h_scale", R * 4),
+            ("y", R * 7168 * 2), ("x_stage", 4096 * 7168 * 2), ("logits_stage", 4096 * 256 * 4),
+            ("out_stage", 4096 * 7168 * 2)]
+    end = 0
+    for name, size in offs:
+        o = getattr(lay, name)
+        assert o % 256 == 0 and o >= end, name
+        end = o + size
+    assert end <= n
+    assert lay.num_chunks == 128
+    # the tile bound covers the worst case of the decode tiling
+    assert lay.max_tiles >= R // 32 + 256
+
+
+@pytest.mark.parametrize("bad", [dict(T=-1), dict(E=0), dict(k=0), dict(k=9, E=8), dict(k=33, E=64),
+                                 dict(H=100), dict(I=96), dict(E=2000)])
+def test_workspace_size_rejects_bad_shapes(lib, bad):
+    kw = dict(T=16, E=8, k=2, H=256, I=128)
+    kw.update(bad)
+    assert P.workspace_size(_shape(**kw)) == 0
+    assert P.workspace_size(_shape(), 7) == 0
+
+
+def _fwd(lib, s, ptrs, nbytes, mode=0, opts=None):
+    args = [ctypes.byref(s), mode] + list(ptrs) + [nbytes, None]
+    if opts is None:
+        return lib.moe_forward(*args)
+    return lib.moe_forward_ex(*args, ctypes.byref(opts))
+
+
+def test_forward_validation_without_gpu(lib):
+    s = _shape()
+    need = P.workspace_size(s)
+    good = [0x100000 * (i + 1) for i in range(8)]
+    assert _fwd(lib, s, [None] + good[1:], need) == L.MOE_ERR_INVALID_ARG
+    mis = list(good)
+    mis[0] += 8                                         # x not 16-byte aligned
+    assert _fwd(lib, s, mis, need) == L.MOE_ERR_MISALIGNED
+    mis = list(good)
+    mis[2] += 32                                        # w1 not 256-byte aligned
+    assert _fwd(lib, s, mis, need) == L.MOE_ERR_MISALIGNED
+    assert _fwd(lib, s, good, need - 1) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert _fwd(lib, s, good, need, mode=2) == L.MOE_ERR_UNSUPPORTED
+    assert _fwd(lib, s, good, need, mode=5) == L.MOE_ERR_INVALID_ARG
+    assert _fwd(lib, _shape(H=200), good, need) == L.MOE_ERR_MISALIGNED
+    assert _fwd(lib, s, good, need, opts=P.options(tile_variant=3)) == L.MOE_ERR_INVALID_ARG
+    o = P.options()
+    o.reserved[2] = 1
+    assert _fwd(lib, s, good, need, opts=o) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_last_error()                          # a message was recorded
+    # zero tokens: a no-op that succeeds without touching the device
+    assert _fwd(lib, _shape(T=0), [None] * 8, 0) == L.MOE_OK
+    assert lib.moe_forward(None, 0, *([None] * 8), 0, None) == L.MOE_ERR_INVALID_ARG
+
+
+def test_prepare_and_misc_validation_without_gpu(lib):
+    s = _shape()
+    p = [0x100000 * (i + 1) for i in range(8)]
+    assert lib.moe_prepare_weights(ctypes.byref(s), 0, None, *p[1:], None) == L.MOE_ERR_INVALID_ARG
+    alias = list(p)
+    alias[4] = alias[0]
+    assert lib.moe_prepare_weights(ctypes.byref(s), 0, *alias, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_prepare_weights(ctypes.byref(s), 1, *p, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_selftest_timeout(None, 10, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_timeout(0x100000, 0, None) == L.MOE_ERR_INVALID_ARG
+    st = ctypes.c_int32(0)
+    assert lib.moe_read_device_status(None, None, ctypes.byref(st)) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_status_string(-6) == b"device-side wait timed out"

@@ -1,0 +1,261 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bit-exact: routing ids, per-expert counts/offsets, the expanded-row maps,
+the FP8 activation codes and the per-token scales.  Floating point (routing
+weights, h, y, output): max|err| <= 2e-2 * max|ref| and
+sum|err| / sum|ref| <= 5e-3 (outputs in bf16)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as MI
+import precision_moe_grouped_gb300 as P
+from oracle import moe as M
+
+from gpu_helpers import GpuRun, dump, max_err_ok, oracle_weights, x_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    P.load()
+
+
+def check_front(run: GpuRun, rt: M.Routing, tq: np.ndarray, ts: np.ndarray, rows=None):
+    """Bit-exact checks of routing, expansion and FP8 activation quantisation
+    (rows: optional subset of expanded rows to compare codes on)."""
+    np.testing.assert_array_equal(run.ids, rt.ids)
+    np.testing.assert_array_equal(run.counts, rt.counts)
+    np.testing.assert_array_equal(run.offsets, rt.offsets)
+    np.testing.assert_array_equal(run.row_of, rt.row_of)
+    ts_gpu = run.token_slot
+    np.testing.assert_array_equal(ts_gpu // run.k, rt.token_of_row)
+    np.testing.assert_array_equal(ts_gpu % run.k, rt.slot_of_row)
+    np.testing.assert_allclose(run.weights, rt.weights, rtol=3e-6, atol=1e-7)
+    np.testing.assert_array_equal(run.x_scale, ts[rt.token_of_row])
+    xq = run.xq
+    sel = np.arange(run.R) if rows is None else np.asarray(rows)
+    np.testing.assert_array_equal(xq[sel], tq[rt.token_of_row[sel]])
+
+
+def check_tiles(run: GpuRun, bn: int):
+    """The work map covers every expanded row exactly once, in expert order,
+    with tiles of at most bn rows."""
+    tiles = run.tiles
+    covered = np.zeros(run.R, np.int32)
+    off = run.offsets
+    for e, r0, n, _ in tiles:
+        assert 0 < n <= bn
+        assert off[e] <= r0 and r0 + n <= off[e + 1]
+        covered[r0:r0 + n] += 1
+    assert np.all(covered == 1)
+
+
+def full_parity(case, variant=0, name="case"):
+    run = GpuRun(case, variant=variant)
+    assert run.status == 0
+    fw = M.forward(x_bits(case), case.logits.cpu().numpy(), oracle_weights(case),
+                   case.cfg.top_k)
+    tq, ts = M.quantize_rows_fp8(
+        np.asarray(case.x.float().cpu().numpy(), np.float32))
+    try:
+        check_front(run, fw.routing, tq, ts)
+        ok_h, st_h = max_err_ok(run.h, fw.h)
+        ok_y, st_y = max_err_ok(run.y, fw.y)
+        ok_o, st_o = max_err_ok(run.out_np(), fw.out)
+        assert ok_h, ("h", st_h)
+        assert ok_y, ("y", st_y)
+        assert ok_o, ("out", st_o)
+    except AssertionError:
+        dump(name, h=run.h, h_ref=fw.h, y=run.y, y_ref=fw.y, out=run.out_np(), out_ref=fw.out,
+             xq=run.xq, xq_ref=fw.xq, ids=run.ids, ids_ref=fw.routing.ids, tiles=run.tiles,
+             hq=run.hq, hq_ref=fw.hq, hs=run.h_scale, hs_ref=fw.h_scale, g_ref=fw.g)
+        raise
+    return run, fw
+
+
+def test_tiny_config_full():
+    cfg = MI.CONFIGS["tiny"]
+    run, _ = full_parity(MI.make_case(cfg, 16), name="tiny")
+    check_tiles(run, 32)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_several_tiles_ragged(variant):
+    """Many token tiles per expert (decode variant), ragged tails, several
+    weight M-tiles and K stages."""
+    cfg = MI.custom_config(8, 2, 512, 256)
+    run, _ = full_parity(MI.make_case(cfg, 200, seed=7), variant=variant, name=f"ragged{variant}")
+    check_tiles(run, 32 if variant == 1 else 224)
+
+
+def test_expert_split_over_tiles_prefill():
+    """Experts with > 224 rows split into balanced tiles (prefill variant)."""
+    cfg = MI.custom_config(4, 2, 256, 128)
+    run, _ = full_parity(MI.make_case(cfg, 700, seed=9), variant=2, name="split")
+    assert run.counts.max() > 224
+    check_tiles(run, 224)
+
+
+def test_variants_agree_bitwise():
+    cfg = MI.custom_config(8, 2, 256, 128)
+    case = MI.make_case(cfg, 96, seed=13)
+    a = GpuRun(case, variant=1)
+    b = GpuRun(case, variant=2, moe=a.moe)
+    np.testing.assert_array_equal(a.out_np(), b.out_np())
+
+
+def test_deterministic():
+    cfg = MI.custom_config(16, 4, 256, 256)
+    case = MI.make_case(cfg, 64, seed=21)
+    a = GpuRun(case)
+    b = GpuRun(case, moe=a.moe)
+    np.testing.assert_array_equal(a.out_np(), b.out_np())
+
+
+@pytest.mark.parametrize("E,k,T", [(1, 1, 5), (4, 4, 33), (32, 1, 7), (16, 16, 3)])
+def test_degenerate_routing(E, k, T):
+    """One expert; every expert selected (k = E); k = 1; more experts than rows."""
+    cfg = MI.custom_config(E, k, 128, 128)
+    full_parity(MI.make_case(cfg, T, seed=31 + T), name=f"degen{E}_{k}_{T}")
+
+
+def test_zero_rows_and_ties():
+    cfg = MI.custom_config(8, 2, 256, 128)
+    case = MI.make_case(cfg, 24, seed=41)
+    case.x[3] = 0                      # amax = 0: s = 1, zero codes
+    case.x[5, 7] = -0.0
+    case.logits[4] = 0.0               # all-equal logits: lowest indices win
+    case.logits[6, 2] = case.logits[6, 5] = case.logits[6].max() + 1.0
+    run, fw = full_parity(case, name="zeros_ties")
+    assert run.x_scale[run.row_of[3, 0]] == 1.0
+    np.testing.assert_array_equal(run.ids[4], [0, 1])
+    np.testing.assert_array_equal(run.ids[6], [2, 5])
+
+
+def test_empty_experts():
+    cfg = MI.custom_config(16, 2, 256, 128)
+    case = MI.make_case(cfg, 40, seed=43)
+    case.logits[:, 3:9] -= 50.0        # experts 3..8 never chosen
+    run, _ = full_parity(case, name="empty")
+    assert np.all(run.counts[3:9] == 0)
+
+
+def test_zero_tokens_is_noop():
+    cfg = MI.custom_config(8, 2, 256, 128)
+    case = MI.make_case(cfg, 4)
+    dev = torch.device("cuda:0")
+    moe = P.FusedMoE(case.w1.to(dev), case.w1_sf.to(dev), case.w2.to(dev), case.w2_sf.to(dev), 2)
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device=dev)
+    lg = torch.empty((0, 8), dtype=torch.float32, device=dev)
+    out = moe(x, lg)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256)
+
+
+def test_prepare_weights_layout():
+    """moe_prepare_weights moves rows and scale bytes exactly as documented."""
+    cfg = MI.custom_config(3, 2, 256, 256)
+    case = MI.make_case(cfg, 1, seed=3)
+    dev = torch.device("cuda:0")
+    moe = P.FusedMoE(case.w1.to(dev), case.w1_sf.to(dev), case.w2.to(dev), case.w2_sf.to(dev), 2)
+    torch.cuda.synchronize()
+    E, I, H = 3, 256, 256
+    w1, sf1 = case.w1.numpy(), case.w1_sf.numpy()
+    src = np.empty(2 * I, np.int64)
+    for p in range(2 * I):
+        mt, r = divmod(p, 128)
+        q, i = divmod(r, 32)
+        f = 64 * mt + 16 * q + (i & 15)
+        src[p] = f if i < 16 else I + f
+    np.testing.assert_array_equal(moe.w1_p.cpu().numpy(), w1[:, src])
+    np.testing.assert_array_equal(moe.w2_p.cpu().numpy(), case.w2.numpy())
+
+    def relayout(sf, rows_src, M, K):
+        out = np.empty((E, M // 128, K // 128, 32, 4, 4), np.uint8)
+        for mt in range(M // 128):
+            for ks in range(K // 128):
+                for l in range(32):
+                    for i in range(4):
+                        out[:, mt, ks, l, i, :] = sf[:, rows_src[mt * 128 + 32 * i + l],
+                                                     4 * ks:4 * ks + 4]
+        return out.reshape(E, -1)
+    np.testing.assert_array_equal(moe.w1_sf_p.cpu().numpy().reshape(E, -1),
+                                  relayout(sf1, src, 2 * I, H))
+    np.testing.assert_array_equal(moe.w2_sf_p.cpu().numpy().reshape(E, -1),
+                                  relayout(case.w2_sf.numpy(), np.arange(H), H, I))
+
+
+def test_forward_host_matches_device_path():
+    cfg = MI.custom_config(8, 2, 256, 128)
+    case = MI.make_case(cfg, 50, seed=17)
+    run = GpuRun(case)
+    s = P.shape(50, 8, 2, 256, 128)
+    xh = case.x.clone().pin_memory()
+    lh = case.logits.clone().pin_memory()
+    oh = torch.empty((50, 256), dtype=torch.bfloat16).pin_memory()
+    ws = torch.zeros(P.workspace_size(s), dtype=torch.uint8, device="cuda:0")
+    P.forward_host(s, xh, lh, run.moe.w1_p, run.moe.w1_sf_p, run.moe.w2_p, run.moe.w2_sf_p, oh,
+                   ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(oh.float().numpy(), run.out_np())
+
+
+def test_device_timeout_status_and_recovery():
+    """A bounded wait that nothing satisfies returns an error status; the
+    context stays usable for the next forward."""
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda:0")
+    P.selftest_timeout(ws, 2000)
+    torch.cuda.synchronize()
+    assert P.read_device_status(ws) == P._lib.MOE_ERR_DEVICE_TIMEOUT
+    cfg = MI.CONFIGS["tiny"]
+    full_parity(MI.make_case(cfg, 16), name="after_timeout")
+
+
+def test_invalid_args_on_device():
+    cfg = MI.custom_config(8, 2, 256, 128)
+    s = P.shape(4, 8, 2, 256, 128)
+    ws = torch.zeros(P.workspace_size(s) - 256, dtype=torch.uint8, device="cuda:0")
+    t = torch.zeros(4096, dtype=torch.uint8, device="cuda:0")
+    with pytest.raises(P.MoeError) as ei:
+        P.forward(s, t, t.view(torch.float32), t, t, t, t, t, ws)
+    assert ei.value.code == P._lib.MOE_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(P.MoeError) as ei:
+        P.forward(s, t, t.view(torch.float32), t, t, t, t, t, ws, mode=P.MOE_W8A8_MXFP8)
+    assert ei.value.code == P._lib.MOE_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ full sizes
+def _sampled_parity(cfg, T, n_sample, variant=0):
+    """Full-size run in the bench's launch configuration; S1-S3 checked
+    bit-exactly on every token, the output on a seeded token sample (a
+    token's output depends only on its own inputs)."""
+    case = MI.make_case(cfg, T, device="cuda")
+    run = GpuRun(case, variant=variant)
+    assert run.status == 0
+    rt, tq, ts = M.route_and_quantize(x_bits(case), case.logits.cpu().numpy(), cfg.top_k)
+    rng = np.random.default_rng(T)
+    rows = rng.choice(run.R, size=min(run.R, 512), replace=False)
+    check_front(run, rt, tq, ts, rows=rows)
+    toks = np.sort(rng.choice(T, size=min(T, n_sample), replace=False))
+    fw = M.forward(x_bits(case), case.logits.cpu().numpy(), oracle_weights(case), cfg.top_k,
+                   tokens=toks)
+    ok, st = max_err_ok(run.out_np()[toks], fw.out)
+    if not ok:
+        dump(f"{cfg.name}_{T}", out=run.out_np()[toks], out_ref=fw.out, toks=toks)
+    assert ok, st
+    return run
+
+
+@pytest.mark.parametrize("T", [1, 8, 64, 512, 4096])
+def test_dsv3_sizes(T):
+    _sampled_parity(MI.CONFIGS["dsv3"], T, n_sample=4 if T > 8 else T)
+
+
+@pytest.mark.parametrize("T", [1, 128, 8192])
+def test_v4pro_sizes(T):
+    _sampled_parity(MI.CONFIGS["v4pro"], T, n_sample=3 if T > 1 else 1)
