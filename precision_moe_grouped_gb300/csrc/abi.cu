@@ -55,6 +55,12 @@ int32_t fail(int32_t code, const char* fmt, ...) {
 
 constexpr size_t kAlign = 256;
 
+// A 128-row x 128-element E2M1 weight box copied with 16U4_ALIGN16B fills
+// 16 KB of shared memory (8 data bytes + an 8-byte gap per 16 elements) but
+// counts as the 8 KB of packed global bytes in the mbarrier transaction
+// count (measured on GB300).
+constexpr uint32_t kWeightBoxTxBytes = 128u * 128u / 2u;
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -272,11 +278,11 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   MOE_CUDA(moe::launch_scatter_quant(x, ids, chunk, T, E, k, H, row_of,
                                      at<int32_t>(ws, L.token_slot), xq, x_scale, st));
   moe::GemmArgs g1{&tm_w1, &tm_x, static_cast<const uint8_t*>(w1_sf), tiles, num_tiles,
-                   x_scale, h, 2 * I, H, I, status, timeout_ns, 16384u, dev.num_sms};
+                   x_scale, h, 2 * I, H, I, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms};
   MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
   moe::GemmArgs g2{&tm_w2, &tm_h, static_cast<const uint8_t*>(w2_sf), tiles, num_tiles,
-                   h_scale, y, H, I, H, status, timeout_ns, 16384u, dev.num_sms};
+                   h_scale, y, H, I, H, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms};
   MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));
   return MOE_OK;

@@ -35,7 +35,7 @@ struct GemmArgs {
   int32_t out_ld;              // I (GEMM1) or H (GEMM2)
   int32_t* status;
   uint64_t timeout_ns;
-  uint32_t a_tx_bytes;         // shared-memory bytes one weight TMA box delivers
+  uint32_t a_tx_bytes;         // transaction bytes one weight TMA box counts
   int32_t num_sms;
 };
 
