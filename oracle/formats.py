@@ -32,9 +32,8 @@ import numpy as np
 E4M3_MAX = 448.0
 
 
-def e2m1_decode(codes) -> np.ndarray:
-    """Value of each 4-bit E2M1 code (low nibble of each uint8), float64."""
-    c = np.asarray(codes, dtype=np.uint8) & 0xF
+def _e2m1_value(c: np.ndarray) -> np.ndarray:
+    """OCP MX E2M1 definition applied to 4-bit codes."""
     sign = np.where((c >> 3) & 1, -1.0, 1.0)
     exp = ((c >> 1) & 3).astype(np.int64)
     man = (c & 1).astype(np.float64)
@@ -43,16 +42,9 @@ def e2m1_decode(codes) -> np.ndarray:
     return sign * mag
 
 
-def e8m0_decode(codes) -> np.ndarray:
-    """Value 2^(b-127) of each E8M0 byte, float64; 0xFF decodes to NaN."""
-    b = np.asarray(codes, dtype=np.uint8).astype(np.int64)
-    v = np.ldexp(1.0, b - 127)
-    return np.where(b == 255, np.nan, v)
-
-
-def e4m3_decode(codes) -> np.ndarray:
-    """Value of each E4M3 (fn variant) byte, float64; 0x7F/0xFF are NaN."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+def _e4m3_value(c: np.ndarray) -> np.ndarray:
+    """OCP MX E4M3 (fn variant) definition applied to 8-bit codes."""
+    c = c.astype(np.int64)
     sign = np.where((c >> 7) & 1, -1.0, 1.0)
     exp = (c >> 3) & 0xF
     man = (c & 7).astype(np.float64)
@@ -61,6 +53,34 @@ def e4m3_decode(codes) -> np.ndarray:
                    np.ldexp(1.0 + man / 8.0, exp - 7))
     out = sign * mag
     return np.where((c & 0x7F) == 0x7F, np.nan, out)
+
+
+def _e8m0_value(b: np.ndarray) -> np.ndarray:
+    """OCP MX E8M0 definition: 2^(b-127), 0xFF is NaN."""
+    b = b.astype(np.int64)
+    return np.where(b == 255, np.nan, np.ldexp(1.0, b - 127))
+
+
+# The definitions above are evaluated once for every code; decoding a tensor
+# is then a table lookup (same values, without per-element exponent work).
+_E2M1_TABLE = _e2m1_value(np.arange(16, dtype=np.uint8))
+_E4M3_TABLE = _e4m3_value(np.arange(256, dtype=np.uint8))
+_E8M0_TABLE = _e8m0_value(np.arange(256, dtype=np.uint8))
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Value of each 4-bit E2M1 code (low nibble of each uint8), float64."""
+    return _E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & 0xF]
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    """Value 2^(b-127) of each E8M0 byte, float64; 0xFF decodes to NaN."""
+    return _E8M0_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each E4M3 (fn variant) byte, float64; 0x7F/0xFF are NaN."""
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
 
 
 def e4m3_encode(values) -> np.ndarray:
@@ -134,9 +154,13 @@ def mxfp4_dequant(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
     [..., N, K/32] (one E8M0 byte per 32 consecutive K elements of a row)
     [P3738 Description; P4793 review comments].  Element (n, k) is
     E2M1(n, k) * 2^(scale(n, k // 32) - 127)."""
-    vals = e2m1_decode(unpack_e2m1(packed))
+    p = np.asarray(packed, dtype=np.uint8)
+    # value pair of every possible byte, through the same unpack + decode
+    pair = e2m1_decode(unpack_e2m1(np.arange(256, dtype=np.uint8)[:, None]))   # [256, 2]
+    vals = pair[p].reshape(p.shape[:-1] + (p.shape[-1] * 2,))
     sc = e8m0_decode(scales)
-    return vals * np.repeat(sc, 32, axis=-1)
+    blk = vals.reshape(vals.shape[:-1] + (vals.shape[-1] // 32, 32))
+    return (blk * sc[..., None]).reshape(vals.shape)
 
 
 def mxfp8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
