@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Throughput of the fused MXFP4 x FP8 MoE forward on GB300 (one JSON line).
+
+Workload (default): the DeepSeek-V3-shaped MoE layer -- E=256 experts, top-8
+softmax routing, H=7168, I=2048, SwiGLU -- at T=4096 tokens, MXFP4 expert
+weights and runtime per-token FP8 activations, synthetic seeded inputs
+(moe_inputs.py).  One step = one full forward (routing, scatter + FP8
+quantisation, GEMM1 + SwiGLU, h quantisation, GEMM2, combine) through the C
+ABI, inputs resident in HBM.  The same metric is also reported end to end
+(`e2e`: host activations copied in and the output copied out inside the
+timed region), per kernel (CUDA events the library records between its
+launches), as a roofline fraction, and over the T sweep 1..4096.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+N > 1 (launched under torch.distributed.run) runs independent replicas, one
+per GPU (the forward has no exchange step on one GPU): value = all tokens
+processed / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused-MoE tokens/s + TFLOP/s at DSV3 shape, T=1..4096; % of roofline"
+UNIT = "tokens/s"
+FP8_OVER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor-rate ratio on GB300
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="dsv3")
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--sweep-steps", type=int, default=30)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 decode, 2 prefill tiles")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as td
+            td.init_process_group(backend=backend)
+            self.pg = td
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def done(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+class Clocks:
+    """nvidia-smi clock / throttle samples over a region (every 100 ms)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self) -> dict:
+        time.sleep(0.15)
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    smax.append(float(c[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "gemm1": ["precision_moe_grouped_gb300/csrc/gemm.cu", "precision_moe_grouped_gb300/csrc/ptx.cuh"],
+    "gemm2": ["precision_moe_grouped_gb300/csrc/gemm.cu", "precision_moe_grouped_gb300/csrc/ptx.cuh"],
+    "combine": ["precision_moe_grouped_gb300/csrc/rowops.cu"],
+    "hquant": ["precision_moe_grouped_gb300/csrc/rowops.cu"],
+    "quant_scatter": ["precision_moe_grouped_gb300/csrc/route.cu"],
+}
+
+
+def ncu_traffic(stage: str, cfg_name: str, T: int):
+    """DRAM bytes per launch of `stage` from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p) or stage not in KERNEL_SOURCES:
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(f"{stage}:{cfg_name}:{T}")
+    if not rec or rec.get("source_sha") != source_hash(KERNEL_SOURCES[stage]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def alg_cost(stage: str, cfg, T: int, n_touched: int):
+    """Algorithmic (bytes, flops) of one launch of `stage`."""
+    E, k, H, I = cfg.num_experts, cfg.top_k, cfg.hidden, cfg.inter
+    R = T * k
+    w1 = 2 * I * H * (0.5 + 1 / 32)
+    w2 = H * I * (0.5 + 1 / 32)
+    table = {
+        "route": (T * E * 4 + R * 8, 0),
+        "scan": (R * 0, 0),
+        "rank": (R * 12, 0),
+        "quant_scatter": (T * H * 2 + R * H + R * 4, 0),
+        "gemm1": (n_touched * w1 + R * H + R * 4 + R * I * 2, 2.0 * R * H * 2 * I),
+        "hquant": (R * I * 2 + R * I + R * 4, 0),
+        "gemm2": (n_touched * w2 + R * I + R * 4 + R * H * 2, 2.0 * R * I * H),
+        "combine": (R * H * 2 + R * 8 + T * H * 2, 0),
+    }
+    return table[stage]
+
+
+def fused_roofline(cfg, T, n_touched, t_s, pk):
+    """Roofline of the whole forward: max(touched weight+scale + activation
+    bytes / HBM, FLOPs / FP8 tensor peak)."""
+    E, k, H, I = cfg.num_experts, cfg.top_k, cfg.hidden, cfg.inter
+    bytes_ = n_touched * 3 * I * H * (0.5 + 1 / 32) + T * H * 2 + T * E * 4 + T * H * 2
+    flops = 2.0 * T * k * 3 * I * H
+    t_mem = bytes_ / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * FP8_OVER_BF16 * 1e12)
+    return {"bytes": bytes_, "flops": flops, "t_hbm_us": t_mem * 1e6, "t_tensor_us": t_tc * 1e6,
+            "bound": "hbm" if t_mem >= t_tc else "tensor",
+            "frac": max(t_mem, t_tc) / t_s, "hbm_frac": t_mem / t_s, "tensor_frac": t_tc / t_s}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, dist: Dist):
+    import torch
+
+    import moe_inputs as MI
+    import precision_moe_grouped_gb300 as P
+
+    torch.cuda.set_device(dist.local)
+    dist.init("nccl")
+    dev = torch.device("cuda", dist.local)
+    cfg = MI.CONFIGS[args.config]
+    T = args.tokens
+    K, W = args.steps, args.warmup
+    pk, pk_src = peaks()
+    case = MI.make_case(cfg, T, device=f"cuda:{dist.local}")
+    moe = P.FusedMoE(case.w1, case.w1_sf, case.w2, case.w2_sf, cfg.top_k)
+    del case.w1, case.w1_sf, case.w2, case.w2_sf
+    torch.cuda.synchronize()
+    x, logits = case.x, case.logits
+    out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    s = moe.shape(T)
+    ws = moe.workspace(T)
+    stream = torch.cuda.current_stream()
+    nst = P._lib.MOE_NUM_STAGES
+    names = P._lib.stage_names()
+
+    def fwd(opts=None):
+        P.forward(s, x, logits, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, out, ws,
+                  opts=opts)
+
+    base = P.options(tile_variant=args.variant)
+    for _ in range(max(W, 3)):
+        fwd(base)
+    torch.cuda.synchronize()
+    if P.read_device_status(ws) != 0:
+        raise RuntimeError("device status error after warm-up")
+    lay = P.workspace_layout(s)
+    counts = ws[lay.counts:lay.counts + 4 * cfg.num_experts].view(torch.int32).cpu().numpy()
+    n_touched = int((counts > 0).sum())
+
+    # per-step stage events (created up front by one record each)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    arrays = [P._lib.stage_event_array(row) for row in evs]
+    opts = [P.options(tile_variant=args.variant, stage_events=a) for a in arrays]
+    torch.cuda.synchronize()
+
+    clocks = Clocks(dist.local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        fwd(opts[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    ms_local = t0.elapsed_time(t1) / K
+    ms = dist.max(ms_local)
+    if P.read_device_status(ws) != 0:
+        raise RuntimeError("device status error in timed region")
+    stage_ms = {names[j]: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                for j in range(nst)}
+    gpu_launches = nst * K
+
+    # end to end: host activations in, output out, inside the timed region
+    xh = x.cpu().pin_memory()
+    lh = logits.cpu().pin_memory()
+    oh = torch.empty((T, cfg.hidden), dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        P.forward_host(s, xh, lh, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, oh, ws, opts=base)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        P.forward_host(s, xh, lh, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, oh, ws, opts=base)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = dist.max(e0.elapsed_time(e1) / K)
+    assert torch.equal(oh.to(dev), out), "host-buffer forward disagrees with device forward"
+
+    # dominant kernel and its roofline
+    dom = max(stage_ms, key=stage_ms.get)
+    dbytes, dflops = alg_cost(dom, cfg, T, n_touched)
+    dsec = stage_ms[dom] / 1e3
+    t_mem = dbytes / (pk["hbm_gbs"] * 1e9)
+    tc_peak = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+    t_tc = dflops / (tc_peak * 1e12)
+    if t_tc > t_mem:
+        roof = {"bound": "tensor", "achieved": dflops / dsec / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dbytes / dsec / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(dom, cfg.name, T)
+    roof.update({"kernel": dom, "alg_bytes_per_launch": dbytes, "alg_flops_per_launch": dflops,
+                 "ms_per_launch": stage_ms[dom], "peak_source": pk_src,
+                 "tensor_frac": (dflops / dsec / 1e12) / tc_peak if dflops else 0.0,
+                 "hbm_frac": dbytes / dsec / 1e9 / pk["hbm_gbs"]})
+
+    fr = fused_roofline(cfg, T, n_touched, ms / 1e3, pk)
+    result = {
+        "metric": METRIC, "value": dist.world * T / (ms / 1e3), "unit": UNIT,
+        "n_gpus": dist.world, "steps": K, "warmup": W, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8e4m3 x fp4e2m1 (mxf8f6f4), fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) activations/logits, N(0,0.02) weights as MXFP4)",
+        "config": {"workload": f"DeepSeek-V3-shaped MoE layer E={cfg.num_experts} top-{cfg.top_k} "
+                               f"H={cfg.hidden} I={cfg.inter} SwiGLU, T={T}, MXFP4xFP8",
+                   "num_tokens": T, "num_experts": cfg.num_experts, "top_k": cfg.top_k,
+                   "hidden": cfg.hidden, "inter": cfg.inter, "parallelism": f"replicas x{dist.world}",
+                   "l2": "no flush: the touched expert weights per step "
+                         f"({n_touched * 3 * cfg.inter * cfg.hidden * 0.53125 / 1e9:.2f} GB) "
+                         "exceed the 129 MB L2",
+                   "tile_variant": args.variant},
+        "tflops": fr["flops"] / (ms / 1e3) / 1e12,
+        "fused_roofline": fr,
+        "roofline": roof,
+        "stage_ms": stage_ms,
+        "e2e": {"value": dist.world * T / (ms_e2e / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": T * cfg.hidden * 2 + T * cfg.num_experts * 4,
+                "d2h_bytes_per_step": T * cfg.hidden * 2, "ms_per_step": ms_e2e},
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "experts_touched": n_touched,
+    }
+
+    if not args.no_sweep:
+        result["sweep"] = sweep(args, cfg, moe, x, logits, dist, pk)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, T, x, logits, 1)
+    dist.done()
+    return result
+
+
+def sweep(args, cfg, moe, x_all, lg_all, dist, pk):
+    """Each T of the configuration's sweep, with 16 rotating token sets (so
+    successive steps route to different experts and do not reuse L2)."""
+    import torch
+
+    import precision_moe_grouped_gb300 as P
+    res = []
+    stream = torch.cuda.current_stream()
+    T_all = x_all.shape[0]
+    for T in cfg.tokens:
+        nsets = max(1, min(16, T_all // T))
+        sets = [(x_all[i * T:(i + 1) * T].contiguous(), lg_all[i * T:(i + 1) * T].contiguous())
+                for i in range(nsets)]
+        s = moe.shape(T)
+        ws = moe.workspace(T) if T == T_all else torch.empty(
+            P.workspace_size(s), dtype=torch.uint8, device=x_all.device)
+        out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=x_all.device)
+        o = P.options(tile_variant=args.variant)
+
+        def fwd(i):
+            xs, ls = sets[i % nsets]
+            P.forward(s, xs, ls, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, out, ws, opts=o)
+        for i in range(5):
+            fwd(i)
+        torch.cuda.synchronize()
+        lay = P.workspace_layout(s)
+        touched = []
+        for i in range(nsets):
+            fwd(i)
+            torch.cuda.synchronize()
+            c = ws[lay.counts:lay.counts + 4 * cfg.num_experts].view(torch.int32)
+            touched.append(int((c > 0).sum().item()))
+        dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.sweep_steps):
+            fwd(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = dist.max(a.elapsed_time(b) / args.sweep_steps)
+        n_t = sum(touched) / len(touched)
+        fr = fused_roofline(cfg, T, n_t, ms / 1e3, pk)
+        res.append({"T": T, "ms": ms, "tokens_s": dist.world * T / (ms / 1e3),
+                    "tflops": fr["flops"] / (ms / 1e3) / 1e12, "experts_touched": n_t,
+                    "roofline_frac": fr["frac"], "bound": fr["bound"],
+                    "hbm_frac": fr["hbm_frac"], "tensor_frac": fr["tensor_frac"],
+                    "token_sets": nsets})
+        if ws is not moe.workspace(T_all):
+            del ws
+    return res
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_sample(cfg, T, x, logits, n_tok):
+    """Host inputs for the oracle on the first n_tok tokens of the workload:
+    the token rows and logits plus the weights of the experts they route to
+    (regenerated from the per-expert seeds, same bytes as the GPU run)."""
+    import numpy as np
+    import torch
+
+    import moe_inputs as MI
+    from oracle import moe as M
+    toks = np.arange(n_tok)
+    xb = x[:n_tok].cpu().view(torch.int16).numpy().view(np.uint16)
+    lg = logits[:n_tok].cpu().numpy()
+    ids, _ = M.route(lg, cfg.top_k)
+    seed = MI.seed_for(cfg, T)
+    experts = sorted(set(ids.ravel().tolist()))
+    dev = "cuda" if x.is_cuda else "cpu"
+    w = {e: [t.cpu().numpy() for t in MI.expert_weights(cfg, seed, e, dev)] for e in experts}
+
+    class Lazy:
+        def __init__(self, j, shape):
+            self.j, self.shape = j, shape
+
+        def __getitem__(self, e):
+            return w[int(e)][self.j]
+    H, I, E = cfg.hidden, cfg.inter, cfg.num_experts
+    W = M.Weights(Lazy(0, (E, 2 * I, H // 2)), Lazy(1, (E, 2 * I, H // 32)),
+                  Lazy(2, (E, H, I // 2)), Lazy(3, (E, H, I // 32)))
+    return xb, lg, W, toks, experts
+
+
+def cpu_baseline(cfg, T, x, logits, n_tok):
+    """The oracle, as it stands, on the first n_tok tokens of the workload."""
+    from oracle import moe as M
+    xb, lg, W, toks, experts = oracle_sample(cfg, T, x, logits, n_tok)
+    t = time.perf_counter()
+    M.forward(xb, lg, W, cfg.top_k)
+    dt = time.perf_counter() - t
+    return {"value": n_tok / dt, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{n_tok} of the {T} tokens ({len(experts)} experts decoded and applied); "
+                      "numpy, BLAS matmuls may use all listed cores", "seconds": dt}
+
+
+def run_reference(args, dist: Dist):
+    """The oracle (CPU) on a bounded sample per step of the same workload."""
+    if dist.rank != 0:
+        return None
+    import moe_inputs as MI
+    cfg = MI.CONFIGS[args.config]
+    T = args.tokens
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x, logits = MI.make_activations(cfg, T, dev)
+    from oracle import moe as M
+    xb, lg, W, toks, experts = oracle_sample(cfg, T, x, logits, 1)
+    for _ in range(args.warmup):
+        M.forward(xb, lg, W, cfg.top_k)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        M.forward(xb, lg, W, cfg.top_k)
+    dt = time.perf_counter() - t
+    v = args.steps / dt
+    sample = (f"1 of the {T} tokens per step ({len(experts)} experts decoded and applied); "
+              "numpy, BLAS matmuls may use all listed cores")
+    return {"metric": METRIC, "value": v, "unit": UNIT, "impl": "reference", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32",
+            "data": "synthetic", "config": {"workload": f"DeepSeek-V3-shaped MoE layer "
+                                                        f"E={cfg.num_experts} top-{cfg.top_k} "
+                                                        f"H={cfg.hidden} I={cfg.inter}, T={T}",
+                                            "num_tokens": T},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        res = run_reference(args, dist)
+    else:
+        res = run_ours(args, dist)
+    if res is not None and dist.rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -78,12 +78,20 @@ typedef struct {
   int32_t inter;        /* I (w1 has 2I rows: gate rows 0..I-1, up rows I..2I-1) */
 } moe_shape;
 
+/* Kernels one forward launches, in stream order: route, scan, rank,
+ * quant_scatter, gemm1, hquant, gemm2, combine (moe_stage_name() names them). */
+#define MOE_NUM_STAGES 8
+
 /* Optional per-call settings (moe_forward_ex); zero-initialise for defaults. */
 typedef struct {
   int32_t tile_variant;  /* 0 auto; 1 decode tiles (<= 32 tokens per GEMM tile,
                             deep weight pipeline); 2 prefill tiles (<= 224)   */
   int32_t timeout_ms;    /* device bounded-wait limit, 0 = 1000 ms           */
-  int32_t reserved[6];   /* must be zero                                     */
+  void* stage_events;    /* NULL, or an array of MOE_NUM_STAGES + 1 cudaEvent_t
+                            (caller-created): event 0 is recorded on `stream`
+                            before the first kernel and event i right after
+                            kernel i, so event pairs time each kernel      */
+  int32_t reserved[4];   /* must be zero                                     */
 } moe_options;
 
 /* Byte offsets of the intermediate tensors inside the workspace, for tests
@@ -180,6 +188,9 @@ int32_t moe_selftest_timeout(void* workspace, int32_t timeout_us, void* stream);
 
 /* Message describing the last error returned on the calling thread. */
 const char* moe_last_error(void);
+
+/* Name of forward kernel `stage` (0 .. MOE_NUM_STAGES-1), or NULL. */
+const char* moe_stage_name(int32_t stage);
 
 /* Static description of a status code. */
 const char* moe_status_string(int32_t status);

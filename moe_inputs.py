@@ -49,6 +49,10 @@ CONFIGS = {
     "v4pro": MoeConfig("v4pro", 3, 384, 6, 7168, 3072, (1, 16, 128, 1024, 8192)),
     "mxfp8_zipf": MoeConfig("mxfp8_zipf", 4, 256, 8, 7168, 2048, (4096,),
                             mode=QUANT_W8A8, zipf=1.2),
+    # DeepSeek-V3 layer shape with 32 experts: at T=512 each expert gets the
+    # same ~128 rows as the full layer at T=4096, in 0.75 GB of weights (used
+    # for profiler captures that must stay small)
+    "dsv3_e32": MoeConfig("dsv3_e32", 5, 32, 8, 7168, 2048, (512,)),
 }
 
 
@@ -115,6 +119,31 @@ class MoeCase:
         return self.cfg.mode
 
 
+def expert_weights(cfg: MoeConfig, seed: int, e: int, device: str = "cpu"):
+    """(w1, w1_sf, w2, w2_sf) of expert e, drawn from the expert's own seed."""
+    quant = quantize_mxfp8_weights if cfg.mode == QUANT_W8A8 else quantize_mxfp4
+    E, H, I = cfg.num_experts, cfg.hidden, cfg.inter
+    ge = torch.Generator(device=device).manual_seed(seed * 1000003 + 7919 * e + 1)
+    a = torch.randn((2 * I, H), generator=ge, device=device, dtype=torch.float32) * 0.02
+    w1, w1_sf = quant(a)
+    b = torch.randn((H, I), generator=ge, device=device, dtype=torch.float32) * 0.02
+    w2, w2_sf = quant(b)
+    return w1, w1_sf, w2, w2_sf
+
+
+def make_activations(cfg: MoeConfig, T: int, device: str = "cpu", seed: int | None = None):
+    """(x bf16 [T, H], logits float32 [T, E]) of the seeded case."""
+    seed = seed_for(cfg, T) if seed is None else seed
+    g = torch.Generator(device=device).manual_seed(seed)
+    x = torch.randn((T, cfg.hidden), generator=g, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    logits = torch.randn((T, cfg.num_experts), generator=g, device=device, dtype=torch.float32)
+    if cfg.zipf > 0:
+        ranks = torch.randperm(cfg.num_experts, generator=g, device=device).to(torch.float32) + 1.0
+        logits = logits - cfg.zipf * torch.log(ranks)[None, :]
+    return x, logits
+
+
 def make_case(cfg: MoeConfig, T: int, device: str = "cpu", seed: int | None = None,
               experts: list | None = None) -> MoeCase:
     """Draw one seeded case.  Weights are drawn expert by expert from a
@@ -122,25 +151,14 @@ def make_case(cfg: MoeConfig, T: int, device: str = "cpu", seed: int | None = No
     other experts' weights are then left zero)."""
     seed = seed_for(cfg, T) if seed is None else seed
     E, H, I = cfg.num_experts, cfg.hidden, cfg.inter
-    g = torch.Generator(device=device).manual_seed(seed)
-    x = torch.randn((T, H), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
-    logits = torch.randn((T, E), generator=g, device=device, dtype=torch.float32)
-    if cfg.zipf > 0:
-        ranks = torch.randperm(E, generator=g, device=device).to(torch.float32) + 1.0
-        logits = logits - cfg.zipf * torch.log(ranks)[None, :]
-    fp8w = cfg.mode == QUANT_W8A8
-    kdiv = 1 if fp8w else 2
+    x, logits = make_activations(cfg, T, device, seed)
+    kdiv = 1 if cfg.mode == QUANT_W8A8 else 2
     w1 = torch.zeros((E, 2 * I, H // kdiv), dtype=torch.uint8, device=device)
     w2 = torch.zeros((E, H, I // kdiv), dtype=torch.uint8, device=device)
     w1_sf = torch.full((E, 2 * I, H // 32), 127, dtype=torch.uint8, device=device)
     w2_sf = torch.full((E, H, I // 32), 127, dtype=torch.uint8, device=device)
-    quant = quantize_mxfp8_weights if fp8w else quantize_mxfp4
     for e in (range(E) if experts is None else experts):
-        ge = torch.Generator(device=device).manual_seed(seed * 1000003 + 7919 * e + 1)
-        a = torch.randn((2 * I, H), generator=ge, device=device, dtype=torch.float32) * 0.02
-        w1[e], w1_sf[e] = quant(a)
-        b = torch.randn((H, I), generator=ge, device=device, dtype=torch.float32) * 0.02
-        w2[e], w2_sf[e] = quant(b)
+        w1[e], w1_sf[e], w2[e], w2_sf[e] = expert_weights(cfg, seed, e, device)
     return MoeCase(cfg=cfg, T=T, x=x, logits=logits, w1=w1, w1_sf=w1_sf, w2=w2, w2_sf=w2_sf)
 
 

@@ -27,7 +27,10 @@ MOE_W8A8_MXFP8 = 2
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_prepare_weights", "moe_forward",
            "moe_forward_ex", "moe_forward_host", "moe_read_device_status",
-           "moe_selftest_timeout", "moe_last_error", "moe_status_string", "moe_version")
+           "moe_selftest_timeout", "moe_last_error", "moe_stage_name", "moe_status_string",
+           "moe_version")
+
+MOE_NUM_STAGES = 8
 
 
 class MoeShape(ctypes.Structure):
@@ -37,7 +40,7 @@ class MoeShape(ctypes.Structure):
 
 class MoeOptions(ctypes.Structure):
     _fields_ = [("tile_variant", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 6)]
+                ("stage_events", ctypes.c_void_p), ("reserved", ctypes.c_int32 * 4)]
 
 
 class WsLayout(ctypes.Structure):
@@ -87,6 +90,8 @@ def load() -> ctypes.CDLL:
     for f in ("moe_last_error", "moe_version"):
         getattr(lib, f).argtypes = []
         getattr(lib, f).restype = ctypes.c_char_p
+    lib.moe_stage_name.argtypes = [i32]
+    lib.moe_stage_name.restype = ctypes.c_char_p
     lib.moe_status_string.argtypes = [i32]
     lib.moe_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -104,10 +109,24 @@ def shape(T: int, E: int, k: int, H: int, I: int) -> MoeShape:
     return MoeShape(T, E, k, H, I)
 
 
-def options(tile_variant: int = 0, timeout_ms: int = 0) -> MoeOptions:
+def options(tile_variant: int = 0, timeout_ms: int = 0, stage_events=None) -> MoeOptions:
+    """stage_events: None, or a ctypes array of MOE_NUM_STAGES + 1 cudaEvent_t
+    handles (e.g. from stage_event_array())."""
     o = MoeOptions()
     o.tile_variant, o.timeout_ms = tile_variant, timeout_ms
+    o.stage_events = ctypes.cast(stage_events, ctypes.c_void_p) if stage_events is not None else None
     return o
+
+
+def stage_names() -> list:
+    lib = load()
+    return [lib.moe_stage_name(i).decode() for i in range(MOE_NUM_STAGES)]
+
+
+def stage_event_array(events) -> "ctypes.Array":
+    """ctypes array of the raw cudaEvent_t handles of torch.cuda.Event objects."""
+    assert len(events) == MOE_NUM_STAGES + 1
+    return (ctypes.c_void_p * len(events))(*[int(e.cuda_event) for e in events])
 
 
 def workspace_size(s: MoeShape, mode: int = MOE_W4A8_MXFP4_FP8) -> int:

@@ -201,7 +201,7 @@ int32_t check_options(const moe_options* o) {
   if (o->tile_variant < 0 || o->tile_variant > 2)
     return fail(MOE_ERR_INVALID_ARG, "tile_variant must be 0, 1 or 2");
   if (o->timeout_ms < 0) return fail(MOE_ERR_INVALID_ARG, "timeout_ms < 0");
-  for (int i = 0; i < 6; ++i)
+  for (int i = 0; i < 4; ++i)
     if (o->reserved[i] != 0) return fail(MOE_ERR_INVALID_ARG, "reserved option fields must be 0");
   return MOE_OK;
 }
@@ -271,20 +271,34 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
       (rc = make_tmap(&tm_h, hq, R, I, false, 128, 32)) != MOE_OK)
     return rc;
 
+  cudaEvent_t* ev = opts ? static_cast<cudaEvent_t*>(opts->stage_events) : nullptr;
+  int stage = 0;
+  auto mark = [&]() -> cudaError_t {
+    return ev ? cudaEventRecord(ev[stage++], st) : cudaSuccess;
+  };
   MOE_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  MOE_CUDA(mark());
   MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, st));
+  MOE_CUDA(mark());
   MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts),
                             at<int32_t>(ws, L.offsets), chunk, tiles, num_tiles, st));
-  MOE_CUDA(moe::launch_scatter_quant(x, ids, chunk, T, E, k, H, row_of,
-                                     at<int32_t>(ws, L.token_slot), xq, x_scale, st));
+  MOE_CUDA(mark());
+  MOE_CUDA(moe::launch_rank(ids, chunk, T, E, k, row_of, at<int32_t>(ws, L.token_slot), st));
+  MOE_CUDA(mark());
+  MOE_CUDA(moe::launch_quant_scatter(x, row_of, T, k, H, xq, x_scale, st));
+  MOE_CUDA(mark());
   moe::GemmArgs g1{&tm_w1, &tm_x, static_cast<const uint8_t*>(w1_sf), tiles, num_tiles,
                    x_scale, h, 2 * I, H, I, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms};
   MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
+  MOE_CUDA(mark());
   MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
+  MOE_CUDA(mark());
   moe::GemmArgs g2{&tm_w2, &tm_h, static_cast<const uint8_t*>(w2_sf), tiles, num_tiles,
                    h_scale, y, H, I, H, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms};
   MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
+  MOE_CUDA(mark());
   MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));
+  MOE_CUDA(mark());
   return MOE_OK;
 }
 
@@ -295,6 +309,12 @@ extern "C" {
 const char* moe_version(void) { return "precision_moe_grouped_gb300 0.1 (sm_103a)"; }
 
 const char* moe_last_error(void) { return g_last_error; }
+
+const char* moe_stage_name(int32_t stage) {
+  static const char* names[MOE_NUM_STAGES] = {"route", "scan", "rank", "quant_scatter",
+                                              "gemm1", "hquant", "gemm2", "combine"};
+  return stage >= 0 && stage < MOE_NUM_STAGES ? names[stage] : nullptr;
+}
 
 const char* moe_status_string(int32_t status) {
   switch (status) {

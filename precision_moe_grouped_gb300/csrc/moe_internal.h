@@ -44,10 +44,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
                         int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
                         int32_t* num_tiles, cudaStream_t s);
-cudaError_t launch_scatter_quant(const void* x, const int32_t* ids, const int32_t* chunk_base,
-                                 int T, int E, int k, int H, int32_t* row_of,
-                                 int32_t* token_slot, uint8_t* xq, float* x_scale,
-                                 cudaStream_t s);
+cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,
+                        int32_t* row_of, int32_t* token_slot, cudaStream_t s);
+cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, int T, int k, int H,
+                                 uint8_t* xq, float* x_scale, cudaStream_t s);
 cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_scale,
                           cudaStream_t s);
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,

@@ -13,8 +13,9 @@
 //
 // Kernel chain: route (one warp per token; per-chunk expert histogram) ->
 // scan (one CTA: counts, offsets, per-chunk bases, GEMM tile list) ->
-// scatter_quant (one CTA per chunk: stable ranks, then FP8 codes written to
-// each of the token's k expanded rows).  Nothing returns to the host.
+// rank (one warp per chunk: stable expert-major row of every (token, slot))
+// -> quant_scatter (one CTA per token: FP8 codes written to each of the
+// token's k expanded rows).  Nothing returns to the host.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cfloat>
@@ -27,12 +28,12 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- routing
-// One warp per token.  Lane l holds logits of experts l, l+32, ... (NV per
+// One warp per token (32 warps = one chunk per CTA).  Lane l holds logits of experts l, l+32, ... (NV per
 // lane).  k rounds of a warp argmax pick the experts in descending logit
 // order, equal logits resolved toward the lower expert index.  Weights are
 // the softmax over the k selected logits (renormalised top-k softmax).
 template <int NV>
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T,
+__global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T,
                                                     int E, int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ wts,
                                                     int32_t* __restrict__ chunk_counts) {
@@ -170,88 +171,90 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
   if (e == 0) *num_tiles = total_tiles;
 }
 
-// One CTA per chunk of kRouteChunk tokens.  Warp 0 walks the chunk's tokens
-// in order and hands out rows from the chunk's per-expert bases (a token's k
-// experts are distinct, so the k lanes never collide), which makes each
-// expert's rows ascend in token order.  Then every warp quantises tokens:
-// amax -> s = amax/448, inv = 448/amax (IEEE divisions) -> E4M3 codes of
-// x*inv (round to nearest even, satfinite), written to all k rows.
-__global__ void __launch_bounds__(256) scatter_quant_kernel(
-    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids,
-    const int32_t* __restrict__ chunk_base, int T, int E, int k, int H,
-    int32_t* __restrict__ row_of, int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq,
-    float* __restrict__ x_scale) {
+// One warp per chunk of kRouteChunk tokens: the warp walks the chunk's
+// tokens in order and hands out rows from the chunk's per-expert bases (a
+// token's k experts are distinct, so the k lanes never collide), which makes
+// each expert's rows ascend in token order.
+__global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ ids,
+                                                   const int32_t* __restrict__ chunk_base,
+                                                   int T, int E, int k, int num_chunks,
+                                                   int32_t* __restrict__ row_of,
+                                                   int32_t* __restrict__ token_slot) {
   extern __shared__ int32_t sm[];
-  int32_t* base = sm;               // [E]
-  int32_t* rows = sm + E;           // [kRouteChunk * k]
-  const int t0 = blockIdx.x * kRouteChunk;
-  for (int i = threadIdx.x; i < E; i += blockDim.x)
-    base[i] = chunk_base[static_cast<size_t>(blockIdx.x) * E + i];
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  if (warp == 0) {
-    for (int tt = 0; tt < kRouteChunk; ++tt) {
-      const int t = t0 + tt;
-      if (t >= T) break;
-      if (lane < k) {
-        const size_t ts = static_cast<size_t>(t) * k + lane;
-        const int e = ids[ts];
-        const int r = base[e];
-        base[e] = r + 1;
-        rows[tt * k + lane] = r;
-        row_of[ts] = r;
-        token_slot[r] = static_cast<int32_t>(ts);
-      }
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-  const int nvec = H / 16;  // 16 elements (two 16-byte loads) per lane step
-  for (int tt = warp; tt < kRouteChunk; tt += nwarps) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (chunk >= num_chunks) return;
+  int32_t* base = sm + warp * E;
+  for (int i = lane; i < E; i += 32) base[i] = chunk_base[static_cast<size_t>(chunk) * E + i];
+  __syncwarp();
+  const int t0 = chunk * kRouteChunk;
+  for (int tt = 0; tt < kRouteChunk; ++tt) {
     const int t = t0 + tt;
     if (t >= T) break;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
-    float amax = 0.f;
-    for (int i = lane; i < nvec; i += 32) {
+    if (lane < k) {
+      const size_t ts = static_cast<size_t>(t) * k + lane;
+      const int e = ids[ts];
+      const int r = base[e];
+      base[e] = r + 1;
+      row_of[ts] = r;
+      token_slot[r] = static_cast<int32_t>(ts);
+    }
+    __syncwarp();
+  }
+}
+
+// One CTA per token: amax -> s = amax/448, inv = 448/amax (IEEE divisions)
+// -> E4M3 codes of x*inv (round to nearest even, satfinite), written to all
+// k expanded rows of the token; an all-zero row gets s = 1 and zero codes.
+__global__ void __launch_bounds__(128) quant_scatter_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of, int k, int H,
+    uint8_t* __restrict__ xq, float* __restrict__ x_scale) {
+  __shared__ int32_t rows[32];
+  __shared__ float warp_max[4];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) rows[threadIdx.x] = row_of[static_cast<size_t>(t) * k + threadIdx.x];
+  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+  const int nvec = H / 16;  // 16 elements (two 16-byte loads) per thread step
+  float amax = 0.f;
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+    uint4 q[2] = {__ldg(xr + 2 * i), __ldg(xr + 2 * i + 1)};
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 f = __bfloat1622float2(b[j]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
+  const bool nz = amax > 0.f;
+  const float s = nz ? amax / 448.0f : 1.0f;
+  const float inv = nz ? 448.0f / amax : 0.0f;
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (nz) {
       uint4 q[2] = {__ldg(xr + 2 * i), __ldg(xr + 2 * i + 1)};
       const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
+      uint32_t w[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float2 f = __bfloat1622float2(b[j]);
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      for (int j = 0; j < 4; ++j) {
+        const float2 f0 = __bfloat1622float2(b[2 * j]);
+        const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv)), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)), __NV_SATFINITE, __NV_E4M3);
+        w[j] = (lo & 0xFFFFu) | (hi << 16);
       }
+      out = make_uint4(w[0], w[1], w[2], w[3]);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const bool nz = amax > 0.f;
-    const float s = nz ? amax / 448.0f : 1.0f;
-    const float inv = nz ? 448.0f / amax : 0.0f;
-    for (int i = lane; i < nvec; i += 32) {
-      uint4 out = make_uint4(0, 0, 0, 0);
-      if (nz) {
-        uint4 q[2] = {__ldg(xr + 2 * i), __ldg(xr + 2 * i + 1)};
-        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f0 = __bfloat1622float2(b[2 * j]);
-          const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
-          const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-              make_float2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv)), __NV_SATFINITE, __NV_E4M3);
-          const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-              make_float2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)), __NV_SATFINITE, __NV_E4M3);
-          w[j] = (lo & 0xFFFFu) | (hi << 16);
-        }
-        out = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      for (int j = 0; j < k; ++j) {
-        uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(rows[tt * k + j]) * H);
-        dst[i] = out;
-      }
-    }
-    if (lane < k) x_scale[rows[tt * k + lane]] = s;
+    for (int j = 0; j < k; ++j)
+      reinterpret_cast<uint4*>(xq + static_cast<size_t>(rows[j]) * H)[i] = out;
   }
+  if (threadIdx.x < k) x_scale[rows[threadIdx.x]] = s;
 }
 
 }  // namespace
@@ -261,12 +264,12 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
   const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
   const size_t smem = static_cast<size_t>(E) * sizeof(int32_t);
   const int nv = (E + 31) / 32;
-  if (nv <= 1) route_kernel<1><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else if (nv <= 2) route_kernel<2><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else if (nv <= 4) route_kernel<4><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else if (nv <= 8) route_kernel<8><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else if (nv <= 16) route_kernel<16><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else route_kernel<32><<<chunks, 256, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  if (nv <= 1) route_kernel<1><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else if (nv <= 2) route_kernel<2><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else if (nv <= 4) route_kernel<4><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else if (nv <= 8) route_kernel<8><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else if (nv <= 16) route_kernel<16><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
+  else route_kernel<32><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
   return cudaGetLastError();
 }
 
@@ -279,15 +282,20 @@ cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_scatter_quant(const void* x, const int32_t* ids, const int32_t* chunk_base,
-                                 int T, int E, int k, int H, int32_t* row_of,
-                                 int32_t* token_slot, uint8_t* xq, float* x_scale,
-                                 cudaStream_t s) {
+cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,
+                        int32_t* row_of, int32_t* token_slot, cudaStream_t s) {
   const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
-  const size_t smem = static_cast<size_t>(E + kRouteChunk * k) * sizeof(int32_t);
-  scatter_quant_kernel<<<chunks, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(x), ids,
-                                                 chunk_base, T, E, k, H, row_of, token_slot, xq,
-                                                 x_scale);
+  const int warps = 8;
+  const size_t smem = static_cast<size_t>(warps) * E * sizeof(int32_t);
+  rank_kernel<<<(chunks + warps - 1) / warps, 32 * warps, smem, s>>>(ids, chunk_base, T, E, k,
+                                                                     chunks, row_of, token_slot);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, int T, int k, int H,
+                                 uint8_t* xq, float* x_scale, cudaStream_t s) {
+  quant_scatter_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(x), row_of, k, H, xq,
+                                         x_scale);
   return cudaGetLastError();
 }
 
