@@ -186,6 +186,36 @@ int32_t moe_read_device_status(const void* workspace, void* stream, int32_t* sta
  * the kernel returns normally.  For tests of the failure path. */
 int32_t moe_selftest_timeout(void* workspace, int32_t timeout_us, void* stream);
 
+/* Size of the static device scratch moe_route_noalloc uses (4 MiB). */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* Routing front end without any caller-provided scratch: top-k softmax
+ * routing, per-expert offsets and the expert-major row map -- the same
+ * kernels and results as the first stages of moe_forward -- for callers that
+ * cannot allocate device memory.  Examples: a plugin inside an inference
+ * server that is handed only its input and output buffers and has no
+ * allocator of its own, or a latency-critical path that must not call
+ * cudaMalloc after start-up (it can synchronise the device and take
+ * unbounded time).  The paper has no counterpart to this entry point.
+ *   router_logits  float [T, E] (device)      input
+ *   ids            int32 [T, k] (device)      output: experts, descending logit
+ *   weights        float [T, k] (device)      output: renormalised weights
+ *   offsets        int32 [E + 1] (device)     output: exclusive scan of counts
+ *   row_of         int32 [T, k] (device)      output: expert-major row of (t, j)
+ * Its scratch is one file-scope device array of MOE_NOALLOC_SCRATCH_BYTES,
+ * which every GPU that loads this library holds until the process exits.
+ * Shapes needing more (about (T/32)*E*4 + T*k*4.5 + E*20 bytes) are rejected
+ * with MOE_ERR_WORKSPACE_TOO_SMALL and a message in moe_last_error().  The
+ * first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the one array, which keeps the last call's contents (every
+ * word a call reads is written earlier in the same call): calls that overlap
+ * on the GPU -- on different streams or from different host threads -- race
+ * on it and must be serialised.  Allocates nothing (no cudaMalloc/cudaFree).
+ * num_tokens == 0 returns MOE_OK and launches nothing. */
+int32_t moe_route_noalloc(const moe_shape* shape, const float* router_logits, int32_t* ids,
+                          float* weights, int32_t* offsets, int32_t* row_of, void* stream);
+
 /* Message describing the last error returned on the calling thread. */
 const char* moe_last_error(void);
 

@@ -28,7 +28,9 @@ MOE_W8A8_MXFP8 = 2
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_prepare_weights", "moe_forward",
            "moe_forward_ex", "moe_forward_host", "moe_read_device_status",
            "moe_selftest_timeout", "moe_last_error", "moe_stage_name", "moe_status_string",
-           "moe_version")
+           "moe_version", "moe_route_noalloc")
+
+MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 MOE_NUM_STAGES = 8
 
@@ -90,6 +92,8 @@ def load() -> ctypes.CDLL:
     for f in ("moe_last_error", "moe_version"):
         getattr(lib, f).argtypes = []
         getattr(lib, f).restype = ctypes.c_char_p
+    lib.moe_route_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp]
+    lib.moe_route_noalloc.restype = i32
     lib.moe_stage_name.argtypes = [i32]
     lib.moe_stage_name.restype = ctypes.c_char_p
     lib.moe_status_string.argtypes = [i32]
@@ -186,3 +190,11 @@ def read_device_status(workspace, stream=None) -> int:
 
 def selftest_timeout(workspace, timeout_us: int, stream=None) -> None:
     check(load().moe_selftest_timeout(_ptr(workspace), timeout_us, _stream(stream)))
+
+
+def route_noalloc(s: MoeShape, logits, ids, weights, offsets, row_of, stream=None) -> None:
+    """Routing front end (ids, weights, offsets, row map) using the library's
+    static device scratch instead of a workspace; see moe_route_noalloc in
+    include/moe.h for the size limit and the no-overlap rule."""
+    check(load().moe_route_noalloc(ctypes.byref(s), _ptr(logits), _ptr(ids), _ptr(weights),
+                                   _ptr(offsets), _ptr(row_of), _stream(stream)))

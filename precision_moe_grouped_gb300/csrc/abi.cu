@@ -304,6 +304,10 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
 
 }  // namespace
 
+namespace moe {
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+}  // namespace moe
+
 extern "C" {
 
 const char* moe_version(void) { return "precision_moe_grouped_gb300 0.1 (sm_103a)"; }

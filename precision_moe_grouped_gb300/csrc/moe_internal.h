@@ -57,6 +57,9 @@ cudaError_t launch_prepare_w1(const uint8_t* w1, const uint8_t* w1_sf, uint8_t* 
                               uint8_t* w1_sf_p, int E, int I, int H, cudaStream_t s);
 cudaError_t launch_prepare_sf_plain(const uint8_t* sf, uint8_t* sf_p, int E, int M, int K,
                                     cudaStream_t s);
+// Sets the message moe_last_error() returns on the calling thread.
+void set_last_error(const char* msg);
+
 cudaError_t launch_timeout_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
 }  // namespace moe
