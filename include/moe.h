@@ -91,7 +91,10 @@ typedef struct {
                             (caller-created): event 0 is recorded on `stream`
                             before the first kernel and event i right after
                             kernel i, so event pairs time each kernel      */
-  int32_t reserved[4];   /* must be zero                                     */
+  int32_t prefetch_stages; /* L2 prefetch distance of the GEMM weight stream in
+                            K stages (8 KB of packed weights each per SM):
+                            0 = default (16), < 0 = off                   */
+  int32_t reserved[3];   /* must be zero                                     */
 } moe_options;
 
 /* Byte offsets of the intermediate tensors inside the workspace, for tests

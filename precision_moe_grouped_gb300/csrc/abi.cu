@@ -61,6 +61,10 @@ constexpr size_t kAlign = 256;
 // count (measured on GB300).
 constexpr uint32_t kWeightBoxTxBytes = 128u * 128u / 2u;
 
+// Default L2 prefetch distance of the GEMMs' weight stream, in K stages of
+// 8 KB of packed weights per SM (0: the shared-memory ring alone).
+constexpr int kDefaultPrefetchStages = 0;
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -165,27 +169,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D tensor map over a row-major [rows, cols] matrix; box = box_cols x
-// box_rows elements, 128-byte swizzle.  fp4: 16U4_ALIGN16B (each group of 16
-// packed codes lands as 16 bytes in shared memory), else uint8.
-int32_t make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, bool fp4,
+enum class MapKind { kFp4Weights, kBytes, kScaleBlocks };
+
+// 2-D tensor map over a row-major [rows, cols] matrix of `kind` elements;
+// box = box_cols x box_rows elements.
+//   kFp4Weights:  E2M1 codes, 16U4_ALIGN16B (each group of 16 packed codes
+//                 lands as 16 bytes in shared memory), 128-byte swizzle
+//   kBytes:       uint8 (FP8 codes), 128-byte swizzle
+//   kScaleBlocks: uint32 words, no swizzle
+int32_t make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, MapKind kind,
                   uint32_t box_cols, uint32_t box_rows) {
   if (!base) return fail(MOE_ERR_INVALID_ARG, "refusing to encode a tensor map for NULL");
   auto fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const bool fp4 = kind == MapKind::kFp4Weights, words = kind == MapKind::kScaleBlocks;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {fp4 ? cols / 2 : cols};
+  const cuuint64_t strides[1] = {fp4 ? cols / 2 : words ? cols * 4 : cols};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m,
-                  fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                  const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  fp4     ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
+                  : words ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                          : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                  2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  words ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
-    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) rows=%llu cols=%llu fp4=%d",
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) rows=%llu cols=%llu kind=%d",
                 static_cast<int>(r), static_cast<unsigned long long>(rows),
-                static_cast<unsigned long long>(cols), fp4 ? 1 : 0);
+                static_cast<unsigned long long>(cols), static_cast<int>(kind));
   return MOE_OK;
 }
 
@@ -201,7 +214,8 @@ int32_t check_options(const moe_options* o) {
   if (o->tile_variant < 0 || o->tile_variant > 2)
     return fail(MOE_ERR_INVALID_ARG, "tile_variant must be 0, 1 or 2");
   if (o->timeout_ms < 0) return fail(MOE_ERR_INVALID_ARG, "timeout_ms < 0");
-  for (int i = 0; i < 4; ++i)
+  if (o->prefetch_stages > 1024) return fail(MOE_ERR_INVALID_ARG, "prefetch_stages > 1024");
+  for (int i = 0; i < 3; ++i)
     if (o->reserved[i] != 0) return fail(MOE_ERR_INVALID_ARG, "reserved option fields must be 0");
   return MOE_OK;
 }
@@ -248,6 +262,8 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   const int R = T * k;
   const int variant = pick_variant(s, opts);
   const int bn = variant == 1 ? moe::kDecodeBN : moe::kPrefillBN;
+  const int prefetch = !opts || opts->prefetch_stages == 0 ? kDefaultPrefetchStages
+                       : opts->prefetch_stages < 0 ? 0 : opts->prefetch_stages;
   const uint64_t timeout_ns =
       static_cast<uint64_t>(opts && opts->timeout_ms > 0 ? opts->timeout_ms : 1000) * 1000000ull;
   int32_t* status = at<int32_t>(ws, L.status);
@@ -264,12 +280,22 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   float* h_scale = at<float>(ws, L.h_scale);
   void* y = at<void>(ws, L.y);
 
-  CUtensorMap tm_w1, tm_x, tm_w2, tm_h;
-  if ((rc = make_tmap(&tm_w1, w1, static_cast<uint64_t>(E) * 2 * I, H, true, 128, 128)) != MOE_OK ||
-      (rc = make_tmap(&tm_x, xq, R, H, false, 128, 32)) != MOE_OK ||
-      (rc = make_tmap(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, true, 128, 128)) != MOE_OK ||
-      (rc = make_tmap(&tm_h, hq, R, I, false, 128, 32)) != MOE_OK)
+  CUtensorMap tm_w1, tm_w2, tm_sf1, tm_sf2, tm_x[moe::kNumXMaps], tm_h[moe::kNumXMaps];
+  // prepared weights: contiguous 128-row x 128-element (64-byte rows) boxes;
+  // prepared scales: one 512-byte block per box
+  const uint64_t w1_boxes = static_cast<uint64_t>(E) * (2 * I / 128) * (H / 128);
+  const uint64_t w2_boxes = static_cast<uint64_t>(E) * (H / 128) * (I / 128);
+  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, 128, MapKind::kFp4Weights, 128, 128)) != MOE_OK ||
+      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, 128, MapKind::kFp4Weights, 128, 128)) != MOE_OK ||
+      (rc = make_tmap(&tm_sf1, w1_sf, w1_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK ||
+      (rc = make_tmap(&tm_sf2, w2_sf, w2_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK)
     return rc;
+  for (int i = 0; i < moe::kNumXMaps; ++i) {
+    const uint32_t rows = static_cast<uint32_t>(moe::kXBoxRowsAt(i));
+    if ((rc = make_tmap(&tm_x[i], xq, R, H, MapKind::kBytes, 128, rows)) != MOE_OK ||
+        (rc = make_tmap(&tm_h[i], hq, R, I, MapKind::kBytes, 128, rows)) != MOE_OK)
+      return rc;
+  }
 
   cudaEvent_t* ev = opts ? static_cast<cudaEvent_t*>(opts->stage_events) : nullptr;
   int stage = 0;
@@ -287,14 +313,16 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_quant_scatter(x, row_of, T, k, H, xq, x_scale, st));
   MOE_CUDA(mark());
-  moe::GemmArgs g1{&tm_w1, &tm_x, static_cast<const uint8_t*>(w1_sf), tiles, num_tiles,
-                   x_scale, h, 2 * I, H, I, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms};
+  moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
+                   x_scale, h, 2 * I, H, I, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms,
+                   prefetch};
   MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
   MOE_CUDA(mark());
-  moe::GemmArgs g2{&tm_w2, &tm_h, static_cast<const uint8_t*>(w2_sf), tiles, num_tiles,
-                   h_scale, y, H, I, H, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms};
+  moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
+                   h_scale, y, H, I, H, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms,
+                   prefetch};
   MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));
@@ -368,14 +396,12 @@ int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode, const vo
   if ((st = device_info(&dev)) != MOE_OK) return st;
   const int E = shape->num_experts, H = shape->hidden, I = shape->inter;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MOE_CUDA(moe::launch_prepare_w1(static_cast<const uint8_t*>(w1),
-                                  static_cast<const uint8_t*>(w1_sf),
-                                  static_cast<uint8_t*>(w1_p), static_cast<uint8_t*>(w1_sf_p), E,
-                                  I, H, s));
-  MOE_CUDA(cudaMemcpyAsync(w2_p, w2, static_cast<size_t>(E) * H * (I / 2),
-                           cudaMemcpyDeviceToDevice, s));
-  MOE_CUDA(moe::launch_prepare_sf_plain(static_cast<const uint8_t*>(w2_sf),
-                                        static_cast<uint8_t*>(w2_sf_p), E, H, I, s));
+  MOE_CUDA(moe::launch_prepare(static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sf),
+                               static_cast<uint8_t*>(w1_p), static_cast<uint8_t*>(w1_sf_p), E,
+                               2 * I, H, I, s));
+  MOE_CUDA(moe::launch_prepare(static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sf),
+                               static_cast<uint8_t*>(w2_p), static_cast<uint8_t*>(w2_sf_p), E, H,
+                               I, 0, s));
   return MOE_OK;
 }
 

@@ -30,10 +30,11 @@
 // handed out statically (item = CTA + i * grid) from the device-built tile
 // list, so nothing returns to the host.
 //
-// Roles (192 threads): warp 0 lane 0 = TMA producer; warp 1 = TMEM owner and
-// (lane 0) MMA issuer; warps 2-5 = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31).  Two TMEM accumulators let the epilogue of one item
-// overlap the main loop of the next.
+// Roles: warp 0 lanes 0..3*STAGES-1 = TMA producers (three per stage);
+// warps 1..NI = MMA issuers (lane 0 each; warp 1 also owns the TMEM
+// allocation); the last 4 warps = epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. +31).  Two TMEM accumulator buffers let the epilogue of one
+// item overlap the main loop of the next.
 //
 // Epilogues:
 //   GEMM1 (SWIGLU): acc * s_x[row] -> h = silu(gate) * up -> bf16 h[row, f].
@@ -50,9 +51,22 @@ namespace moe {
 
 namespace {
 
-template <int BN, int STAGES>
+// Activation tensor maps with box heights 32, 64, ..., 224 rows: a tile
+// loads the smallest box covering its MMA-N rows in one copy.
+struct XMaps {
+  CUtensorMap m[kNumXMaps];
+};
+
+__device__ __forceinline__ int x_map_for(int rows) {
+  return (rows + 31) / 32 - 1;
+}
+
+template <int BN, int STAGES, int NI>
 struct GemmCfg {
-  static_assert(BN % 32 == 0 && BN <= 256, "token tile must be a multiple of 32 rows");
+  static_assert(BN % 32 == 0 && BN <= kXBoxRowsAt(kNumXMaps - 1),
+                "token tile must be a multiple of 32 rows and fit the largest box");
+  static_assert(3 * STAGES <= 32, "three producer lanes per stage must fit one warp");
+  static_assert(STAGES % NI == 0, "each stage must belong to one MMA issuer");
   static constexpr int kABytes = kTileM * 128;       // FP4 expanded to 1 byte/element in smem
   static constexpr int kBBytes = BN * 128;           // FP8 tokens x 128 K
   static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes
@@ -60,16 +74,19 @@ struct GemmCfg {
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffSF = kOffB + STAGES * kBBytes;
   static constexpr int kOffSFB = kOffSF + STAGES * kSFBytes;
-  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kNumBars = 2 * STAGES + 5 + NI;
   static constexpr int kOffBar = kOffSFB + 512;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  // TMEM columns: two fp32 accumulators of BN columns, 8 columns of constant
-  // activation scales (up to 256 tokens), 4 columns of weight scales per stage.
-  static constexpr int kColSFB = 2 * BN;
-  static constexpr int kColSFA = 2 * BN + 8;
-  static constexpr int kColsUsed = 2 * BN + 8 + 4 * STAGES;
+  // TMEM columns: for each of the two accumulator buffers, one fp32
+  // accumulator of BN columns per MMA issuer (buffer a, issuer i at column
+  // (a * NI + i) * BN); 8 columns of constant activation scales (up to 256
+  // tokens); 4 columns of weight scales per stage.
+  static constexpr int kThreads = 32 * (NI + 5);    // producer, NI issuers, 4 epilogue warps
+  static constexpr int kColSFB = 2 * NI * BN;
+  static constexpr int kColSFA = 2 * NI * BN + 8;
+  static constexpr int kColsUsed = 2 * NI * BN + 8 + 4 * STAGES;
   static constexpr int kTmemCols = kColsUsed <= 32    ? 32
                                    : kColsUsed <= 64  ? 64
                                    : kColsUsed <= 128 ? 128
@@ -78,16 +95,17 @@ struct GemmCfg {
   static_assert(kColsUsed <= 512, "TMEM budget exceeded");
 };
 
-template <int BN, int STAGES, bool SWIGLU>
-__global__ void __launch_bounds__(192, 1)
+template <int BN, int STAGES, int NI, bool SWIGLU>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                        const __grid_constant__ CUtensorMap tmap_x,
-                        const uint8_t* __restrict__ w_sf, const int4* __restrict__ tiles,
+                        const __grid_constant__ XMaps tmap_x,
+                        const __grid_constant__ CUtensorMap tmap_sf,
+                        const int4* __restrict__ tiles,
                         const int32_t* __restrict__ num_tiles_p,
                         const float* __restrict__ row_scale, __nv_bfloat16* __restrict__ out,
                         int m_per_expert, int K, int out_ld, int32_t* __restrict__ status,
-                        uint64_t timeout_ns, uint32_t a_tx_bytes) {
-  using C = GemmCfg<BN, STAGES>;
+                        uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages) {
+  using C = GemmCfg<BN, STAGES, NI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -101,22 +119,32 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MT = m_per_expert / kTileM, KS = K / kTileK;
-  const int64_t num_items = static_cast<int64_t>(*num_tiles_p) * MT;
+  const int num_items = *num_tiles_p * MT;   // < 2^31: tiles <= R/32 + E + 1
+  // Issuers with work: the largest divisor of STAGES that is <= min(NI, KS).
+  // Dividing STAGES makes every stage always consumed by the same issuer
+  // (fill f -> stage f % STAGES -> issuer f % ni), so each full barrier is
+  // waited on in phase order by one thread; a second thread waiting on the
+  // same barrier could see the parity of an older phase and run ahead.
+  // ni <= KS gives every issuer at least one stage of every item.
+  int ni = NI < KS ? NI : KS;
+  while (STAGES % ni != 0) --ni;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full + s, 1);
+      mbar_init(full + s, 3);   // weight, activation and scale copies arrive separately
       mbar_init(empty + s, 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull + a, 1);
-      mbar_init(tempty + a, 4);
+      mbar_init(tfull + a, ni);   // every issuer commits its share of an item
+      mbar_init(tempty + a, 4);   // every epilogue warp releases the buffer
     }
-    mbar_init(drain, 1);
+    for (int j = 0; j < NI; ++j) mbar_init(drain + j, 1);
+    mbar_init(drain + NI, 1);   // constant-scale copy done
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_w);
-    prefetch_tmap(&tmap_x);
+    prefetch_tmap(&tmap_sf);
+    for (int i = 0; i < kNumXMaps; ++i) prefetch_tmap(&tmap_x.m[i]);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   // Activation (B) scales are all 1.0: E8M0 byte 127 everywhere.
@@ -127,119 +155,170 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Constant activation scales into TMEM once, finished before any issuer
+  // (each a different thread) runs an MMA that reads them.
+  if (warp == 1 && lane == 0) {
+    const uint64_t sfb_desc = smem_desc(smem_u32(smem + C::kOffSFB), 0, 128, 0);
+    tc_cp_32x128b_x4(tmem + C::kColSFB, sfb_desc);
+    tc_cp_32x128b_x4(tmem + C::kColSFB + 4, sfb_desc);
+    tc_commit(drain + NI);
+    int32_t none = 0;
+    mbar_wait(drain + NI, 0, timeout_ns, status, kDevTimeout, &none);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
+    // Three issuing lanes per pipeline stage: lane 3s copies the weight box,
+    // lane 3s+1 the activation box and lane 3s+2 the scale block of stage s,
+    // each arriving on the stage's full barrier with its own byte count, for
+    // this CTA's fills f = s, s + STAGES, ... (fill f = K stage f % KS of the
+    // CTA's (f / KS)-th item).  Spreading the copies over threads keeps their
+    // issue off any single thread's critical path.
+    if (lane < 3 * STAGES) {
+      const int s = lane / 3, role = lane % 3;
       uint32_t phase = 0;
-      int64_t fills = 0;
-      bool ok = true;
-      for (int64_t item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
-        const int tile = static_cast<int>(item / MT), mt = static_cast<int>(item % MT);
-        const int4 td = tiles[tile];
-        const int nmma = (td.z + 15) & ~15;
-        const int nbox = (nmma + 31) >> 5;
-        const uint32_t bytes = a_tx_bytes + static_cast<uint32_t>(nbox) * 4096u + 512u;
-        const int wrow = td.x * m_per_expert + mt * kTileM;
-        const uint8_t* sf = w_sf + (static_cast<int64_t>(td.x) * MT + mt) * KS * 512;
-        for (int ks = 0; ks < KS; ++ks) {
-          if (!mbar_wait(empty + stage, phase ^ 1u, timeout_ns, status, kDevTimeout,
-                         abort_flag)) {
-            ok = false;
-            break;
+      bool issued = false;
+      // fill f = s + j * STAGES: K stage ks of the CTA's it-th item (KS >= STAGES
+      // is not assumed; the counters advance without divisions)
+      int ks = s % KS, item = blockIdx.x + (s / KS) * gridDim.x;
+      while (item < num_items) {
+        const int mt = item % MT;
+        const int4 td = tiles[item / MT];
+        // prepared weights: one contiguous 128 x 128 box per (expert, M-tile,
+        // K stage); box row = ((e * MT + mt) * KS + ks) * 128
+        const int64_t blk = (static_cast<int64_t>(td.x) * MT + mt) * KS + ks;
+        if (!mbar_wait(empty + s, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag)) break;
+        if (role == 0) {
+          mbar_arrive_expect_tx(full + s, a_tx_bytes);
+          tma_load_2d(smem + C::kOffA + s * C::kABytes, &tmap_w, 0,
+                      static_cast<int32_t>(blk * kTileM), full + s);
+          if (prefetch_stages > 0) {
+            // optional L2 prefetch of the weight box `prefetch_stages` fills ahead
+            int kp = ks + prefetch_stages, itp = item;
+            while (kp >= KS) {
+              kp -= KS;
+              itp += gridDim.x;
+            }
+            if (itp < num_items) {
+              const int64_t bp =
+                  (static_cast<int64_t>(tiles[itp / MT].x) * MT + itp % MT) * KS + kp;
+              tma_prefetch_l2_2d(&tmap_w, 0, static_cast<int32_t>(bp * kTileM));
+            }
           }
-          mbar_arrive_expect_tx(full + stage, bytes);
-          uint8_t* sa = smem + C::kOffA + stage * C::kABytes;
-          uint8_t* sb = smem + C::kOffB + stage * C::kBBytes;
-          tma_load_2d(sa, &tmap_w, ks * kTileK, wrow, full + stage);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(sb + b * 4096, &tmap_x, ks * kTileK, td.y + 32 * b, full + stage);
-          bulk_load(smem + C::kOffSF + stage * C::kSFBytes, sf + static_cast<int64_t>(ks) * 512,
-                    512u, full + stage);
-          ++fills;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        } else if (role == 1) {
+          // smallest activation box that covers the tile's MMA-N rows
+          const int nmma = (td.z + 15) & ~15;
+          const int xm = x_map_for(nmma);
+          mbar_arrive_expect_tx(full + s, static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u);
+          tma_load_2d(smem + C::kOffB + s * C::kBBytes, &tmap_x.m[xm], ks * kTileK, td.y,
+                      full + s);
+        } else {
+          mbar_arrive_expect_tx(full + s, 512u);
+          tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0, static_cast<int32_t>(blk),
+                      full + s);
+        }
+        issued = true;
+        phase ^= 1u;
+        ks += STAGES;
+        while (ks >= KS) {
+          ks -= KS;
+          item += gridDim.x;
         }
       }
-      // Every issued copy must land before the CTA may exit: wait for the
-      // last fill of each stage (ignores the abort flag, still bounded).
-      int32_t none = 0;
-      for (int64_t i = 0; i < STAGES && i < fills; ++i) {
-        const int64_t f = fills - 1 - i;
-        mbar_wait(full + static_cast<int>(f % STAGES), static_cast<uint32_t>((f / STAGES) & 1),
-                  timeout_ns, status, kDevTimeout, &none);
+      // Every issued copy must land before the CTA may exit: wait for this
+      // stage's last fill (ignores the abort flag, still bounded).
+      if (issued) {
+        int32_t none = 0;
+        mbar_wait(full + s, phase ^ 1u, timeout_ns, status, kDevTimeout, &none);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint64_t sfb_desc = smem_desc(smem_u32(smem + C::kOffSFB), 0, 128, 0);
-      tc_cp_32x128b_x4(tmem + C::kColSFB, sfb_desc);
-      tc_cp_32x128b_x4(tmem + C::kColSFB + 4, sfb_desc);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int64_t item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
-        const int4 td = tiles[static_cast<int>(item / MT)];
-        const uint32_t nmma = static_cast<uint32_t>((td.z + 15) & ~15);
-        if (!mbar_wait(tempty + acc, acc_phase ^ 1u, timeout_ns, status, kDevTimeout,
-                       abort_flag))
-          break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-        for (int ks = 0; ks < KS; ++ks) {
-          if (!mbar_wait(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag)) {
-            ok = false;
+  } else if (warp <= NI) {
+    // ------------------------------------------------------------ MMA issuers
+    // Each tcgen05 instruction occupies its issuing thread (measured ~540
+    // cycles per stage of one copy + 4 MMAs, independent of N), so with small
+    // token tiles one issuing thread cannot keep pace with the weight stream.
+    // Issuer i (warp 1 + i) takes fills f = i, i + ni, i + 2 ni, ... -- i.e.
+    // the stages s with s % ni == i -- and accumulates its K stages of an item
+    // into its own TMEM accumulator; the epilogue sums the ni partials.
+    // Every descriptor is precomputed: stage s and K sub-step kk only add
+    // constant start-address offsets (address >> 4 lives in the low 14 bits).
+    const int i = warp - 1;
+    if (lane == 0 && i < ni) {
+      const uint64_t adesc0 = smem_desc(smem_u32(smem + C::kOffA), 0, 1024, 2);
+      const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
+      const uint64_t sdesc0 = smem_desc(smem_u32(smem + C::kOffSF), 0, 128, 0);
+      int stage = i % STAGES, ks = i % KS, it = i / KS;   // ni <= KS, so it == 0
+      uint32_t phase = (i / STAGES) & 1;
+      bool new_item = true;
+      uint32_t d_tmem = 0, id0 = 0;
+      int acc = 0;
+      while (blockIdx.x + it * static_cast<int>(gridDim.x) < num_items) {
+        if (new_item) {
+          const int item = blockIdx.x + it * gridDim.x;
+          const int4 td = tiles[item / MT];
+          id0 = idesc_mx(5, 0, static_cast<uint32_t>((td.z + 15) & ~15), 0, 0);
+          acc = it & 1;
+          if (!mbar_wait(tempty + acc, ((it >> 1) & 1) ^ 1u, timeout_ns, status, kDevTimeout,
+                         abort_flag))
             break;
-          }
           tc_fence_after();
-          const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
-          tc_cp_32x128b_x4(sfa, smem_desc(smem_u32(smem + C::kOffSF + stage * C::kSFBytes), 0,
-                                          128, 0));
-          const uint32_t a0 = smem_u32(smem + C::kOffA + stage * C::kABytes);
-          const uint32_t b0 = smem_u32(smem + C::kOffB + stage * C::kBBytes);
-#pragma unroll
-          for (uint32_t kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = smem_desc(a0 + 32 * kk, 0, 1024, 2);
-            const uint64_t bdesc = smem_desc(b0 + 32 * kk, 0, 1024, 2);
-            tc_mma_mx(d_tmem, adesc, bdesc, idesc_mx(5, 0, nmma, kk, kk), sfa,
-                      tmem + C::kColSFB, (ks > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(empty + stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          d_tmem = tmem + static_cast<uint32_t>((acc * NI + i) * BN);
         }
-        if (!ok) break;
-        tc_commit(tfull + acc);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (!mbar_wait(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
+        tc_cp_32x128b_x4(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
+        const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
+#pragma unroll
+        for (uint32_t kk = 0; kk < 4; ++kk)
+          tc_mma_mx(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
+                    tmem + C::kColSFB, (!new_item || kk > 0) ? 1u : 0u);
+        tc_commit(empty + stage);
+        stage += ni;
+        if (stage >= STAGES) {
+          stage -= STAGES;
+          phase ^= 1u;
+        }
+        ks += ni;
+        new_item = false;
+        while (ks >= KS) {
+          ks -= KS;
+          ++it;
+          new_item = true;
+        }
+        if (new_item) tc_commit(tfull + acc);   // this issuer's share of the item is queued
       }
       // No MMA or TMEM copy may still be running when TMEM is freed.
-      tc_commit(drain);
+      tc_commit(drain + i);
       int32_t none = 0;
-      mbar_wait(drain, 0, timeout_ns, status, kDevTimeout, &none);
+      mbar_wait(drain + i, 0, timeout_ns, status, kDevTimeout, &none);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;   // 4 consecutive warps cover the four TMEM lane quarters
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t item = blockIdx.x; item < num_items; item += gridDim.x) {
-      const int tile = static_cast<int>(item / MT), mt = static_cast<int>(item % MT);
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+      const int tile = item / MT, mt = item % MT;
       const int4 td = tiles[tile];
       const int row0 = td.y, ntok = td.z, nmma = (td.z + 15) & ~15;
       if (!mbar_wait(tfull + acc, acc_phase, timeout_ns, status, kDevTimeout, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase =
-          tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * BN);
+          tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * NI * BN);
       for (int c0 = 0; c0 < nmma; c0 += 16) {
         float v[16];
         tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
+        for (int p = 1; p < ni; ++p) {   // partial sums of the other issuers
+          float w[16];
+          tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(p * BN + c0), w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += w[j];
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int n = c0 + j;
@@ -284,10 +363,10 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int BN, int STAGES, bool SWIGLU>
+template <int BN, int STAGES, int NI, bool SWIGLU>
 cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
-  using C = GemmCfg<BN, STAGES>;
-  auto kern = grouped_gemm_kernel<BN, STAGES, SWIGLU>;
+  using C = GemmCfg<BN, STAGES, NI>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, NI, SWIGLU>;
   static bool attr_set = false;  // per instantiation; set before first launch
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -295,24 +374,28 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<a.num_sms, 192, C::kSmemBytes, s>>>(
-      *a.tmap_w, *a.tmap_x, a.w_sf, a.tiles, a.num_tiles, a.row_scale,
+  XMaps xm;
+  for (int i = 0; i < kNumXMaps; ++i) xm.m[i] = a.tmap_x[i];
+  kern<<<a.num_sms, C::kThreads, C::kSmemBytes, s>>>(
+      *a.tmap_w, xm, *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
       static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status, a.timeout_ns,
-      a.a_tx_bytes);
+      a.a_tx_bytes, a.prefetch_stages);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// variant 1: decode tiles (<= 32 tokens, 10-stage weight pipeline);
-// variant 2: prefill tiles (<= 224 tokens, 5 stages).
+// variant 1: decode tiles (<= 32 tokens, 10-stage weight pipeline, 5 MMA
+// issuers -- tcgen05 issue from one thread costs ~540 cycles per 128-K stage
+// of 4 MMAs, so one issuer cannot keep pace with the weight stream);
+// variant 2: prefill tiles (<= 224 tokens, 5 stages, 1 issuer).
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s) {
   if (variant == 1) {
-    return swiglu ? launch_variant<kDecodeBN, 10, true>(a, s)
-                  : launch_variant<kDecodeBN, 10, false>(a, s);
+    return swiglu ? launch_variant<kDecodeBN, 10, 5, true>(a, s)
+                  : launch_variant<kDecodeBN, 10, 5, false>(a, s);
   }
-  return swiglu ? launch_variant<kPrefillBN, 5, true>(a, s)
-                : launch_variant<kPrefillBN, 5, false>(a, s);
+  return swiglu ? launch_variant<kPrefillBN, 5, 1, true>(a, s)
+                : launch_variant<kPrefillBN, 5, 1, false>(a, s);
 }
 
 }  // namespace moe

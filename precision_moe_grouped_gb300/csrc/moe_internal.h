@@ -22,10 +22,15 @@ constexpr int kTileK = 128;          // K elements per pipeline stage
 constexpr int kDecodeBN = 32;        // max tokens per tile, decode variant
 constexpr int kPrefillBN = 224;      // max tokens per tile, prefill variant
 
+// Activation box heights (rows) of the GEMM's activation tensor maps:
+// 32, 64, ..., 224.
+constexpr int kNumXMaps = 7;
+__host__ __device__ constexpr int kXBoxRowsAt(int i) { return 32 * (i + 1); }
+
 struct GemmArgs {
-  const CUtensorMap* tmap_w;   // host copy, passed by value to the kernel
-  const CUtensorMap* tmap_x;
-  const uint8_t* w_sf;         // prepared scale bytes
+  const CUtensorMap* tmap_w;   // host copies, passed by value to the kernel
+  const CUtensorMap* tmap_x;   // kNumXMaps maps, box heights kXBoxRows
+  const CUtensorMap* tmap_sf;  // prepared scale blocks as uint32 [blocks, 128]
   const int4* tiles;           // (expert, first row, rows, 0)
   const int32_t* num_tiles;    // device scalar
   const float* row_scale;      // per-row activation scale
@@ -37,6 +42,7 @@ struct GemmArgs {
   uint64_t timeout_ns;
   uint32_t a_tx_bytes;         // transaction bytes one weight TMA box counts
   int32_t num_sms;
+  int32_t prefetch_stages;     // L2 prefetch distance of weight tiles, in K stages
 };
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
@@ -53,10 +59,11 @@ cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_sca
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
                            int H, void* out, cudaStream_t s);
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);
-cudaError_t launch_prepare_w1(const uint8_t* w1, const uint8_t* w1_sf, uint8_t* w1_p,
-                              uint8_t* w1_sf_p, int E, int I, int H, cudaStream_t s);
-cudaError_t launch_prepare_sf_plain(const uint8_t* sf, uint8_t* sf_p, int E, int M, int K,
-                                    cudaStream_t s);
+// Re-lays one weight tensor [E, M, K] (E2M1, K/2 bytes per row) and its
+// scales [E, M, K/32] for the GEMM; swiglu_I > 0 applies GEMM1's gate/up row
+// interleave (M = 2 * swiglu_I).
+cudaError_t launch_prepare(const uint8_t* w, const uint8_t* sf, uint8_t* w_p, uint8_t* sf_p,
+                           int E, int M, int K, int swiglu_I, cudaStream_t s);
 // Sets the message moe_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 

@@ -172,8 +172,15 @@ def test_prepare_weights_layout():
         q, i = divmod(r, 32)
         f = 64 * mt + 16 * q + (i & 15)
         src[p] = f if i < 16 else I + f
-    np.testing.assert_array_equal(moe.w1_p.cpu().numpy(), w1[:, src])
-    np.testing.assert_array_equal(moe.w2_p.cpu().numpy(), case.w2.numpy())
+
+    def blocked(w, rows_src, M, K):
+        """[E, M, K/2] -> boxes [E, M/128, K/128, 128 rows, 64 bytes]."""
+        wp = w[:, rows_src].reshape(E, M // 128, 128, K // 128, 64)
+        return wp.transpose(0, 1, 3, 2, 4).reshape(E, -1)
+    np.testing.assert_array_equal(moe.w1_p.cpu().numpy().reshape(E, -1),
+                                  blocked(w1, src, 2 * I, H))
+    np.testing.assert_array_equal(moe.w2_p.cpu().numpy().reshape(E, -1),
+                                  blocked(case.w2.numpy(), np.arange(H), H, I))
 
     def relayout(sf, rows_src, M, K):
         out = np.empty((E, M // 128, K // 128, 32, 4, 4), np.uint8)
