@@ -85,7 +85,8 @@ typedef struct {
 /* Optional per-call settings (moe_forward_ex); zero-initialise for defaults. */
 typedef struct {
   int32_t tile_variant;  /* 0 auto; 1 decode tiles (<= 32 tokens per GEMM tile,
-                            deep weight pipeline); 2 prefill tiles (<= 224)   */
+                            deep weight pipeline); 2 prefill tiles (<= 224);
+                            3 decode tiles of <= 16 tokens                 */
   int32_t timeout_ms;    /* device bounded-wait limit, 0 = 1000 ms           */
   void* stage_events;    /* NULL, or an array of MOE_NUM_STAGES + 1 cudaEvent_t
                             (caller-created): event 0 is recorded on `stream`

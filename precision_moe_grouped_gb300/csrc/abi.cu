@@ -95,7 +95,7 @@ void compute_layout(const moe_shape* s, moe_ws_layout* L) {
                 I = s->inter;
   const int64_t R = T * k;
   const int64_t chunks = (T + moe::kRouteChunk - 1) / moe::kRouteChunk;
-  const int64_t max_tiles = R / moe::kDecodeBN + (E < R ? E : R) + 1;
+  const int64_t max_tiles = R / moe::kTinyBN + (E < R ? E : R) + 1;
   size_t off = 0;
   auto take = [&](int64_t bytes) {
     off = align_up(off, kAlign);
@@ -203,7 +203,7 @@ int32_t make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
 }
 
 int pick_variant(const moe_shape* s, const moe_options* o) {
-  if (o && (o->tile_variant == 1 || o->tile_variant == 2)) return o->tile_variant;
+  if (o && o->tile_variant >= 1 && o->tile_variant <= 3) return o->tile_variant;
   const double rows_per_expert =
       static_cast<double>(s->num_tokens) * s->top_k / static_cast<double>(s->num_experts);
   return rows_per_expert <= 16.0 ? 1 : 2;
@@ -211,8 +211,8 @@ int pick_variant(const moe_shape* s, const moe_options* o) {
 
 int32_t check_options(const moe_options* o) {
   if (!o) return MOE_OK;
-  if (o->tile_variant < 0 || o->tile_variant > 2)
-    return fail(MOE_ERR_INVALID_ARG, "tile_variant must be 0, 1 or 2");
+  if (o->tile_variant < 0 || o->tile_variant > 3)
+    return fail(MOE_ERR_INVALID_ARG, "tile_variant must be 0, 1, 2 or 3");
   if (o->timeout_ms < 0) return fail(MOE_ERR_INVALID_ARG, "timeout_ms < 0");
   if (o->prefetch_stages > 1024) return fail(MOE_ERR_INVALID_ARG, "prefetch_stages > 1024");
   for (int i = 0; i < 3; ++i)
@@ -261,7 +261,7 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   const int T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden, I = s->inter;
   const int R = T * k;
   const int variant = pick_variant(s, opts);
-  const int bn = variant == 1 ? moe::kDecodeBN : moe::kPrefillBN;
+  const int bn = variant == 1 ? moe::kDecodeBN : variant == 3 ? moe::kTinyBN : moe::kPrefillBN;
   const int prefetch = !opts || opts->prefetch_stages == 0 ? kDefaultPrefetchStages
                        : opts->prefetch_stages < 0 ? 0 : opts->prefetch_stages;
   const uint64_t timeout_ns =

@@ -51,20 +51,20 @@ namespace moe {
 
 namespace {
 
-// Activation tensor maps with box heights 32, 64, ..., 224 rows: a tile
+// Activation tensor maps with box heights 16, 32, 64, ..., 224 rows: a tile
 // loads the smallest box covering its MMA-N rows in one copy.
 struct XMaps {
   CUtensorMap m[kNumXMaps];
 };
 
 __device__ __forceinline__ int x_map_for(int rows) {
-  return (rows + 31) / 32 - 1;
+  return rows <= 16 ? 0 : (rows + 31) / 32;
 }
 
 template <int BN, int STAGES, int NI>
 struct GemmCfg {
-  static_assert(BN % 32 == 0 && BN <= kXBoxRowsAt(kNumXMaps - 1),
-                "token tile must be a multiple of 32 rows and fit the largest box");
+  static_assert(BN % 16 == 0 && BN <= kXBoxRowsAt(kNumXMaps - 1),
+                "token tile must be a multiple of 16 rows and fit the largest box");
   static_assert(3 * STAGES <= 32, "three producer lanes per stage must fit one warp");
   static_assert(STAGES % NI == 0, "each stage must belong to one MMA issuer");
   static constexpr int kABytes = kTileM * 128;       // FP4 expanded to 1 byte/element in smem
@@ -388,8 +388,14 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
 // variant 1: decode tiles (<= 32 tokens, 10-stage weight pipeline, 5 MMA
 // issuers -- tcgen05 issue from one thread costs ~540 cycles per 128-K stage
 // of 4 MMAs, so one issuer cannot keep pace with the weight stream);
-// variant 2: prefill tiles (<= 224 tokens, 5 stages, 1 issuer).
+// variant 2: prefill tiles (<= 224 tokens, 5 stages, 1 issuer);
+// variant 3: 16-token decode tiles (10 stages, one MMA issuer per stage,
+// 2 KB activation boxes).
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s) {
+  if (variant == 3) {
+    return swiglu ? launch_variant<kTinyBN, 10, 10, true>(a, s)
+                  : launch_variant<kTinyBN, 10, 10, false>(a, s);
+  }
   if (variant == 1) {
     return swiglu ? launch_variant<kDecodeBN, 10, 5, true>(a, s)
                   : launch_variant<kDecodeBN, 10, 5, false>(a, s);

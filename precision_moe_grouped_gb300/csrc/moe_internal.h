@@ -20,12 +20,13 @@ constexpr int kRouteChunk = 32;
 constexpr int kTileM = 128;
 constexpr int kTileK = 128;          // K elements per pipeline stage
 constexpr int kDecodeBN = 32;        // max tokens per tile, decode variant
+constexpr int kTinyBN = 16;          // max tokens per tile, 16-token decode variant
 constexpr int kPrefillBN = 224;      // max tokens per tile, prefill variant
 
 // Activation box heights (rows) of the GEMM's activation tensor maps:
-// 32, 64, ..., 224.
-constexpr int kNumXMaps = 7;
-__host__ __device__ constexpr int kXBoxRowsAt(int i) { return 32 * (i + 1); }
+// 16, 32, 64, 96, ..., 224.
+constexpr int kNumXMaps = 8;
+__host__ __device__ constexpr int kXBoxRowsAt(int i) { return i == 0 ? 16 : 32 * i; }
 
 struct GemmArgs {
   const CUtensorMap* tmap_w;   // host copies, passed by value to the kernel
