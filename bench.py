@@ -250,15 +250,9 @@ def run_ours(args, dist: Dist):
     counts = ws[lay.counts:lay.counts + 4 * cfg.num_experts].view(torch.int32).cpu().numpy()
     n_touched = int((counts > 0).sum())
 
-    # per-step stage events (created up front by one record each)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
-    for row in evs:
-        for e in row:
-            e.record(stream)
-    arrays = [P._lib.stage_event_array(row) for row in evs]
-    opts = [P.options(tile_variant=args.variant, stage_events=a) for a in arrays]
-    torch.cuda.synchronize()
-
+    # Timed region: K forwards, nothing else on the stream (events recorded
+    # between the library's kernels would break its programmatic-launch
+    # overlap, so per-kernel times come from a second pass below).
     clocks = Clocks(dist.local)
     clocks.start()
     dist.barrier()
@@ -267,7 +261,7 @@ def run_ours(args, dist: Dist):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(K):
-        fwd(opts[i])
+        fwd(base)
     t1.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
@@ -276,9 +270,22 @@ def run_ours(args, dist: Dist):
     ms = dist.max(ms_local)
     if P.read_device_status(ws) != 0:
         raise RuntimeError("device status error in timed region")
+    gpu_launches = P._lib.kernels_per_forward(T) * K
+
+    # Kernel timing pass: the same K forwards with CUDA events the library
+    # records on its stream before its first kernel and after each kernel.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record(stream)          # creates the event handles up front
+    arrays = [P._lib.stage_event_array(row) for row in evs]
+    opts = [P.options(tile_variant=args.variant, stage_events=a) for a in arrays]
+    torch.cuda.synchronize()
+    for i in range(K):
+        fwd(opts[i])
+    torch.cuda.synchronize()
     stage_ms = {names[j]: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                 for j in range(nst)}
-    gpu_launches = nst * K
 
     # end to end: host activations in, output out, inside the timed region
     xh = x.cpu().pin_memory()
@@ -337,6 +344,9 @@ def run_ours(args, dist: Dist):
         "fused_roofline": fr,
         "roofline": roof,
         "stage_ms": stage_ms,
+        "stage_ms_note": "per-kernel CUDA-event times from a second pass of the same K steps "
+                         "(events between kernels add launch gaps; the headline value is "
+                         "timed without them)",
         "e2e": {"value": dist.world * T / (ms_e2e / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": T * cfg.hidden * 2 + T * cfg.num_experts * 4,
                 "d2h_bytes_per_step": T * cfg.hidden * 2, "ms_per_step": ms_e2e},

@@ -79,8 +79,14 @@ typedef struct {
 } moe_shape;
 
 /* Kernels one forward launches, in stream order: route, scan, rank,
- * quant_scatter, gemm1, hquant, gemm2, combine (moe_stage_name() names them). */
+ * quant_scatter, gemm1, hquant, gemm2, combine (moe_stage_name() names them).
+ * For num_tokens <= MOE_SMALL_BATCH_TOKENS the expansion (scan, rank,
+ * quant_scatter) runs as one kernel, timed as stage "scan"; the "rank" and
+ * "quant_scatter" stages are then empty and the forward launches 6 kernels.
+ * Kernels are launched with programmatic dependent launch: each may start
+ * while its predecessor finishes and waits for the predecessor's results. */
 #define MOE_NUM_STAGES 8
+#define MOE_SMALL_BATCH_TOKENS 1024
 
 /* Optional per-call settings (moe_forward_ex); zero-initialise for defaults. */
 typedef struct {

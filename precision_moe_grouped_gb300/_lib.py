@@ -33,6 +33,14 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_prepare_weights", 
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 MOE_NUM_STAGES = 8
+MOE_SMALL_BATCH_TOKENS = 1024
+
+
+def kernels_per_forward(num_tokens: int) -> int:
+    """Kernels one forward launches (0 for an empty batch)."""
+    if num_tokens == 0:
+        return 0
+    return 6 if num_tokens <= MOE_SMALL_BATCH_TOKENS else 8
 
 
 class MoeShape(ctypes.Structure):

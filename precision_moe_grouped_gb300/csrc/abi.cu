@@ -302,17 +302,26 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   auto mark = [&]() -> cudaError_t {
     return ev ? cudaEventRecord(ev[stage++], st) : cudaSuccess;
   };
-  MOE_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  // route clears the status word; small batches expand in one kernel
   MOE_CUDA(mark());
-  MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, st));
+  MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
   MOE_CUDA(mark());
-  MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts),
-                            at<int32_t>(ws, L.offsets), chunk, tiles, num_tiles, st));
-  MOE_CUDA(mark());
-  MOE_CUDA(moe::launch_rank(ids, chunk, T, E, k, row_of, at<int32_t>(ws, L.token_slot), st));
-  MOE_CUDA(mark());
-  MOE_CUDA(moe::launch_quant_scatter(x, row_of, T, k, H, xq, x_scale, st));
-  MOE_CUDA(mark());
+  if (T <= moe::kSmallT) {
+    MOE_CUDA(moe::launch_expand_small(x, ids, T, E, k, H, bn, at<int32_t>(ws, L.counts),
+                                      at<int32_t>(ws, L.offsets), tiles, num_tiles, row_of,
+                                      at<int32_t>(ws, L.token_slot), xq, x_scale, st));
+    MOE_CUDA(mark());
+    MOE_CUDA(mark());
+    MOE_CUDA(mark());
+  } else {
+    MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts),
+                              at<int32_t>(ws, L.offsets), chunk, tiles, num_tiles, st));
+    MOE_CUDA(mark());
+    MOE_CUDA(moe::launch_rank(ids, chunk, T, E, k, row_of, at<int32_t>(ws, L.token_slot), st));
+    MOE_CUDA(mark());
+    MOE_CUDA(moe::launch_quant_scatter(x, row_of, T, k, H, xq, x_scale, st));
+    MOE_CUDA(mark());
+  }
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
                    x_scale, h, 2 * I, H, I, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms,
                    prefetch};

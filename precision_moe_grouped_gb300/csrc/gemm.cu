@@ -119,7 +119,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MT = m_per_expert / kTileM, KS = K / kTileK;
-  const int num_items = *num_tiles_p * MT;   // < 2^31: tiles <= R/32 + E + 1
   // Issuers with work: the largest divisor of STAGES that is <= min(NI, KS).
   // Dividing STAGES makes every stage always consumed by the same issuer
   // (fill f -> stage f % STAGES -> issuer f % ni), so each full barrier is
@@ -168,6 +167,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Everything above overlaps the previous kernel's tail; the tile list and
+  // the activations are that kernel's (or an earlier one's) output.
+  griddep_wait();
+  griddep_launch_dependents();
+  const int num_items = *num_tiles_p * MT;   // < 2^31: tiles <= R/16 + E + 1
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -376,11 +380,10 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
   }
   XMaps xm;
   for (int i = 0; i < kNumXMaps; ++i) xm.m[i] = a.tmap_x[i];
-  kern<<<a.num_sms, C::kThreads, C::kSmemBytes, s>>>(
-      *a.tmap_w, xm, *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
-      static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status, a.timeout_ns,
-      a.a_tx_bytes, a.prefetch_stages);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.num_sms), dim3(C::kThreads), C::kSmemBytes, s, *a.tmap_w, xm,
+                    *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
+                    static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status,
+                    a.timeout_ns, a.a_tx_bytes, a.prefetch_stages);
 }
 
 }  // namespace

@@ -7,10 +7,37 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
+#include "../../include/moe.h"
+
 namespace moe {
 
 // Device status codes written to the workspace status word (match moe_status).
 constexpr int32_t kDevTimeout = -6;
+
+// Launches `kern` with programmatic stream serialisation (PDL): the kernel may
+// begin while its stream predecessor finishes; every kernel of this library
+// calls griddep_wait() before it reads a predecessor's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Largest token count that uses the one-kernel small-batch expansion
+// (expand_small_kernel) instead of scan + rank + quant_scatter.
+constexpr int kSmallT = MOE_SMALL_BATCH_TOKENS;
 
 // Tokens per routing chunk: the unit of the per-chunk expert histogram that
 // makes the expert-major scatter deterministic (stable in token order).
@@ -47,7 +74,11 @@ struct GemmArgs {
 };
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
-                         int32_t* chunk_counts, cudaStream_t s);
+                         int32_t* chunk_counts, int32_t* status, cudaStream_t s);
+cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
+                                int bn, int32_t* counts, int32_t* offsets, int4* tiles,
+                                int32_t* num_tiles, int32_t* row_of, int32_t* token_slot,
+                                uint8_t* xq, float* x_scale, cudaStream_t s);
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
                         int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
                         int32_t* num_tiles, cudaStream_t s);

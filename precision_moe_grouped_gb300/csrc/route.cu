@@ -22,6 +22,7 @@
 #include <climits>
 
 #include "moe_internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -36,8 +37,13 @@ template <int NV>
 __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T,
                                                     int E, int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ wts,
-                                                    int32_t* __restrict__ chunk_counts) {
+                                                    int32_t* __restrict__ chunk_counts,
+                                                    int32_t* __restrict__ status) {
   extern __shared__ int32_t hist[];
+  griddep_wait();
+  griddep_launch_dependents();
+  // the forward's first kernel clears the device status word
+  if (status && blockIdx.x == 0 && threadIdx.x == 0) status[0] = 0;
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
@@ -126,6 +132,28 @@ __device__ int block_exclusive_scan(int v, int* total) {
   return base + x - v;
 }
 
+// Tile list of one expert (thread e of a block with blockDim >= E; every
+// thread of the block must call it): a tile is a run of at most `bn`
+// consecutive rows of one expert; an expert with c rows gets ceil(c / tsz)
+// tiles of tsz = roundup16(ceil(c / ceil(c / bn))) rows, so its tiles are
+// balanced and every MMA-N is a multiple of 16.
+__device__ void write_tiles(int e, int E, int c, int off, int bn, int4* __restrict__ tiles,
+                            int32_t* __restrict__ num_tiles) {
+  int nt = 0, tsz = 0;
+  if (e < E && c > 0) {
+    const int n0 = (c + bn - 1) / bn;
+    tsz = (((c + n0 - 1) / n0) + 15) & ~15;
+    nt = (c + tsz - 1) / tsz;
+  }
+  int total_tiles;
+  const int toff = block_exclusive_scan(nt, &total_tiles);
+  for (int i = 0; i < nt; ++i) {
+    const int r0 = i * tsz;
+    tiles[toff + i] = make_int4(e, off + r0, min(tsz, c - r0), 0);
+  }
+  if (threadIdx.x == 0) *num_tiles = total_tiles;
+}
+
 // One CTA (blockDim >= E): per-expert counts, offsets, per-chunk bases
 // (stable ranks start there), and the GEMM tile list.  A tile is a run of
 // at most `bn` consecutive rows of one expert; an expert with c rows gets
@@ -138,6 +166,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ chunk_base,
                                                     int4* __restrict__ tiles,
                                                     int32_t* __restrict__ num_tiles) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int e = threadIdx.x;
   int c = 0;
   if (e < E)
@@ -156,19 +186,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     }
   }
   if (e == 0) offsets[E] = total_rows;
-  int nt = 0, tsz = 0;
-  if (e < E && c > 0) {
-    const int n0 = (c + bn - 1) / bn;
-    tsz = (((c + n0 - 1) / n0) + 15) & ~15;
-    nt = (c + tsz - 1) / tsz;
-  }
-  int total_tiles;
-  const int toff = block_exclusive_scan(nt, &total_tiles);
-  for (int i = 0; i < nt; ++i) {
-    const int r0 = i * tsz;
-    tiles[toff + i] = make_int4(e, off + r0, min(tsz, c - r0), 0);
-  }
-  if (e == 0) *num_tiles = total_tiles;
+  write_tiles(e, E, e < E ? c : 0, off, bn, tiles, num_tiles);
 }
 
 // One warp per chunk of kRouteChunk tokens: the warp walks the chunk's
@@ -181,6 +199,8 @@ __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ i
                                                    int32_t* __restrict__ row_of,
                                                    int32_t* __restrict__ token_slot) {
   extern __shared__ int32_t sm[];
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * (blockDim.x >> 5) + warp;
   if (chunk >= num_chunks) return;
@@ -203,16 +223,14 @@ __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ i
   }
 }
 
-// One CTA per token: amax -> s = amax/448, inv = 448/amax (IEEE divisions)
-// -> E4M3 codes of x*inv (round to nearest even, satfinite), written to all
-// k expanded rows of the token; an all-zero row gets s = 1 and zero codes.
-__global__ void __launch_bounds__(128) quant_scatter_kernel(
-    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of, int k, int H,
-    uint8_t* __restrict__ xq, float* __restrict__ x_scale) {
-  __shared__ int32_t rows[32];
-  __shared__ float warp_max[4];
-  const int t = blockIdx.x;
-  if (threadIdx.x < k) rows[threadIdx.x] = row_of[static_cast<size_t>(t) * k + threadIdx.x];
+// Quantises token t's row of x (H bf16) with the block's threads and writes
+// the codes to the k expanded rows rows[0..k): amax -> s = amax/448, inv =
+// 448/amax (IEEE divisions) -> E4M3 codes of x*inv (round to nearest even,
+// satfinite); an all-zero row gets s = 1 and zero codes.  `warp_max` holds
+// one float per warp of the block.
+__device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
+                               const int32_t* rows, float* warp_max, uint8_t* __restrict__ xq,
+                               float* __restrict__ x_scale) {
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
   const int nvec = H / 16;  // 16 elements (two 16-byte loads) per thread step
   float amax = 0.f;
@@ -229,7 +247,8 @@ __global__ void __launch_bounds__(128) quant_scatter_kernel(
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
   __syncthreads();
-  amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
+  amax = 0.f;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) amax = fmaxf(amax, warp_max[w]);
   const bool nz = amax > 0.f;
   const float s = nz ? amax / 448.0f : 1.0f;
   const float inv = nz ? 448.0f / amax : 0.0f;
@@ -254,32 +273,104 @@ __global__ void __launch_bounds__(128) quant_scatter_kernel(
     for (int j = 0; j < k; ++j)
       reinterpret_cast<uint4*>(xq + static_cast<size_t>(rows[j]) * H)[i] = out;
   }
-  if (threadIdx.x < k) x_scale[rows[threadIdx.x]] = s;
+  if (static_cast<int>(threadIdx.x) < k) x_scale[rows[threadIdx.x]] = s;
+}
+
+// One CTA per token: FP8 quantisation of the token into its k rows.
+__global__ void __launch_bounds__(128) quant_scatter_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of, int k, int H,
+    uint8_t* __restrict__ xq, float* __restrict__ x_scale) {
+  __shared__ int32_t rows[32];
+  __shared__ float warp_max[32];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int t = blockIdx.x;
+  if (static_cast<int>(threadIdx.x) < k) rows[threadIdx.x] = row_of[static_cast<size_t>(t) * k + threadIdx.x];
+  __syncthreads();
+  quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
+}
+
+// Small batches (T <= kSmallT): one kernel replaces scan + rank +
+// quant_scatter.  CTA t (1024 threads, one expert per thread) rebuilds the
+// per-expert counts and offsets from all T*k routed ids in shared memory,
+// ranks its own token's k slots (rank of (t, e) = number of earlier tokens
+// routed to e, i.e. stable ascending token order), writes their rows, and
+// quantises its token into them.  CTA 0 also writes counts, offsets and the
+// GEMM tile list.  The redundant O(T*k) counting per CTA is cheap at these
+// sizes and removes three launches from the decode path.
+__global__ void __launch_bounds__(1024) expand_small_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids, int T, int E, int k,
+    int H, int bn, int32_t* __restrict__ counts_out, int32_t* __restrict__ offsets_out,
+    int4* __restrict__ tiles, int32_t* __restrict__ num_tiles, int32_t* __restrict__ row_of,
+    int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq, float* __restrict__ x_scale) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;            // [E]
+  int32_t* my_e = sm + E;       // [k] experts of this token
+  int32_t* my_rank = my_e + 32; // [k]
+  int32_t* rows = my_rank + 32; // [k]
+  __shared__ float warp_max[32];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int t = blockIdx.x, e = threadIdx.x;
+  if (e < E) cnt[e] = 0;
+  if (e < k) {
+    my_e[e] = ids[static_cast<size_t>(t) * k + e];
+    my_rank[e] = 0;
+  }
+  __syncthreads();
+  const int n = T * k, mine = t * k;   // ids of earlier tokens are [0, mine)
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int ei = ids[i];
+    atomicAdd(&cnt[ei], 1);
+    if (i < mine)
+      for (int j = 0; j < k; ++j)
+        if (my_e[j] == ei) atomicAdd(&my_rank[j], 1);
+  }
+  __syncthreads();
+  int total_rows;
+  const int c = e < E ? cnt[e] : 0;
+  const int off = block_exclusive_scan(c, &total_rows);
+  __syncthreads();
+  if (e < E) cnt[e] = off;     // cnt now holds the offsets
+  __syncthreads();
+  if (e < k) {
+    const size_t ts = static_cast<size_t>(t) * k + e;
+    const int r = cnt[my_e[e]] + my_rank[e];
+    rows[e] = r;
+    row_of[ts] = r;
+    token_slot[r] = static_cast<int32_t>(ts);
+  }
+  if (t == 0) {
+    if (e < E) {
+      counts_out[e] = c;
+      offsets_out[e] = off;
+    }
+    if (e == 0) offsets_out[E] = total_rows;
+    write_tiles(e, E, c, off, bn, tiles, num_tiles);
+  }
+  __syncthreads();
+  quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
-                         int32_t* chunk_counts, cudaStream_t s) {
+                         int32_t* chunk_counts, int32_t* status, cudaStream_t s) {
   const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
   const size_t smem = static_cast<size_t>(E) * sizeof(int32_t);
   const int nv = (E + 31) / 32;
-  if (nv <= 1) route_kernel<1><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else if (nv <= 2) route_kernel<2><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else if (nv <= 4) route_kernel<4><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else if (nv <= 8) route_kernel<8><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else if (nv <= 16) route_kernel<16><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  else route_kernel<32><<<chunks, 1024, smem, s>>>(logits, T, E, k, ids, wts, chunk_counts);
-  return cudaGetLastError();
+  auto kern = nv <= 1 ? route_kernel<1> : nv <= 2 ? route_kernel<2> : nv <= 4 ? route_kernel<4>
+            : nv <= 8 ? route_kernel<8> : nv <= 16 ? route_kernel<16> : route_kernel<32>;
+  return launch_pdl(kern, dim3(chunks), dim3(1024), smem, s, logits, T, E, k, ids, wts,
+                    chunk_counts, status);
 }
 
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
                         int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
                         int32_t* num_tiles, cudaStream_t s) {
   const int threads = ((E + 31) / 32) * 32;
-  scan_kernel<<<1, threads, 0, s>>>(chunk_counts, num_chunks, E, bn, counts, offsets, chunk_base,
-                                    tiles, num_tiles);
-  return cudaGetLastError();
+  return launch_pdl(scan_kernel, dim3(1), dim3(threads), 0, s, chunk_counts, num_chunks, E, bn,
+                    counts, offsets, chunk_base, tiles, num_tiles);
 }
 
 cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,
@@ -287,16 +378,24 @@ cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, in
   const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
   const int warps = 8;
   const size_t smem = static_cast<size_t>(warps) * E * sizeof(int32_t);
-  rank_kernel<<<(chunks + warps - 1) / warps, 32 * warps, smem, s>>>(ids, chunk_base, T, E, k,
-                                                                     chunks, row_of, token_slot);
-  return cudaGetLastError();
+  return launch_pdl(rank_kernel, dim3((chunks + warps - 1) / warps), dim3(32 * warps), smem, s,
+                    ids, chunk_base, T, E, k, chunks, row_of, token_slot);
 }
 
 cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, int T, int k, int H,
                                  uint8_t* xq, float* x_scale, cudaStream_t s) {
-  quant_scatter_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(x), row_of, k, H, xq,
-                                         x_scale);
-  return cudaGetLastError();
+  return launch_pdl(quant_scatter_kernel, dim3(T), dim3(128), 0, s,
+                    static_cast<const __nv_bfloat16*>(x), row_of, k, H, xq, x_scale);
+}
+
+cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
+                                int bn, int32_t* counts, int32_t* offsets, int4* tiles,
+                                int32_t* num_tiles, int32_t* row_of, int32_t* token_slot,
+                                uint8_t* xq, float* x_scale, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(E + 96) * sizeof(int32_t);
+  return launch_pdl(expand_small_kernel, dim3(T), dim3(1024), smem, s,
+                    static_cast<const __nv_bfloat16*>(x), ids, T, E, k, H, bn, counts, offsets,
+                    tiles, num_tiles, row_of, token_slot, xq, x_scale);
 }
 
 }  // namespace moe

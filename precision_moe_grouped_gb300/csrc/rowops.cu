@@ -26,6 +26,8 @@ namespace {
 __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __restrict__ h, int R,
                                                      int I, uint8_t* __restrict__ hq,
                                                      float* __restrict__ h_scale) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= R) return;
@@ -69,8 +71,9 @@ __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __rest
   if (lane == 0) h_scale[warp] = nz ? amax / 448.0f : 1.0f;
 }
 
-// One CTA per token: out[t] = bf16( sum_j w[t,j] * y[row_of[t,j]] ), float32
-// accumulation in slot order, 8 bf16 (16 bytes) per thread step.
+// Grid (T, ceil(H / 1024)): CTA (t, b) computes out[t, 1024 b .. 1024 b + 1023]
+// = bf16( sum_j w[t,j] * y[row_of[t,j]] ), float32 accumulation in slot order,
+// 8 bf16 (16 bytes) per thread.
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ y,
                                                       const float* __restrict__ wts,
                                                       const int32_t* __restrict__ row_of,
@@ -78,34 +81,34 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
                                                       __nv_bfloat16* __restrict__ out) {
   __shared__ int32_t rows[32];
   __shared__ float w[32];
+  griddep_wait();
+  griddep_launch_dependents();
   const int t = blockIdx.x;
-  if (threadIdx.x < k) {
+  if (static_cast<int>(threadIdx.x) < k) {
     rows[threadIdx.x] = row_of[static_cast<size_t>(t) * k + threadIdx.x];
     w[threadIdx.x] = wts[static_cast<size_t>(t) * k + threadIdx.x];
   }
   __syncthreads();
-  const int nvec = H / 8;
-  uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H);
-  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const uint4 q =
-          __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(rows[j]) * H) + i);
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&q);
-      const float wj = w[j];
+  const int i = blockIdx.y * blockDim.x + threadIdx.x;   // 16-byte vector index
+  if (i >= H / 8) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < k; ++j) {
+    const uint4 q =
+        __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(rows[j]) * H) + i);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&q);
+    const float wj = w[j];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const float2 f = __bfloat1622float2(b[p]);
-        acc[2 * p] = fmaf(wj, f.x, acc[2 * p]);
-        acc[2 * p + 1] = fmaf(wj, f.y, acc[2 * p + 1]);
-      }
+    for (int p = 0; p < 4; ++p) {
+      const float2 f = __bfloat1622float2(b[p]);
+      acc[2 * p] = fmaf(wj, f.x, acc[2 * p]);
+      acc[2 * p + 1] = fmaf(wj, f.y, acc[2 * p + 1]);
     }
-    uint4 r;
-    __nv_bfloat162* rb = reinterpret_cast<__nv_bfloat162*>(&r);
-#pragma unroll
-    for (int p = 0; p < 4; ++p) rb[p] = __floats2bfloat162_rn(acc[2 * p], acc[2 * p + 1]);
-    o[i] = r;
   }
+  uint4 r;
+  __nv_bfloat162* rb = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) rb[p] = __floats2bfloat162_rn(acc[2 * p], acc[2 * p + 1]);
+  reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[i] = r;
 }
 
 // Waits on a barrier that nothing ever completes, with a bounded wait.
@@ -128,15 +131,16 @@ cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_sca
                           cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   const int blocks = (R + 7) / 8;
-  hquant_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(h), R, I, hq, h_scale);
-  return cudaGetLastError();
+  return launch_pdl(hquant_kernel, dim3(blocks), dim3(256), 0, s,
+                    static_cast<const __nv_bfloat16*>(h), R, I, hq, h_scale);
 }
 
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
                            int H, void* out, cudaStream_t s) {
-  combine_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(y), wts, row_of, k, H,
-                                   static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  const int nvec = H / 8;
+  return launch_pdl(combine_kernel, dim3(T, (nvec + 127) / 128), dim3(128), 0, s,
+                    static_cast<const __nv_bfloat16*>(y), wts, row_of, k, H,
+                    static_cast<__nv_bfloat16*>(out));
 }
 
 cudaError_t launch_timeout_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t s) {
