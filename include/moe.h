@@ -92,7 +92,9 @@ typedef struct {
 typedef struct {
   int32_t tile_variant;  /* 0 auto; 1 decode tiles (<= 32 tokens per GEMM tile,
                             deep weight pipeline); 2 prefill tiles (<= 224);
-                            3 decode tiles of <= 16 tokens                 */
+                            3 decode tiles of <= 16 tokens; 4 prefill tiles
+                            with two MMA issuers; 5 tiles of <= 160 tokens
+                            with a 6-stage pipeline                       */
   int32_t timeout_ms;    /* device bounded-wait limit, 0 = 1000 ms           */
   void* stage_events;    /* NULL, or an array of MOE_NUM_STAGES + 1 cudaEvent_t
                             (caller-created): event 0 is recorded on `stream`

@@ -61,7 +61,7 @@ __device__ __forceinline__ int x_map_for(int rows) {
   return rows <= 16 ? 0 : (rows + 31) / 32;
 }
 
-template <int BN, int STAGES, int NI>
+template <int BN, int STAGES, int NI, int NB>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN <= kXBoxRowsAt(kNumXMaps - 1),
                 "token tile must be a multiple of 16 rows and fit the largest box");
@@ -74,19 +74,19 @@ struct GemmCfg {
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffSF = kOffB + STAGES * kBBytes;
   static constexpr int kOffSFB = kOffSF + STAGES * kSFBytes;
-  static constexpr int kNumBars = 2 * STAGES + 5 + NI;
+  static constexpr int kNumBars = 2 * STAGES + 2 * NB + 1 + NI;
   static constexpr int kOffBar = kOffSFB + 512;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  // TMEM columns: for each of the two accumulator buffers, one fp32
+  // TMEM columns: for each of the NB accumulator buffers, one fp32
   // accumulator of BN columns per MMA issuer (buffer a, issuer i at column
   // (a * NI + i) * BN); 8 columns of constant activation scales (up to 256
   // tokens); 4 columns of weight scales per stage.
   static constexpr int kThreads = 32 * (NI + 5);    // producer, NI issuers, 4 epilogue warps
-  static constexpr int kColSFB = 2 * NI * BN;
-  static constexpr int kColSFA = 2 * NI * BN + 8;
-  static constexpr int kColsUsed = 2 * NI * BN + 8 + 4 * STAGES;
+  static constexpr int kColSFB = NB * NI * BN;
+  static constexpr int kColSFA = NB * NI * BN + 8;
+  static constexpr int kColsUsed = NB * NI * BN + 8 + 4 * STAGES;
   static constexpr int kTmemCols = kColsUsed <= 32    ? 32
                                    : kColsUsed <= 64  ? 64
                                    : kColsUsed <= 128 ? 128
@@ -95,8 +95,8 @@ struct GemmCfg {
   static_assert(kColsUsed <= 512, "TMEM budget exceeded");
 };
 
-template <int BN, int STAGES, int NI, bool SWIGLU>
-__global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
+template <int BN, int STAGES, int NI, int NB, bool SWIGLU>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ XMaps tmap_x,
                         const __grid_constant__ CUtensorMap tmap_sf,
@@ -105,15 +105,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
                         const float* __restrict__ row_scale, __nv_bfloat16* __restrict__ out,
                         int m_per_expert, int K, int out_ld, int32_t* __restrict__ status,
                         uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages) {
-  using C = GemmCfg<BN, STAGES, NI>;
+  using C = GemmCfg<BN, STAGES, NI, NB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + NB;
+  uint64_t* drain = tempty + NB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 4);
 
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
       mbar_init(full + s, 3);   // weight, activation and scale copies arrive separately
       mbar_init(empty + s, 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NB; ++a) {
       mbar_init(tfull + a, ni);   // every issuer commits its share of an item
       mbar_init(tempty + a, 4);   // every epilogue warp releases the buffer
     }
@@ -264,9 +264,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
           const int item = blockIdx.x + it * gridDim.x;
           const int4 td = tiles[item / MT];
           id0 = idesc_mx(5, 0, static_cast<uint32_t>((td.z + 15) & ~15), 0, 0);
-          acc = it & 1;
-          if (!mbar_wait(tempty + acc, ((it >> 1) & 1) ^ 1u, timeout_ns, status, kDevTimeout,
-                         abort_flag))
+          acc = it % NB;
+          if (!mbar_wait(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
+                         status, kDevTimeout, abort_flag))
             break;
           tc_fence_after();
           d_tmem = tmem + static_cast<uint32_t>((acc * NI + i) * BN);
@@ -354,8 +354,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty + acc);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == NB) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
 
@@ -367,10 +369,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI>::kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, int NI, bool SWIGLU>
+template <int BN, int STAGES, int NI, int NB, bool SWIGLU>
 cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
-  using C = GemmCfg<BN, STAGES, NI>;
-  auto kern = grouped_gemm_kernel<BN, STAGES, NI, SWIGLU>;
+  using C = GemmCfg<BN, STAGES, NI, NB>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, NI, NB, SWIGLU>;
   static bool attr_set = false;  // per instantiation; set before first launch
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -393,18 +395,28 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
 // of 4 MMAs, so one issuer cannot keep pace with the weight stream);
 // variant 2: prefill tiles (<= 224 tokens, 5 stages, 1 issuer);
 // variant 3: 16-token decode tiles (10 stages, one MMA issuer per stage,
-// 2 KB activation boxes).
+// 2 KB activation boxes); variant 4: prefill tiles with 2 MMA issuers and
+// one accumulator buffer (4 stages; the epilogue no longer overlaps the
+// next item's MMAs); variant 5: tiles of <= 160 tokens with 6 stages.
+// NB = accumulator buffers.
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s) {
-  if (variant == 3) {
-    return swiglu ? launch_variant<kTinyBN, 10, 10, true>(a, s)
-                  : launch_variant<kTinyBN, 10, 10, false>(a, s);
+  switch (variant) {
+    case 1:
+      return swiglu ? launch_variant<kDecodeBN, 10, 5, 2, true>(a, s)
+                    : launch_variant<kDecodeBN, 10, 5, 2, false>(a, s);
+    case 3:
+      return swiglu ? launch_variant<kTinyBN, 10, 10, 2, true>(a, s)
+                    : launch_variant<kTinyBN, 10, 10, 2, false>(a, s);
+    case 4:
+      return swiglu ? launch_variant<kPrefillBN, 4, 2, 1, true>(a, s)
+                    : launch_variant<kPrefillBN, 4, 2, 1, false>(a, s);
+    case 5:
+      return swiglu ? launch_variant<kMidBN, 6, 1, 2, true>(a, s)
+                    : launch_variant<kMidBN, 6, 1, 2, false>(a, s);
+    default:
+      return swiglu ? launch_variant<kPrefillBN, 5, 1, 2, true>(a, s)
+                    : launch_variant<kPrefillBN, 5, 1, 2, false>(a, s);
   }
-  if (variant == 1) {
-    return swiglu ? launch_variant<kDecodeBN, 10, 5, true>(a, s)
-                  : launch_variant<kDecodeBN, 10, 5, false>(a, s);
-  }
-  return swiglu ? launch_variant<kPrefillBN, 5, 1, true>(a, s)
-                : launch_variant<kPrefillBN, 5, 1, false>(a, s);
 }
 
 }  // namespace moe

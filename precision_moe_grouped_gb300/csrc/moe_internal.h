@@ -49,6 +49,7 @@ constexpr int kTileK = 128;          // K elements per pipeline stage
 constexpr int kDecodeBN = 32;        // max tokens per tile, decode variant
 constexpr int kTinyBN = 16;          // max tokens per tile, 16-token decode variant
 constexpr int kPrefillBN = 224;      // max tokens per tile, prefill variant
+constexpr int kMidBN = 160;          // max tokens per tile, 6-stage prefill variant
 
 // Activation box heights (rows) of the GEMM's activation tensor maps:
 // 16, 32, 64, 96, ..., 224.

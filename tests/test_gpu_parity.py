@@ -84,28 +84,29 @@ def test_tiny_config_full():
     check_tiles(run, 32)
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
 def test_several_tiles_ragged(variant):
     """Many token tiles per expert (decode variant), ragged tails, several
     weight M-tiles and K stages."""
     cfg = MI.custom_config(8, 2, 512, 256)
     run, _ = full_parity(MI.make_case(cfg, 200, seed=7), variant=variant, name=f"ragged{variant}")
-    check_tiles(run, {1: 32, 2: 224, 3: 16}[variant])
+    check_tiles(run, {1: 32, 2: 224, 3: 16, 4: 224, 5: 160}[variant])
 
 
-def test_expert_split_over_tiles_prefill():
-    """Experts with > 224 rows split into balanced tiles (prefill variant)."""
+@pytest.mark.parametrize("variant", [2, 4, 5])
+def test_expert_split_over_tiles_prefill(variant):
+    """Experts with > 224 rows split into balanced tiles (prefill variants)."""
     cfg = MI.custom_config(4, 2, 256, 128)
-    run, _ = full_parity(MI.make_case(cfg, 700, seed=9), variant=2, name="split")
+    run, _ = full_parity(MI.make_case(cfg, 700, seed=9), variant=variant, name=f"split{variant}")
     assert run.counts.max() > 224
-    check_tiles(run, 224)
+    check_tiles(run, 160 if variant == 5 else 224)
 
 
 def test_variants_agree_bitwise():
     cfg = MI.custom_config(8, 2, 256, 128)
     case = MI.make_case(cfg, 96, seed=13)
     a = GpuRun(case, variant=1)
-    for v in (2, 3):
+    for v in (2, 3, 4, 5):
         b = GpuRun(case, variant=v, moe=a.moe)
         np.testing.assert_array_equal(a.out_np(), b.out_np())
 
