@@ -90,11 +90,13 @@ typedef struct {
 
 /* Optional per-call settings (moe_forward_ex); zero-initialise for defaults. */
 typedef struct {
-  int32_t tile_variant;  /* 0 auto; 1 decode tiles (<= 32 tokens per GEMM tile,
-                            deep weight pipeline); 2 prefill tiles (<= 224);
-                            3 decode tiles of <= 16 tokens; 4 prefill tiles
-                            with two MMA issuers; 5 tiles of <= 160 tokens
-                            with a 6-stage pipeline                       */
+  int32_t tile_variant;  /* 0 auto (3 while experts average <= 8 rows, 1 up
+                            to 16, else 5); 1 decode tiles (<= 32 tokens per
+                            GEMM tile, 10-stage weight pipeline); 2 prefill
+                            tiles (<= 224); 3 decode tiles of <= 16 tokens
+                            (12 stages); 4 prefill tiles with two MMA
+                            issuers; 5 tiles of <= 160 tokens with a 6-stage
+                            pipeline                                      */
   int32_t timeout_ms;    /* device bounded-wait limit, 0 = 1000 ms           */
   void* stage_events;    /* NULL, or an array of MOE_NUM_STAGES + 1 cudaEvent_t
                             (caller-created): event 0 is recorded on `stream`
@@ -102,7 +104,7 @@ typedef struct {
                             kernel i, so event pairs time each kernel      */
   int32_t prefetch_stages; /* L2 prefetch distance of the GEMM weight stream in
                             K stages (8 KB of packed weights each per SM):
-                            0 = default (16), < 0 = off                   */
+                            0 = default (off: measured slower), < 0 = off */
   int32_t reserved[3];   /* must be zero                                     */
 } moe_options;
 

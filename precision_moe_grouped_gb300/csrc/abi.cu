@@ -203,19 +203,22 @@ int32_t make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
 }
 
 int pick_variant(const moe_shape* s, const moe_options* o) {
-  if (o && o->tile_variant >= 1 && o->tile_variant <= 5) return o->tile_variant;
+  if (o && o->tile_variant >= 1 && o->tile_variant <= moe::kMaxTileVariant) return o->tile_variant;
   const double rows_per_expert =
       static_cast<double>(s->num_tokens) * s->top_k / static_cast<double>(s->num_experts);
-  // Decode tiles while experts average <= 16 rows; above that the 6-stage
-  // 160-token prefill tiles (measured faster than 5-stage 224-token tiles at
-  // DSV3 T=512 and T=4096: more weight bytes in flight per SM).
-  return rows_per_expert <= 16.0 ? 1 : 5;
+  // 16-token tiles (12 stages) while experts average <= 8 rows (measured
+  // faster than 32-token tiles at DSV3 T = 1..256, slower at T = 512 where
+  // many experts need a second 16-token tile); 32-token tiles (10 stages) up
+  // to 16 rows; above that the 6-stage 160-token prefill tiles (measured faster
+  // than 5-stage 224-token tiles at DSV3 T=512 and T=4096: more weight bytes
+  // in flight per SM).
+  return rows_per_expert <= 8.0 ? 3 : rows_per_expert <= 16.0 ? 1 : 5;
 }
 
 int32_t check_options(const moe_options* o) {
   if (!o) return MOE_OK;
-  if (o->tile_variant < 0 || o->tile_variant > 5)
-    return fail(MOE_ERR_INVALID_ARG, "tile_variant must be in [0, 5]");
+  if (o->tile_variant < 0 || o->tile_variant > moe::kMaxTileVariant)
+    return fail(MOE_ERR_INVALID_ARG, "tile_variant must be in [0, %d]", moe::kMaxTileVariant);
   if (o->timeout_ms < 0) return fail(MOE_ERR_INVALID_ARG, "timeout_ms < 0");
   if (o->prefetch_stages > 1024) return fail(MOE_ERR_INVALID_ARG, "prefetch_stages > 1024");
   for (int i = 0; i < 3; ++i)
@@ -264,10 +267,7 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   const int T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden, I = s->inter;
   const int R = T * k;
   const int variant = pick_variant(s, opts);
-  const int bn = variant == 1   ? moe::kDecodeBN
-                 : variant == 3 ? moe::kTinyBN
-                 : variant == 5 ? moe::kMidBN
-                                : moe::kPrefillBN;
+  const int bn = moe::gemm_tile_tokens(variant);
   const int prefetch = !opts || opts->prefetch_stages == 0 ? kDefaultPrefetchStages
                        : opts->prefetch_stages < 0 ? 0 : opts->prefetch_stages;
   const uint64_t timeout_ns =

@@ -31,10 +31,11 @@
 // list, so nothing returns to the host.
 //
 // Roles: warp 0 lanes 0..3*STAGES-1 = TMA producers (three per stage);
-// warps 1..NI = MMA issuers (lane 0 each; warp 1 also owns the TMEM
-// allocation); the last 4 warps = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31).  Two TMEM accumulator buffers let the epilogue of one
-// item overlap the main loop of the next.
+// warps 1..NI = MMA issuers (one elected lane each; warp 1 also owns the TMEM
+// allocation); the last 8 warps = epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. +31; two warps per lane quarter split the columns).  Two TMEM
+// accumulator buffers let the epilogue of one item overlap the main loop of
+// the next.
 //
 // Epilogues:
 //   GEMM1 (SWIGLU): acc * s_x[row] -> h = silu(gate) * up -> bf16 h[row, f].
@@ -65,7 +66,10 @@ template <int BN, int STAGES, int NI, int NB>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN <= kXBoxRowsAt(kNumXMaps - 1),
                 "token tile must be a multiple of 16 rows and fit the largest box");
-  static_assert(3 * STAGES <= 32, "three producer lanes per stage must fit one warp");
+  // Producer lanes per stage: three (weight, activation, scale copies) when
+  // they fit one warp, else two (the scale copy rides with the activation).
+  static constexpr int kLanesPerStage = 3 * STAGES <= 32 ? 3 : 2;
+  static_assert(kLanesPerStage * STAGES <= 32, "producer lanes must fit one warp");
   static_assert(STAGES % NI == 0, "each stage must belong to one MMA issuer");
   static constexpr int kABytes = kTileM * 128;       // FP4 expanded to 1 byte/element in smem
   static constexpr int kBBytes = BN * 128;           // FP8 tokens x 128 K
@@ -83,7 +87,8 @@ struct GemmCfg {
   // accumulator of BN columns per MMA issuer (buffer a, issuer i at column
   // (a * NI + i) * BN); 8 columns of constant activation scales (up to 256
   // tokens); 4 columns of weight scales per stage.
-  static constexpr int kThreads = 32 * (NI + 5);    // producer, NI issuers, 4 epilogue warps
+  static constexpr int kEpiWarps = 8;               // two per TMEM lane quarter
+  static constexpr int kThreads = 32 * (NI + 1 + kEpiWarps);   // producer, issuers, epilogue
   static constexpr int kColSFB = NB * NI * BN;
   static constexpr int kColSFA = NB * NI * BN + 8;
   static constexpr int kColsUsed = NB * NI * BN + 8 + 4 * STAGES;
@@ -130,12 +135,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full + s, 3);   // weight, activation and scale copies arrive separately
+      mbar_init(full + s, C::kLanesPerStage);   // each producer lane arrives with its bytes
       mbar_init(empty + s, 1);
     }
     for (int a = 0; a < NB; ++a) {
       mbar_init(tfull + a, ni);   // every issuer commits its share of an item
-      mbar_init(tempty + a, 4);   // every epilogue warp releases the buffer
+      mbar_init(tempty + a, C::kEpiWarps);   // every epilogue warp releases the buffer
     }
     for (int j = 0; j < NI; ++j) mbar_init(drain + j, 1);
     mbar_init(drain + NI, 1);   // constant-scale copy done
@@ -175,14 +180,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Three issuing lanes per pipeline stage: lane 3s copies the weight box,
-    // lane 3s+1 the activation box and lane 3s+2 the scale block of stage s,
-    // each arriving on the stage's full barrier with its own byte count, for
-    // this CTA's fills f = s, s + STAGES, ... (fill f = K stage f % KS of the
-    // CTA's (f / KS)-th item).  Spreading the copies over threads keeps their
-    // issue off any single thread's critical path.
-    if (lane < 3 * STAGES) {
-      const int s = lane / 3, role = lane % 3;
+    // Issuing lanes per pipeline stage (LPS = 3): lane 3s copies the weight
+    // box, lane 3s+1 the activation box and lane 3s+2 the scale block of
+    // stage s; with LPS = 2 (more than ten stages) the activation lane also
+    // copies the scale block.  Each lane arrives on the stage's full barrier
+    // with its own byte count, for this CTA's fills f = s, s + STAGES, ...
+    // (fill f = K stage f % KS of the CTA's (f / KS)-th item).  Spreading the
+    // copies over threads keeps their issue off any single thread's critical
+    // path.
+    constexpr int LPS = C::kLanesPerStage;
+    if (lane < LPS * STAGES) {
+      const int s = lane / LPS, role = lane % LPS;
       uint32_t phase = 0;
       bool issued = false;
       // fill f = s + j * STAGES: K stage ks of the CTA's it-th item (KS >= STAGES
@@ -216,9 +224,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
           // smallest activation box that covers the tile's MMA-N rows
           const int nmma = (td.z + 15) & ~15;
           const int xm = x_map_for(nmma);
-          mbar_arrive_expect_tx(full + s, static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u);
+          const uint32_t bx = static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u;
+          mbar_arrive_expect_tx(full + s, LPS == 2 ? bx + 512u : bx);
           tma_load_2d(smem + C::kOffB + s * C::kBBytes, &tmap_x.m[xm], ks * kTileK, td.y,
                       full + s);
+          if (LPS == 2)
+            tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0,
+                        static_cast<int32_t>(blk), full + s);
         } else {
           mbar_arrive_expect_tx(full + s, 512u);
           tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0, static_cast<int32_t>(blk),
@@ -241,16 +253,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
     }
   } else if (warp <= NI) {
     // ------------------------------------------------------------ MMA issuers
-    // Each tcgen05 instruction occupies its issuing thread (measured ~540
-    // cycles per stage of one copy + 4 MMAs, independent of N), so with small
-    // token tiles one issuing thread cannot keep pace with the weight stream.
+    // Each tcgen05 instruction occupies its issuing warp (measured ~310
+    // cycles per stage of one copy + 4 MMAs from a warp-uniform loop, ~510
+    // from a loop that only lane 0 runs, independent of N up to 128), so with
+    // small token tiles one issuing warp cannot keep pace with the weight
+    // stream.
     // Issuer i (warp 1 + i) takes fills f = i, i + ni, i + 2 ni, ... -- i.e.
     // the stages s with s % ni == i -- and accumulates its K stages of an item
     // into its own TMEM accumulator; the epilogue sums the ni partials.
     // Every descriptor is precomputed: stage s and K sub-step kk only add
     // constant start-address offsets (address >> 4 lives in the low 14 bits).
+    // The whole warp runs the loop (uniform control flow); one elected lane
+    // issues each tcgen05 instruction.
     const int i = warp - 1;
-    if (lane == 0 && i < ni) {
+    if (i < ni) {
       const uint64_t adesc0 = smem_desc(smem_u32(smem + C::kOffA), 0, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
       const uint64_t sdesc0 = smem_desc(smem_u32(smem + C::kOffSF), 0, 128, 0);
@@ -265,23 +281,24 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
           const int4 td = tiles[item / MT];
           id0 = idesc_mx(5, 0, static_cast<uint32_t>((td.z + 15) & ~15), 0, 0);
           acc = it % NB;
-          if (!mbar_wait(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
-                         status, kDevTimeout, abort_flag))
+          if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
+                              status, kDevTimeout, abort_flag))
             break;
           tc_fence_after();
           d_tmem = tmem + static_cast<uint32_t>((acc * NI + i) * BN);
         }
-        if (!mbar_wait(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag)) break;
+        if (!mbar_wait_warp(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag))
+          break;
         tc_fence_after();
         const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
-        tc_cp_32x128b_x4(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
+        tc_cp_32x128b_x4_warp(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
         const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
         const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
 #pragma unroll
         for (uint32_t kk = 0; kk < 4; ++kk)
-          tc_mma_mx(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
-                    tmem + C::kColSFB, (!new_item || kk > 0) ? 1u : 0u);
-        tc_commit(empty + stage);
+          tc_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
+                         tmem + C::kColSFB, (!new_item || kk > 0) ? 1u : 0u);
+        tc_commit_warp(empty + stage);
         stage += ni;
         if (stage >= STAGES) {
           stage -= STAGES;
@@ -294,27 +311,37 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
           ++it;
           new_item = true;
         }
-        if (new_item) tc_commit(tfull + acc);   // this issuer's share of the item is queued
+        if (new_item) tc_commit_warp(tfull + acc);   // this issuer's share of the item is queued
       }
       // No MMA or TMEM copy may still be running when TMEM is freed.
-      tc_commit(drain + i);
+      tc_commit_warp(drain + i);
       int32_t none = 0;
-      mbar_wait(drain + i, 0, timeout_ns, status, kDevTimeout, &none);
+      mbar_wait_warp(drain + i, 0, timeout_ns, status, kDevTimeout, &none);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;   // 4 consecutive warps cover the four TMEM lane quarters
+    // Eight warps: warp w reads TMEM lanes 32 * (w % 4) .. +31 (the only
+    // quarter it may access), and the two warps of each quarter split the
+    // item's 16-column chunks between them.
+    const int q = warp & 3;
+    const int half = (warp - (NI + 1)) >> 2;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
       const int tile = item / MT, mt = item % MT;
       const int4 td = tiles[tile];
-      const int row0 = td.y, ntok = td.z, nmma = (td.z + 15) & ~15;
+      const int row0 = td.y, ntok = td.z, nchunks = (td.z + 15) >> 4;
+      const int split = (nchunks + 1) >> 1;
+      const int ch_begin = half == 0 ? 0 : split, ch_end = half == 0 ? split : nchunks;
       if (!mbar_wait(tfull + acc, acc_phase, timeout_ns, status, kDevTimeout, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * NI * BN);
-      for (int c0 = 0; c0 < nmma; c0 += 16) {
+      for (int ch = ch_begin; ch < ch_end; ++ch) {
+        const int c0 = ch * 16;
+        // one row-scale load per chunk: lane j (and j + 16) holds column c0 + j
+        const int nl = c0 + (lane & 15);
+        const float sc = nl < ntok ? __ldg(row_scale + row0 + nl) : 0.f;
         float v[16];
         tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
         for (int p = 1; p < ni; ++p) {   // partial sums of the other issuers
@@ -324,10 +351,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
           for (int j = 0; j < 16; ++j) v[j] += w[j];
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = c0 + j;
-          v[j] *= n < ntok ? __ldg(row_scale + row0 + n) : 0.f;
-        }
+        for (int j = 0; j < 16; ++j) v[j] *= __shfl_sync(0xffffffffu, sc, j);
         if constexpr (SWIGLU) {
           const bool lo = lane < 16;
           const int f = 64 * mt + 16 * q + (lane & 15);
@@ -390,32 +414,44 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-// variant 1: decode tiles (<= 32 tokens, 10-stage weight pipeline, 5 MMA
-// issuers -- tcgen05 issue from one thread costs ~540 cycles per 128-K stage
-// of 4 MMAs, so one issuer cannot keep pace with the weight stream);
-// variant 2: prefill tiles (<= 224 tokens, 5 stages, 1 issuer);
-// variant 3: 16-token decode tiles (10 stages, one MMA issuer per stage,
-// 2 KB activation boxes); variant 4: prefill tiles with 2 MMA issuers and
-// one accumulator buffer (4 stages; the epilogue no longer overlaps the
-// next item's MMAs); variant 5: tiles of <= 160 tokens with 6 stages.
-// NB = accumulator buffers.
+// Variants: <token tile BN, pipeline stages, MMA issuers NI, accumulator
+// buffers NB>.
+//   1: decode tiles of <= 32 tokens, 10 stages, 5 issuers;
+//   2: prefill tiles of <= 224 tokens, 5 stages;
+//   3: decode tiles of <= 16 tokens, 12 stages (the smallest stage, so the
+//      most weight bytes in flight), 6 issuers;
+//   4: tiles of <= 224 tokens with 2 issuers and one accumulator buffer (the
+//      epilogue no longer overlaps the next item's MMAs);
+//   5: tiles of <= 160 tokens, 6 stages.
+#define MOE_GEMM_VARIANTS(X)  \
+  X(1, kDecodeBN, 10, 5, 2)   \
+  X(2, kPrefillBN, 5, 1, 2)   \
+  X(3, kTinyBN, 12, 6, 2)     \
+  X(4, kPrefillBN, 4, 2, 1)   \
+  X(5, kMidBN, 6, 1, 2)
+
+int gemm_tile_tokens(int variant) {
+  switch (variant) {
+#define MOE_X(v, bn, st, ni, nb) \
+  case v:                        \
+    return bn;
+    MOE_GEMM_VARIANTS(MOE_X)
+#undef MOE_X
+    default:
+      return kMidBN;
+  }
+}
+
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s) {
   switch (variant) {
-    case 1:
-      return swiglu ? launch_variant<kDecodeBN, 10, 5, 2, true>(a, s)
-                    : launch_variant<kDecodeBN, 10, 5, 2, false>(a, s);
-    case 3:
-      return swiglu ? launch_variant<kTinyBN, 10, 10, 2, true>(a, s)
-                    : launch_variant<kTinyBN, 10, 10, 2, false>(a, s);
-    case 4:
-      return swiglu ? launch_variant<kPrefillBN, 4, 2, 1, true>(a, s)
-                    : launch_variant<kPrefillBN, 4, 2, 1, false>(a, s);
-    case 5:
-      return swiglu ? launch_variant<kMidBN, 6, 1, 2, true>(a, s)
-                    : launch_variant<kMidBN, 6, 1, 2, false>(a, s);
+#define MOE_X(v, bn, st, ni, nb)                                  \
+  case v:                                                         \
+    return swiglu ? launch_variant<bn, st, ni, nb, true>(a, s) \
+                  : launch_variant<bn, st, ni, nb, false>(a, s);
+    MOE_GEMM_VARIANTS(MOE_X)
+#undef MOE_X
     default:
-      return swiglu ? launch_variant<kPrefillBN, 5, 1, 2, true>(a, s)
-                    : launch_variant<kPrefillBN, 5, 1, 2, false>(a, s);
+      return cudaErrorInvalidValue;
   }
 }
 

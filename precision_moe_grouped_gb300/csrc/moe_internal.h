@@ -92,6 +92,10 @@ cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_sca
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
                            int H, void* out, cudaStream_t s);
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);
+// Tile variants 1..kMaxTileVariant; the largest token tile of each (the tile
+// list is built with this bound).
+constexpr int kMaxTileVariant = 5;
+int gemm_tile_tokens(int variant);
 // Re-lays one weight tensor [E, M, K] (E2M1, K/2 bytes per row) and its
 // scales [E, M, K/32] for the GEMM; swiglu_I > 0 applies GEMM1's gate/up row
 // interleave (M = 2 * swiglu_I).

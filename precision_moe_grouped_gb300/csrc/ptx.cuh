@@ -165,6 +165,28 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
       : "memory");
 }
 
+// Warp-wide forms: the whole warp executes the call with identical
+// arguments and one elected lane issues the instruction.  Keeping the issue
+// loop warp-uniform (instead of running it in lane 0 alone) measured ~30%
+// fewer cycles per issued stage on sm_103a.
+__device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// All lanes wait (bounded) and agree on the outcome, so a loop that breaks
+// on failure stays warp-uniform.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               uint64_t timeout_ns, int32_t* status, int32_t code,
+                                               volatile int32_t* abort) {
+  const bool ok = mbar_wait(bar, parity, timeout_ns, status, code, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), fixed version bits 46-47 = 1, layout
 // type in bits 61-63 (0 = no swizzle, 2 = 128-byte swizzle).
@@ -186,6 +208,15 @@ __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
                : "memory");
 }
 
+__device__ __forceinline__ void tc_cp_32x128b_x4_warp(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+
 // D(tmem) (+)= A(smem) x B(smem)^T with per-32-K E8M0 scale factors read from
 // TMEM, .kind::mxf8f6f4 (operand types come from the instruction descriptor).
 __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -195,6 +226,20 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint6
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Warp-wide form of tc_mma_mx (one elected lane issues).
+__device__ __forceinline__ void tc_mma_mx_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
       " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");

@@ -98,7 +98,8 @@ def test_forward_validation_without_gpu(lib):
     assert _fwd(lib, s, good, need, mode=2) == L.MOE_ERR_UNSUPPORTED
     assert _fwd(lib, s, good, need, mode=5) == L.MOE_ERR_INVALID_ARG
     assert _fwd(lib, _shape(H=200), good, need) == L.MOE_ERR_MISALIGNED
-    assert _fwd(lib, s, good, need, opts=P.options(tile_variant=6)) == L.MOE_ERR_INVALID_ARG
+    assert _fwd(lib, s, good, need, opts=P.options(tile_variant=99)) == L.MOE_ERR_INVALID_ARG
+    assert _fwd(lib, s, good, need, opts=P.options(tile_variant=-1)) == L.MOE_ERR_INVALID_ARG
     o = P.options()
     o.reserved[2] = 1
     assert _fwd(lib, s, good, need, opts=o) == L.MOE_ERR_INVALID_ARG
