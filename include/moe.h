@@ -124,10 +124,17 @@ typedef struct {
  *   hq          uint8[R,I]    FP8 E4M3 codes of h
  *   h_scale     float[R]      per-row scale of hq
  *   y           bf16[R,H]     GEMM2 output (scaled)
- *   x_stage, logits_stage, out_stage: device staging used by moe_forward_host */
+ *   x_stage, logits_stage, out_stage: device staging used by moe_forward_host
+ *   tile_plan   int32[E,2]    per expert: first GEMM tile, rows per tile
+ * MXFP8 (W8A8) only (0 bytes otherwise; x_scale / h_scale unused):
+ *   x_sf        uint8[R,H/32] E8M0 block scales of xq, row-major
+ *   h_sf        uint8[R,I/32] E8M0 block scales of hq, row-major
+ *   x_sf_tiled, h_sf_tiled    the same scales in the GEMMs' per-tile layout:
+ *                             1024 bytes per (tile, 128-K stage) */
 typedef struct {
   uint64_t status, ids, weights, row_of, counts, offsets, chunk_counts, token_slot,
-      tiles, xq, x_scale, h, hq, h_scale, y, x_stage, logits_stage, out_stage, total;
+      tiles, xq, x_scale, h, hq, h_scale, y, x_stage, logits_stage, out_stage, tile_plan,
+      x_sf, h_sf, x_sf_tiled, h_sf_tiled, total;
   int32_t max_tiles, num_chunks, reserved[6];
 } moe_ws_layout;
 

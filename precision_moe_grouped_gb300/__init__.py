@@ -25,13 +25,15 @@ class FusedMoE:
 
     w1 uint8 [E, 2I, H/2], w1_sf uint8 [E, 2I, H/32], w2 uint8 [E, H, I/2],
     w2_sf uint8 [E, H, I/32] (MXFP4: E2M1 codes two per byte, low nibble =
-    even K index; E8M0 scale per 32 K).  Rows 0..I-1 of w1 are the gate
+    even K index; E8M0 scale per 32 K); in the W8A8 mode w1 [E, 2I, H] and
+    w2 [E, H, I] hold E4M3 codes.  Rows 0..I-1 of w1 are the gate
     projection, I..2I-1 the up projection."""
 
     def __init__(self, w1, w1_sf, w2, w2_sf, top_k: int, mode: int = MOE_W4A8_MXFP4_FP8):
         import torch
-        E, I2, Hh = w1.shape
-        self.E, self.I, self.H, self.top_k, self.mode = E, I2 // 2, Hh * 2, top_k, mode
+        E, I2, Hk = w1.shape   # Hk = H/2 packed E2M1 bytes, or H E4M3 bytes (W8A8)
+        H = Hk if mode == MOE_W8A8_MXFP8 else Hk * 2
+        self.E, self.I, self.H, self.top_k, self.mode = E, I2 // 2, H, top_k, mode
         self.device = w1.device
         self.w1_p = torch.empty_like(w1)
         self.w1_sf_p = torch.empty_like(w1_sf)

@@ -58,7 +58,7 @@ class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "status", "ids", "weights", "row_of", "counts", "offsets", "chunk_counts", "token_slot",
         "tiles", "xq", "x_scale", "h", "hq", "h_scale", "y", "x_stage", "logits_stage",
-        "out_stage", "total")] + [("max_tiles", ctypes.c_int32), ("num_chunks", ctypes.c_int32),
+        "out_stage", "tile_plan", "x_sf", "h_sf", "x_sf_tiled", "h_sf_tiled", "total")] + [("max_tiles", ctypes.c_int32), ("num_chunks", ctypes.c_int32),
                                   ("reserved", ctypes.c_int32 * 6)]
 
 

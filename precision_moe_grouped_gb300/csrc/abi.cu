@@ -89,7 +89,7 @@ int32_t check_shape(const moe_shape* s, int32_t mode) {
   return MOE_OK;
 }
 
-void compute_layout(const moe_shape* s, moe_ws_layout* L) {
+void compute_layout(const moe_shape* s, int32_t mode, moe_ws_layout* L) {
   std::memset(L, 0, sizeof(*L));
   const int64_t T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden,
                 I = s->inter;
@@ -121,6 +121,13 @@ void compute_layout(const moe_shape* s, moe_ws_layout* L) {
   L->x_stage = take(T * H * 2);
   L->logits_stage = take(T * E * 4);
   L->out_stage = take(T * H * 2);
+  L->tile_plan = take(E * 8);
+  // MXFP8 activation scales: row-major bytes and the GEMMs' per-tile layout
+  const bool mx = mode == MOE_W8A8_MXFP8;
+  L->x_sf = take(mx ? R * (H / 32) : 0);
+  L->h_sf = take(mx ? R * (I / 32) : 0);
+  L->x_sf_tiled = take(mx ? max_tiles * (H / 128) * moe::kSfbTileBytes : 0);
+  L->h_sf_tiled = take(mx ? max_tiles * (I / 128) * moe::kSfbTileBytes : 0);
   L->total = align_up(off, kAlign);
   L->max_tiles = static_cast<int32_t>(max_tiles);
   L->num_chunks = static_cast<int32_t>(chunks);
@@ -233,7 +240,7 @@ int32_t check_forward_args(const moe_shape* shape, int32_t mode, const void* x,
   int32_t st = check_shape(shape, mode);
   if (st != MOE_OK) return st;
   if ((st = check_options(opts)) != MOE_OK) return st;
-  if (mode != MOE_W4A8_MXFP4_FP8)
+  if (mode == MOE_W4A16_MXFP4_BF16)
     return fail(MOE_ERR_UNSUPPORTED, "quant_mode %d is not implemented in this build", mode);
   if (shape->num_tokens == 0) return MOE_OK;
   if (!x || !logits || !w1 || !w1_sf || !w2 || !w2_sf || !out || !ws)
@@ -244,7 +251,7 @@ int32_t check_forward_args(const moe_shape* shape, int32_t mode, const void* x,
       !aligned(ws, 256))
     return fail(MOE_ERR_MISALIGNED, "weights, scales and workspace must be 256-byte aligned");
   moe_ws_layout L;
-  compute_layout(shape, &L);
+  compute_layout(shape, mode, &L);
   if (ws_bytes < L.total)
     return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < required %llu", ws_bytes,
                 static_cast<unsigned long long>(L.total));
@@ -256,14 +263,15 @@ T* at(void* ws, uint64_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
-int32_t run_forward(const moe_shape* s, const void* x, const float* logits, const void* w1,
-                    const void* w1_sf, const void* w2, const void* w2_sf, void* out, void* ws,
-                    cudaStream_t st, const moe_options* opts) {
+int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float* logits,
+                    const void* w1, const void* w1_sf, const void* w2, const void* w2_sf,
+                    void* out, void* ws, cudaStream_t st, const moe_options* opts) {
   DeviceInfo dev;
   int32_t rc = device_info(&dev);
   if (rc != MOE_OK) return rc;
   moe_ws_layout L;
-  compute_layout(s, &L);
+  compute_layout(s, mode, &L);
+  const bool mx = mode == MOE_W8A8_MXFP8;
   const int T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden, I = s->inter;
   const int R = T * k;
   const int variant = pick_variant(s, opts);
@@ -285,14 +293,22 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   uint8_t* hq = at<uint8_t>(ws, L.hq);
   float* h_scale = at<float>(ws, L.h_scale);
   void* y = at<void>(ws, L.y);
+  int2* tile_plan = at<int2>(ws, L.tile_plan);
+  uint8_t* x_sf = mx ? at<uint8_t>(ws, L.x_sf) : nullptr;
+  uint8_t* h_sf = mx ? at<uint8_t>(ws, L.h_sf) : nullptr;
+  uint8_t* sfb1 = mx ? at<uint8_t>(ws, L.x_sf_tiled) : nullptr;
+  uint8_t* sfb2 = mx ? at<uint8_t>(ws, L.h_sf_tiled) : nullptr;
 
   CUtensorMap tm_w1, tm_w2, tm_sf1, tm_sf2, tm_x[moe::kNumXMaps], tm_h[moe::kNumXMaps];
-  // prepared weights: contiguous 128-row x 128-element (64-byte rows) boxes;
-  // prepared scales: one 512-byte block per box
+  // prepared weights: contiguous 128-row x 128-element boxes (64-byte rows
+  // of E2M1 codes, or 128-byte rows of E4M3 codes in MXFP8); prepared
+  // scales: one 512-byte block per box
   const uint64_t w1_boxes = static_cast<uint64_t>(E) * (2 * I / 128) * (H / 128);
   const uint64_t w2_boxes = static_cast<uint64_t>(E) * (H / 128) * (I / 128);
-  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, 128, MapKind::kFp4Weights, 128, 128)) != MOE_OK ||
-      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, 128, MapKind::kFp4Weights, 128, 128)) != MOE_OK ||
+  const MapKind wkind = mx ? MapKind::kBytes : MapKind::kFp4Weights;
+  const uint32_t w_tx = mx ? 128u * 128u : kWeightBoxTxBytes;
+  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, 128, wkind, 128, 128)) != MOE_OK ||
+      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, 128, wkind, 128, 128)) != MOE_OK ||
       (rc = make_tmap(&tm_sf1, w1_sf, w1_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK ||
       (rc = make_tmap(&tm_sf2, w2_sf, w2_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK)
     return rc;
@@ -312,32 +328,40 @@ int32_t run_forward(const moe_shape* s, const void* x, const float* logits, cons
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
   MOE_CUDA(mark());
+  const moe::QuantOut qx{xq, x_scale, mx, x_sf, sfb1};
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* token_slot = at<int32_t>(ws, L.token_slot);
   if (T <= moe::kSmallT) {
-    MOE_CUDA(moe::launch_expand_small(x, ids, T, E, k, H, bn, at<int32_t>(ws, L.counts),
-                                      at<int32_t>(ws, L.offsets), tiles, num_tiles, row_of,
-                                      at<int32_t>(ws, L.token_slot), xq, x_scale, st));
+    MOE_CUDA(moe::launch_expand_small(x, ids, T, E, k, H, bn, at<int32_t>(ws, L.counts), offsets,
+                                      tiles, num_tiles, tile_plan, row_of, token_slot, qx, st));
     MOE_CUDA(mark());
     MOE_CUDA(mark());
     MOE_CUDA(mark());
   } else {
-    MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts),
-                              at<int32_t>(ws, L.offsets), chunk, tiles, num_tiles, st));
+    MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts), offsets,
+                              chunk, tiles, num_tiles, tile_plan, st));
     MOE_CUDA(mark());
-    MOE_CUDA(moe::launch_rank(ids, chunk, T, E, k, row_of, at<int32_t>(ws, L.token_slot), st));
+    MOE_CUDA(moe::launch_rank(ids, chunk, T, E, k, row_of, token_slot, st));
     MOE_CUDA(mark());
-    MOE_CUDA(moe::launch_quant_scatter(x, row_of, T, k, H, xq, x_scale, st));
+    MOE_CUDA(moe::launch_quant_scatter(x, row_of, ids, offsets, tile_plan, T, k, H, qx, st));
     MOE_CUDA(mark());
   }
+  // W4A8: the per-row token scale is applied in the epilogues; MXFP8: the
+  // block scales ride with the operands into the MMA
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
-                   x_scale, h, 2 * I, H, I, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms,
-                   prefetch};
+                   mx ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, dev.num_sms,
+                   prefetch, mx, sfb1};
   MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
-  MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
+  if (mx)
+    MOE_CUDA(moe::launch_hquant_mx(h, R, I, ids, token_slot, offsets, tile_plan, hq, h_sf, sfb2,
+                                   st));
+  else
+    MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
   MOE_CUDA(mark());
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
-                   h_scale, y, H, I, H, status, timeout_ns, kWeightBoxTxBytes, dev.num_sms,
-                   prefetch};
+                   mx ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, dev.num_sms,
+                   prefetch, mx, sfb2};
   MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));
@@ -379,7 +403,7 @@ const char* moe_status_string(int32_t status) {
 size_t moe_workspace_size(const moe_shape* shape, int32_t quant_mode) {
   if (check_shape(shape, quant_mode) != MOE_OK) return 0;
   moe_ws_layout L;
-  compute_layout(shape, &L);
+  compute_layout(shape, quant_mode, &L);
   return static_cast<size_t>(L.total);
 }
 
@@ -387,7 +411,7 @@ int32_t moe_workspace_layout(const moe_shape* shape, int32_t quant_mode, moe_ws_
   int32_t st = check_shape(shape, quant_mode);
   if (st != MOE_OK) return st;
   if (!layout) return fail(MOE_ERR_INVALID_ARG, "layout is NULL");
-  compute_layout(shape, layout);
+  compute_layout(shape, quant_mode, layout);
   return MOE_OK;
 }
 
@@ -396,9 +420,10 @@ int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode, const vo
                             void* w1_sf_p, void* w2_p, void* w2_sf_p, void* stream) {
   int32_t st = check_shape(shape, quant_mode);
   if (st != MOE_OK) return st;
-  if (quant_mode != MOE_W4A8_MXFP4_FP8)
+  if (quant_mode == MOE_W4A16_MXFP4_BF16)
     return fail(MOE_ERR_UNSUPPORTED, "quant_mode %d is not implemented in this build",
                 quant_mode);
+  const bool fp8 = quant_mode == MOE_W8A8_MXFP8;
   const void* ins[4] = {w1, w1_sf, w2, w2_sf};
   const void* outs[4] = {w1_p, w1_sf_p, w2_p, w2_sf_p};
   for (int i = 0; i < 4; ++i) {
@@ -413,10 +438,10 @@ int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode, const vo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_CUDA(moe::launch_prepare(static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sf),
                                static_cast<uint8_t*>(w1_p), static_cast<uint8_t*>(w1_sf_p), E,
-                               2 * I, H, I, s));
+                               2 * I, H, I, fp8, s));
   MOE_CUDA(moe::launch_prepare(static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sf),
                                static_cast<uint8_t*>(w2_p), static_cast<uint8_t*>(w2_sf_p), E, H,
-                               I, 0, s));
+                               I, 0, fp8, s));
   return MOE_OK;
 }
 
@@ -427,8 +452,8 @@ int32_t moe_forward_ex(const moe_shape* shape, int32_t quant_mode, const void* x
   int32_t st = check_forward_args(shape, quant_mode, x, router_logits, w1_p, w1_sf_p, w2_p,
                                   w2_sf_p, out, workspace, workspace_bytes, opts);
   if (st != MOE_OK || shape->num_tokens == 0) return st;
-  return run_forward(shape, x, router_logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out, workspace,
-                     static_cast<cudaStream_t>(stream), opts);
+  return run_forward(shape, quant_mode, x, router_logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out,
+                     workspace, static_cast<cudaStream_t>(stream), opts);
 }
 
 int32_t moe_forward(const moe_shape* shape, int32_t quant_mode, const void* x,
@@ -450,7 +475,7 @@ int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void*
   if (!x_host || !logits_host || !out_host || !workspace)
     return fail(MOE_ERR_INVALID_ARG, "a required pointer is NULL");
   moe_ws_layout L;
-  compute_layout(shape, &L);
+  compute_layout(shape, quant_mode, &L);
   void* xs = at<void>(workspace, L.x_stage);
   float* ls = at<float>(workspace, L.logits_stage);
   void* os = at<void>(workspace, L.out_stage);
@@ -461,7 +486,8 @@ int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void*
   const size_t T = shape->num_tokens, H = shape->hidden, E = shape->num_experts;
   MOE_CUDA(cudaMemcpyAsync(xs, x_host, T * H * 2, cudaMemcpyHostToDevice, s));
   MOE_CUDA(cudaMemcpyAsync(ls, logits_host, T * E * 4, cudaMemcpyHostToDevice, s));
-  st = run_forward(shape, xs, ls, w1_p, w1_sf_p, w2_p, w2_sf_p, os, workspace, s, opts);
+  st = run_forward(shape, quant_mode, xs, ls, w1_p, w1_sf_p, w2_p, w2_sf_p, os, workspace, s,
+                   opts);
   if (st != MOE_OK) return st;
   MOE_CUDA(cudaMemcpyAsync(out_host, os, T * H * 2, cudaMemcpyDeviceToHost, s));
   return MOE_OK;

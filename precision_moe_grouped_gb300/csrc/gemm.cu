@@ -62,7 +62,7 @@ __device__ __forceinline__ int x_map_for(int rows) {
   return rows <= 16 ? 0 : (rows + 31) / 32;
 }
 
-template <int BN, int STAGES, int NI, int NB>
+template <int BN, int STAGES, int NI, int NB, bool MX8>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN <= kXBoxRowsAt(kNumXMaps - 1),
                 "token tile must be a multiple of 16 rows and fit the largest box");
@@ -74,24 +74,28 @@ struct GemmCfg {
   static constexpr int kABytes = kTileM * 128;       // FP4 expanded to 1 byte/element in smem
   static constexpr int kBBytes = BN * 128;           // FP8 tokens x 128 K
   static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes
+  // MXFP8: the activation scales of a stage, 512 bytes per 128 tile rows
+  static constexpr int kSFBSlot = MX8 ? 512 * ((BN + 127) / 128) : 0;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffSF = kOffB + STAGES * kBBytes;
-  static constexpr int kOffSFB = kOffSF + STAGES * kSFBytes;
+  static constexpr int kOffSFBs = kOffSF + STAGES * kSFBytes;
+  static constexpr int kOffSFB = kOffSFBs + STAGES * kSFBSlot;   // constant scales (W4A8)
   static constexpr int kNumBars = 2 * STAGES + 2 * NB + 1 + NI;
-  static constexpr int kOffBar = kOffSFB + 512;
+  static constexpr int kOffBar = kOffSFB + (MX8 ? 0 : 512);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
   // TMEM columns: for each of the NB accumulator buffers, one fp32
   // accumulator of BN columns per MMA issuer (buffer a, issuer i at column
-  // (a * NI + i) * BN); 8 columns of constant activation scales (up to 256
-  // tokens); 4 columns of weight scales per stage.
+  // (a * NI + i) * BN); 4 columns of weight scales per stage; activation
+  // scales: 8 columns of constants (W4A8, up to 256 tokens) or 8 columns per
+  // stage (MXFP8).
   static constexpr int kEpiWarps = 8;               // two per TMEM lane quarter
   static constexpr int kThreads = 32 * (NI + 1 + kEpiWarps);   // producer, issuers, epilogue
-  static constexpr int kColSFB = NB * NI * BN;
-  static constexpr int kColSFA = NB * NI * BN + 8;
-  static constexpr int kColsUsed = NB * NI * BN + 8 + 4 * STAGES;
+  static constexpr int kColSFA = NB * NI * BN;
+  static constexpr int kColSFB = kColSFA + 4 * STAGES;
+  static constexpr int kColsUsed = kColSFB + (MX8 ? 8 * STAGES : 8);
   static constexpr int kTmemCols = kColsUsed <= 32    ? 32
                                    : kColsUsed <= 64  ? 64
                                    : kColsUsed <= 128 ? 128
@@ -100,8 +104,8 @@ struct GemmCfg {
   static_assert(kColsUsed <= 512, "TMEM budget exceeded");
 };
 
-template <int BN, int STAGES, int NI, int NB, bool SWIGLU>
-__global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
+template <int BN, int STAGES, int NI, int NB, bool SWIGLU, bool MX8>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ XMaps tmap_x,
                         const __grid_constant__ CUtensorMap tmap_sf,
@@ -109,8 +113,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
                         const int32_t* __restrict__ num_tiles_p,
                         const float* __restrict__ row_scale, __nv_bfloat16* __restrict__ out,
                         int m_per_expert, int K, int out_ld, int32_t* __restrict__ status,
-                        uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages) {
-  using C = GemmCfg<BN, STAGES, NI, NB>;
+                        uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages,
+                        const uint8_t* __restrict__ sfb_tiled) {
+  using C = GemmCfg<BN, STAGES, NI, NB, MX8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -151,9 +156,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
     for (int i = 0; i < kNumXMaps; ++i) prefetch_tmap(&tmap_x.m[i]);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
-  // Activation (B) scales are all 1.0: E8M0 byte 127 everywhere.
-  for (int i = threadIdx.x; i < 128; i += blockDim.x)
-    reinterpret_cast<uint32_t*>(smem + C::kOffSFB)[i] = 0x7F7F7F7Fu;
+  // W4A8: activation (B) scales are all 1.0 (E8M0 byte 127 everywhere); the
+  // per-token scale is applied in the epilogue.
+  if (!MX8)
+    for (int i = threadIdx.x; i < 128; i += blockDim.x)
+      reinterpret_cast<uint32_t*>(smem + C::kOffSFB)[i] = 0x7F7F7F7Fu;
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -161,7 +168,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // Constant activation scales into TMEM once, finished before any issuer
   // (each a different thread) runs an MMA that reads them.
-  if (warp == 1 && lane == 0) {
+  if (!MX8 && warp == 1 && lane == 0) {
     const uint64_t sfb_desc = smem_desc(smem_u32(smem + C::kOffSFB), 0, 128, 0);
     tc_cp_32x128b_x4(tmem + C::kColSFB, sfb_desc);
     tc_cp_32x128b_x4(tmem + C::kColSFB + 4, sfb_desc);
@@ -225,9 +232,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
           const int nmma = (td.z + 15) & ~15;
           const int xm = x_map_for(nmma);
           const uint32_t bx = static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u;
-          mbar_arrive_expect_tx(full + s, LPS == 2 ? bx + 512u : bx);
+          // MXFP8: the tile's activation scales for this K stage (one 512-byte
+          // block per 128 rows of the MMA-N)
+          const uint32_t sfb_bytes = MX8 ? (nmma > 128 ? 1024u : 512u) : 0u;
+          mbar_arrive_expect_tx(full + s, (LPS == 2 ? bx + 512u : bx) + sfb_bytes);
           tma_load_2d(smem + C::kOffB + s * C::kBBytes, &tmap_x.m[xm], ks * kTileK, td.y,
                       full + s);
+          if (MX8)
+            bulk_load(smem + C::kOffSFBs + s * C::kSFBSlot,
+                      sfb_tiled + (static_cast<int64_t>(item / MT) * KS + ks) * kSfbTileBytes,
+                      sfb_bytes, full + s);
           if (LPS == 2)
             tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0,
                         static_cast<int32_t>(blk), full + s);
@@ -270,7 +284,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
       const uint64_t adesc0 = smem_desc(smem_u32(smem + C::kOffA), 0, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
       const uint64_t sdesc0 = smem_desc(smem_u32(smem + C::kOffSF), 0, 128, 0);
+      const uint64_t sbdesc0 = smem_desc(smem_u32(smem + C::kOffSFBs), 0, 128, 0);
       int stage = i % STAGES, ks = i % KS, it = i / KS;   // ni <= KS, so it == 0
+      int nmma = 16;
       uint32_t phase = (i / STAGES) & 1;
       bool new_item = true;
       uint32_t d_tmem = 0, id0 = 0;
@@ -279,7 +295,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
         if (new_item) {
           const int item = blockIdx.x + it * gridDim.x;
           const int4 td = tiles[item / MT];
-          id0 = idesc_mx(5, 0, static_cast<uint32_t>((td.z + 15) & ~15), 0, 0);
+          nmma = (td.z + 15) & ~15;
+          // A = weights: E2M1, or E4M3 in MXFP8; B = activations: E4M3
+          id0 = idesc_mx(MX8 ? 0 : 5, 0, static_cast<uint32_t>(nmma), 0, 0);
           acc = it % NB;
           if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
                               status, kDevTimeout, abort_flag))
@@ -292,12 +310,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
         tc_fence_after();
         const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
         tc_cp_32x128b_x4_warp(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
+        uint32_t sfb = tmem + C::kColSFB;
+        if (MX8) {
+          sfb += static_cast<uint32_t>(8 * stage);
+          const uint64_t sbd = sbdesc0 + static_cast<uint64_t>(stage * (C::kSFBSlot >> 4));
+          tc_cp_32x128b_x4_warp(sfb, sbd);
+          if (nmma > 128) tc_cp_32x128b_x4_warp(sfb + 4, sbd + (512 >> 4));
+        }
         const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
         const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
 #pragma unroll
         for (uint32_t kk = 0; kk < 4; ++kk)
           tc_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
-                         tmem + C::kColSFB, (!new_item || kk > 0) ? 1u : 0u);
+                         sfb, (!new_item || kk > 0) ? 1u : 0u);
         tc_commit_warp(empty + stage);
         stage += ni;
         if (stage >= STAGES) {
@@ -341,7 +366,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
         const int c0 = ch * 16;
         // one row-scale load per chunk: lane j (and j + 16) holds column c0 + j
         const int nl = c0 + (lane & 15);
-        const float sc = nl < ntok ? __ldg(row_scale + row0 + nl) : 0.f;
+        const float sc = nl < ntok ? (row_scale ? __ldg(row_scale + row0 + nl) : 1.f) : 0.f;
         float v[16];
         tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
         for (int p = 1; p < ni; ++p) {   // partial sums of the other issuers
@@ -393,10 +418,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB>::kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, int NI, int NB, bool SWIGLU>
+template <int BN, int STAGES, int NI, int NB, bool SWIGLU, bool MX8>
 cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
-  using C = GemmCfg<BN, STAGES, NI, NB>;
-  auto kern = grouped_gemm_kernel<BN, STAGES, NI, NB, SWIGLU>;
+  using C = GemmCfg<BN, STAGES, NI, NB, MX8>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, NI, NB, SWIGLU, MX8>;
   static bool attr_set = false;  // per instantiation; set before first launch
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -409,13 +434,15 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
   return launch_pdl(kern, dim3(a.num_sms), dim3(C::kThreads), C::kSmemBytes, s, *a.tmap_w, xm,
                     *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
                     static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status,
-                    a.timeout_ns, a.a_tx_bytes, a.prefetch_stages);
+                    a.timeout_ns, a.a_tx_bytes, a.prefetch_stages, a.sfb_tiled);
 }
 
 }  // namespace
 
 // Variants: <token tile BN, pipeline stages, MMA issuers NI, accumulator
-// buffers NB>.
+// buffers NB>, then the stages and issuers of the MXFP8 instantiation (its
+// stages also hold the activation scales, so the deepest rings lose a
+// stage).
 //   1: decode tiles of <= 32 tokens, 10 stages, 5 issuers;
 //   2: prefill tiles of <= 224 tokens, 5 stages;
 //   3: decode tiles of <= 16 tokens, 12 stages (the smallest stage, so the
@@ -423,17 +450,17 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
 //   4: tiles of <= 224 tokens with 2 issuers and one accumulator buffer (the
 //      epilogue no longer overlaps the next item's MMAs);
 //   5: tiles of <= 160 tokens, 6 stages.
-#define MOE_GEMM_VARIANTS(X)  \
-  X(1, kDecodeBN, 10, 5, 2)   \
-  X(2, kPrefillBN, 5, 1, 2)   \
-  X(3, kTinyBN, 12, 6, 2)     \
-  X(4, kPrefillBN, 4, 2, 1)   \
-  X(5, kMidBN, 6, 1, 2)
+#define MOE_GEMM_VARIANTS(X)          \
+  X(1, kDecodeBN, 10, 5, 2, 10, 5)    \
+  X(2, kPrefillBN, 5, 1, 2, 4, 1)     \
+  X(3, kTinyBN, 12, 6, 2, 10, 5)      \
+  X(4, kPrefillBN, 4, 2, 1, 4, 2)     \
+  X(5, kMidBN, 6, 1, 2, 6, 1)
 
 int gemm_tile_tokens(int variant) {
   switch (variant) {
-#define MOE_X(v, bn, st, ni, nb) \
-  case v:                        \
+#define MOE_X(v, bn, st, ni, nb, st8, ni8) \
+  case v:                                  \
     return bn;
     MOE_GEMM_VARIANTS(MOE_X)
 #undef MOE_X
@@ -444,10 +471,13 @@ int gemm_tile_tokens(int variant) {
 
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s) {
   switch (variant) {
-#define MOE_X(v, bn, st, ni, nb)                                  \
-  case v:                                                         \
-    return swiglu ? launch_variant<bn, st, ni, nb, true>(a, s) \
-                  : launch_variant<bn, st, ni, nb, false>(a, s);
+#define MOE_X(v, bn, st, ni, nb, st8, ni8)                                        \
+  case v:                                                                         \
+    if (a.mx8)                                                                    \
+      return swiglu ? launch_variant<bn, st8, ni8, nb, true, true>(a, s)          \
+                    : launch_variant<bn, st8, ni8, nb, false, true>(a, s);        \
+    return swiglu ? launch_variant<bn, st, ni, nb, true, false>(a, s)             \
+                  : launch_variant<bn, st, ni, nb, false, false>(a, s);
     MOE_GEMM_VARIANTS(MOE_X)
 #undef MOE_X
     default:

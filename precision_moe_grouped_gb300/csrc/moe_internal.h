@@ -56,6 +56,24 @@ constexpr int kMidBN = 160;          // max tokens per tile, 6-stage prefill var
 constexpr int kNumXMaps = 8;
 __host__ __device__ constexpr int kXBoxRowsAt(int i) { return i == 0 ? 16 : 32 * i; }
 
+// MXFP8 mode: the activation (B operand) scale bytes are written by the
+// quantisers straight into the GEMM's per-tile layout.  For tile t of the
+// GEMM tile list and K stage ks there is one kSfbTileBytes block at
+// (t * KS + ks) * kSfbTileBytes; tile row n's four scale bytes (K blocks
+// 4ks .. 4ks+3) sit at sfb_row_offset(n): the 32-lane x 16-byte shape of the
+// weight scale blocks, one 512-byte half per 128 rows.
+constexpr int kSfbTileBytes = 1024;   // up to 256 tile rows
+__host__ __device__ inline uint32_t sfb_row_offset(int n) {
+  return static_cast<uint32_t>((n >> 7) * 512 + 16 * (n & 31) + 4 * ((n >> 5) & 3));
+}
+// Byte offset (K stage 0) of expanded row r's scales, from its expert's
+// first row off_e and tile plan (first tile, rows per tile).
+__host__ __device__ inline int64_t sfb_row_base(int r, int off_e, int2 plan, int KS) {
+  const int j = r - off_e;
+  const int q = j / plan.y;
+  return (static_cast<int64_t>(plan.x) + q) * KS * kSfbTileBytes + sfb_row_offset(j - q * plan.y);
+}
+
 struct GemmArgs {
   const CUtensorMap* tmap_w;   // host copies, passed by value to the kernel
   const CUtensorMap* tmap_x;   // kNumXMaps maps, box heights kXBoxRows
@@ -72,23 +90,43 @@ struct GemmArgs {
   uint32_t a_tx_bytes;         // transaction bytes one weight TMA box counts
   int32_t num_sms;
   int32_t prefetch_stages;     // L2 prefetch distance of weight tiles, in K stages
+  bool mx8;                    // MXFP8 operands: E4M3 weights, per-32 activation scales
+  const uint8_t* sfb_tiled;    // MXFP8: activation scales in the per-tile layout
 };
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
                          int32_t* chunk_counts, int32_t* status, cudaStream_t s);
+// Activation quantisation outputs of the expansion kernels.  W4A8: x_scale
+// (per-row float).  MXFP8 (mx8): x_sf (row-major scale bytes [R, H/32]) and
+// sfb (per-tile layout above).
+struct QuantOut {
+  uint8_t* xq;
+  float* x_scale;
+  bool mx8;
+  uint8_t* x_sf;
+  uint8_t* sfb;
+};
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
                                 int bn, int32_t* counts, int32_t* offsets, int4* tiles,
-                                int32_t* num_tiles, int32_t* row_of, int32_t* token_slot,
-                                uint8_t* xq, float* x_scale, cudaStream_t s);
+                                int32_t* num_tiles, int2* tile_plan, int32_t* row_of,
+                                int32_t* token_slot, const QuantOut& q, cudaStream_t s);
+// tile_plan (nullable): per expert (first tile, rows per tile).
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
                         int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
-                        int32_t* num_tiles, cudaStream_t s);
+                        int32_t* num_tiles, int2* tile_plan, cudaStream_t s);
 cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,
                         int32_t* row_of, int32_t* token_slot, cudaStream_t s);
-cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, int T, int k, int H,
-                                 uint8_t* xq, float* x_scale, cudaStream_t s);
+cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, const int32_t* ids,
+                                 const int32_t* offsets, const int2* tile_plan, int T, int k,
+                                 int H, const QuantOut& q, cudaStream_t s);
 cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_scale,
                           cudaStream_t s);
+// MXFP8 quantisation of h: codes, row-major scale bytes [R, I/32] and the
+// per-tile scale layout of GEMM2.
+cudaError_t launch_hquant_mx(const void* h, int R, int I, const int32_t* ids,
+                             const int32_t* token_slot, const int32_t* offsets,
+                             const int2* tile_plan, uint8_t* hq, uint8_t* h_sf, uint8_t* sfb,
+                             cudaStream_t s);
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
                            int H, void* out, cudaStream_t s);
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);
@@ -96,11 +134,11 @@ cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_
 // list is built with this bound).
 constexpr int kMaxTileVariant = 5;
 int gemm_tile_tokens(int variant);
-// Re-lays one weight tensor [E, M, K] (E2M1, K/2 bytes per row) and its
-// scales [E, M, K/32] for the GEMM; swiglu_I > 0 applies GEMM1's gate/up row
-// interleave (M = 2 * swiglu_I).
+// Re-lays one weight tensor [E, M, K] (E2M1 with K/2 bytes per row, or E4M3
+// with K bytes per row when fp8) and its scales [E, M, K/32] for the GEMM;
+// swiglu_I > 0 applies GEMM1's gate/up row interleave (M = 2 * swiglu_I).
 cudaError_t launch_prepare(const uint8_t* w, const uint8_t* sf, uint8_t* w_p, uint8_t* sf_p,
-                           int E, int M, int K, int swiglu_I, cudaStream_t s);
+                           int E, int M, int K, int swiglu_I, bool fp8, cudaStream_t s);
 // Sets the message moe_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 

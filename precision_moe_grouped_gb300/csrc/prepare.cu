@@ -9,9 +9,11 @@
 //           work on 16-row x 64-K groups and need n % 16 == 0, k % 64 == 0).
 //
 // Layouts produced (per expert e, M rows of weights, K reduction elements):
-//   * weights: blocked into contiguous 8 KB boxes, one per (e, M-tile mt,
+//   * weights: blocked into contiguous boxes, one per (e, M-tile mt,
 //     K-stage ks of 128 elements): box ((e * MT + mt) * KS + ks) holds tile
-//     rows 0..127 of that K range, 64 bytes (128 packed E2M1 codes) per row.
+//     rows 0..127 of that K range, 64 bytes (128 packed E2M1 codes) per row
+//     -- 8 KB boxes -- or, for the MXFP8 weights of the W8A8 mode, 128 bytes
+//     (128 E4M3 codes) per row -- 16 KB boxes.
 //     A GEMM work item then streams one contiguous run of KS boxes, and every
 //     TMA box load is a single 8 KB read.  GEMM1's w1 rows are also permuted
 //     so that every 128-row M-tile holds 64 gate rows and the 64 matching up
@@ -38,23 +40,26 @@ __host__ __device__ inline int w1_src_row(int p, int I) {
   return i < 16 ? f : I + f;
 }
 
-// One thread per destination 16-byte vector of the blocked weight layout.
+// One thread per destination 16-byte vector of the blocked weight layout;
+// VPR = 16-byte vectors per box row (4: 128 packed E2M1 codes, 8: 128 E4M3
+// codes).
+template <int VPR>
 __global__ void block_weights_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                      int64_t total_vec, int M, int K, int swiglu_I) {
   const int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (v >= total_vec) return;
   const int KS = K / 128, MT = M / 128;
-  const int q = static_cast<int>(v & 3);           // 16-byte quarter of a 64-byte box row
-  const int r = static_cast<int>((v >> 2) & 127);  // box row
-  const int64_t blk = v >> 9;                      // (e * MT + mt) * KS + ks
+  const int q = static_cast<int>(v % VPR);              // 16-byte piece of a box row
+  const int r = static_cast<int>((v / VPR) & 127);      // box row
+  const int64_t blk = v / (VPR * 128);                  // (e * MT + mt) * KS + ks
   const int ks = static_cast<int>(blk % KS);
   const int64_t emt = blk / KS;
   const int mt = static_cast<int>(emt % MT);
   const int64_t e = emt / MT;
   const int p = mt * 128 + r;
   const int srow = swiglu_I > 0 ? w1_src_row(p, swiglu_I) : p;
-  const int64_t vec_per_row = K / 32;              // K/2 bytes per row / 16
-  dst[v] = src[(e * M + srow) * vec_per_row + ks * 4 + q];
+  const int64_t vec_per_row = static_cast<int64_t>(K / 128) * VPR;
+  dst[v] = src[(e * M + srow) * vec_per_row + ks * VPR + q];
 }
 
 // One thread per destination 32-bit word.
@@ -79,9 +84,11 @@ __global__ void sf_layout_kernel(const uint32_t* __restrict__ src, uint32_t* __r
 }  // namespace
 
 cudaError_t launch_prepare(const uint8_t* w, const uint8_t* sf, uint8_t* w_p, uint8_t* sf_p,
-                           int E, int M, int K, int swiglu_I, cudaStream_t s) {
-  const int64_t vecs = static_cast<int64_t>(E) * M * (K / 32);
-  block_weights_kernel<<<static_cast<unsigned>((vecs + 255) / 256), 256, 0, s>>>(
+                           int E, int M, int K, int swiglu_I, bool fp8, cudaStream_t s) {
+  const int vpr = fp8 ? 8 : 4;
+  const int64_t vecs = static_cast<int64_t>(E) * M * (K / 128) * vpr;
+  auto kern = fp8 ? block_weights_kernel<8> : block_weights_kernel<4>;
+  kern<<<static_cast<unsigned>((vecs + 255) / 256), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(w), reinterpret_cast<uint4*>(w_p), vecs, M, K, swiglu_I);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;

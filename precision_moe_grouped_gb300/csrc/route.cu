@@ -22,6 +22,7 @@
 #include <climits>
 
 #include "moe_internal.h"
+#include "mxfp8.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -132,14 +133,17 @@ __device__ int block_exclusive_scan(int v, int* total) {
   return base + x - v;
 }
 
-// Tile list of one expert (thread e of a block with blockDim >= E; every
+// Tile plan of one expert (thread e of a block with blockDim >= E; every
 // thread of the block must call it): a tile is a run of at most `bn`
 // consecutive rows of one expert; an expert with c rows gets ceil(c / tsz)
 // tiles of tsz = roundup16(ceil(c / ceil(c / bn))) rows, so its tiles are
-// balanced and every MMA-N is a multiple of 16.
-__device__ void write_tiles(int e, int E, int c, int off, int bn, int4* __restrict__ tiles,
-                            int32_t* __restrict__ num_tiles) {
-  int nt = 0, tsz = 0;
+// balanced and every MMA-N is a multiple of 16.  Returns (first tile, tsz);
+// with `write` the block also stores the tile list, the tile count and (if
+// tile_plan is not null) the per-expert plan.
+__device__ int2 plan_tiles(int e, int E, int c, int off, int bn, bool write,
+                           int4* __restrict__ tiles, int32_t* __restrict__ num_tiles,
+                           int2* __restrict__ tile_plan) {
+  int nt = 0, tsz = 1;
   if (e < E && c > 0) {
     const int n0 = (c + bn - 1) / bn;
     tsz = (((c + n0 - 1) / n0) + 15) & ~15;
@@ -147,11 +151,15 @@ __device__ void write_tiles(int e, int E, int c, int off, int bn, int4* __restri
   }
   int total_tiles;
   const int toff = block_exclusive_scan(nt, &total_tiles);
-  for (int i = 0; i < nt; ++i) {
-    const int r0 = i * tsz;
-    tiles[toff + i] = make_int4(e, off + r0, min(tsz, c - r0), 0);
+  if (write) {
+    for (int i = 0; i < nt; ++i) {
+      const int r0 = i * tsz;
+      tiles[toff + i] = make_int4(e, off + r0, min(tsz, c - r0), 0);
+    }
+    if (tile_plan && e < E) tile_plan[e] = make_int2(toff, tsz);
+    if (threadIdx.x == 0) *num_tiles = total_tiles;
   }
-  if (threadIdx.x == 0) *num_tiles = total_tiles;
+  return make_int2(toff, tsz);
 }
 
 // One CTA (blockDim >= E): per-expert counts, offsets, per-chunk bases
@@ -165,7 +173,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ chunk_base,
                                                     int4* __restrict__ tiles,
-                                                    int32_t* __restrict__ num_tiles) {
+                                                    int32_t* __restrict__ num_tiles,
+                                                    int2* __restrict__ tile_plan) {
   griddep_wait();
   griddep_launch_dependents();
   const int e = threadIdx.x;
@@ -186,7 +195,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     }
   }
   if (e == 0) offsets[E] = total_rows;
-  write_tiles(e, E, e < E ? c : 0, off, bn, tiles, num_tiles);
+  plan_tiles(e, E, e < E ? c : 0, off, bn, true, tiles, num_tiles, tile_plan);
 }
 
 // One warp per chunk of kRouteChunk tokens: the warp walks the chunk's
@@ -276,18 +285,65 @@ __device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k
   if (static_cast<int>(threadIdx.x) < k) x_scale[rows[threadIdx.x]] = s;
 }
 
+// MXFP8 (the W8A8 mode) quantisation of token t's row, per 32-element
+// block: X = 2^clamp(floor(log2 amax) - 8, -127, 127) (8 = E4M3's emax),
+// codes = E4M3_rne_satfinite(x / X), scale byte = exponent + 127; an
+// all-zero block gets byte 127 (its codes are those of +-0).  Dividing by a
+// power of two is exact, so x * 2^-e rounds once, in the conversion.  Codes
+// go to the k expanded rows; scale bytes to the row-major x_sf [R, H/32] and
+// to the GEMM's per-tile layout at sfb_base[j] + (b / 4) * kSfbTileBytes +
+// b % 4 for block b of row rows[j].
+__device__ void quantize_token_mx(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
+                                  const int32_t* rows, const int64_t* sfb_base,
+                                  uint8_t* __restrict__ xq, uint8_t* __restrict__ x_sf,
+                                  uint8_t* __restrict__ sfb) {
+  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+  const int nblk = H / 32;
+  for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+    uint4 q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = __ldg(xr + 4 * b + i);
+    uint8_t sbyte;
+    uint4 codes[2];
+    mx_quant_block(q, &sbyte, codes);
+    for (int j = 0; j < k; ++j) {
+      const int64_t r = rows[j];
+      uint4* dst = reinterpret_cast<uint4*>(xq + r * H + 32 * b);
+      dst[0] = codes[0];
+      dst[1] = codes[1];
+      x_sf[r * nblk + b] = sbyte;
+      sfb[sfb_base[j] + static_cast<int64_t>(b >> 2) * kSfbTileBytes + (b & 3)] = sbyte;
+    }
+  }
+}
+
 // One CTA per token: FP8 quantisation of the token into its k rows.
+template <bool MX>
 __global__ void __launch_bounds__(128) quant_scatter_kernel(
-    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of, int k, int H,
-    uint8_t* __restrict__ xq, float* __restrict__ x_scale) {
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of,
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets,
+    const int2* __restrict__ tile_plan, int k, int H, uint8_t* __restrict__ xq,
+    float* __restrict__ x_scale, uint8_t* __restrict__ x_sf, uint8_t* __restrict__ sfb) {
   __shared__ int32_t rows[32];
+  __shared__ int64_t sfb_base[32];
   __shared__ float warp_max[32];
   griddep_wait();
   griddep_launch_dependents();
   const int t = blockIdx.x;
-  if (static_cast<int>(threadIdx.x) < k) rows[threadIdx.x] = row_of[static_cast<size_t>(t) * k + threadIdx.x];
+  if (static_cast<int>(threadIdx.x) < k) {
+    const size_t ts = static_cast<size_t>(t) * k + threadIdx.x;
+    const int r = row_of[ts];
+    rows[threadIdx.x] = r;
+    if (MX) {
+      const int e = ids[ts];
+      sfb_base[threadIdx.x] = sfb_row_base(r, offsets[e], tile_plan[e], H / kTileK);
+    }
+  }
   __syncthreads();
-  quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
+  if (MX)
+    quantize_token_mx(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
+  else
+    quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
 }
 
 // Small batches (T <= kSmallT): one kernel replaces scan + rank +
@@ -298,17 +354,21 @@ __global__ void __launch_bounds__(128) quant_scatter_kernel(
 // quantises its token into them.  CTA 0 also writes counts, offsets and the
 // GEMM tile list.  The redundant O(T*k) counting per CTA is cheap at these
 // sizes and removes three launches from the decode path.
+template <bool MX>
 __global__ void __launch_bounds__(1024) expand_small_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids, int T, int E, int k,
     int H, int bn, int32_t* __restrict__ counts_out, int32_t* __restrict__ offsets_out,
-    int4* __restrict__ tiles, int32_t* __restrict__ num_tiles, int32_t* __restrict__ row_of,
-    int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq, float* __restrict__ x_scale) {
+    int4* __restrict__ tiles, int32_t* __restrict__ num_tiles, int2* __restrict__ tile_plan,
+    int32_t* __restrict__ row_of, int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq,
+    float* __restrict__ x_scale, uint8_t* __restrict__ x_sf, uint8_t* __restrict__ sfb) {
   extern __shared__ int32_t sm[];
-  int32_t* cnt = sm;            // [E]
-  int32_t* my_e = sm + E;       // [k] experts of this token
+  int2* plan = reinterpret_cast<int2*>(sm);   // [E] tile plan (MXFP8)
+  int32_t* cnt = sm + 2 * E;    // [E]
+  int32_t* my_e = cnt + E;      // [k] experts of this token
   int32_t* my_rank = my_e + 32; // [k]
   int32_t* rows = my_rank + 32; // [k]
   __shared__ float warp_max[32];
+  __shared__ int64_t sfb_base[32];
   griddep_wait();
   griddep_launch_dependents();
   const int t = blockIdx.x, e = threadIdx.x;
@@ -346,10 +406,18 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
       offsets_out[e] = off;
     }
     if (e == 0) offsets_out[E] = total_rows;
-    write_tiles(e, E, c, off, bn, tiles, num_tiles);
   }
+  // every CTA plans the tiles (its rows' tile positions); CTA 0 writes them
+  const int2 pl = plan_tiles(e, E, c, off, bn, t == 0, tiles, num_tiles, tile_plan);
+  if (MX && e < E) plan[e] = pl;
   __syncthreads();
-  quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
+  if (MX) {
+    if (e < k) sfb_base[e] = sfb_row_base(rows[e], cnt[my_e[e]], plan[my_e[e]], H / kTileK);
+    __syncthreads();
+    quantize_token_mx(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
+  } else {
+    quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
+  }
 }
 
 }  // namespace
@@ -367,10 +435,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
 
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
                         int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
-                        int32_t* num_tiles, cudaStream_t s) {
+                        int32_t* num_tiles, int2* tile_plan, cudaStream_t s) {
   const int threads = ((E + 31) / 32) * 32;
   return launch_pdl(scan_kernel, dim3(1), dim3(threads), 0, s, chunk_counts, num_chunks, E, bn,
-                    counts, offsets, chunk_base, tiles, num_tiles);
+                    counts, offsets, chunk_base, tiles, num_tiles, tile_plan);
 }
 
 cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,
@@ -382,20 +450,24 @@ cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, in
                     ids, chunk_base, T, E, k, chunks, row_of, token_slot);
 }
 
-cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, int T, int k, int H,
-                                 uint8_t* xq, float* x_scale, cudaStream_t s) {
-  return launch_pdl(quant_scatter_kernel, dim3(T), dim3(128), 0, s,
-                    static_cast<const __nv_bfloat16*>(x), row_of, k, H, xq, x_scale);
+cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, const int32_t* ids,
+                                 const int32_t* offsets, const int2* tile_plan, int T, int k,
+                                 int H, const QuantOut& q, cudaStream_t s) {
+  auto kern = q.mx8 ? quant_scatter_kernel<true> : quant_scatter_kernel<false>;
+  return launch_pdl(kern, dim3(T), dim3(128), 0, s, static_cast<const __nv_bfloat16*>(x), row_of,
+                    ids, offsets, tile_plan, k, H, q.xq, q.x_scale, q.x_sf, q.sfb);
 }
 
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
                                 int bn, int32_t* counts, int32_t* offsets, int4* tiles,
-                                int32_t* num_tiles, int32_t* row_of, int32_t* token_slot,
-                                uint8_t* xq, float* x_scale, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(E + 96) * sizeof(int32_t);
-  return launch_pdl(expand_small_kernel, dim3(T), dim3(1024), smem, s,
-                    static_cast<const __nv_bfloat16*>(x), ids, T, E, k, H, bn, counts, offsets,
-                    tiles, num_tiles, row_of, token_slot, xq, x_scale);
+                                int32_t* num_tiles, int2* tile_plan, int32_t* row_of,
+                                int32_t* token_slot, const QuantOut& q, cudaStream_t s) {
+  // plan int2[E], cnt[E], my_e/my_rank/rows [32] each
+  const size_t smem = static_cast<size_t>(3 * E + 96) * sizeof(int32_t);
+  auto kern = q.mx8 ? expand_small_kernel<true> : expand_small_kernel<false>;
+  return launch_pdl(kern, dim3(T), dim3(1024), smem, s, static_cast<const __nv_bfloat16*>(x),
+                    ids, T, E, k, H, bn, counts, offsets, tiles, num_tiles, tile_plan, row_of,
+                    token_slot, q.xq, q.x_scale, q.x_sf, q.sfb);
 }
 
 }  // namespace moe

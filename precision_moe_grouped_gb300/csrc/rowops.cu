@@ -14,6 +14,7 @@
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
+#include "mxfp8.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -69,6 +70,39 @@ __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __rest
     dst[i] = out;
   }
   if (lane == 0) h_scale[warp] = nz ? amax / 448.0f : 1.0f;
+}
+
+// MXFP8 (the W8A8 mode) quantisation of h: one warp per expanded row r,
+// lane l converts the 32-element blocks l, l + 32, ...; codes to hq, scale
+// bytes to the row-major h_sf [R, I/32] and to GEMM2's per-tile layout
+// (row r's expert from its (token, slot), its tile from the expert's plan).
+__global__ void __launch_bounds__(256) hquant_mx_kernel(
+    const __nv_bfloat16* __restrict__ h, int R, int I, const int32_t* __restrict__ ids,
+    const int32_t* __restrict__ token_slot, const int32_t* __restrict__ offsets,
+    const int2* __restrict__ tile_plan, uint8_t* __restrict__ hq, uint8_t* __restrict__ h_sf,
+    uint8_t* __restrict__ sfb) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const int e = ids[token_slot[r]];
+  const int64_t base = sfb_row_base(r, offsets[e], tile_plan[e], I / kTileK);
+  const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(r) * I);
+  const int nblk = I / 32;
+  for (int b = lane; b < nblk; b += 32) {
+    uint4 q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = __ldg(hr + 4 * b + i);
+    uint8_t sbyte;
+    uint4 codes[2];
+    mx_quant_block(q, &sbyte, codes);
+    uint4* dst = reinterpret_cast<uint4*>(hq + static_cast<size_t>(r) * I + 32 * b);
+    dst[0] = codes[0];
+    dst[1] = codes[1];
+    h_sf[static_cast<size_t>(r) * nblk + b] = sbyte;
+    sfb[base + static_cast<int64_t>(b >> 2) * kSfbTileBytes + (b & 3)] = sbyte;
+  }
 }
 
 // Grid (T, ceil(H / 1024)): CTA (t, b) computes out[t, 1024 b .. 1024 b + 1023]
@@ -133,6 +167,17 @@ cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_sca
   const int blocks = (R + 7) / 8;
   return launch_pdl(hquant_kernel, dim3(blocks), dim3(256), 0, s,
                     static_cast<const __nv_bfloat16*>(h), R, I, hq, h_scale);
+}
+
+cudaError_t launch_hquant_mx(const void* h, int R, int I, const int32_t* ids,
+                             const int32_t* token_slot, const int32_t* offsets,
+                             const int2* tile_plan, uint8_t* hq, uint8_t* h_sf, uint8_t* sfb,
+                             cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const int blocks = (R + 7) / 8;
+  return launch_pdl(hquant_mx_kernel, dim3(blocks), dim3(256), 0, s,
+                    static_cast<const __nv_bfloat16*>(h), R, I, ids, token_slot, offsets,
+                    tile_plan, hq, h_sf, sfb);
 }
 
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,

@@ -62,19 +62,21 @@ class GpuRun:
         cfg = case.cfg
         self.case = case
         T, E, k, H, I = case.T, cfg.num_experts, cfg.top_k, cfg.hidden, cfg.inter
+        self.mode = mode = case.mode
         self.moe = moe or P.FusedMoE(case.w1.to(dev), case.w1_sf.to(dev), case.w2.to(dev),
-                                     case.w2_sf.to(dev), k)
+                                     case.w2_sf.to(dev), k, mode=mode)
         x = case.x.to(dev)
         logits = case.logits.to(dev)
         s = P.shape(T, E, k, H, I)
-        self.ws = torch.zeros(max(P.workspace_size(s), 256), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(max(P.workspace_size(s, mode), 256), dtype=torch.uint8,
+                              device=dev)
         self.out = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=dev)
         opts = P.options(tile_variant=variant)
         P.forward(s, x, logits, self.moe.w1_p, self.moe.w1_sf_p, self.moe.w2_p,
-                  self.moe.w2_sf_p, self.out, self.ws, opts=opts)
+                  self.moe.w2_sf_p, self.out, self.ws, mode=mode, opts=opts)
         torch.cuda.synchronize()
         self.status = P.read_device_status(self.ws)
-        self.L = P.workspace_layout(s)
+        self.L = P.workspace_layout(s, mode)
         self.T, self.E, self.k, self.H, self.I, self.R = T, E, k, H, I, T * k
 
     def _view(self, off, n, dtype):
@@ -118,6 +120,23 @@ class GpuRun:
     @property
     def x_scale(self):
         return self.floats("x_scale", self.R)
+
+    def bytes_(self, name, n):
+        return self._view(getattr(self.L, name), n, torch.uint8).numpy()
+
+    @property
+    def x_sf(self):
+        """MXFP8 mode: E8M0 block scales of xq, [R, H/32]."""
+        return self.bytes_("x_sf", self.R * self.H // 32).reshape(self.R, self.H // 32)
+
+    @property
+    def h_sf(self):
+        """MXFP8 mode: E8M0 block scales of hq, [R, I/32]."""
+        return self.bytes_("h_sf", self.R * self.I // 32).reshape(self.R, self.I // 32)
+
+    @property
+    def tile_plan(self):
+        return self.ints("tile_plan", 2 * self.E).reshape(self.E, 2)
 
     @property
     def h(self):

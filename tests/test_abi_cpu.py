@@ -67,6 +67,26 @@ def test_workspace_size_and_layout(lib):
     assert lay.max_tiles >= R // 32 + 256
 
 
+def test_workspace_layout_mxfp8(lib):
+    """W8A8 adds the E8M0 block-scale regions (row-major and per-tile); the
+    W4A8 layout gives them no bytes."""
+    T, E, k, H, I = 4096, 256, 8, 7168, 2048
+    s, R = _shape(T, E, k, H, I), T * k
+    l0, l2 = P.workspace_layout(s, 0), P.workspace_layout(s, 2)
+    assert l2.max_tiles == l0.max_tiles
+    sizes = [("tile_plan", E * 8), ("x_sf", R * H // 32), ("h_sf", R * I // 32),
+             ("x_sf_tiled", l2.max_tiles * (H // 128) * 1024),
+             ("h_sf_tiled", l2.max_tiles * (I // 128) * 1024)]
+    end = l2.out_stage
+    for name, size in sizes:
+        o = getattr(l2, name)
+        assert o % 256 == 0 and o >= end, name
+        end = o + size
+    assert end <= l2.total == P.workspace_size(s, 2)
+    assert l0.x_sf == l0.h_sf == l0.x_sf_tiled == l0.h_sf_tiled   # zero-size in W4A8
+    assert l0.total < l2.total
+
+
 @pytest.mark.parametrize("bad", [dict(T=-1), dict(E=0), dict(k=0), dict(k=9, E=8), dict(k=33, E=64),
                                  dict(H=100), dict(I=96), dict(E=2000)])
 def test_workspace_size_rejects_bad_shapes(lib, bad):
@@ -95,7 +115,7 @@ def test_forward_validation_without_gpu(lib):
     mis[2] += 32                                        # w1 not 256-byte aligned
     assert _fwd(lib, s, mis, need) == L.MOE_ERR_MISALIGNED
     assert _fwd(lib, s, good, need - 1) == L.MOE_ERR_WORKSPACE_TOO_SMALL
-    assert _fwd(lib, s, good, need, mode=2) == L.MOE_ERR_UNSUPPORTED
+    assert _fwd(lib, s, good, need, mode=1) == L.MOE_ERR_UNSUPPORTED   # W4A16 not built
     assert _fwd(lib, s, good, need, mode=5) == L.MOE_ERR_INVALID_ARG
     assert _fwd(lib, _shape(H=200), good, need) == L.MOE_ERR_MISALIGNED
     assert _fwd(lib, s, good, need, opts=P.options(tile_variant=99)) == L.MOE_ERR_INVALID_ARG
