@@ -112,7 +112,7 @@ void compute_layout(const moe_shape* s, int32_t mode, moe_ws_layout* L) {
   L->chunk_counts = take(chunks * E * 4);
   L->token_slot = take(R * 4);
   L->tiles = take(max_tiles * 16);
-  L->xq = take(R * H);
+  L->xq = take(R * H * (mode == MOE_W4A16_MXFP4_BF16 ? 2 : 1));   // bf16 copy in W4A16
   L->x_scale = take(R * 4);
   L->h = take(R * I * 2);
   L->hq = take(R * I);
@@ -176,7 +176,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-enum class MapKind { kFp4Weights, kBytes, kScaleBlocks };
+enum class MapKind { kFp4Weights, kBytes, kScaleBlocks, kPackedBytes, kBf16 };
 
 // 2-D tensor map over a row-major [rows, cols] matrix of `kind` elements;
 // box = box_cols x box_rows elements.
@@ -184,23 +184,27 @@ enum class MapKind { kFp4Weights, kBytes, kScaleBlocks };
 //                 lands as 16 bytes in shared memory), 128-byte swizzle
 //   kBytes:       uint8 (FP8 codes), 128-byte swizzle
 //   kScaleBlocks: uint32 words, no swizzle
+//   kPackedBytes: uint8, no swizzle (packed E2M1 rows copied as they are)
+//   kBf16:        bf16 activations, 128-byte swizzle (64-element boxes)
 int32_t make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, MapKind kind,
                   uint32_t box_cols, uint32_t box_rows) {
   if (!base) return fail(MOE_ERR_INVALID_ARG, "refusing to encode a tensor map for NULL");
   auto fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const bool fp4 = kind == MapKind::kFp4Weights, words = kind == MapKind::kScaleBlocks;
+  const bool bf16 = kind == MapKind::kBf16, plain = words || kind == MapKind::kPackedBytes;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {fp4 ? cols / 2 : words ? cols * 4 : cols};
+  const cuuint64_t strides[1] = {fp4 ? cols / 2 : words ? cols * 4 : bf16 ? cols * 2 : cols};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m,
                   fp4     ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
                   : words ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                  : bf16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                           : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                   2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  words ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  plain ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) rows=%llu cols=%llu kind=%d",
@@ -240,8 +244,6 @@ int32_t check_forward_args(const moe_shape* shape, int32_t mode, const void* x,
   int32_t st = check_shape(shape, mode);
   if (st != MOE_OK) return st;
   if ((st = check_options(opts)) != MOE_OK) return st;
-  if (mode == MOE_W4A16_MXFP4_BF16)
-    return fail(MOE_ERR_UNSUPPORTED, "quant_mode %d is not implemented in this build", mode);
   if (shape->num_tokens == 0) return MOE_OK;
   if (!x || !logits || !w1 || !w1_sf || !w2 || !w2_sf || !out || !ws)
     return fail(MOE_ERR_INVALID_ARG, "a required pointer is NULL");
@@ -274,8 +276,9 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   const bool mx = mode == MOE_W8A8_MXFP8;
   const int T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden, I = s->inter;
   const int R = T * k;
+  const bool w4a16 = mode == MOE_W4A16_MXFP4_BF16;
   const int variant = pick_variant(s, opts);
-  const int bn = moe::gemm_tile_tokens(variant);
+  const int bn = w4a16 ? moe::kW4A16BN : moe::gemm_tile_tokens(variant);
   const int prefetch = !opts || opts->prefetch_stages == 0 ? kDefaultPrefetchStages
                        : opts->prefetch_stages < 0 ? 0 : opts->prefetch_stages;
   const uint64_t timeout_ns =
@@ -305,17 +308,24 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   // scales: one 512-byte block per box
   const uint64_t w1_boxes = static_cast<uint64_t>(E) * (2 * I / 128) * (H / 128);
   const uint64_t w2_boxes = static_cast<uint64_t>(E) * (H / 128) * (I / 128);
-  const MapKind wkind = mx ? MapKind::kBytes : MapKind::kFp4Weights;
+  // W4A16: packed code rows (64 bytes) as they are, for the in-kernel
+  // conversion to bf16
+  const MapKind wkind = mx ? MapKind::kBytes : w4a16 ? MapKind::kPackedBytes : MapKind::kFp4Weights;
+  const uint32_t wcols = w4a16 ? 64 : 128;
   const uint32_t w_tx = mx ? 128u * 128u : kWeightBoxTxBytes;
-  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, 128, wkind, 128, 128)) != MOE_OK ||
-      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, 128, wkind, 128, 128)) != MOE_OK ||
+  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, wcols, wkind, wcols, 128)) != MOE_OK ||
+      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, wcols, wkind, wcols, 128)) != MOE_OK ||
       (rc = make_tmap(&tm_sf1, w1_sf, w1_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK ||
       (rc = make_tmap(&tm_sf2, w2_sf, w2_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK)
     return rc;
   for (int i = 0; i < moe::kNumXMaps; ++i) {
     const uint32_t rows = static_cast<uint32_t>(moe::kXBoxRowsAt(i));
-    if ((rc = make_tmap(&tm_x[i], xq, R, H, MapKind::kBytes, 128, rows)) != MOE_OK ||
-        (rc = make_tmap(&tm_h[i], hq, R, I, MapKind::kBytes, 128, rows)) != MOE_OK)
+    // W4A16: bf16 activations (the expanded copy of x, and h itself) in
+    // 64-element (128-byte) boxes
+    if ((rc = w4a16 ? make_tmap(&tm_x[i], xq, R, H, MapKind::kBf16, 64, rows)
+                    : make_tmap(&tm_x[i], xq, R, H, MapKind::kBytes, 128, rows)) != MOE_OK ||
+        (rc = w4a16 ? make_tmap(&tm_h[i], h, R, I, MapKind::kBf16, 64, rows)
+                    : make_tmap(&tm_h[i], hq, R, I, MapKind::kBytes, 128, rows)) != MOE_OK)
       return rc;
   }
 
@@ -328,7 +338,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
   MOE_CUDA(mark());
-  const moe::QuantOut qx{xq, x_scale, mx, x_sf, sfb1};
+  const moe::QuantOut qx{xq, x_scale, mx, x_sf, sfb1, w4a16};
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* token_slot = at<int32_t>(ws, L.token_slot);
   if (T <= moe::kSmallT) {
@@ -351,9 +361,11 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
                    mx ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, dev.num_sms,
                    prefetch, mx, sfb1};
-  MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
+  MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(true, g1, st) : moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
-  if (mx)
+  if (w4a16) {
+    // GEMM2 reads h (bf16) directly: nothing to quantise
+  } else if (mx)
     MOE_CUDA(moe::launch_hquant_mx(h, R, I, ids, token_slot, offsets, tile_plan, hq, h_sf, sfb2,
                                    st));
   else
@@ -362,7 +374,8 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
                    mx ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, dev.num_sms,
                    prefetch, mx, sfb2};
-  MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
+  MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(false, g2, st)
+                 : moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));
   MOE_CUDA(mark());
@@ -420,9 +433,6 @@ int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode, const vo
                             void* w1_sf_p, void* w2_p, void* w2_sf_p, void* stream) {
   int32_t st = check_shape(shape, quant_mode);
   if (st != MOE_OK) return st;
-  if (quant_mode == MOE_W4A16_MXFP4_BF16)
-    return fail(MOE_ERR_UNSUPPORTED, "quant_mode %d is not implemented in this build",
-                quant_mode);
   const bool fp8 = quant_mode == MOE_W8A8_MXFP8;
   const void* ins[4] = {w1, w1_sf, w2, w2_sf};
   const void* outs[4] = {w1_p, w1_sf_p, w2_p, w2_sf_p};

@@ -45,22 +45,13 @@
 //   GEMM2: acc * s_h[row] -> bf16 y[row, c].
 #include <cuda_bf16.h>
 
+#include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 
 namespace moe {
 
 namespace {
-
-// Activation tensor maps with box heights 16, 32, 64, ..., 224 rows: a tile
-// loads the smallest box covering its MMA-N rows in one copy.
-struct XMaps {
-  CUtensorMap m[kNumXMaps];
-};
-
-__device__ __forceinline__ int x_map_for(int rows) {
-  return rows <= 16 ? 0 : (rows + 31) / 32;
-}
 
 template <int BN, int STAGES, int NI, int NB, bool MX8>
 struct GemmCfg {
@@ -91,7 +82,6 @@ struct GemmCfg {
   // (a * NI + i) * BN); 4 columns of weight scales per stage; activation
   // scales: 8 columns of constants (W4A8, up to 256 tokens) or 8 columns per
   // stage (MXFP8).
-  static constexpr int kEpiWarps = 8;               // two per TMEM lane quarter
   static constexpr int kThreads = 32 * (NI + 1 + kEpiWarps);   // producer, issuers, epilogue
   static constexpr int kColSFA = NB * NI * BN;
   static constexpr int kColSFB = kColSFA + 4 * STAGES;
@@ -145,7 +135,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
     }
     for (int a = 0; a < NB; ++a) {
       mbar_init(tfull + a, ni);   // every issuer commits its share of an item
-      mbar_init(tempty + a, C::kEpiWarps);   // every epilogue warp releases the buffer
+      mbar_init(tempty + a, kEpiWarps);   // every epilogue warp releases the buffer
     }
     for (int j = 0; j < NI; ++j) mbar_init(drain + j, 1);
     mbar_init(drain + NI, 1);   // constant-scale copy done
@@ -345,69 +335,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Eight warps: warp w reads TMEM lanes 32 * (w % 4) .. +31 (the only
-    // quarter it may access), and the two warps of each quarter split the
-    // item's 16-column chunks between them.
-    const int q = warp & 3;
-    const int half = (warp - (NI + 1)) >> 2;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-      const int tile = item / MT, mt = item % MT;
-      const int4 td = tiles[tile];
-      const int row0 = td.y, ntok = td.z, nchunks = (td.z + 15) >> 4;
-      const int split = (nchunks + 1) >> 1;
-      const int ch_begin = half == 0 ? 0 : split, ch_end = half == 0 ? split : nchunks;
-      if (!mbar_wait(tfull + acc, acc_phase, timeout_ns, status, kDevTimeout, abort_flag)) break;
-      tc_fence_after();
-      const uint32_t tbase =
-          tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * NI * BN);
-      for (int ch = ch_begin; ch < ch_end; ++ch) {
-        const int c0 = ch * 16;
-        // one row-scale load per chunk: lane j (and j + 16) holds column c0 + j
-        const int nl = c0 + (lane & 15);
-        const float sc = nl < ntok ? (row_scale ? __ldg(row_scale + row0 + nl) : 1.f) : 0.f;
-        float v[16];
-        tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
-        for (int p = 1; p < ni; ++p) {   // partial sums of the other issuers
-          float w[16];
-          tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(p * BN + c0), w);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] += w[j];
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] *= __shfl_sync(0xffffffffu, sc, j);
-        if constexpr (SWIGLU) {
-          const bool lo = lane < 16;
-          const int f = 64 * mt + 16 * q + (lane & 15);
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const float send = lo ? v[2 * jj + 1] : v[2 * jj];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float g = lo ? v[2 * jj] : recv;
-            const float u = lo ? recv : v[2 * jj + 1];
-            const float hval = g / (1.0f + expf(-g)) * u;
-            const int n = c0 + 2 * jj + (lo ? 0 : 1);
-            if (n < ntok)
-              out[static_cast<int64_t>(row0 + n) * out_ld + f] = __float2bfloat16_rn(hval);
-          }
-        } else {
-          const int c = mt * kTileM + 32 * q + lane;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = c0 + j;
-            if (n < ntok) out[static_cast<int64_t>(row0 + n) * out_ld + c] = __float2bfloat16_rn(v[j]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty + acc);
-      if (++acc == NB) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
+    epilogue_loop<BN, NI, NB, SWIGLU>(NI + 1, ni, tiles, num_items, MT, tfull, tempty, tmem,
+                                       row_scale, out, out_ld, timeout_ns, status, abort_flag);
   }
 
   tc_fence_before();

@@ -1,0 +1,340 @@
+// gemm_bf16.cu -- the grouped GEMM of the W4A16 mode: MXFP4 weights x bf16
+// activations on the sm_103a tensor cores (tcgen05 .kind::f16, TMEM
+// accumulators).
+//
+// Pages cited (title and section):
+//   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add
+//           MXFP4xFP8 CUTLASS MoE backend for SM90": title and Description
+//           (the MXFP4 x BF16 MoE GEMM: bf16 activations fed unquantised,
+//           MXFP4 weights dequantised inside the kernel).
+//
+// The tensor cores have no mixed FP4 x BF16 MMA, so the weights are
+// converted in shared memory: a weight box (128 rows x 128 K, packed E2M1
+// codes, 64 bytes per row) and its E8M0 scales land in a raw slot, four
+// transform warps rewrite it as bf16 values
+// e2m1 * 2^(scale - 127) -- exact in bf16 (a product of two powers of two
+// times at most two significant bits) -- into a converted slot (two 128 B x
+// 128-row K atoms, 128-byte swizzle), and the MMA reads the converted slot
+// and the bf16 activation box.  Everything else (tile list, swap-AB
+// orientation, persistent static striding, epilogue) is the FP8 GEMM's.
+//
+// Roles: warp 0 = TMA producers (lane s < S: weight box + scales into raw
+// slot s; lane S + s: activation box into activation slot s); warp 1 = MMA
+// issuer (warp-uniform, one elected lane issues); warps 2..5 = transform;
+// warps 6..13 = epilogue.
+#include <cuda_bf16.h>
+
+#include "gemm_common.cuh"
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTransformWarps = 4;
+
+template <int BN, int S, int Q>
+struct Bf16Cfg {
+  static_assert(BN % 16 == 0 && BN <= 128, "token tile of the W4A16 GEMM: 16..128 rows");
+  static_assert(2 * S <= 32, "producer lanes must fit one warp");
+  static constexpr int kRawBytes = kTileM * 64;      // packed E2M1 box
+  static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes
+  static constexpr int kBAtom = BN * 128;            // 64 bf16 of K per row
+  static constexpr int kBBytes = 2 * kBAtom;         // 128 K per stage
+  static constexpr int kCvAtom = kTileM * 128;
+  static constexpr int kCvBytes = 2 * kCvAtom;       // 128 x 128 bf16
+  static constexpr int kOffRaw = 0;
+  static constexpr int kOffB = kOffRaw + S * kRawBytes;
+  static constexpr int kOffCv = kOffB + S * kBBytes;
+  static constexpr int kOffSF = kOffCv + Q * kCvBytes;
+  static constexpr int kNumBars = 4 * S + 2 * Q + 2 * 2 + 1;
+  static constexpr int kOffBar = kOffSF + S * kSFBytes;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+  static constexpr int kFirstEpiWarp = 2 + kTransformWarps;
+  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+  static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 256;
+};
+
+// Instruction descriptor of .kind::f16 with bf16 A and B, fp32 accumulate,
+// M = 128, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_f16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Value of each E2M1 code (sign, 2-bit exponent with bias 1, 1-bit
+// mantissa; OCP MX v1.0), as a float.
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  const uint32_t mag = code & 7u;
+  // magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 = (2 + m) * 2^(e - 2) for e > 0,
+  // m * 0.5 for e = 0
+  const uint32_t e = mag >> 1, m = mag & 1u;
+  const float v = e == 0 ? 0.5f * static_cast<float>(m)
+                         : static_cast<float>(2u + m) * __uint_as_float((125u + e) << 23);
+  return (code & 8u) ? -v : v;
+}
+
+template <int BN, int S, int Q, bool SWIGLU>
+__global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
+    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                             const __grid_constant__ XMaps tmap_x,
+                             const __grid_constant__ CUtensorMap tmap_sf,
+                             const int4* __restrict__ tiles,
+                             const int32_t* __restrict__ num_tiles_p,
+                             __nv_bfloat16* __restrict__ out, int m_per_expert, int K,
+                             int out_ld, int32_t* __restrict__ status, uint64_t timeout_ns) {
+  using C = Bf16Cfg<BN, S, Q>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* raw_empty = raw_full + S;
+  uint64_t* b_full = raw_empty + S;
+  uint64_t* b_empty = b_full + S;
+  uint64_t* cv_full = b_empty + S;
+  uint64_t* cv_empty = cv_full + Q;
+  uint64_t* tfull = cv_empty + Q;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int MT = m_per_expert / kTileM, KS = K / kTileK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(raw_full + s, 1);
+      mbar_init(raw_empty + s, kTransformWarps);   // every transform warp has read it
+      mbar_init(b_full + s, 1);
+      mbar_init(b_empty + s, 1);
+    }
+    for (int q = 0; q < Q; ++q) {
+      mbar_init(cv_full + q, kTransformWarps);
+      mbar_init(cv_empty + q, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull + a, 1);
+      mbar_init(tempty + a, kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_sf);
+    for (int i = 0; i < kNumXMaps; ++i) prefetch_tmap(&tmap_x.m[i]);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int num_items = *num_tiles_p * MT;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane < 2 * S) {
+      const bool is_w = lane < S;
+      const int s = is_w ? lane : lane - S;
+      uint32_t phase = 0;
+      bool issued = false;
+      int ks = s % KS, item = blockIdx.x + (s / KS) * gridDim.x;
+      uint64_t* full = is_w ? raw_full + s : b_full + s;
+      uint64_t* empty = is_w ? raw_empty + s : b_empty + s;
+      while (item < num_items) {
+        const int mt = item % MT;
+        const int4 td = tiles[item / MT];
+        if (!mbar_wait(empty, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag)) break;
+        if (is_w) {
+          const int64_t blk = (static_cast<int64_t>(td.x) * MT + mt) * KS + ks;
+          mbar_arrive_expect_tx(full, 128u * 128u / 2u + 512u);
+          tma_load_2d(smem + C::kOffRaw + s * C::kRawBytes, &tmap_w, 0,
+                      static_cast<int32_t>(blk * kTileM), full);
+          tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0, static_cast<int32_t>(blk),
+                      full);
+        } else {
+          // two 64-element K atoms of the smallest box covering the MMA-N rows
+          const int nmma = (td.z + 15) & ~15;
+          const int xm = x_map_for(nmma);
+          mbar_arrive_expect_tx(full, 2u * static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u);
+          uint8_t* dst = smem + C::kOffB + s * C::kBBytes;
+          tma_load_2d(dst, &tmap_x.m[xm], ks * kTileK, td.y, full);
+          tma_load_2d(dst + C::kBAtom, &tmap_x.m[xm], ks * kTileK + 64, td.y, full);
+        }
+        issued = true;
+        phase ^= 1u;
+        ks += S;
+        while (ks >= KS) {
+          ks -= KS;
+          item += gridDim.x;
+        }
+      }
+      if (issued) {
+        int32_t none = 0;
+        mbar_wait(full, phase ^ 1u, timeout_ns, status, kDevTimeout, &none);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint64_t cdesc0 = smem_desc(smem_u32(smem + C::kOffCv), 0, 1024, 2);
+    const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
+    int s = 0, q = 0, ks = 0, it = 0;
+    uint32_t ps = 0, pq = 0;
+    bool new_item = true;
+    uint32_t d_tmem = 0, id = 0;
+    int acc = 0;
+    while (blockIdx.x + it * static_cast<int>(gridDim.x) < num_items) {
+      if (new_item) {
+        const int item = blockIdx.x + it * gridDim.x;
+        id = idesc_bf16(static_cast<uint32_t>((tiles[item / MT].z + 15) & ~15));
+        acc = it & 1;
+        if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it >> 1) & 1) ^ 1u, timeout_ns,
+                            status, kDevTimeout, abort_flag))
+          break;
+        tc_fence_after();
+        d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+      }
+      if (!mbar_wait_warp(cv_full + q, pq, timeout_ns, status, kDevTimeout, abort_flag)) break;
+      if (!mbar_wait_warp(b_full + s, ps, timeout_ns, status, kDevTimeout, abort_flag)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const uint64_t ad = cdesc0 + static_cast<uint64_t>((q * C::kCvBytes + a * C::kCvAtom) >> 4);
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>((s * C::kBBytes + a * C::kBAtom) >> 4);
+#pragma unroll
+        for (uint32_t kk = 0; kk < 4; ++kk)   // K = 16 bf16 = 32 bytes per MMA
+          tc_mma_f16_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id,
+                          (!new_item || a > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit_warp(cv_empty + q);
+      tc_commit_warp(b_empty + s);
+      if (++s == S) {
+        s = 0;
+        ps ^= 1u;
+      }
+      if (++q == Q) {
+        q = 0;
+        pq ^= 1u;
+      }
+      new_item = false;
+      if (++ks == KS) {
+        ks = 0;
+        ++it;
+        new_item = true;
+        tc_commit_warp(tfull + acc);
+      }
+    }
+    tc_commit_warp(drain);
+    int32_t none = 0;
+    mbar_wait_warp(drain, 0, timeout_ns, status, kDevTimeout, &none);
+  } else if (warp < C::kFirstEpiWarp) {
+    // ------------------------------------------------------------ transform
+    // 128 threads convert a fill's 512 16-byte units of packed codes: unit v
+    // = row v / 4, K-block p = v % 4 (32 codes, one scale byte) -> 32 bf16
+    // = four 16-byte units of the converted slot (K atom p / 2, units
+    // 4 (p % 2) .. +3 of the row, 128-byte swizzled).  Consecutive threads
+    // read consecutive units, so the reads are conflict-free.
+    const int t = threadIdx.x - 64;
+    int total_fills = 0;
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x) total_fills += KS;
+    for (int f = 0; f < total_fills; ++f) {
+      const int s = f % S, q = f % Q;
+      if (!mbar_wait(raw_full + s, static_cast<uint32_t>((f / S) & 1), timeout_ns, status,
+                     kDevTimeout, abort_flag))
+        break;
+      if (!mbar_wait(cv_empty + q, static_cast<uint32_t>((f / Q) & 1) ^ 1u, timeout_ns, status,
+                     kDevTimeout, abort_flag))
+        break;
+      const uint8_t* raw = smem + C::kOffRaw + s * C::kRawBytes;
+      const uint8_t* sf = smem + C::kOffSF + s * C::kSFBytes;
+      uint8_t* cv = smem + C::kOffCv + q * C::kCvBytes;
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        const int v = pass * 128 + t, r = v >> 2, p = v & 3;
+        const uint4 codes = *reinterpret_cast<const uint4*>(raw + 16 * v);
+        // scale 2^(byte - 127) of K-block p; byte 0 -> 2^-127 (subnormal),
+        // byte 255 (NaN) -> NaN
+        const uint32_t sb = sf[16 * (r & 31) + 4 * (r >> 5) + p];
+        const float scale = sb == 0 ? __uint_as_float(0x00400000u)
+                            : sb == 255 ? __uint_as_float(0x7FC00000u)
+                                        : __uint_as_float(sb << 23);
+        const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+        uint8_t* dst = cv + (p >> 1) * C::kCvAtom + r * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // 8 codes (4 bytes) -> 8 bf16 -> one 16-byte unit
+          uint32_t w[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t byte = (cw[j] >> (8 * b)) & 0xFFu;
+            const float lo = e2m1_value(byte & 0xFu) * scale;   // even k: low nibble
+            const float hi = e2m1_value(byte >> 4) * scale;
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+            w[b] = *reinterpret_cast<const uint32_t*>(&pr);
+          }
+          const int u = 4 * (p & 1) + j;
+          *reinterpret_cast<uint4*>(dst + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();   // generic-proxy writes -> the MMA's async proxy
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(cv_full + q);
+        mbar_arrive(raw_empty + s);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    epilogue_loop<BN, 1, 2, SWIGLU>(C::kFirstEpiWarp, 1, tiles, num_items, MT, tfull, tempty,
+                                    tmem, nullptr, out, out_ld, timeout_ns, status, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int BN, int S, int Q, bool SWIGLU>
+cudaError_t launch_bf16_variant(const GemmArgs& a, cudaStream_t s) {
+  using C = Bf16Cfg<BN, S, Q>;
+  auto kern = grouped_gemm_bf16_kernel<BN, S, Q, SWIGLU>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  XMaps xm;
+  for (int i = 0; i < kNumXMaps; ++i) xm.m[i] = a.tmap_x[i];
+  return launch_pdl(kern, dim3(a.num_sms), dim3(C::kThreads), C::kSmemBytes, s, *a.tmap_w, xm,
+                    *a.tmap_sf, a.tiles, a.num_tiles, static_cast<__nv_bfloat16*>(a.out),
+                    a.m_per_expert, a.k, a.out_ld, a.status, a.timeout_ns);
+}
+
+}  // namespace
+
+// W4A16: 64-token tiles, 6 raw/activation slots, 2 converted slots.
+cudaError_t launch_gemm_bf16(bool swiglu, const GemmArgs& a, cudaStream_t s) {
+  return swiglu ? launch_bf16_variant<kW4A16BN, 6, 2, true>(a, s)
+                : launch_bf16_variant<kW4A16BN, 6, 2, false>(a, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,118 @@
+// gemm_common.cuh -- pieces shared by the grouped GEMM kernels (gemm.cu:
+// block-scaled FP8 operands; gemm_bf16.cu: the W4A16 mode): the activation
+// tensor-map set and the TMEM -> registers -> global epilogue.
+//
+// Pages cited (title and section):
+//   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add
+//           MXFP4xFP8 CUTLASS MoE backend for SM90": Implementation Notes
+//           (the activation token scale is applied in the epilogue).
+//   [P4793] flashinfer PR #4793, "Unify MoE CuTe DSL dispatch to be dtype
+//           agnostic": walkthrough (grouped GEMM with activation (SwiGLU)
+//           fusion).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+// Activation tensor maps with box heights 16, 32, 64, ..., 224 rows: a tile
+// loads the smallest box covering its MMA-N rows in one copy.
+struct XMaps {
+  CUtensorMap m[kNumXMaps];
+};
+
+__device__ __forceinline__ int x_map_for(int rows) {
+  return rows <= 16 ? 0 : (rows + 31) / 32;
+}
+
+// Number of epilogue warps: two per TMEM lane quarter.
+constexpr int kEpiWarps = 8;
+
+// The epilogue of a persistent grouped GEMM whose TMEM holds, per
+// accumulator buffer a, NI partial accumulators of BN fp32 columns (issuer
+// i's at column (a * NI + i) * BN; ni of them in use), row m = weight row
+// (output feature) m of the item's 128-row M-tile, column n = the tile's
+// n-th token.  Warps first_warp .. first_warp + 7: warp w reads TMEM lanes
+// 32 * (w % 4) .. +31 (the only quarter it may access); the two warps of a
+// quarter split the item's 16-column chunks.  Each chunk: sum the partials,
+// multiply column n by row_scale[row0 + n] (1 when row_scale is null), then
+//   SWIGLU: tile rows 32q + i (gate) and 32q + 16 + i (up) of feature
+//     64 mt + 16q + i sit in lanes i and i + 16 of one warp; one shuffle
+//     pairs them, h = silu(g) * u -> bf16 out[row, feature];
+//   else:   bf16 out[row, 128 mt + 32q + lane].
+// Releases the accumulator buffer (tempty) after reading it.
+template <int BN, int NI, int NB, bool SWIGLU>
+__device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4* __restrict__ tiles,
+                                              int num_items, int MT, uint64_t* tfull,
+                                              uint64_t* tempty, uint32_t tmem,
+                                              const float* __restrict__ row_scale,
+                                              __nv_bfloat16* __restrict__ out, int out_ld,
+                                              uint64_t timeout_ns, int32_t* status,
+                                              volatile int32_t* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;
+  const int half = (warp - first_warp) >> 2;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+    const int tile = item / MT, mt = item % MT;
+    const int4 td = tiles[tile];
+    const int row0 = td.y, ntok = td.z, nchunks = (td.z + 15) >> 4;
+    const int split = (nchunks + 1) >> 1;
+    const int ch_begin = half == 0 ? 0 : split, ch_end = half == 0 ? split : nchunks;
+    if (!mbar_wait(tfull + acc, acc_phase, timeout_ns, status, kDevTimeout, abort_flag)) break;
+    tc_fence_after();
+    const uint32_t tbase =
+        tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * NI * BN);
+    for (int ch = ch_begin; ch < ch_end; ++ch) {
+      const int c0 = ch * 16;
+      // one row-scale load per chunk: lane j (and j + 16) holds column c0 + j
+      const int nl = c0 + (lane & 15);
+      const float sc = nl < ntok ? (row_scale ? __ldg(row_scale + row0 + nl) : 1.f) : 0.f;
+      float v[16];
+      tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(c0), v);
+      for (int p = 1; p < ni; ++p) {   // partial sums of the other issuers
+        float w[16];
+        tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(p * BN + c0), w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] += w[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] *= __shfl_sync(0xffffffffu, sc, j);
+      if constexpr (SWIGLU) {
+        const bool lo = lane < 16;
+        const int f = 64 * mt + 16 * q + (lane & 15);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const float send = lo ? v[2 * jj + 1] : v[2 * jj];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+          const float g = lo ? v[2 * jj] : recv;
+          const float u = lo ? recv : v[2 * jj + 1];
+          const float hval = g / (1.0f + expf(-g)) * u;
+          const int n = c0 + 2 * jj + (lo ? 0 : 1);
+          if (n < ntok)
+            out[static_cast<int64_t>(row0 + n) * out_ld + f] = __float2bfloat16_rn(hval);
+        }
+      } else {
+        const int c = mt * kTileM + 32 * q + lane;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int n = c0 + j;
+          if (n < ntok) out[static_cast<int64_t>(row0 + n) * out_ld + c] = __float2bfloat16_rn(v[j]);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty + acc);
+    if (++acc == NB) {
+      acc = 0;
+      acc_phase ^= 1u;
+    }
+  }
+}
+
+}  // namespace moe

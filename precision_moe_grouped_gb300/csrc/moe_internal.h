@@ -50,6 +50,7 @@ constexpr int kDecodeBN = 32;        // max tokens per tile, decode variant
 constexpr int kTinyBN = 16;          // max tokens per tile, 16-token decode variant
 constexpr int kPrefillBN = 224;      // max tokens per tile, prefill variant
 constexpr int kMidBN = 160;          // max tokens per tile, 6-stage prefill variant
+constexpr int kW4A16BN = 64;         // max tokens per tile of the W4A16 GEMM
 
 // Activation box heights (rows) of the GEMM's activation tensor maps:
 // 16, 32, 64, 96, ..., 224.
@@ -96,15 +97,17 @@ struct GemmArgs {
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
                          int32_t* chunk_counts, int32_t* status, cudaStream_t s);
-// Activation quantisation outputs of the expansion kernels.  W4A8: x_scale
-// (per-row float).  MXFP8 (mx8): x_sf (row-major scale bytes [R, H/32]) and
-// sfb (per-tile layout above).
+// Activation outputs of the expansion kernels, by mode.  W4A8: FP8 codes
+// xq and x_scale (per-row float).  MXFP8 (mx8): codes, x_sf (row-major scale
+// bytes [R, H/32]) and sfb (per-tile layout above).  W4A16 (bf16_copy): xq
+// receives the rows' bf16 values unchanged (2 bytes per element).
 struct QuantOut {
   uint8_t* xq;
   float* x_scale;
   bool mx8;
   uint8_t* x_sf;
   uint8_t* sfb;
+  bool bf16_copy;
 };
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
                                 int bn, int32_t* counts, int32_t* offsets, int4* tiles,
@@ -130,6 +133,10 @@ cudaError_t launch_hquant_mx(const void* h, int R, int I, const int32_t* ids,
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
                            int H, void* out, cudaStream_t s);
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);
+// The W4A16 GEMM (tiles of <= kW4A16BN tokens; tmap_w over the packed
+// weight boxes as bytes, tmap_x over bf16 activations with 64-element
+// boxes; row_scale, mx8 and sfb_tiled unused).
+cudaError_t launch_gemm_bf16(bool swiglu, const GemmArgs& a, cudaStream_t s);
 // Tile variants 1..kMaxTileVariant; the largest token tile of each (the tile
 // list is built with this bound).
 constexpr int kMaxTileVariant = 5;

@@ -317,8 +317,21 @@ __device__ void quantize_token_mx(const __nv_bfloat16* __restrict__ x, int t, in
   }
 }
 
-// One CTA per token: FP8 quantisation of the token into its k rows.
-template <bool MX>
+// W4A16: the token's bf16 row copied unchanged into its k expanded rows.
+__device__ void copy_token(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
+                           const int32_t* rows, __nv_bfloat16* __restrict__ xb) {
+  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+  const int nvec = H / 8;
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+    const uint4 v = __ldg(xr + i);
+    for (int j = 0; j < k; ++j)
+      reinterpret_cast<uint4*>(xb + static_cast<size_t>(rows[j]) * H)[i] = v;
+  }
+}
+
+// One CTA per token: FP8 quantisation of the token into its k rows
+// (MX: MXFP8; COPY: the bf16 copy of the W4A16 mode).
+template <bool MX, bool COPY = false>
 __global__ void __launch_bounds__(128) quant_scatter_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of,
     const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets,
@@ -340,7 +353,9 @@ __global__ void __launch_bounds__(128) quant_scatter_kernel(
     }
   }
   __syncthreads();
-  if (MX)
+  if (COPY)
+    copy_token(x, t, k, H, rows, reinterpret_cast<__nv_bfloat16*>(xq));
+  else if (MX)
     quantize_token_mx(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
   else
     quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(128) quant_scatter_kernel(
 // quantises its token into them.  CTA 0 also writes counts, offsets and the
 // GEMM tile list.  The redundant O(T*k) counting per CTA is cheap at these
 // sizes and removes three launches from the decode path.
-template <bool MX>
+template <bool MX, bool COPY = false>
 __global__ void __launch_bounds__(1024) expand_small_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids, int T, int E, int k,
     int H, int bn, int32_t* __restrict__ counts_out, int32_t* __restrict__ offsets_out,
@@ -411,7 +426,9 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
   const int2 pl = plan_tiles(e, E, c, off, bn, t == 0, tiles, num_tiles, tile_plan);
   if (MX && e < E) plan[e] = pl;
   __syncthreads();
-  if (MX) {
+  if (COPY) {
+    copy_token(x, t, k, H, rows, reinterpret_cast<__nv_bfloat16*>(xq));
+  } else if (MX) {
     if (e < k) sfb_base[e] = sfb_row_base(rows[e], cnt[my_e[e]], plan[my_e[e]], H / kTileK);
     __syncthreads();
     quantize_token_mx(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
@@ -453,7 +470,9 @@ cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, in
 cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, const int32_t* ids,
                                  const int32_t* offsets, const int2* tile_plan, int T, int k,
                                  int H, const QuantOut& q, cudaStream_t s) {
-  auto kern = q.mx8 ? quant_scatter_kernel<true> : quant_scatter_kernel<false>;
+  auto kern = q.bf16_copy ? quant_scatter_kernel<false, true>
+              : q.mx8     ? quant_scatter_kernel<true>
+                          : quant_scatter_kernel<false>;
   return launch_pdl(kern, dim3(T), dim3(128), 0, s, static_cast<const __nv_bfloat16*>(x), row_of,
                     ids, offsets, tile_plan, k, H, q.xq, q.x_scale, q.x_sf, q.sfb);
 }
@@ -464,7 +483,9 @@ cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E,
                                 int32_t* token_slot, const QuantOut& q, cudaStream_t s) {
   // plan int2[E], cnt[E], my_e/my_rank/rows [32] each
   const size_t smem = static_cast<size_t>(3 * E + 96) * sizeof(int32_t);
-  auto kern = q.mx8 ? expand_small_kernel<true> : expand_small_kernel<false>;
+  auto kern = q.bf16_copy ? expand_small_kernel<false, true>
+              : q.mx8     ? expand_small_kernel<true>
+                          : expand_small_kernel<false>;
   return launch_pdl(kern, dim3(T), dim3(1024), smem, s, static_cast<const __nv_bfloat16*>(x),
                     ids, T, E, k, H, bn, counts, offsets, tiles, num_tiles, tile_plan, row_of,
                     token_slot, q.xq, q.x_scale, q.x_sf, q.sfb);

@@ -115,7 +115,10 @@ def test_forward_validation_without_gpu(lib):
     mis[2] += 32                                        # w1 not 256-byte aligned
     assert _fwd(lib, s, mis, need) == L.MOE_ERR_MISALIGNED
     assert _fwd(lib, s, good, need - 1) == L.MOE_ERR_WORKSPACE_TOO_SMALL
-    assert _fwd(lib, s, good, need, mode=1) == L.MOE_ERR_UNSUPPORTED   # W4A16 not built
+    # W4A16 keeps bf16 expanded rows: the W4A8 workspace is too small for it
+    assert P.workspace_size(s, 1) > need
+    assert _fwd(lib, s, good, need, mode=1) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert _fwd(lib, s, good, need, mode=2) == L.MOE_ERR_WORKSPACE_TOO_SMALL
     assert _fwd(lib, s, good, need, mode=5) == L.MOE_ERR_INVALID_ARG
     assert _fwd(lib, _shape(H=200), good, need) == L.MOE_ERR_MISALIGNED
     assert _fwd(lib, s, good, need, opts=P.options(tile_variant=99)) == L.MOE_ERR_INVALID_ARG
@@ -136,7 +139,9 @@ def test_prepare_and_misc_validation_without_gpu(lib):
     alias = list(p)
     alias[4] = alias[0]
     assert lib.moe_prepare_weights(ctypes.byref(s), 0, *alias, None) == L.MOE_ERR_INVALID_ARG
-    assert lib.moe_prepare_weights(ctypes.byref(s), 1, *p, None) == L.MOE_ERR_UNSUPPORTED
+    for mode in (1, 2):   # W4A16 and W8A8 validate their arguments the same way
+        assert lib.moe_prepare_weights(ctypes.byref(s), mode, *alias, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_prepare_weights(ctypes.byref(s), 7, *p, None) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_selftest_timeout(None, 10, None) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_selftest_timeout(0x100000, 0, None) == L.MOE_ERR_INVALID_ARG
     st = ctypes.c_int32(0)

@@ -234,8 +234,8 @@ def test_invalid_args_on_device():
         P.forward(s, t, t.view(torch.float32), t, t, t, t, t, ws)
     assert ei.value.code == P._lib.MOE_ERR_WORKSPACE_TOO_SMALL
     with pytest.raises(P.MoeError) as ei:
-        P.forward(s, t, t.view(torch.float32), t, t, t, t, t, ws, mode=P.MOE_W4A16_MXFP4_BF16)
-    assert ei.value.code == P._lib.MOE_ERR_UNSUPPORTED
+        P.forward(s, t, t.view(torch.float32), t, t, t, t, t, ws, mode=7)
+    assert ei.value.code == P._lib.MOE_ERR_INVALID_ARG
 
 
 # ------------------------------------------------------------------ full sizes

@@ -1,0 +1,85 @@
+"""GPU parity of the W4A16 mode (MXFP4 weights x bf16 activations fed
+unquantised) against the CPU oracle on the same seeded inputs.
+
+Bit-exact: routing, expansion and the expanded bf16 activation rows (a
+copy).  Floating point (h, y, output): max|err| <= 2e-2 * max|ref| and
+sum|err| / sum|ref| <= 5e-3."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as MI
+import precision_moe_grouped_gb300 as P
+from oracle import moe as M
+
+from gpu_helpers import GpuRun, dump, max_err_ok, oracle_weights, x_bits
+
+pytestmark = pytest.mark.gpu
+
+W4A16 = MI.QUANT_W4A16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    P.load()
+
+
+def w16_parity(case, name="w16"):
+    assert case.mode == W4A16
+    run = GpuRun(case)
+    assert run.status == 0
+    fw = M.forward(x_bits(case), case.logits.cpu().numpy(), oracle_weights(case),
+                   case.cfg.top_k, mode=M.QUANT_W4A16)
+    rt = fw.routing
+    try:
+        np.testing.assert_array_equal(run.ids, rt.ids)
+        np.testing.assert_array_equal(run.offsets, rt.offsets)
+        np.testing.assert_array_equal(run.row_of, rt.row_of)
+        np.testing.assert_array_equal(run.token_slot // run.k, rt.token_of_row)
+        # the expanded activations are the tokens' bf16 rows, bit for bit
+        xb = run._view(run.L.xq, run.R * run.H, torch.int16).numpy().reshape(run.R, run.H)
+        np.testing.assert_array_equal(xb.view(np.uint16), x_bits(case)[rt.token_of_row])
+        for label, got, ref in (("h", run.h, fw.h), ("y", run.y, fw.y),
+                                ("out", run.out_np(), fw.out)):
+            ok, st = max_err_ok(got, ref)
+            assert ok, (label, st)
+    except AssertionError:
+        dump(name, h=run.h, h_ref=fw.h, y=run.y, y_ref=fw.y, out=run.out_np(), out_ref=fw.out,
+             tiles=run.tiles)
+        raise
+    return run, fw
+
+
+def _cfg(E, k, H, I):
+    return MI.custom_config(E, k, H, I, mode=W4A16, name="w16_custom")
+
+
+def test_w16_tiny():
+    w16_parity(MI.make_case(_cfg(8, 2, 256, 128), 16), name="w16_tiny")
+
+
+def test_w16_ragged_tiles():
+    """Several 64-token tiles per expert, ragged tails, several M-tiles and
+    K stages."""
+    run, _ = w16_parity(MI.make_case(_cfg(8, 2, 512, 256), 300, seed=7), name="w16_ragged")
+    assert run.tiles[:, 2].max() <= 64 and run.counts.max() > 64
+
+
+@pytest.mark.parametrize("E,k,T", [(1, 1, 5), (16, 16, 3), (32, 1, 7)])
+def test_w16_degenerate_routing(E, k, T):
+    w16_parity(MI.make_case(_cfg(E, k, 128, 128), T, seed=31 + T), name=f"w16_degen{E}_{k}")
+
+
+def test_w16_zero_rows():
+    case = MI.make_case(_cfg(8, 2, 256, 128), 24, seed=41)
+    case.x[3] = 0
+    case.x[5, 7] = -0.0
+    w16_parity(case, name="w16_zeros")
+
+
+def test_w16_config_full():
+    """The W4A16 workload in full: E=64, top-4, H=2048, I=1024, T=256."""
+    cfg = MI.CONFIGS["w4a16"]
+    w16_parity(MI.make_case(cfg, 256, device="cuda"), name="w16_config")
