@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--sweep-steps", type=int, default=30)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-modes", action="store_true",
+                    help="skip the W4A16 and MXFP8 workloads")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 decode, 2 prefill tiles")
     return ap.parse_args()
 
@@ -197,14 +199,16 @@ def alg_cost(stage: str, cfg, T: int, n_touched: int):
     return table[stage]
 
 
-def fused_roofline(cfg, T, n_touched, t_s, pk):
+def fused_roofline(cfg, T, n_touched, t_s, pk, mode=0):
     """Roofline of the whole forward: max(touched weight+scale + activation
-    bytes / HBM, FLOPs / FP8 tensor peak)."""
+    bytes / HBM, FLOPs / tensor peak of the MMA kind the mode runs: FP8 for
+    W4A8 (mxf8f6f4) and W8A8, bf16 for W4A16 (kind::f16))."""
     E, k, H, I = cfg.num_experts, cfg.top_k, cfg.hidden, cfg.inter
-    bytes_ = n_touched * 3 * I * H * (0.5 + 1 / 32) + T * H * 2 + T * E * 4 + T * H * 2
+    w_bytes = 1.0 if mode == 2 else 0.5          # E4M3 or packed E2M1 per weight
+    bytes_ = n_touched * 3 * I * H * (w_bytes + 1 / 32) + T * H * 2 + T * E * 4 + T * H * 2
     flops = 2.0 * T * k * 3 * I * H
     t_mem = bytes_ / (pk["hbm_gbs"] * 1e9)
-    t_tc = flops / (pk["bf16_tflops"] * FP8_OVER_BF16 * 1e12)
+    t_tc = flops / (pk["bf16_tflops"] * (1.0 if mode == 1 else FP8_OVER_BF16) * 1e12)
     return {"bytes": bytes_, "flops": flops, "t_hbm_us": t_mem * 1e6, "t_tensor_us": t_tc * 1e6,
             "bound": "hbm" if t_mem >= t_tc else "tensor",
             "frac": max(t_mem, t_tc) / t_s, "hbm_frac": t_mem / t_s, "tensor_frac": t_tc / t_s}
@@ -358,9 +362,76 @@ def run_ours(args, dist: Dist):
     if not args.no_sweep:
         result["sweep"] = sweep(args, cfg, moe, x, logits, dist, pk)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(cfg, T, x, logits, 1)
+        result["cpu_baseline"] = cpu_baseline(cfg, T, x, logits, 6)
+    if not args.no_other_modes:
+        del moe, ws, out, case
+        torch.cuda.empty_cache()
+        result["other_modes"] = other_modes(args, dist, pk)
     dist.done()
     return result
+
+
+def other_modes(args, dist, pk):
+    """The other quantisation modes on their own workloads (device-resident
+    inputs, CUDA events, 16 rotating token sets where the tokens allow):
+    W4A16 (MXFP4 x bf16) at E=64/top-4/H=2048/I=1024/T=256, and MXFP8 x MXFP8
+    with Zipf(1.2) routing skew at E=256/top-8/H=7168/I=2048/T=4096."""
+    import torch
+
+    import moe_inputs as MI
+    import precision_moe_grouped_gb300 as P
+    res = []
+    stream = torch.cuda.current_stream()
+    for name, T in (("w4a16", 256), ("mxfp8_zipf", 4096)):
+        cfg = MI.CONFIGS[name]
+        nsets = 16 if T <= 512 else 1
+        case = MI.make_case(cfg, T * nsets, device=f"cuda:{dist.local}")
+        moe = P.FusedMoE(case.w1, case.w1_sf, case.w2, case.w2_sf, cfg.top_k, mode=cfg.mode)
+        del case.w1, case.w1_sf, case.w2, case.w2_sf
+        sets = [(case.x[i * T:(i + 1) * T].contiguous(),
+                 case.logits[i * T:(i + 1) * T].contiguous()) for i in range(nsets)]
+        s = moe.shape(T)
+        ws = moe.workspace(T)
+        out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=case.x.device)
+
+        def fwd(i):
+            xs, ls = sets[i % nsets]
+            P.forward(s, xs, ls, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, out, ws,
+                      mode=cfg.mode)
+        lay = P.workspace_layout(s, cfg.mode)
+        touched, empty = [], []
+        for i in range(max(3, nsets)):
+            fwd(i)
+            torch.cuda.synchronize()
+            c = ws[lay.counts:lay.counts + 4 * cfg.num_experts].view(torch.int32)
+            touched.append(int((c > 0).sum().item()))
+            empty.append(int((c == 0).sum().item()))
+        status = P.read_device_status(ws)
+        dist.barrier()
+        steps = 20
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            fwd(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = dist.max(a.elapsed_time(b) / steps)
+        n_t = sum(touched) / len(touched)
+        fr = fused_roofline(cfg, T, n_t, ms / 1e3, pk, cfg.mode)
+        res.append({"workload": f"{name}: E={cfg.num_experts} top-{cfg.top_k} H={cfg.hidden} "
+                                f"I={cfg.inter} T={T}" + (f" zipf={cfg.zipf}" if cfg.zipf else ""),
+                    "mode": {0: "W4A8", 1: "W4A16", 2: "W8A8 (MXFP8)"}[cfg.mode],
+                    "ms": ms, "tokens_s": dist.world * T / (ms / 1e3),
+                    "tflops": fr["flops"] / (ms / 1e3) / 1e12, "experts_touched": n_t,
+                    "experts_empty": sum(empty) / len(empty), "roofline_frac": fr["frac"],
+                    "bound": fr["bound"], "hbm_frac": fr["hbm_frac"],
+                    "tensor_frac": fr["tensor_frac"],
+                    "tensor_peak": "bf16" if cfg.mode == 1 else "fp8 (2 x measured bf16)",
+                    "token_sets": nsets, "device_status": status})
+        del moe, ws, out, case, sets
+        torch.cuda.empty_cache()
+    return res
 
 
 def sweep(args, cfg, moe, x_all, lg_all, dist, pk):

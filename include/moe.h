@@ -102,9 +102,9 @@ typedef struct {
                             (caller-created): event 0 is recorded on `stream`
                             before the first kernel and event i right after
                             kernel i, so event pairs time each kernel      */
-  int32_t prefetch_stages; /* L2 prefetch distance of the GEMM weight stream in
-                            K stages (8 KB of packed weights each per SM):
-                            0 = default (off: measured slower), < 0 = off */
+  int32_t prefetch_stages; /* L2 prefetch distance of the GEMM weight stream,
+                            in K stages: 0 = default (8 for the prefill
+                            tiles, off for decode tiles), < 0 = off      */
   int32_t reserved[3];   /* must be zero                                     */
 } moe_options;
 

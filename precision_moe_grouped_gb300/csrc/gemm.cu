@@ -32,8 +32,9 @@
 //
 // Roles: warp 0 lanes 0..3*STAGES-1 = TMA producers (three per stage);
 // warps 1..NI = MMA issuers (one elected lane each; warp 1 also owns the TMEM
-// allocation); the last 8 warps = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31; two warps per lane quarter split the columns).  Two TMEM
+// allocation); the next 8 warps = epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. +31; two warps per lane quarter split the columns); the last
+// warp = optional L2 prefetcher.  Two TMEM
 // accumulator buffers let the epilogue of one item overlap the main loop of
 // the next.
 //
@@ -82,7 +83,8 @@ struct GemmCfg {
   // (a * NI + i) * BN); 4 columns of weight scales per stage; activation
   // scales: 8 columns of constants (W4A8, up to 256 tokens) or 8 columns per
   // stage (MXFP8).
-  static constexpr int kThreads = 32 * (NI + 1 + kEpiWarps);   // producer, issuers, epilogue
+  // producer, issuers, epilogue, L2 prefetcher
+  static constexpr int kThreads = 32 * (NI + 1 + kEpiWarps + 1);
   static constexpr int kColSFA = NB * NI * BN;
   static constexpr int kColSFB = kColSFA + 4 * STAGES;
   static constexpr int kColsUsed = kColSFB + (MX8 ? 8 * STAGES : 8);
@@ -104,7 +106,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
                         const float* __restrict__ row_scale, __nv_bfloat16* __restrict__ out,
                         int m_per_expert, int K, int out_ld, int32_t* __restrict__ status,
                         uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages,
-                        const uint8_t* __restrict__ sfb_tiled) {
+                        const uint8_t* __restrict__ sfb_tiled,
+                        const uint8_t* __restrict__ w_base) {
   using C = GemmCfg<BN, STAGES, NI, NB, MX8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -116,6 +119,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
   uint64_t* drain = tempty + NB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 4);
+  // last fill whose MMAs the first issuer has issued (paces the prefetcher)
+  volatile int32_t* progress = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MT = m_per_expert / kTileM, KS = K / kTileK;
@@ -140,6 +145,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
     for (int j = 0; j < NI; ++j) mbar_init(drain + j, 1);
     mbar_init(drain + NI, 1);   // constant-scale copy done
     *abort_flag = 0;
+    *progress = -1;
     fence_mbar_init();
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_sf);
@@ -204,19 +210,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
           mbar_arrive_expect_tx(full + s, a_tx_bytes);
           tma_load_2d(smem + C::kOffA + s * C::kABytes, &tmap_w, 0,
                       static_cast<int32_t>(blk * kTileM), full + s);
-          if (prefetch_stages > 0) {
-            // optional L2 prefetch of the weight box `prefetch_stages` fills ahead
-            int kp = ks + prefetch_stages, itp = item;
-            while (kp >= KS) {
-              kp -= KS;
-              itp += gridDim.x;
-            }
-            if (itp < num_items) {
-              const int64_t bp =
-                  (static_cast<int64_t>(tiles[itp / MT].x) * MT + itp % MT) * KS + kp;
-              tma_prefetch_l2_2d(&tmap_w, 0, static_cast<int32_t>(bp * kTileM));
-            }
-          }
         } else if (role == 1) {
           // smallest activation box that covers the tile's MMA-N rows
           const int nmma = (td.z + 15) & ~15;
@@ -276,7 +269,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
       const uint64_t sdesc0 = smem_desc(smem_u32(smem + C::kOffSF), 0, 128, 0);
       const uint64_t sbdesc0 = smem_desc(smem_u32(smem + C::kOffSFBs), 0, 128, 0);
       int stage = i % STAGES, ks = i % KS, it = i / KS;   // ni <= KS, so it == 0
-      int nmma = 16;
+      int nmma = 16, fidx = i;
       uint32_t phase = (i / STAGES) & 1;
       bool new_item = true;
       uint32_t d_tmem = 0, id0 = 0;
@@ -314,6 +307,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
           tc_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
                          sfb, (!new_item || kk > 0) ? 1u : 0u);
         tc_commit_warp(empty + stage);
+        if (i == 0 && lane == 0) *progress = fidx;
+        fidx += ni;
         stage += ni;
         if (stage >= STAGES) {
           stage -= STAGES;
@@ -335,8 +330,48 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    epilogue_loop<BN, NI, NB, SWIGLU>(NI + 1, ni, tiles, num_items, MT, tfull, tempty, tmem,
-                                       row_scale, out, out_ld, timeout_ns, status, abort_flag);
+    if (warp < NI + 1 + kEpiWarps) {
+      epilogue_loop<BN, NI, NB, SWIGLU>(NI + 1, ni, tiles, num_items, MT, tfull, tempty, tmem,
+                                         row_scale, out, out_ld, timeout_ns, status, abort_flag);
+    } else if (prefetch_stages > 0) {
+      // ---------------------------------------------------------- prefetcher
+      // Optional: asks L2 for the weight box of fill g while the first issuer
+      // has consumed fills up to g - prefetch_stages (plain prefetch
+      // instructions, 128 bytes per lane-instruction, outside the TMA
+      // unit), so that box's TMA load later hits L2.  It paces itself on a
+      // progress word the first issuer publishes -- no barrier -- and stops
+      // quietly when the pipeline does; a prefetch changes no result.
+      int total = 0;
+      for (int it2 = blockIdx.x; it2 < num_items; it2 += gridDim.x) total += KS;
+      int g = STAGES < total ? STAGES : total, kp = g % KS;
+      int itp = blockIdx.x + (g / KS) * static_cast<int>(gridDim.x);
+      int last_seen = -2;
+      uint64_t t_last = globaltimer_ns();
+      while (g < total) {
+        const int p = *progress;
+        if (g <= p + prefetch_stages) {
+          const int64_t bp = (static_cast<int64_t>(tiles[itp / MT].x) * MT + itp % MT) * KS + kp;
+          const uint8_t* box = w_base + bp * a_tx_bytes;
+          for (uint32_t off = static_cast<uint32_t>(lane) * 128u; off < a_tx_bytes;
+               off += 32u * 128u)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(box + off));
+          ++g;
+          if (++kp == KS) {
+            kp = 0;
+            itp += gridDim.x;
+          }
+          continue;
+        }
+        if (*abort_flag) break;
+        const uint64_t now = globaltimer_ns();
+        if (p != last_seen) {
+          last_seen = p;
+          t_last = now;
+        } else if (now - t_last > timeout_ns) {
+          break;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -363,7 +398,7 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
   return launch_pdl(kern, dim3(a.num_sms), dim3(C::kThreads), C::kSmemBytes, s, *a.tmap_w, xm,
                     *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
                     static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status,
-                    a.timeout_ns, a.a_tx_bytes, a.prefetch_stages, a.sfb_tiled);
+                    a.timeout_ns, a.a_tx_bytes, a.prefetch_stages, a.sfb_tiled, a.w_base);
 }
 
 }  // namespace

@@ -48,8 +48,9 @@ struct Bf16Cfg {
   static constexpr int kOffB = kOffRaw + S * kRawBytes;
   static constexpr int kOffCv = kOffB + S * kBBytes;
   static constexpr int kOffSF = kOffCv + Q * kCvBytes;
+  static constexpr int kOffLut = kOffSF + S * kSFBytes;   // 256 x bf16x2 (code byte -> pair)
   static constexpr int kNumBars = 4 * S + 2 * Q + 2 * 2 + 1;
-  static constexpr int kOffBar = kOffSF + S * kSFBytes;
+  static constexpr int kOffBar = kOffLut + 256 * 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
@@ -138,6 +139,11 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
     for (int i = 0; i < kNumXMaps; ++i) prefetch_tmap(&tmap_x.m[i]);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  // Code byte -> the bf16 pair (low nibble = even k) of its two E2M1 values.
+  for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+    const __nv_bfloat162 pr = __floats2bfloat162_rn(e2m1_value(b & 0xF), e2m1_value(b >> 4));
+    reinterpret_cast<__nv_bfloat162*>(smem + C::kOffLut)[b] = pr;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -248,8 +254,12 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
     // = row v / 4, K-block p = v % 4 (32 codes, one scale byte) -> 32 bf16
     // = four 16-byte units of the converted slot (K atom p / 2, units
     // 4 (p % 2) .. +3 of the row, 128-byte swizzled).  Consecutive threads
-    // read consecutive units, so the reads are conflict-free.
+    // read consecutive units, so the reads are conflict-free.  Each code
+    // byte becomes a bf16 pair through the shared table, then one bf16x2
+    // multiply applies the scale -- exact: a value with at most two
+    // significant bits times a power of two.
     const int t = threadIdx.x - 64;
+    const __nv_bfloat162* lut = reinterpret_cast<const __nv_bfloat162*>(smem + C::kOffLut);
     int total_fills = 0;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) total_fills += KS;
     for (int f = 0; f < total_fills; ++f) {
@@ -270,9 +280,13 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
         // scale 2^(byte - 127) of K-block p; byte 0 -> 2^-127 (subnormal),
         // byte 255 (NaN) -> NaN
         const uint32_t sb = sf[16 * (r & 31) + 4 * (r >> 5) + p];
-        const float scale = sb == 0 ? __uint_as_float(0x00400000u)
-                            : sb == 255 ? __uint_as_float(0x7FC00000u)
-                                        : __uint_as_float(sb << 23);
+        // 2^(sb - 127) as bf16: exponent field sb (sb = 0: the subnormal
+        // 2^-127; sb = 255: NaN)
+        const uint16_t sbits = sb == 0 ? 0x0040u : sb == 255 ? 0x7FC0u
+                                                           : static_cast<uint16_t>(sb << 7);
+        __nv_bfloat162 scale2;
+        scale2.x = __ushort_as_bfloat16(sbits);
+        scale2.y = scale2.x;
         const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
         uint8_t* dst = cv + (p >> 1) * C::kCvAtom + r * 128;
 #pragma unroll
@@ -280,10 +294,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
           uint32_t w[4];
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
-            const uint32_t byte = (cw[j] >> (8 * b)) & 0xFFu;
-            const float lo = e2m1_value(byte & 0xFu) * scale;   // even k: low nibble
-            const float hi = e2m1_value(byte >> 4) * scale;
-            const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+            const __nv_bfloat162 pr = __hmul2(lut[(cw[j] >> (8 * b)) & 0xFFu], scale2);
             w[b] = *reinterpret_cast<const uint32_t*>(&pr);
           }
           const int u = 4 * (p & 1) + j;

@@ -93,6 +93,7 @@ struct GemmArgs {
   int32_t prefetch_stages;     // L2 prefetch distance of weight tiles, in K stages
   bool mx8;                    // MXFP8 operands: E4M3 weights, per-32 activation scales
   const uint8_t* sfb_tiled;    // MXFP8: activation scales in the per-tile layout
+  const uint8_t* w_base;       // prepared weight boxes (for the optional L2 prefetcher)
 };
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
