@@ -157,9 +157,12 @@ def source_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
+GEMM_SOURCES = ["precision_moe_grouped_gb300/csrc/gemm.cu",
+                "precision_moe_grouped_gb300/csrc/gemm_common.cuh",
+                "precision_moe_grouped_gb300/csrc/ptx.cuh"]
 KERNEL_SOURCES = {
-    "gemm1": ["precision_moe_grouped_gb300/csrc/gemm.cu", "precision_moe_grouped_gb300/csrc/ptx.cuh"],
-    "gemm2": ["precision_moe_grouped_gb300/csrc/gemm.cu", "precision_moe_grouped_gb300/csrc/ptx.cuh"],
+    "gemm1": GEMM_SOURCES,
+    "gemm2": GEMM_SOURCES,
     "combine": ["precision_moe_grouped_gb300/csrc/rowops.cu"],
     "hquant": ["precision_moe_grouped_gb300/csrc/rowops.cu"],
     "quant_scatter": ["precision_moe_grouped_gb300/csrc/route.cu"],
