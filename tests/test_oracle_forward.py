@@ -80,9 +80,12 @@ def _to_np(case):
     return xbits, case.logits.numpy(), W
 
 
-def brute_force(case, top_k):
+def brute_force(case, top_k, mode=MI.QUANT_W4A8):
     """Every expert on every token, dense, then masked: an independent
-    formulation of the same forward (torch float64, ml_dtypes decoding)."""
+    formulation of the same forward (torch float64, ml_dtypes decoding), in
+    each quantisation mode: W4A8 (per-token FP8), W8A8 (MXFP8 blocks, exponent
+    from torch.frexp, codes from torch's E4M3 cast) and W4A16 (no activation
+    quantisation)."""
     ml = pytest.importorskip("ml_dtypes")
     x = case.x.to(torch.float32)
     L = case.logits.to(torch.float64)
@@ -104,35 +107,52 @@ def brute_force(case, top_k):
         q = (rows * inv[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn)
         return q.to(torch.float64), s
 
+    def quant_mx(rows):
+        blk = rows.to(torch.float64).reshape(rows.shape[0], -1, 32)
+        amax = blk.abs().amax(-1)
+        _, ex = torch.frexp(torch.where(amax > 0, amax, torch.ones_like(amax)))
+        e = torch.where(amax > 0, (ex - 1 - 8).clamp(-127, 127), torch.zeros_like(ex))
+        scale = torch.pow(2.0, e.to(torch.float64))[..., None]
+        q = (blk / scale).clamp(-448, 448).to(torch.float8_e4m3fn).to(torch.float64)
+        return (q * scale).reshape(rows.shape), torch.ones(rows.shape[0], dtype=torch.float64)
+
+    def no_quant(rows):
+        return rows.to(torch.float64), torch.ones(rows.shape[0], dtype=torch.float64)
+
     def dense(packed, sf):
-        pk = packed.numpy()
-        codes = np.empty(pk.shape[:-1] + (pk.shape[-1] * 2,), np.uint8)
-        codes[..., 0::2], codes[..., 1::2] = pk & 0xF, pk >> 4
-        v = codes.view(ml.float4_e2m1fn).astype(np.float64)
+        if mode == MI.QUANT_W8A8:
+            v = packed.numpy().view(ml.float8_e4m3fn).astype(np.float64)
+        else:
+            pk = packed.numpy()
+            codes = np.empty(pk.shape[:-1] + (pk.shape[-1] * 2,), np.uint8)
+            codes[..., 0::2], codes[..., 1::2] = pk & 0xF, pk >> 4
+            v = codes.view(ml.float4_e2m1fn).astype(np.float64)
         s = sf.numpy().view(ml.float8_e8m0fnu).astype(np.float64)
         return torch.from_numpy(v * np.repeat(s, 32, axis=-1))
 
+    quant = {MI.QUANT_W4A8: quant, MI.QUANT_W8A8: quant_mx, MI.QUANT_W4A16: no_quant}[mode]
     xd, xs = quant(x)
     I = case.cfg.inter
     out = torch.zeros(T, case.cfg.hidden, dtype=torch.float64)
     for e in range(E):
-        G = (xd @ dense(case.w1[e], case.w1_sf[e]).T).to(torch.float32) * xs[:, None]
+        G = (xd @ dense(case.w1[e], case.w1_sf[e]).T).to(torch.float32) * xs[:, None].to(torch.float32)
         g, u = G[:, :I], G[:, I:]
         h = (g / (1 + torch.exp(-g)) * u).to(torch.bfloat16).to(torch.float32)
         hd, hs = quant(h)
-        Y = (hd @ dense(case.w2[e], case.w2_sf[e]).T).to(torch.float32) * hs[:, None]
+        Y = (hd @ dense(case.w2[e], case.w2_sf[e]).T).to(torch.float32) * hs[:, None].to(torch.float32)
         out += wsel[:, e:e + 1] * Y.to(torch.float64)
     return out.to(torch.float32).to(torch.bfloat16).to(torch.float32).numpy(), sel
 
 
+@pytest.mark.parametrize("mode", [MI.QUANT_W4A8, MI.QUANT_W8A8, MI.QUANT_W4A16])
 @pytest.mark.parametrize("E,k,H,I,T", [(8, 2, 256, 128, 16), (6, 3, 128, 64, 40),
                                        (4, 4, 64, 32, 9), (16, 1, 128, 96, 23)])
-def test_forward_vs_brute_force(E, k, H, I, T):
-    cfg = MI.custom_config(E, k, H, I)
+def test_forward_vs_brute_force(E, k, H, I, T, mode):
+    cfg = MI.custom_config(E, k, H, I, mode=mode)
     case = MI.make_case(cfg, T, seed=100 + T)
-    ref, sel = brute_force(case, k)
+    ref, sel = brute_force(case, k, mode)
     xbits, logits, W = _to_np(case)
-    fw = M.forward(xbits, logits, W, k)
+    fw = M.forward(xbits, logits, W, k, mode=mode)
     np.testing.assert_array_equal(np.sort(fw.routing.ids, 1),
                                   np.sort(np.nonzero(sel.numpy())[1].reshape(T, k), 1))
     # equal up to the order of the final float64 sum (one bf16 ulp at most)

@@ -16,7 +16,7 @@ from oracle import moe as M
 
 def _pins_forward():
     TW.test_exact_swiglu_golden_case()
-    TW.test_forward_vs_brute_force(6, 3, 128, 64, 40)
+    TW.test_forward_vs_brute_force(6, 3, 128, 64, 40, M.QUANT_W4A8)
 
 
 def _expect_caught(pin):
@@ -64,7 +64,7 @@ def test_e8m0_bias_off_by_one_is_caught(monkeypatch):
 def test_reversed_slot_weights_in_combine_is_caught(monkeypatch):
     orig = M.combine
     monkeypatch.setattr(M, "combine", lambda w, y, r: orig(w[:, ::-1].copy(), y, r))
-    _expect_caught(lambda: TW.test_forward_vs_brute_force(6, 3, 128, 64, 40))
+    _expect_caught(lambda: TW.test_forward_vs_brute_force(6, 3, 128, 64, 40, M.QUANT_W4A8))
 
 
 def test_tie_rule_reversed_is_caught(monkeypatch):
@@ -109,3 +109,52 @@ def test_transposed_gemm_operand_is_caught(monkeypatch):
         return d[::-1].copy()                # output features permuted
     monkeypatch.setattr(M.Weights, "dense", bad)
     _expect_caught(_pins_forward)
+
+
+# ------------------------------------------------- W8A8 (MXFP8) and W4A16 modes
+def _pins_forward_mx():
+    TW.test_forward_vs_brute_force(6, 3, 128, 64, 40, M.QUANT_W8A8)
+
+
+def _pins_forward_w16():
+    TW.test_forward_vs_brute_force(6, 3, 128, 64, 40, M.QUANT_W4A16)
+
+
+def test_mode_pins_pass_unmutated():
+    _pins_forward_mx()
+    _pins_forward_w16()
+
+
+def test_mxfp8_exponent_off_by_one_is_caught(monkeypatch):
+    """X = 2^(floor(log2 amax) - 7) instead of - 8 (E4M3's emax is 8)."""
+    orig = M.quantize_rows_mxfp8
+
+    def bad(rows):
+        _, sc = orig(rows)                                  # the correct exponents e
+        v = np.asarray(rows, np.float32).astype(np.float64)
+        blk = v.reshape(v.shape[:-1] + (v.shape[-1] // 32, 32))
+        e1 = sc.astype(np.int32) - 127 + 1                  # one too large
+        codes = F.e4m3_encode(blk / np.ldexp(1.0, e1)[..., None])
+        return codes.reshape(v.shape).astype(np.uint8), (e1 + 127).astype(np.uint8)
+    monkeypatch.setattr(M, "quantize_rows_mxfp8", bad)
+    _expect_caught(_pins_forward_mx)
+
+
+def test_mxfp8_dropped_activation_scale_is_caught(monkeypatch):
+    """The activation block scales dropped: codes of x / X paired with X = 1."""
+    orig = M.quantize_rows_mxfp8
+
+    def bad(rows):
+        codes, sc = orig(rows)
+        return codes, np.full_like(sc, 127)
+    monkeypatch.setattr(M, "quantize_rows_mxfp8", bad)
+    _expect_caught(_pins_forward_mx)
+
+
+def test_w4a16_h_not_rounded_to_bf16_is_caught(monkeypatch):
+    """W4A16 feeds h to GEMM2 as bf16: skipping the rounding changes y."""
+    def bad(g):
+        I = g.shape[1] // 2
+        return (M.silu_f32(g[:, :I]) * g[:, I:]).astype(np.float32) * np.float32(1.0 + 2.0 ** -7)
+    monkeypatch.setattr(M, "swiglu_bf16", bad)
+    _expect_caught(_pins_forward_w16)
