@@ -277,7 +277,7 @@ def run_ours(args, dist: Dist):
     ms = dist.max(ms_local)
     if P.read_device_status(ws) != 0:
         raise RuntimeError("device status error in timed region")
-    gpu_launches = P._lib.kernels_per_forward(T) * K
+    gpu_launches = P._lib.kernels_per_forward(T, 0) * K
 
     # Kernel timing pass: the same K forwards with CUDA events the library
     # records on its stream before its first kernel and after each kernel.

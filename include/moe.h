@@ -83,10 +83,14 @@ typedef struct {
  * For num_tokens <= MOE_SMALL_BATCH_TOKENS the expansion (scan, rank,
  * quant_scatter) runs as one kernel, timed as stage "scan"; the "rank" and
  * "quant_scatter" stages are then empty and the forward launches 6 kernels.
+ * For num_tokens <= MOE_TINY_BATCH_TOKENS in the W4A8 mode routing and
+ * expansion run as one kernel, timed as stage "route" (5 kernels).  The
+ * W4A16 mode has no hquant kernel (its stage is empty).
  * Kernels are launched with programmatic dependent launch: each may start
  * while its predecessor finishes and waits for the predecessor's results. */
 #define MOE_NUM_STAGES 8
 #define MOE_SMALL_BATCH_TOKENS 1024
+#define MOE_TINY_BATCH_TOKENS 32
 
 /* Optional per-call settings (moe_forward_ex); zero-initialise for defaults. */
 typedef struct {

@@ -336,20 +336,31 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   auto mark = [&]() -> cudaError_t {
     return ev ? cudaEventRecord(ev[stage++], st) : cudaSuccess;
   };
-  // route clears the status word; small batches expand in one kernel
-  MOE_CUDA(mark());
-  MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
-  MOE_CUDA(mark());
+  // the first kernel clears the status word; tiny batches (W4A8) route,
+  // expand and quantise in one kernel, small batches expand in one kernel
   const moe::QuantOut qx{xq, x_scale, mx, x_sf, sfb1, w4a16};
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* token_slot = at<int32_t>(ws, L.token_slot);
-  if (T <= moe::kSmallT) {
+  MOE_CUDA(mark());
+  if (T <= moe::kTinyT && mode == MOE_W4A8_MXFP4_FP8) {
+    MOE_CUDA(moe::launch_route_expand_tiny(logits, x, T, E, k, H, bn, ids, wts,
+                                           at<int32_t>(ws, L.counts), offsets, tiles, num_tiles,
+                                           tile_plan, row_of, token_slot, xq, x_scale, status, st));
+    MOE_CUDA(mark());
+    MOE_CUDA(mark());
+    MOE_CUDA(mark());
+    MOE_CUDA(mark());
+  } else if (T <= moe::kSmallT) {
+    MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
+    MOE_CUDA(mark());
     MOE_CUDA(moe::launch_expand_small(x, ids, T, E, k, H, bn, at<int32_t>(ws, L.counts), offsets,
                                       tiles, num_tiles, tile_plan, row_of, token_slot, qx, st));
     MOE_CUDA(mark());
     MOE_CUDA(mark());
     MOE_CUDA(mark());
   } else {
+    MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
+    MOE_CUDA(mark());
     MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts), offsets,
                               chunk, tiles, num_tiles, tile_plan, st));
     MOE_CUDA(mark());

@@ -39,6 +39,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // (expand_small_kernel) instead of scan + rank + quant_scatter.
 constexpr int kSmallT = MOE_SMALL_BATCH_TOKENS;
 
+// Largest token count that routes, expands and quantises in one single-CTA
+// kernel (route_expand_tiny_kernel; W4A8 only): one warp per token.
+constexpr int kTinyT = MOE_TINY_BATCH_TOKENS;
+
 // Tokens per routing chunk: the unit of the per-chunk expert histogram that
 // makes the expert-major scatter deterministic (stable in token order).
 constexpr int kRouteChunk = 32;
@@ -110,6 +114,11 @@ struct QuantOut {
   uint8_t* sfb;
   bool bf16_copy;
 };
+cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, int E, int k,
+                                     int H, int bn, int32_t* ids, float* wts, int32_t* counts,
+                                     int32_t* offsets, int4* tiles, int32_t* num_tiles,
+                                     int2* tile_plan, int32_t* row_of, int32_t* token_slot,
+                                     uint8_t* xq, float* x_scale, int32_t* status, cudaStream_t s);
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
                                 int bn, int32_t* counts, int32_t* offsets, int4* tiles,
                                 int32_t* num_tiles, int2* tile_plan, int32_t* row_of,

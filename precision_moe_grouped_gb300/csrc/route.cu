@@ -437,6 +437,127 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
   }
 }
 
+// Tiny batches (T <= kTinyT, W4A8): routing, expansion and quantisation in
+// one kernel of T CTAs (1024 threads each), so the routed rows need no
+// second launch and each token row is fetched while the routing runs.
+// CTA t:
+//   1. prefetches token t's row into L2; warp w routes token w (every CTA
+//      routes all T tokens -- the same selection and softmax as
+//      route_kernel; the logits are L2-resident after the first CTA);
+//   2. counts (shared atomics), offsets (block scan), the tile plan and the
+//      stable rank of token t's slots (earlier tokens routed to the same
+//      expert); CTA 0 writes counts, offsets and the tile list;
+//   3. quantises token t into its k rows (quantize_token).
+template <int NV>
+__global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
+    const float* __restrict__ logits, const __nv_bfloat16* __restrict__ x, int T, int E, int k,
+    int H, int bn, int32_t* __restrict__ ids, float* __restrict__ wts,
+    int32_t* __restrict__ counts_out, int32_t* __restrict__ offsets_out, int4* __restrict__ tiles,
+    int32_t* __restrict__ num_tiles, int2* __restrict__ tile_plan, int32_t* __restrict__ row_of,
+    int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq, float* __restrict__ x_scale,
+    int32_t* __restrict__ status) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;                        // [E] counts, then offsets
+  int32_t* sid = sm + E;                    // [kTinyT * 32] routed experts
+  __shared__ int32_t rows[32];
+  __shared__ float warp_max[32];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int t = blockIdx.x;
+  if (t == 0 && threadIdx.x == 0) status[0] = 0;   // first kernel of the forward
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {   // L2 prefetch of token t's row (2H bytes), 128-byte lines
+    const char* base = reinterpret_cast<const char*>(x + static_cast<size_t>(t) * H);
+    for (int i = threadIdx.x; i < (2 * H + 127) / 128; i += blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(base + static_cast<size_t>(i) * 128));
+  }
+  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  if (warp < T) {
+    const float* row = logits + static_cast<size_t>(warp) * E;
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? row[e] : -FLT_MAX;
+    }
+    uint32_t taken = 0;
+    float my_v = 0.f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      float best = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
+          best = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ob > best || (ob == best && oi < bi)) {
+          best = ob;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_v = best;
+        my_id = bi;
+      }
+    }
+    const float lmax = __shfl_sync(0xffffffffu, my_v, 0);
+    float ex = lane < k ? expf(my_v - lmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+      if (warp == t) {
+        const size_t ts = static_cast<size_t>(warp) * k + lane;
+        ids[ts] = my_id;
+        wts[ts] = ex / sum;
+      }
+      sid[warp * 32 + lane] = my_id;
+      atomicAdd(&cnt[my_id], 1);
+    }
+  }
+  __syncthreads();
+  // counts -> offsets; the tile list
+  const int e = threadIdx.x;
+  const int c = e < E ? cnt[e] : 0;
+  int total_rows;
+  const int off = block_exclusive_scan(c, &total_rows);
+  __syncthreads();
+  if (e < E) cnt[e] = off;
+  if (t == 0) {
+    if (e < E) {
+      counts_out[e] = c;
+      offsets_out[e] = off;
+    }
+    if (e == 0) offsets_out[E] = total_rows;
+  }
+  plan_tiles(e, E, c, off, bn, t == 0, tiles, num_tiles, tile_plan);
+  __syncthreads();
+  // token t's rows: stable rank among earlier tokens routed to the same expert
+  if (threadIdx.x < k) {
+    const int j = threadIdx.x;
+    const int ej = sid[t * 32 + j];
+    int rank = 0;
+    for (int t2 = 0; t2 < t; ++t2)
+      for (int j2 = 0; j2 < k; ++j2) rank += sid[t2 * 32 + j2] == ej;
+    const int r = cnt[ej] + rank;
+    rows[j] = r;
+    row_of[static_cast<size_t>(t) * k + j] = r;
+    token_slot[r] = t * k + j;
+  }
+  __syncthreads();
+  quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
+}
+
 }  // namespace
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
@@ -448,6 +569,21 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
             : nv <= 8 ? route_kernel<8> : nv <= 16 ? route_kernel<16> : route_kernel<32>;
   return launch_pdl(kern, dim3(chunks), dim3(1024), smem, s, logits, T, E, k, ids, wts,
                     chunk_counts, status);
+}
+
+cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, int E, int k,
+                                     int H, int bn, int32_t* ids, float* wts, int32_t* counts,
+                                     int32_t* offsets, int4* tiles, int32_t* num_tiles,
+                                     int2* tile_plan, int32_t* row_of, int32_t* token_slot,
+                                     uint8_t* xq, float* x_scale, int32_t* status, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(E + kTinyT * 32) * sizeof(int32_t);
+  const int nv = (E + 31) / 32;
+  auto kern = nv <= 1 ? route_expand_tiny_kernel<1> : nv <= 2 ? route_expand_tiny_kernel<2>
+            : nv <= 4 ? route_expand_tiny_kernel<4> : nv <= 8 ? route_expand_tiny_kernel<8>
+            : nv <= 16 ? route_expand_tiny_kernel<16> : route_expand_tiny_kernel<32>;
+  return launch_pdl(kern, dim3(T), dim3(1024), smem, s, logits,
+                    static_cast<const __nv_bfloat16*>(x), T, E, k, H, bn, ids, wts, counts,
+                    offsets, tiles, num_tiles, tile_plan, row_of, token_slot, xq, x_scale, status);
 }
 
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
