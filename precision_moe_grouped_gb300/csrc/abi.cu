@@ -313,10 +313,11 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   // W4A16: packed code rows (64 bytes) as they are, for the in-kernel
   // conversion to bf16
   const MapKind wkind = mx ? MapKind::kBytes : w4a16 ? MapKind::kPackedBytes : MapKind::kFp4Weights;
-  const uint32_t wcols = w4a16 ? 64 : 128;
+  // (W4A16 copies half a box row -- 64 K, 32 bytes -- per sub-stage)
+  const uint32_t wcols = w4a16 ? 64 : 128, wbox = w4a16 ? 32 : 128;
   const uint32_t w_tx = mx ? 128u * 128u : kWeightBoxTxBytes;
-  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, wcols, wkind, wcols, 128)) != MOE_OK ||
-      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, wcols, wkind, wcols, 128)) != MOE_OK ||
+  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, wcols, wkind, wbox, 128)) != MOE_OK ||
+      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, wcols, wkind, wbox, 128)) != MOE_OK ||
       (rc = make_tmap(&tm_sf1, w1_sf, w1_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK ||
       (rc = make_tmap(&tm_sf2, w2_sf, w2_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK)
     return rc;

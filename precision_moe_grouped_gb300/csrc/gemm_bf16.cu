@@ -9,19 +9,20 @@
 //           MXFP4 weights dequantised inside the kernel).
 //
 // The tensor cores have no mixed FP4 x BF16 MMA, so the weights are
-// converted in shared memory: a weight box (128 rows x 128 K, packed E2M1
-// codes, 64 bytes per row) and its E8M0 scales land in a raw slot, four
-// transform warps rewrite it as bf16 values
-// e2m1 * 2^(scale - 127) -- exact in bf16 (a product of two powers of two
-// times at most two significant bits) -- into a converted slot (two 128 B x
-// 128-row K atoms, 128-byte swizzle), and the MMA reads the converted slot
-// and the bf16 activation box.  Everything else (tile list, swap-AB
+// converted in shared memory, in sub-stages of 64 K: the packed E2M1 codes of
+// 128 weight rows x 64 K (half of a prepared 128 x 128 box, 32 bytes per row)
+// and the box's E8M0 scales land in a raw slot; eight transform warps rewrite
+// them as bf16 values e2m1 * 2^(scale - 127) -- exact in bf16 (a power of two
+// times at most two significant bits) -- into a converted slot (one 128 B x
+// 128-row K atom, 128-byte swizzle); the MMA reads the converted slot and
+// the sub-stage's bf16 activation atom.  Everything else (tile list, swap-AB
 // orientation, persistent static striding, epilogue) is the FP8 GEMM's.
 //
-// Roles: warp 0 = TMA producers (lane s < S: weight box + scales into raw
-// slot s; lane S + s: activation box into activation slot s); warp 1 = MMA
-// issuer (warp-uniform, one elected lane issues); warps 2..5 = transform;
-// warps 6..13 = epilogue.
+// Roles: warp 0 = TMA producers (lane s < S: weight half-box + scales into
+// raw slot s; lane S + s: activation atom into activation slot s); warps
+// 1..NI = MMA issuers (warp-uniform, one elected lane issues; issuer i takes
+// the sub-stages g = i mod NI into its own accumulator); the next 8 warps =
+// transform; the last 8 warps = epilogue.
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -32,31 +33,37 @@ namespace moe {
 
 namespace {
 
-constexpr int kTransformWarps = 4;
+constexpr int kTransformWarps = 8;
+constexpr int kBf16Issuers = 2;
 
 template <int BN, int S, int Q>
 struct Bf16Cfg {
   static_assert(BN % 16 == 0 && BN <= 128, "token tile of the W4A16 GEMM: 16..128 rows");
   static_assert(2 * S <= 32, "producer lanes must fit one warp");
-  static constexpr int kRawBytes = kTileM * 64;      // packed E2M1 box
-  static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes
-  static constexpr int kBAtom = BN * 128;            // 64 bf16 of K per row
-  static constexpr int kBBytes = 2 * kBAtom;         // 128 K per stage
-  static constexpr int kCvAtom = kTileM * 128;
-  static constexpr int kCvBytes = 2 * kCvAtom;       // 128 x 128 bf16
+  static_assert(S % kBf16Issuers == 0 && Q % kBf16Issuers == 0,
+                "each slot must belong to one MMA issuer");
+  static constexpr int kRawBytes = kTileM * 32;      // packed E2M1, 64 K per row
+  static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes (128 K)
+  static constexpr int kBBytes = BN * 128;           // 64 bf16 of K per token row
+  static constexpr int kCvBytes = kTileM * 128;      // 128 rows x 64 bf16
   static constexpr int kOffRaw = 0;
   static constexpr int kOffB = kOffRaw + S * kRawBytes;
   static constexpr int kOffCv = kOffB + S * kBBytes;
   static constexpr int kOffSF = kOffCv + Q * kCvBytes;
-  static constexpr int kOffLut = kOffSF + S * kSFBytes;   // 256 x bf16x2 (code byte -> pair)
-  static constexpr int kNumBars = 4 * S + 2 * Q + 2 * 2 + 1;
-  static constexpr int kOffBar = kOffLut + 256 * 4;
+  // code byte -> bf16x2 table, one copy per shared-memory bank: entry b of
+  // lane l at word 32 b + l, so a warp's lookups never conflict
+  static constexpr int kOffLut = kOffSF + S * kSFBytes;
+  static constexpr int kNumBars = 4 * S + 2 * Q + 2 * 2 + kBf16Issuers;
+  static constexpr int kOffBar = kOffLut + 256 * 32 * 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static constexpr int kFirstEpiWarp = 2 + kTransformWarps;
+  static constexpr int kFirstXfWarp = 1 + kBf16Issuers;
+  static constexpr int kFirstEpiWarp = kFirstXfWarp + kTransformWarps;
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
-  static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 256;
+  static constexpr int kCols = 2 * kBf16Issuers * BN;   // 2 buffers x NI partials
+  static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
+                                   : kCols <= 256 ? 256 : 512;
 };
 
 // Instruction descriptor of .kind::f16 with bf16 A and B, fp32 accumulate,
@@ -98,6 +105,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
                              __nv_bfloat16* __restrict__ out, int m_per_expert, int K,
                              int out_ld, int32_t* __restrict__ status, uint64_t timeout_ns) {
   using C = Bf16Cfg<BN, S, Q>;
+  constexpr int NI = kBf16Issuers;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -115,6 +123,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MT = m_per_expert / kTileM, KS = K / kTileK;
+  const int KH = 2 * KS;   // 64-K sub-stages per item (>= 2 = NI)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -128,10 +137,10 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
       mbar_init(cv_empty + q, 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull + a, 1);
+      mbar_init(tfull + a, NI);                     // every issuer commits its share
       mbar_init(tempty + a, kEpiWarps);
     }
-    mbar_init(drain, 1);
+    for (int i = 0; i < NI; ++i) mbar_init(drain + i, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_w);
@@ -139,10 +148,12 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
     for (int i = 0; i < kNumXMaps; ++i) prefetch_tmap(&tmap_x.m[i]);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
-  // Code byte -> the bf16 pair (low nibble = even k) of its two E2M1 values.
-  for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+  // Code byte -> the bf16 pair (low nibble = even k) of its two E2M1 values,
+  // replicated per bank.
+  for (int w = threadIdx.x; w < 256 * 32; w += blockDim.x) {
+    const int b = w >> 5;
     const __nv_bfloat162 pr = __floats2bfloat162_rn(e2m1_value(b & 0xF), e2m1_value(b >> 4));
-    reinterpret_cast<__nv_bfloat162*>(smem + C::kOffLut)[b] = pr;
+    reinterpret_cast<__nv_bfloat162*>(smem + C::kOffLut)[w] = pr;
   }
   tc_fence_before();
   __syncthreads();
@@ -154,12 +165,15 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane s < S fills raw slot s for this CTA's sub-stages g = s, s + S, ...
+    // (sub-stage g = 64-K half (g % KH) % 2 of the 128-K box (g % KH) / 2 of
+    // the CTA's (g / KH)-th item); lane S + s fills activation slot s.
     if (lane < 2 * S) {
       const bool is_w = lane < S;
       const int s = is_w ? lane : lane - S;
       uint32_t phase = 0;
       bool issued = false;
-      int ks = s % KS, item = blockIdx.x + (s / KS) * gridDim.x;
+      int kh = s % KH, item = blockIdx.x + (s / KH) * gridDim.x;
       uint64_t* full = is_w ? raw_full + s : b_full + s;
       uint64_t* empty = is_w ? raw_empty + s : b_empty + s;
       while (item < num_items) {
@@ -167,26 +181,24 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
         const int4 td = tiles[item / MT];
         if (!mbar_wait(empty, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag)) break;
         if (is_w) {
-          const int64_t blk = (static_cast<int64_t>(td.x) * MT + mt) * KS + ks;
-          mbar_arrive_expect_tx(full, 128u * 128u / 2u + 512u);
-          tma_load_2d(smem + C::kOffRaw + s * C::kRawBytes, &tmap_w, 0,
+          const int64_t blk = (static_cast<int64_t>(td.x) * MT + mt) * KS + (kh >> 1);
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(C::kRawBytes) + 512u);
+          tma_load_2d(smem + C::kOffRaw + s * C::kRawBytes, &tmap_w, (kh & 1) * 32,
                       static_cast<int32_t>(blk * kTileM), full);
           tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0, static_cast<int32_t>(blk),
                       full);
         } else {
-          // two 64-element K atoms of the smallest box covering the MMA-N rows
+          // the smallest box covering the MMA-N rows, 64 K elements
           const int nmma = (td.z + 15) & ~15;
           const int xm = x_map_for(nmma);
-          mbar_arrive_expect_tx(full, 2u * static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u);
-          uint8_t* dst = smem + C::kOffB + s * C::kBBytes;
-          tma_load_2d(dst, &tmap_x.m[xm], ks * kTileK, td.y, full);
-          tma_load_2d(dst + C::kBAtom, &tmap_x.m[xm], ks * kTileK + 64, td.y, full);
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u);
+          tma_load_2d(smem + C::kOffB + s * C::kBBytes, &tmap_x.m[xm], kh * 64, td.y, full);
         }
         issued = true;
         phase ^= 1u;
-        ks += S;
-        while (ks >= KS) {
-          ks -= KS;
+        kh += S;
+        while (kh >= KH) {
+          kh -= KH;
           item += gridDim.x;
         }
       }
@@ -195,12 +207,12 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
         mbar_wait(full, phase ^ 1u, timeout_ns, status, kDevTimeout, &none);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp <= NI) {
+    // ------------------------------------------------------------ MMA issuers
+    const int i = warp - 1;
     const uint64_t cdesc0 = smem_desc(smem_u32(smem + C::kOffCv), 0, 1024, 2);
     const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
-    int s = 0, q = 0, ks = 0, it = 0;
-    uint32_t ps = 0, pq = 0;
+    int g = i, kh = i, it = 0;
     bool new_item = true;
     uint32_t d_tmem = 0, id = 0;
     int acc = 0;
@@ -213,93 +225,81 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
                             status, kDevTimeout, abort_flag))
           break;
         tc_fence_after();
-        d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+        d_tmem = tmem + static_cast<uint32_t>((acc * NI + i) * BN);
       }
-      if (!mbar_wait_warp(cv_full + q, pq, timeout_ns, status, kDevTimeout, abort_flag)) break;
-      if (!mbar_wait_warp(b_full + s, ps, timeout_ns, status, kDevTimeout, abort_flag)) break;
+      const int s = g % S, q = g % Q;
+      if (!mbar_wait_warp(cv_full + q, static_cast<uint32_t>((g / Q) & 1), timeout_ns, status,
+                          kDevTimeout, abort_flag))
+        break;
+      if (!mbar_wait_warp(b_full + s, static_cast<uint32_t>((g / S) & 1), timeout_ns, status,
+                          kDevTimeout, abort_flag))
+        break;
       tc_fence_after();
+      const uint64_t ad = cdesc0 + static_cast<uint64_t>((q * C::kCvBytes) >> 4);
+      const uint64_t bd = bdesc0 + static_cast<uint64_t>((s * C::kBBytes) >> 4);
 #pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const uint64_t ad = cdesc0 + static_cast<uint64_t>((q * C::kCvBytes + a * C::kCvAtom) >> 4);
-        const uint64_t bd = bdesc0 + static_cast<uint64_t>((s * C::kBBytes + a * C::kBAtom) >> 4);
-#pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)   // K = 16 bf16 = 32 bytes per MMA
-          tc_mma_f16_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id,
-                          (!new_item || a > 0 || kk > 0) ? 1u : 0u);
-      }
+      for (uint32_t kk = 0; kk < 4; ++kk)   // K = 16 bf16 = 32 bytes per MMA
+        tc_mma_f16_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id, (!new_item || kk > 0) ? 1u : 0u);
       tc_commit_warp(cv_empty + q);
       tc_commit_warp(b_empty + s);
-      if (++s == S) {
-        s = 0;
-        ps ^= 1u;
-      }
-      if (++q == Q) {
-        q = 0;
-        pq ^= 1u;
-      }
+      g += NI;
+      kh += NI;
       new_item = false;
-      if (++ks == KS) {
-        ks = 0;
+      if (kh >= KH) {   // NI <= KH: at most one item boundary per step
+        kh -= KH;
         ++it;
         new_item = true;
         tc_commit_warp(tfull + acc);
       }
     }
-    tc_commit_warp(drain);
+    tc_commit_warp(drain + i);
     int32_t none = 0;
-    mbar_wait_warp(drain, 0, timeout_ns, status, kDevTimeout, &none);
+    mbar_wait_warp(drain + i, 0, timeout_ns, status, kDevTimeout, &none);
   } else if (warp < C::kFirstEpiWarp) {
     // ------------------------------------------------------------ transform
-    // 128 threads convert a fill's 512 16-byte units of packed codes: unit v
-    // = row v / 4, K-block p = v % 4 (32 codes, one scale byte) -> 32 bf16
-    // = four 16-byte units of the converted slot (K atom p / 2, units
-    // 4 (p % 2) .. +3 of the row, 128-byte swizzled).  Consecutive threads
-    // read consecutive units, so the reads are conflict-free.  Each code
-    // byte becomes a bf16 pair through the shared table, then one bf16x2
-    // multiply applies the scale -- exact: a value with at most two
-    // significant bits times a power of two.
-    const int t = threadIdx.x - 64;
+    // 256 threads convert a sub-stage's 256 16-byte units of packed codes:
+    // unit v = row v / 2, 32-K block p = v % 2 of the sub-stage (one scale
+    // byte) -> 32 bf16 = four 16-byte units of the converted slot (units
+    // 4p .. 4p+3 of the row, 128-byte swizzled).  Consecutive threads read
+    // consecutive units.  Each code byte becomes a bf16 pair through the
+    // shared table (this lane's bank copy: no conflicts); one bf16x2
+    // multiply applies the scale -- exact.
+    const int v = threadIdx.x - 32 * C::kFirstXfWarp, r = v >> 1, p = v & 1;
     const __nv_bfloat162* lut = reinterpret_cast<const __nv_bfloat162*>(smem + C::kOffLut);
-    int total_fills = 0;
-    for (int item = blockIdx.x; item < num_items; item += gridDim.x) total_fills += KS;
-    for (int f = 0; f < total_fills; ++f) {
-      const int s = f % S, q = f % Q;
-      if (!mbar_wait(raw_full + s, static_cast<uint32_t>((f / S) & 1), timeout_ns, status,
+    int total = 0;
+    for (int item = blockIdx.x; item < num_items; item += gridDim.x) total += KH;
+    for (int g = 0; g < total; ++g) {
+      const int s = g % S, q = g % Q;
+      if (!mbar_wait(raw_full + s, static_cast<uint32_t>((g / S) & 1), timeout_ns, status,
                      kDevTimeout, abort_flag))
         break;
-      if (!mbar_wait(cv_empty + q, static_cast<uint32_t>((f / Q) & 1) ^ 1u, timeout_ns, status,
+      if (!mbar_wait(cv_empty + q, static_cast<uint32_t>((g / Q) & 1) ^ 1u, timeout_ns, status,
                      kDevTimeout, abort_flag))
         break;
-      const uint8_t* raw = smem + C::kOffRaw + s * C::kRawBytes;
-      const uint8_t* sf = smem + C::kOffSF + s * C::kSFBytes;
-      uint8_t* cv = smem + C::kOffCv + q * C::kCvBytes;
-#pragma unroll 1
-      for (int pass = 0; pass < 4; ++pass) {
-        const int v = pass * 128 + t, r = v >> 2, p = v & 3;
-        const uint4 codes = *reinterpret_cast<const uint4*>(raw + 16 * v);
-        // scale 2^(byte - 127) of K-block p; byte 0 -> 2^-127 (subnormal),
-        // byte 255 (NaN) -> NaN
-        const uint32_t sb = sf[16 * (r & 31) + 4 * (r >> 5) + p];
-        // 2^(sb - 127) as bf16: exponent field sb (sb = 0: the subnormal
-        // 2^-127; sb = 255: NaN)
-        const uint16_t sbits = sb == 0 ? 0x0040u : sb == 255 ? 0x7FC0u
-                                                           : static_cast<uint16_t>(sb << 7);
-        __nv_bfloat162 scale2;
-        scale2.x = __ushort_as_bfloat16(sbits);
-        scale2.y = scale2.x;
-        const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-        uint8_t* dst = cv + (p >> 1) * C::kCvAtom + r * 128;
+      const uint4 codes = *reinterpret_cast<const uint4*>(smem + C::kOffRaw + s * C::kRawBytes + 16 * v);
+      // the scale of 32-K block 2 * (64-K half) + p of the 128-K box
+      const int half = (g % KH) & 1;
+      const uint32_t sb =
+          smem[C::kOffSF + s * C::kSFBytes + 16 * (r & 31) + 4 * (r >> 5) + 2 * half + p];
+      // 2^(sb - 127) as bf16: exponent field sb (sb = 0: the subnormal
+      // 2^-127; sb = 255: NaN)
+      const uint16_t sbits = sb == 0 ? 0x0040u : sb == 255 ? 0x7FC0u
+                                                         : static_cast<uint16_t>(sb << 7);
+      __nv_bfloat162 scale2;
+      scale2.x = __ushort_as_bfloat16(sbits);
+      scale2.y = scale2.x;
+      const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+      uint8_t* dst = smem + C::kOffCv + q * C::kCvBytes + r * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {   // 8 codes (4 bytes) -> 8 bf16 -> one 16-byte unit
-          uint32_t w[4];
+      for (int j = 0; j < 4; ++j) {   // 8 codes (4 bytes) -> 8 bf16 -> one 16-byte unit
+        uint32_t w[4];
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const __nv_bfloat162 pr = __hmul2(lut[(cw[j] >> (8 * b)) & 0xFFu], scale2);
-            w[b] = *reinterpret_cast<const uint32_t*>(&pr);
-          }
-          const int u = 4 * (p & 1) + j;
-          *reinterpret_cast<uint4*>(dst + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int b = 0; b < 4; ++b) {
+          const __nv_bfloat162 pr = __hmul2(lut[(((cw[j] >> (8 * b)) & 0xFFu) << 5) + lane], scale2);
+          w[b] = *reinterpret_cast<const uint32_t*>(&pr);
         }
+        const int u = 4 * p + j;
+        *reinterpret_cast<uint4*>(dst + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       fence_proxy_async_smem();   // generic-proxy writes -> the MMA's async proxy
       __syncwarp();
@@ -310,8 +310,8 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    epilogue_loop<BN, 1, 2, SWIGLU>(C::kFirstEpiWarp, 1, tiles, num_items, MT, tfull, tempty,
-                                    tmem, nullptr, out, out_ld, timeout_ns, status, abort_flag);
+    epilogue_loop<BN, NI, 2, SWIGLU>(C::kFirstEpiWarp, NI, tiles, num_items, MT, tfull, tempty,
+                                     tmem, nullptr, out, out_ld, timeout_ns, status, abort_flag);
   }
 
   tc_fence_before();
@@ -342,10 +342,10 @@ cudaError_t launch_bf16_variant(const GemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-// W4A16: 64-token tiles, 6 raw/activation slots, 2 converted slots.
+// W4A16: 64-token tiles, 8 raw/activation slots and 4 converted slots of 64 K.
 cudaError_t launch_gemm_bf16(bool swiglu, const GemmArgs& a, cudaStream_t s) {
-  return swiglu ? launch_bf16_variant<kW4A16BN, 6, 2, true>(a, s)
-                : launch_bf16_variant<kW4A16BN, 6, 2, false>(a, s);
+  return swiglu ? launch_bf16_variant<kW4A16BN, 8, 4, true>(a, s)
+                : launch_bf16_variant<kW4A16BN, 8, 4, false>(a, s);
 }
 
 }  // namespace moe

@@ -72,6 +72,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// try_wait that lets the thread sleep until the phase completes or
+// `suspend_ns` pass (the hardware wakes it on completion), so waiting warps
+// do not take issue slots from the warps doing work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar_addr, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Longest sleep of one suspended try_wait: the abort flag and the wall-clock
+// limit are checked between sleeps.
+constexpr uint32_t kSuspendNs = 20000;
+
 // Waits until the phase with parity `parity` of `bar` has completed, at most
 // `timeout_ns`; also gives up early when *abort is set by another role.  On
 // giving up it records `code` in *status (first error wins) and sets *abort.
@@ -82,7 +102,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait_suspend(a, parity, kSuspendNs)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > timeout_ns) {
       atomicCAS(status, 0, code);
