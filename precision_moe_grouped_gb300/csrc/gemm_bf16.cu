@@ -11,7 +11,7 @@
 // The tensor cores have no mixed FP4 x BF16 MMA, so the weights are
 // converted in shared memory, in sub-stages of 64 K: the packed E2M1 codes of
 // 128 weight rows x 64 K (half of a prepared 128 x 128 box, 32 bytes per row)
-// and the box's E8M0 scales land in a raw slot; eight transform warps rewrite
+// and the box's E8M0 scales land in a raw slot; a transform warp rewrites
 // them as bf16 values e2m1 * 2^(scale - 127) -- exact in bf16 (a power of two
 // times at most two significant bits) -- into a converted slot (one 128 B x
 // 128-row K atom, 128-byte swizzle); the MMA reads the converted slot and
@@ -21,8 +21,9 @@
 // Roles: warp 0 = TMA producers (lane s < S: weight half-box + scales into
 // raw slot s; lane S + s: activation atom into activation slot s); warps
 // 1..NI = MMA issuers (warp-uniform, one elected lane issues; issuer i takes
-// the sub-stages g = i mod NI into its own accumulator); the next 8 warps =
-// transform; the last 8 warps = epilogue.
+// the sub-stages g = i mod NI into its own accumulator); the next 4 warps =
+// transform (warp w converts the sub-stages g = w mod 4); the last 8 warps =
+// epilogue.
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -33,7 +34,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kTransformWarps = 8;
+constexpr int kTransformWarps = 4;
 constexpr int kBf16Issuers = 2;
 
 template <int BN, int S, int Q>
@@ -42,6 +43,8 @@ struct Bf16Cfg {
   static_assert(2 * S <= 32, "producer lanes must fit one warp");
   static_assert(S % kBf16Issuers == 0 && Q % kBf16Issuers == 0,
                 "each slot must belong to one MMA issuer");
+  static_assert(S % kTransformWarps == 0 && Q % kTransformWarps == 0,
+                "each slot must belong to one transform warp");
   static constexpr int kRawBytes = kTileM * 32;      // packed E2M1, 64 K per row
   static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes (128 K)
   static constexpr int kBBytes = BN * 128;           // 64 bf16 of K per token row
@@ -128,12 +131,12 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(raw_full + s, 1);
-      mbar_init(raw_empty + s, kTransformWarps);   // every transform warp has read it
+      mbar_init(raw_empty + s, 1);   // its transform warp has read it
       mbar_init(b_full + s, 1);
       mbar_init(b_empty + s, 1);
     }
     for (int q = 0; q < Q; ++q) {
-      mbar_init(cv_full + q, kTransformWarps);
+      mbar_init(cv_full + q, 1);
       mbar_init(cv_empty + q, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -257,18 +260,20 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
     mbar_wait_warp(drain + i, 0, timeout_ns, status, kDevTimeout, &none);
   } else if (warp < C::kFirstEpiWarp) {
     // ------------------------------------------------------------ transform
-    // 256 threads convert a sub-stage's 256 16-byte units of packed codes:
-    // unit v = row v / 2, 32-K block p = v % 2 of the sub-stage (one scale
-    // byte) -> 32 bf16 = four 16-byte units of the converted slot (units
-    // 4p .. 4p+3 of the row, 128-byte swizzled).  Consecutive threads read
-    // consecutive units.  Each code byte becomes a bf16 pair through the
-    // shared table (this lane's bank copy: no conflicts); one bf16x2
-    // multiply applies the scale -- exact.
-    const int v = threadIdx.x - 32 * C::kFirstXfWarp, r = v >> 1, p = v & 1;
+    // Transform warp w converts the sub-stages g = w, w + 4, ... whole: lane
+    // l takes the 16-byte units v = l + 32 u (u < 8) of packed codes (row
+    // v / 2, 32-K block p = v % 2 of the sub-stage, one scale byte) -> 32
+    // bf16 = four 16-byte units of the converted slot (units 4p .. 4p+3 of
+    // the row, 128-byte swizzled).  Consecutive lanes read consecutive units;
+    // the eight units of a lane are independent, which keeps the loads and
+    // the table lookups in flight together.  Each code byte becomes a bf16
+    // pair through the shared table (this lane's bank copy: no conflicts);
+    // one bf16x2 multiply applies the scale -- exact.
+    const int w = warp - C::kFirstXfWarp;
     const __nv_bfloat162* lut = reinterpret_cast<const __nv_bfloat162*>(smem + C::kOffLut);
     int total = 0;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) total += KH;
-    for (int g = 0; g < total; ++g) {
+    for (int g = w; g < total; g += kTransformWarps) {
       const int s = g % S, q = g % Q;
       if (!mbar_wait(raw_full + s, static_cast<uint32_t>((g / S) & 1), timeout_ns, status,
                      kDevTimeout, abort_flag))
@@ -276,30 +281,40 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
       if (!mbar_wait(cv_empty + q, static_cast<uint32_t>((g / Q) & 1) ^ 1u, timeout_ns, status,
                      kDevTimeout, abort_flag))
         break;
-      const uint4 codes = *reinterpret_cast<const uint4*>(smem + C::kOffRaw + s * C::kRawBytes + 16 * v);
-      // the scale of 32-K block 2 * (64-K half) + p of the 128-K box
-      const int half = (g % KH) & 1;
-      const uint32_t sb =
-          smem[C::kOffSF + s * C::kSFBytes + 16 * (r & 31) + 4 * (r >> 5) + 2 * half + p];
-      // 2^(sb - 127) as bf16: exponent field sb (sb = 0: the subnormal
-      // 2^-127; sb = 255: NaN)
-      const uint16_t sbits = sb == 0 ? 0x0040u : sb == 255 ? 0x7FC0u
-                                                         : static_cast<uint16_t>(sb << 7);
-      __nv_bfloat162 scale2;
-      scale2.x = __ushort_as_bfloat16(sbits);
-      scale2.y = scale2.x;
-      const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-      uint8_t* dst = smem + C::kOffCv + q * C::kCvBytes + r * 128;
+      const uint8_t* raw = smem + C::kOffRaw + s * C::kRawBytes;
+      const uint8_t* sf = smem + C::kOffSF + s * C::kSFBytes;
+      uint8_t* cv = smem + C::kOffCv + q * C::kCvBytes;
+      const int half = (g % KH) & 1;   // the 64-K half of the 128-K box
+      uint4 codes[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {   // 8 codes (4 bytes) -> 8 bf16 -> one 16-byte unit
-        uint32_t w[4];
+      for (int u = 0; u < 8; ++u)
+        codes[u] = *reinterpret_cast<const uint4*>(raw + 16 * (lane + 32 * u));
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const __nv_bfloat162 pr = __hmul2(lut[(((cw[j] >> (8 * b)) & 0xFFu) << 5) + lane], scale2);
-          w[b] = *reinterpret_cast<const uint32_t*>(&pr);
+      for (int u = 0; u < 8; ++u) {
+        const int v = lane + 32 * u, r = v >> 1, p = v & 1;
+        // scale 2^(sb - 127) of 32-K block 2 * half + p of the box, as bf16:
+        // exponent field sb (sb = 0: the subnormal 2^-127; sb = 255: NaN)
+        const uint32_t sb = sf[16 * (r & 31) + 4 * (r >> 5) + 2 * half + p];
+        const uint16_t sbits = sb == 0 ? 0x0040u : sb == 255 ? 0x7FC0u
+                                                           : static_cast<uint16_t>(sb << 7);
+        __nv_bfloat162 scale2;
+        scale2.x = __ushort_as_bfloat16(sbits);
+        scale2.y = scale2.x;
+        const uint32_t cw[4] = {codes[u].x, codes[u].y, codes[u].z, codes[u].w};
+        uint8_t* dst = cv + r * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // 8 codes (4 bytes) -> 8 bf16 -> one 16-byte unit
+          uint32_t wd[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const __nv_bfloat162 pr =
+                __hmul2(lut[(((cw[j] >> (8 * b)) & 0xFFu) << 5) + lane], scale2);
+            wd[b] = *reinterpret_cast<const uint32_t*>(&pr);
+          }
+          const int un = 4 * p + j;
+          *reinterpret_cast<uint4*>(dst + ((un ^ (r & 7)) << 4)) =
+              make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
-        const int u = 4 * p + j;
-        *reinterpret_cast<uint4*>(dst + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       fence_proxy_async_smem();   // generic-proxy writes -> the MMA's async proxy
       __syncwarp();
