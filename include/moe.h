@@ -107,8 +107,7 @@ typedef struct {
                             before the first kernel and event i right after
                             kernel i, so event pairs time each kernel      */
   int32_t prefetch_stages; /* L2 prefetch distance of the GEMM weight stream,
-                            in K stages: 0 = default (8 for the prefill
-                            tiles, off for decode tiles), < 0 = off      */
+                            in K stages: 0 = default (off), < 0 = off   */
   int32_t reserved[3];   /* must be zero                                     */
 } moe_options;
 

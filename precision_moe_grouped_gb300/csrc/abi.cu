@@ -62,10 +62,10 @@ constexpr size_t kAlign = 256;
 constexpr uint32_t kWeightBoxTxBytes = 128u * 128u / 2u;
 
 // Default L2 prefetch distance of the GEMMs' weight stream (the prefetch
-// warp), in fills: on for the prefill tiles (DSV3 T=4096: 1993 -> 1947 us),
-// off for the decode tiles, whose weight stream is already HBM-bound and
-// measured 15-25% slower with it.
-int default_prefetch(int variant) { return moe::gemm_tile_tokens(variant) >= moe::kMidBN ? 8 : 0; }
+// warp), in fills: off.  It measured 15-25% slower on decode tiles and, once
+// waiting warps sleep instead of spinning, neutral on prefill tiles (DSV3
+// T=4096: 1797 us with a distance of 8, 1800 us without).
+int default_prefetch(int) { return 0; }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
