@@ -95,7 +95,7 @@ typedef struct {
 /* Optional per-call settings (moe_forward_ex); zero-initialise for defaults. */
 typedef struct {
   int32_t tile_variant;  /* 0 auto (3 while experts average <= 8 rows, 1 up
-                            to 16, else 5); 1 decode tiles (<= 32 tokens per
+                            to 32, else 5); 1 decode tiles (<= 32 tokens per
                             GEMM tile, 10-stage weight pipeline); 2 prefill
                             tiles (<= 224); 3 decode tiles of <= 16 tokens
                             (12 stages); 4 prefill tiles with two MMA

@@ -219,13 +219,12 @@ int pick_variant(const moe_shape* s, const moe_options* o) {
   if (o && o->tile_variant >= 1 && o->tile_variant <= moe::kMaxTileVariant) return o->tile_variant;
   const double rows_per_expert =
       static_cast<double>(s->num_tokens) * s->top_k / static_cast<double>(s->num_experts);
-  // 16-token tiles (12 stages) while experts average <= 8 rows (measured
-  // faster than 32-token tiles at DSV3 T = 1..256, slower at T = 512 where
-  // many experts need a second 16-token tile); 32-token tiles (10 stages) up
-  // to 16 rows; above that the 6-stage 160-token prefill tiles (measured faster
-  // than 5-stage 224-token tiles at DSV3 T=512 and T=4096: more weight bytes
-  // in flight per SM).
-  return rows_per_expert <= 8.0 ? 3 : rows_per_expert <= 16.0 ? 1 : 5;
+  // Measured on the DSV3 shape (T = 64 .. 4096): 16-token tiles (12 stages)
+  // are fastest while experts average <= 8 rows; 32-token tiles (10 stages)
+  // up to 32 rows (T=1024: 1.27 ms against 1.35 ms for 160-token tiles);
+  // from 48 rows on the 6-stage 160-token tiles (T=1536: 1.39 ms against
+  // 1.63 ms), which also beat 5-stage 224-token tiles at T=4096.
+  return rows_per_expert <= 8.0 ? 3 : rows_per_expert <= 32.0 ? 1 : 5;
 }
 
 int32_t check_options(const moe_options* o) {
