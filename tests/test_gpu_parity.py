@@ -126,6 +126,22 @@ def test_degenerate_routing(E, k, T):
     full_parity(MI.make_case(cfg, T, seed=31 + T), name=f"degen{E}_{k}_{T}")
 
 
+@pytest.mark.parametrize("T", [32, 33])
+def test_tiny_batch_boundary(T):
+    """T = 32 routes, expands and quantises in one kernel; T = 33 takes the
+    two-kernel small-batch path.  Both must match the oracle bit for bit on
+    the front end."""
+    cfg = MI.custom_config(64, 8, 256, 128)
+    run, _ = full_parity(MI.make_case(cfg, T, seed=61 + T), name=f"tiny_boundary{T}")
+    check_tiles(run, 16 if run.R / 64 <= 8 else 32)
+
+
+def test_many_experts_and_top32():
+    """The routing limits: E = 1024 experts (32 logits per lane) and top-32."""
+    cfg = MI.custom_config(1024, 32, 128, 128)
+    full_parity(MI.make_case(cfg, 20, seed=71), name="e1024_k32")
+
+
 def test_zero_rows_and_ties():
     cfg = MI.custom_config(8, 2, 256, 128)
     case = MI.make_case(cfg, 24, seed=41)

@@ -83,3 +83,10 @@ def test_w16_config_full():
     """The W4A16 workload in full: E=64, top-4, H=2048, I=1024, T=256."""
     cfg = MI.CONFIGS["w4a16"]
     w16_parity(MI.make_case(cfg, 256, device="cuda"), name="w16_config")
+
+
+def test_w16_large_batch_expansion():
+    """T > 1024: the bf16 rows are copied by the multi-kernel expansion
+    (scan, rank, scatter) instead of the one-kernel small-batch path."""
+    run, _ = w16_parity(MI.make_case(_cfg(8, 2, 256, 128), 1500, seed=5), name="w16_large")
+    assert run.T > P._lib.MOE_SMALL_BATCH_TOKENS
