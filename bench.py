@@ -158,6 +158,7 @@ def source_hash(paths) -> str:
 
 
 GEMM_SOURCES = ["precision_moe_grouped_gb300/csrc/gemm.cu",
+                "precision_moe_grouped_gb300/csrc/gemm_pair.cu",
                 "precision_moe_grouped_gb300/csrc/gemm_common.cuh",
                 "precision_moe_grouped_gb300/csrc/ptx.cuh"]
 KERNEL_SOURCES = {

@@ -100,7 +100,10 @@ typedef struct {
                             tiles (<= 224); 3 decode tiles of <= 16 tokens
                             (12 stages); 4 prefill tiles with two MMA
                             issuers; 5 tiles of <= 160 tokens with a 6-stage
-                            pipeline                                      */
+                            pipeline; 6 tiles of <= 160 tokens on CTA pairs
+                            (two SMs share each 256-row MMA; W4A8 with
+                            hidden a multiple of 256 -- otherwise the GEMM
+                            runs as 5)                                    */
   int32_t timeout_ms;    /* device bounded-wait limit, 0 = 1000 ms           */
   void* stage_events;    /* NULL, or an array of MOE_NUM_STAGES + 1 cudaEvent_t
                             (caller-created): event 0 is recorded on `stream`

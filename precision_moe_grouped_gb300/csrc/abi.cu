@@ -304,6 +304,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   uint8_t* sfb2 = mx ? at<uint8_t>(ws, L.h_sf_tiled) : nullptr;
 
   CUtensorMap tm_w1, tm_w2, tm_sf1, tm_sf2, tm_x[moe::kNumXMaps], tm_h[moe::kNumXMaps];
+  CUtensorMap tm_xp[moe::kNumXMaps], tm_hp[moe::kNumXMaps];   // CTA-pair half boxes
   // prepared weights: contiguous 128-row x 128-element boxes (64-byte rows
   // of E2M1 codes, or 128-byte rows of E4M3 codes in MXFP8); prepared
   // scales: one 512-byte block per box
@@ -330,6 +331,14 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
                     : make_tmap(&tm_h[i], hq, R, I, MapKind::kBytes, 128, rows)) != MOE_OK)
       return rc;
   }
+  const bool pair = variant == 6 && mode == MOE_W4A8_MXFP4_FP8;
+  if (pair)
+    for (int i = 0; i < moe::kNumXMaps; ++i) {
+      const uint32_t rows = static_cast<uint32_t>(moe::kPairBoxRowsAt(i));
+      if ((rc = make_tmap(&tm_xp[i], xq, R, H, MapKind::kBytes, 128, rows)) != MOE_OK ||
+          (rc = make_tmap(&tm_hp[i], hq, R, I, MapKind::kBytes, 128, rows)) != MOE_OK)
+        return rc;
+    }
 
   cudaEvent_t* ev = opts ? static_cast<cudaEvent_t*>(opts->stage_events) : nullptr;
   int stage = 0;
@@ -373,7 +382,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   // block scales ride with the operands into the MMA
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
                    mx ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, dev.num_sms,
-                   prefetch, mx, sfb1, static_cast<const uint8_t*>(w1)};
+                   prefetch, mx, sfb1, static_cast<const uint8_t*>(w1), pair ? tm_xp : nullptr};
   MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(true, g1, st) : moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
   if (w4a16) {
@@ -386,7 +395,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   MOE_CUDA(mark());
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
                    mx ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, dev.num_sms,
-                   prefetch, mx, sfb2, static_cast<const uint8_t*>(w2)};
+                   prefetch, mx, sfb2, static_cast<const uint8_t*>(w2), pair ? tm_hp : nullptr};
   MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(false, g2, st)
                  : moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());

@@ -273,6 +273,63 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
       const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
       const uint64_t sdesc0 = smem_desc(smem_u32(smem + C::kOffSF), 0, 128, 0);
       const uint64_t sbdesc0 = smem_desc(smem_u32(smem + C::kOffSFBs), 0, 128, 0);
+      // One stage: weight scales into TMEM, the 4 MMAs of its 128 K (the
+      // first of an item's first stage overwrites the accumulator), and the
+      // commit that frees the slot when they complete.
+      auto issue_stage = [&](int stage, uint32_t d_tmem, uint32_t id0, int nmma, bool first) {
+        const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
+        tc_cp_32x128b_x4_warp(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
+        uint32_t sfb = tmem + C::kColSFB;
+        if (MX8) {
+          sfb += static_cast<uint32_t>(8 * stage);
+          const uint64_t sbd = sbdesc0 + static_cast<uint64_t>(stage * (C::kSFBSlot >> 4));
+          tc_cp_32x128b_x4_warp(sfb, sbd);
+          if (nmma > 128) tc_cp_32x128b_x4_warp(sfb + 4, sbd + (512 >> 4));
+        }
+        const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
+        const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
+#pragma unroll
+        for (uint32_t kk = 0; kk < 4; ++kk)
+          tc_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
+                         sfb, (!first || kk > 0) ? 1u : 0u);
+        tc_commit_warp(empty + stage);
+      };
+      if constexpr (NI == 1) {
+        // One issuer (prefill tiles): items in order, an item's K stages in
+        // order.  The issuing warp's serial instruction stream bounds the
+        // MMA rate on these tiles, so the loop carries nothing but the stage
+        // and phase counters.
+        uint32_t stage = 0, phase = 0;
+        int fidx = 0;
+        bool ok = true;
+        for (int item = blockIdx.x, it = 0; ok && item < num_items;
+             item += static_cast<int>(gridDim.x), ++it) {
+          const int4 td = tiles[item / MT];
+          const int nmma = (td.z + 15) & ~15;
+          const uint32_t id0 = idesc_mx(MX8 ? 0 : 5, 0, static_cast<uint32_t>(nmma), 0, 0);
+          const int acc = it % NB;
+          if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
+                              status, kDevTimeout, abort_flag))
+            break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+          for (int ks = 0; ks < KS; ++ks) {
+            if (!mbar_wait_warp(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_stage(static_cast<int>(stage), d_tmem, id0, nmma, ks == 0);
+            if (prefetch_stages > 0 && lane == 0) *progress = fidx;
+            ++fidx;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) tc_commit_warp(tfull + acc);   // the item's accumulator is final
+        }
+      } else {
       int stage = i % STAGES, ks = i % KS, it = i / KS;   // ni <= KS, so it == 0
       int nmma = 16, fidx = i;
       uint32_t phase = (i / STAGES) & 1;
@@ -296,22 +353,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
         if (!mbar_wait_warp(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag))
           break;
         tc_fence_after();
-        const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
-        tc_cp_32x128b_x4_warp(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
-        uint32_t sfb = tmem + C::kColSFB;
-        if (MX8) {
-          sfb += static_cast<uint32_t>(8 * stage);
-          const uint64_t sbd = sbdesc0 + static_cast<uint64_t>(stage * (C::kSFBSlot >> 4));
-          tc_cp_32x128b_x4_warp(sfb, sbd);
-          if (nmma > 128) tc_cp_32x128b_x4_warp(sfb + 4, sbd + (512 >> 4));
-        }
-        const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
-        const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
-#pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)
-          tc_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
-                         sfb, (!new_item || kk > 0) ? 1u : 0u);
-        tc_commit_warp(empty + stage);
+        issue_stage(stage, d_tmem, id0, nmma, new_item);
         if (i == 0 && lane == 0) *progress = fidx;
         fidx += ni;
         stage += ni;
@@ -328,6 +370,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
         }
         if (new_item) tc_commit_warp(tfull + acc);   // this issuer's share of the item is queued
       }
+      }
       // No MMA or TMEM copy may still be running when TMEM is freed.
       tc_commit_warp(drain + i);
       int32_t none = 0;
@@ -336,8 +379,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     if (warp < C::kIssuer0 + NI + kEpiWarps) {
-      epilogue_loop<BN, NI, NB, SWIGLU>(C::kIssuer0 + NI, ni, tiles, num_items, MT, tfull, tempty, tmem,
-                                         row_scale, out, out_ld, timeout_ns, status, abort_flag);
+      const EpiSched sch{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), MT, 1, 0, 0u};
+      epilogue_loop<BN, NI, NB, SWIGLU>(C::kIssuer0 + NI, ni, tiles, num_items, sch, tfull, tempty,
+                                         tmem, row_scale, out, out_ld, timeout_ns, status,
+                                         abort_flag);
     } else if (prefetch_stages > 0) {
       // ---------------------------------------------------------- prefetcher
       // Optional: asks L2 for the weight box of fill g while the first issuer
@@ -419,7 +464,8 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
 //      most weight bytes in flight), 6 issuers;
 //   4: tiles of <= 224 tokens with 2 issuers and one accumulator buffer (the
 //      epilogue no longer overlaps the next item's MMAs);
-//   5: tiles of <= 160 tokens, 6 stages.
+//   5: tiles of <= 160 tokens, 6 stages;
+//   6: tiles of <= 160 tokens on CTA pairs (gemm_pair.cu), 8 stages.
 #define MOE_GEMM_VARIANTS(X)          \
   X(1, kDecodeBN, 10, 5, 2, 10, 5)    \
   X(2, kPrefillBN, 5, 1, 2, 4, 1)     \
@@ -428,6 +474,7 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
   X(5, kMidBN, 6, 1, 2, 6, 1)
 
 int gemm_tile_tokens(int variant) {
+  if (variant == 6) return kPairBN;
   switch (variant) {
 #define MOE_X(v, bn, st, ni, nb, st8, ni8) \
   case v:                                  \
@@ -440,6 +487,14 @@ int gemm_tile_tokens(int variant) {
 }
 
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s) {
+  // Variant 6: CTA pairs where the operands allow (W4A8, an even number of
+  // M-tiles), else the one-CTA kernel with the same 160-token tiles.
+  static_assert(kPairBN == kMidBN, "variant 6 falls back to variant 5's tile size");
+  if (variant == 6) {
+    if (gemm_pair_supported(a.m_per_expert, a.mx8) && a.tmap_x_pair && a.num_sms >= 2)
+      return launch_gemm_pair(swiglu, a, s);
+    variant = 5;
+  }
   switch (variant) {
 #define MOE_X(v, bn, st, ni, nb, st8, ni8)                                        \
   case v:                                                                         \

@@ -325,7 +325,8 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    epilogue_loop<BN, NI, 2, SWIGLU>(C::kFirstEpiWarp, NI, tiles, num_items, MT, tfull, tempty,
+    const EpiSched sch{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), MT, 1, 0, 0u};
+    epilogue_loop<BN, NI, 2, SWIGLU>(C::kFirstEpiWarp, NI, tiles, num_items, sch, tfull, tempty,
                                      tmem, nullptr, out, out_ld, timeout_ns, status, abort_flag);
   }
 

@@ -44,9 +44,27 @@ constexpr int kEpiWarps = 8;
 //     pairs them, h = silu(g) * u -> bf16 out[row, feature];
 //   else:   bf16 out[row, 128 mt + 32q + lane].
 // Releases the accumulator buffer (tempty) after reading it.
+//
+// EpiSched says which items this CTA's epilogue visits and where their
+// weight M-tile is: items item0, item0 + item_step, ...; item -> tile
+// item / items_per_tile, M-tile (item % items_per_tile) * mt_mul + mt_add.
+// A CTA that runs its own MMAs uses (blockIdx.x, gridDim.x, MT, 1, 0).  In a
+// CTA pair the item is an M-tile pair and CTA rank r holds M-tile 2p + r;
+// its buffer release goes to the MMA-issuing CTA's tempty barrier, whose
+// shared::cluster address is release_cluster (0: the local tempty).
+struct EpiSched {
+  int item0, item_step, items_per_tile, mt_mul, mt_add;
+  uint32_t release_cluster;
+};
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 template <int BN, int NI, int NB, bool SWIGLU>
 __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4* __restrict__ tiles,
-                                              int num_items, int MT, uint64_t* tfull,
+                                              int num_items, EpiSched sch, uint64_t* tfull,
                                               uint64_t* tempty, uint32_t tmem,
                                               const float* __restrict__ row_scale,
                                               __nv_bfloat16* __restrict__ out, int out_ld,
@@ -57,8 +75,9 @@ __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4
   const int half = (warp - first_warp) >> 2;
   int acc = 0;
   uint32_t acc_phase = 0;
-  for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-    const int tile = item / MT, mt = item % MT;
+  for (int item = sch.item0; item < num_items; item += sch.item_step) {
+    const int tile = item / sch.items_per_tile;
+    const int mt = (item % sch.items_per_tile) * sch.mt_mul + sch.mt_add;
     const int4 td = tiles[tile];
     const int row0 = td.y, ntok = td.z, nchunks = (td.z + 15) >> 4;
     const int split = (nchunks + 1) >> 1;
@@ -107,7 +126,12 @@ __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(tempty + acc);
+    if (lane == 0) {
+      if (sch.release_cluster)
+        mbar_arrive_cluster(sch.release_cluster + static_cast<uint32_t>(8 * acc));
+      else
+        mbar_arrive(tempty + acc);
+    }
     if (++acc == NB) {
       acc = 0;
       acc_phase ^= 1u;

@@ -60,6 +60,11 @@ constexpr int kW4A16BN = 64;         // max tokens per tile of the W4A16 GEMM
 // 16, 32, 64, 96, ..., 224.
 constexpr int kNumXMaps = 8;
 __host__ __device__ constexpr int kXBoxRowsAt(int i) { return i == 0 ? 16 : 32 * i; }
+// CTA-pair GEMM (gemm_pair.cu): token tiles of up to kPairBN rows, each CTA
+// staging half a tile through maps with box heights 16, 32, ..., 128 rows.
+constexpr int kPairBN = 160;
+constexpr int kPairStages = 8;
+__host__ __device__ constexpr int kPairBoxRowsAt(int i) { return 16 * (i + 1); }
 
 // MXFP8 mode: the activation (B operand) scale bytes are written by the
 // quantisers straight into the GEMM's per-tile layout.  For tile t of the
@@ -98,6 +103,7 @@ struct GemmArgs {
   bool mx8;                    // MXFP8 operands: E4M3 weights, per-32 activation scales
   const uint8_t* sfb_tiled;    // MXFP8: activation scales in the per-tile layout
   const uint8_t* w_base;       // prepared weight boxes (for the optional L2 prefetcher)
+  const CUtensorMap* tmap_x_pair;  // kNumXMaps maps, box heights kPairBoxRowsAt (or null)
 };
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
@@ -147,9 +153,14 @@ cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_
 // weight boxes as bytes, tmap_x over bf16 activations with 64-element
 // boxes; row_scale, mx8 and sfb_tiled unused).
 cudaError_t launch_gemm_bf16(bool swiglu, const GemmArgs& a, cudaStream_t s);
+// The grouped GEMM on CTA pairs (gemm_pair.cu): W4A8 operands, M-tiles
+// taken two at a time, so m_per_expert must be a multiple of 256; needs
+// tmap_x_pair.
+bool gemm_pair_supported(int m_per_expert, bool mx8);
+cudaError_t launch_gemm_pair(bool swiglu, const GemmArgs& a, cudaStream_t s);
 // Tile variants 1..kMaxTileVariant; the largest token tile of each (the tile
 // list is built with this bound).
-constexpr int kMaxTileVariant = 5;
+constexpr int kMaxTileVariant = 6;
 int gemm_tile_tokens(int variant);
 // Re-lays one weight tensor [E, M, K] (E2M1 with K/2 bytes per row, or E4M3
 // with K bytes per row when fp8) and its scales [E, M, K/32] for the GEMM;
