@@ -204,12 +204,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
       // fill f = s + j * STAGES: K stage ks of the CTA's it-th item (KS >= STAGES
       // is not assumed; the counters advance without divisions)
       int ks = s % KS, item = blockIdx.x + (s / KS) * gridDim.x;
+      // the lane's current item: its tile and first weight box, re-read only
+      // when the item changes (runtime divisions stay off the per-fill path)
+      int cur_item = -1;
+      int4 td = make_int4(0, 0, 0, 0);
+      int64_t blk0 = 0;
       while (item < num_items) {
-        const int mt = item % MT;
-        const int4 td = tiles[item / MT];
-        // prepared weights: one contiguous 128 x 128 box per (expert, M-tile,
-        // K stage); box row = ((e * MT + mt) * KS + ks) * 128
-        const int64_t blk = (static_cast<int64_t>(td.x) * MT + mt) * KS + ks;
+        if (item != cur_item) {
+          cur_item = item;
+          td = tiles[item / MT];
+          // prepared weights: one contiguous 128 x 128 box per (expert,
+          // M-tile, K stage); box row = ((e * MT + mt) * KS + ks) * 128
+          blk0 = (static_cast<int64_t>(td.x) * MT + item % MT) * KS;
+        }
+        const int64_t blk = blk0 + ks;
         if (!mbar_wait(empty + s, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag)) break;
         if (role == 0) {
           mbar_arrive_expect_tx(full + s, a_tx_bytes);

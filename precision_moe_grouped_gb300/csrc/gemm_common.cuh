@@ -99,23 +99,28 @@ __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] += w[j];
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] *= __shfl_sync(0xffffffffu, sc, j);
       if constexpr (SWIGLU) {
+        // After the exchange a lane holds gate and up of one (feature, token)
+        // pair, so the token's scale is applied to those two values only.
         const bool lo = lane < 16;
         const int f = 64 * mt + 16 * q + (lane & 15);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           const float send = lo ? v[2 * jj + 1] : v[2 * jj];
           const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-          const float g = lo ? v[2 * jj] : recv;
-          const float u = lo ? recv : v[2 * jj + 1];
-          const float hval = g / (1.0f + expf(-g)) * u;
+          const float s_n = __shfl_sync(0xffffffffu, sc, 2 * jj + (lo ? 0 : 1));
+          const float g = (lo ? v[2 * jj] : recv) * s_n;
+          const float u = (lo ? recv : v[2 * jj + 1]) * s_n;
+          // silu(g) = g / (1 + e^-g); fast exp and division (relative error
+          // ~1e-6, far below the bf16 rounding of h that follows)
+          const float hval = __fdividef(g, 1.0f + __expf(-g)) * u;
           const int n = c0 + 2 * jj + (lo ? 0 : 1);
           if (n < ntok)
             out[static_cast<int64_t>(row0 + n) * out_ld + f] = __float2bfloat16_rn(hval);
         }
       } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] *= __shfl_sync(0xffffffffu, sc, j);
         const int c = mt * kTileM + 32 * q + lane;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
