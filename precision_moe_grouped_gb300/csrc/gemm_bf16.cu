@@ -9,21 +9,25 @@
 //           MXFP4 weights dequantised inside the kernel).
 //
 // The tensor cores have no mixed FP4 x BF16 MMA, so the weights are
-// converted in shared memory, in sub-stages of 64 K: the packed E2M1 codes of
-// 128 weight rows x 64 K (half of a prepared 128 x 128 box, 32 bytes per row)
-// and the box's E8M0 scales land in a raw slot; a transform warp rewrites
-// them as bf16 values e2m1 * 2^(scale - 127) -- exact in bf16 (a power of two
-// times at most two significant bits) -- into a converted slot (one 128 B x
-// 128-row K atom, 128-byte swizzle); the MMA reads the converted slot and
-// the sub-stage's bf16 activation atom.  Everything else (tile list, swap-AB
-// orientation, persistent static striding, epilogue) is the FP8 GEMM's.
+// converted on the fly, in sub-stages of 64 K: the packed E2M1 codes of 128
+// weight rows x 64 K (half of a prepared 128 x 128 box, 32 bytes per row)
+// and the box's E8M0 scales land in a raw shared-memory slot; transform
+// warps turn them into bf16 values e2m1 * 2^(scale - 127) -- exact in bf16
+// (a power of two times at most two significant bits) -- and store them
+// straight into TMEM, where the MMA (.kind::f16) reads its A operand; only
+// the bf16 activation atom (B) is read from shared memory.  Keeping the
+// converted weights in TMEM frees shared memory for a deep raw ring and
+// gives the conversion 8 slots to run ahead in.  Everything else (tile
+// list, swap-AB orientation, persistent static striding, epilogue) is the
+// FP8 GEMM's.
 //
 // Roles: warp 0 = TMA producers (lane s < S: weight half-box + scales into
 // raw slot s; lane S + s: activation atom into activation slot s); warps
 // 1..NI = MMA issuers (warp-uniform, one elected lane issues; issuer i takes
-// the sub-stages g = i mod NI into its own accumulator); the next 4 warps =
-// transform (warp w converts the sub-stages g = w mod 4); the last 8 warps =
-// epilogue.
+// the sub-stages g = i mod NI into its own accumulator); the next 8 warps =
+// transform, two per TMEM lane quarter (warp w handles the rows of its
+// quarter, warp % 4, of the sub-stages g = w' mod 2, w' = its rank among
+// the transform warps / 4); the last 8 warps = epilogue.
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -34,29 +38,28 @@ namespace moe {
 
 namespace {
 
-constexpr int kTransformWarps = 4;
+constexpr int kTransformWarps = 8;   // two per TMEM lane quarter
 constexpr int kBf16Issuers = 2;
 
-template <int BN, int S, int Q>
+template <int BN, int S, int QA>
 struct Bf16Cfg {
   static_assert(BN % 16 == 0 && BN <= 128, "token tile of the W4A16 GEMM: 16..128 rows");
   static_assert(2 * S <= 32, "producer lanes must fit one warp");
-  static_assert(S % kBf16Issuers == 0 && Q % kBf16Issuers == 0,
-                "each slot must belong to one MMA issuer");
-  static_assert(S % kTransformWarps == 0 && Q % kTransformWarps == 0,
-                "each slot must belong to one transform warp");
+  // slot s (raw, activation) and TMEM slot a always belong to one issuer and
+  // one transform pair, so each barrier is waited on in phase order by the
+  // same threads
+  static_assert(S % kBf16Issuers == 0 && QA % kBf16Issuers == 0 && S % 2 == 0 && QA % 2 == 0,
+                "slots must map to single issuers and transform pairs");
   static constexpr int kRawBytes = kTileM * 32;      // packed E2M1, 64 K per row
   static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes (128 K)
   static constexpr int kBBytes = BN * 128;           // 64 bf16 of K per token row
-  static constexpr int kCvBytes = kTileM * 128;      // 128 rows x 64 bf16
   static constexpr int kOffRaw = 0;
   static constexpr int kOffB = kOffRaw + S * kRawBytes;
-  static constexpr int kOffCv = kOffB + S * kBBytes;
-  static constexpr int kOffSF = kOffCv + Q * kCvBytes;
+  static constexpr int kOffSF = kOffB + S * kBBytes;
   // code byte -> bf16x2 table, one copy per shared-memory bank: entry b of
   // lane l at word 32 b + l, so a warp's lookups never conflict
   static constexpr int kOffLut = kOffSF + S * kSFBytes;
-  static constexpr int kNumBars = 4 * S + 2 * Q + 2 * 2 + kBf16Issuers;
+  static constexpr int kNumBars = 4 * S + 2 * QA + 2 * 2 + kBf16Issuers;
   static constexpr int kOffBar = kOffLut + 256 * 32 * 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
@@ -64,9 +67,12 @@ struct Bf16Cfg {
   static constexpr int kFirstXfWarp = 1 + kBf16Issuers;
   static constexpr int kFirstEpiWarp = kFirstXfWarp + kTransformWarps;
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
-  static constexpr int kCols = 2 * kBf16Issuers * BN;   // 2 buffers x NI partials
-  static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
-                                   : kCols <= 256 ? 256 : 512;
+  // TMEM: 2 accumulator buffers x NI partials x BN columns, then QA slots of
+  // converted weights, 32 columns each (128 rows x 64 bf16)
+  static constexpr int kColA = 2 * kBf16Issuers * BN;
+  static constexpr int kColsUsed = kColA + 32 * QA;
+  static_assert(kColsUsed <= 512, "TMEM budget exceeded");
+  static constexpr int kTmemCols = kColsUsed <= 256 ? 256 : 512;
 };
 
 // Instruction descriptor of .kind::f16 with bf16 A and B, fp32 accumulate,
@@ -75,15 +81,34 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma_f16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                                uint32_t idesc, uint32_t accumulate) {
+// D (+)= A x B^T with A read from TMEM (128 lanes = rows; K = 16 bf16 in 8
+// columns, two per column, the lower K index in the low half) and B from
+// shared memory; one elected lane of the warp issues.
+__device__ __forceinline__ void tc_mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint64_t bdesc, uint32_t idesc,
+                                                   uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Each thread of the warp writes 32 consecutive 32-bit TMEM columns of its
+// lane (the warp's lane quarter), then waits until the stores are done.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Value of each E2M1 code (sign, 2-bit exponent with bias 1, 1-bit
@@ -98,8 +123,19 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
   return (code & 8u) ? -v : v;
 }
 
-template <int BN, int S, int Q, bool SWIGLU>
-__global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
+// bf16 of the E8M0 scale 2^(sb - 127), twice: the exponent field is sb
+// (sb = 0: the subnormal 2^-127; sb = 255: NaN).
+__device__ __forceinline__ __nv_bfloat162 e8m0_bf16x2(uint32_t sb) {
+  const uint16_t bits =
+      sb == 0 ? 0x0040u : sb == 255 ? 0x7FC0u : static_cast<uint16_t>(sb << 7);
+  __nv_bfloat162 r;
+  r.x = __ushort_as_bfloat16(bits);
+  r.y = r.x;
+  return r;
+}
+
+template <int BN, int S, int QA, bool SWIGLU>
+__global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_w,
                              const __grid_constant__ XMaps tmap_x,
                              const __grid_constant__ CUtensorMap tmap_sf,
@@ -107,7 +143,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
                              const int32_t* __restrict__ num_tiles_p,
                              __nv_bfloat16* __restrict__ out, int m_per_expert, int K,
                              int out_ld, int32_t* __restrict__ status, uint64_t timeout_ns) {
-  using C = Bf16Cfg<BN, S, Q>;
+  using C = Bf16Cfg<BN, S, QA>;
   constexpr int NI = kBf16Issuers;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -116,9 +152,9 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
   uint64_t* raw_empty = raw_full + S;
   uint64_t* b_full = raw_empty + S;
   uint64_t* b_empty = b_full + S;
-  uint64_t* cv_full = b_empty + S;
-  uint64_t* cv_empty = cv_full + Q;
-  uint64_t* tfull = cv_empty + Q;
+  uint64_t* a_full = b_empty + S;
+  uint64_t* a_empty = a_full + QA;
+  uint64_t* tfull = a_empty + QA;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -131,13 +167,13 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(raw_full + s, 1);
-      mbar_init(raw_empty + s, 1);   // its transform warp has read it
+      mbar_init(raw_empty + s, 4);   // the four quarter warps of its transform pair
       mbar_init(b_full + s, 1);
       mbar_init(b_empty + s, 1);
     }
-    for (int q = 0; q < Q; ++q) {
-      mbar_init(cv_full + q, 1);
-      mbar_init(cv_empty + q, 1);
+    for (int a = 0; a < QA; ++a) {
+      mbar_init(a_full + a, 4);      // each quarter of the 128 rows stored
+      mbar_init(a_empty + a, 1);     // the MMAs that read it completed
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull + a, NI);                     // every issuer commits its share
@@ -213,7 +249,6 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
   } else if (warp <= NI) {
     // ------------------------------------------------------------ MMA issuers
     const int i = warp - 1;
-    const uint64_t cdesc0 = smem_desc(smem_u32(smem + C::kOffCv), 0, 1024, 2);
     const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
     int g = i, kh = i, it = 0;
     bool new_item = true;
@@ -230,20 +265,20 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
         tc_fence_after();
         d_tmem = tmem + static_cast<uint32_t>((acc * NI + i) * BN);
       }
-      const int s = g % S, q = g % Q;
-      if (!mbar_wait_warp(cv_full + q, static_cast<uint32_t>((g / Q) & 1), timeout_ns, status,
+      const int s = g % S, a = g % QA;
+      if (!mbar_wait_warp(a_full + a, static_cast<uint32_t>((g / QA) & 1), timeout_ns, status,
                           kDevTimeout, abort_flag))
         break;
       if (!mbar_wait_warp(b_full + s, static_cast<uint32_t>((g / S) & 1), timeout_ns, status,
                           kDevTimeout, abort_flag))
         break;
       tc_fence_after();
-      const uint64_t ad = cdesc0 + static_cast<uint64_t>((q * C::kCvBytes) >> 4);
+      const uint32_t at = tmem + static_cast<uint32_t>(C::kColA + 32 * a);
       const uint64_t bd = bdesc0 + static_cast<uint64_t>((s * C::kBBytes) >> 4);
 #pragma unroll
-      for (uint32_t kk = 0; kk < 4; ++kk)   // K = 16 bf16 = 32 bytes per MMA
-        tc_mma_f16_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id, (!new_item || kk > 0) ? 1u : 0u);
-      tc_commit_warp(cv_empty + q);
+      for (uint32_t kk = 0; kk < 4; ++kk)   // K = 16 bf16 per MMA: 8 TMEM columns, 32 smem bytes
+        tc_mma_f16_ts_warp(d_tmem, at + 8 * kk, bd + 2 * kk, id, (!new_item || kk > 0) ? 1u : 0u);
+      tc_commit_warp(a_empty + a);
       tc_commit_warp(b_empty + s);
       g += NI;
       kh += NI;
@@ -260,68 +295,50 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
     mbar_wait_warp(drain + i, 0, timeout_ns, status, kDevTimeout, &none);
   } else if (warp < C::kFirstEpiWarp) {
     // ------------------------------------------------------------ transform
-    // Transform warp w converts the sub-stages g = w, w + 4, ... whole: lane
-    // l takes the 16-byte units v = l + 32 u (u < 8) of packed codes (row
-    // v / 2, 32-K block p = v % 2 of the sub-stage, one scale byte) -> 32
-    // bf16 = four 16-byte units of the converted slot (units 4p .. 4p+3 of
-    // the row, 128-byte swizzled).  Consecutive lanes read consecutive units;
-    // the eight units of a lane are independent, which keeps the loads and
-    // the table lookups in flight together.  Each code byte becomes a bf16
-    // pair through the shared table (this lane's bank copy: no conflicts);
-    // one bf16x2 multiply applies the scale -- exact.
-    const int w = warp - C::kFirstXfWarp;
+    // Transform warp w (quarter q = warp % 4, pair p) converts, for the
+    // sub-stages g = p, p + 2, ..., the 32 rows r = 32 q + lane: lane l reads
+    // its row's 32 code bytes and two scale bytes, turns each code byte into
+    // a bf16 pair through the shared table (this lane's bank copy: no
+    // conflicts), applies the 32-K block's scale with one exact bf16x2
+    // multiply, and stores the row's 64 values into 32 columns of its TMEM
+    // lane in TMEM slot g % QA.
+    const int q = warp & 3, p = (warp - C::kFirstXfWarp) >> 2;
+    const int r = 32 * q + lane;
     const __nv_bfloat162* lut = reinterpret_cast<const __nv_bfloat162*>(smem + C::kOffLut);
+    const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
     int total = 0;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) total += KH;
-    for (int g = w; g < total; g += kTransformWarps) {
-      const int s = g % S, q = g % Q;
-      if (!mbar_wait(raw_full + s, static_cast<uint32_t>((g / S) & 1), timeout_ns, status,
-                     kDevTimeout, abort_flag))
+    for (int g = p; g < total; g += 2) {
+      const int s = g % S, a = g % QA;
+      if (!mbar_wait_warp(raw_full + s, static_cast<uint32_t>((g / S) & 1), timeout_ns, status,
+                          kDevTimeout, abort_flag))
         break;
-      if (!mbar_wait(cv_empty + q, static_cast<uint32_t>((g / Q) & 1) ^ 1u, timeout_ns, status,
-                     kDevTimeout, abort_flag))
+      if (!mbar_wait_warp(a_empty + a, static_cast<uint32_t>((g / QA) & 1) ^ 1u, timeout_ns,
+                          status, kDevTimeout, abort_flag))
         break;
-      const uint8_t* raw = smem + C::kOffRaw + s * C::kRawBytes;
+      tc_fence_after();
+      const uint8_t* raw = smem + C::kOffRaw + s * C::kRawBytes + 32 * r;
       const uint8_t* sf = smem + C::kOffSF + s * C::kSFBytes;
-      uint8_t* cv = smem + C::kOffCv + q * C::kCvBytes;
       const int half = (g % KH) & 1;   // the 64-K half of the 128-K box
-      uint4 codes[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        codes[u] = *reinterpret_cast<const uint4*>(raw + 16 * (lane + 32 * u));
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int v = lane + 32 * u, r = v >> 1, p = v & 1;
-        // scale 2^(sb - 127) of 32-K block 2 * half + p of the box, as bf16:
-        // exponent field sb (sb = 0: the subnormal 2^-127; sb = 255: NaN)
-        const uint32_t sb = sf[16 * (r & 31) + 4 * (r >> 5) + 2 * half + p];
-        const uint16_t sbits = sb == 0 ? 0x0040u : sb == 255 ? 0x7FC0u
-                                                           : static_cast<uint16_t>(sb << 7);
-        __nv_bfloat162 scale2;
-        scale2.x = __ushort_as_bfloat16(sbits);
-        scale2.y = scale2.x;
-        const uint32_t cw[4] = {codes[u].x, codes[u].y, codes[u].z, codes[u].w};
-        uint8_t* dst = cv + r * 128;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {   // 8 codes (4 bytes) -> 8 bf16 -> one 16-byte unit
-          uint32_t wd[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const __nv_bfloat162 pr =
-                __hmul2(lut[(((cw[j] >> (8 * b)) & 0xFFu) << 5) + lane], scale2);
-            wd[b] = *reinterpret_cast<const uint32_t*>(&pr);
-          }
-          const int un = 4 * p + j;
-          *reinterpret_cast<uint4*>(dst + ((un ^ (r & 7)) << 4)) =
-              make_uint4(wd[0], wd[1], wd[2], wd[3]);
-        }
-      }
-      fence_proxy_async_smem();   // generic-proxy writes -> the MMA's async proxy
+      const uint4 c0 = *reinterpret_cast<const uint4*>(raw);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(raw + 16);
+      const int sfo = 16 * (r & 31) + 4 * (r >> 5) + 2 * half;
+      const __nv_bfloat162 s0 = e8m0_bf16x2(sf[sfo]), s1 = e8m0_bf16x2(sf[sfo + 1]);
+      // the raw slot has been read: its producer may refill it
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(cv_full + q);
-        mbar_arrive(raw_empty + s);
+      if (lane == 0) mbar_arrive(raw_empty + s);
+      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      uint32_t v[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {   // code byte c = K elements 2c, 2c + 1
+        const uint32_t byte = (cw[c >> 2] >> (8 * (c & 3))) & 0xFFu;
+        const __nv_bfloat162 pr = __hmul2(lut[(byte << 5) + lane], c < 16 ? s0 : s1);
+        v[c] = *reinterpret_cast<const uint32_t*>(&pr);
       }
+      tmem_st_32x32b_x32(tmem + tlane + static_cast<uint32_t>(C::kColA + 32 * a), v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_full + a);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -338,10 +355,10 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, Q>::kThreads, 1)
   }
 }
 
-template <int BN, int S, int Q, bool SWIGLU>
+template <int BN, int S, int QA, bool SWIGLU>
 cudaError_t launch_bf16_variant(const GemmArgs& a, cudaStream_t s) {
-  using C = Bf16Cfg<BN, S, Q>;
-  auto kern = grouped_gemm_bf16_kernel<BN, S, Q, SWIGLU>;
+  using C = Bf16Cfg<BN, S, QA>;
+  auto kern = grouped_gemm_bf16_kernel<BN, S, QA, SWIGLU>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -358,10 +375,11 @@ cudaError_t launch_bf16_variant(const GemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-// W4A16: 64-token tiles, 8 raw/activation slots and 4 converted slots of 64 K.
+// W4A16: 64-token tiles, 12 raw/activation slots, 8 TMEM slots of converted
+// weights (64 K each).
 cudaError_t launch_gemm_bf16(bool swiglu, const GemmArgs& a, cudaStream_t s) {
-  return swiglu ? launch_bf16_variant<kW4A16BN, 8, 4, true>(a, s)
-                : launch_bf16_variant<kW4A16BN, 8, 4, false>(a, s);
+  return swiglu ? launch_bf16_variant<kW4A16BN, 12, 8, true>(a, s)
+                : launch_bf16_variant<kW4A16BN, 12, 8, false>(a, s);
 }
 
 }  // namespace moe
