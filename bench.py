@@ -184,23 +184,39 @@ def ncu_traffic(stage: str, cfg_name: str, T: int):
     return rec.get("dram_bytes_per_launch")
 
 
-def alg_cost(stage: str, cfg, T: int, n_touched: int):
-    """Algorithmic (bytes, flops) of one launch of `stage`."""
+def alg_cost(stage: str, cfg, T: int, n_touched: int, mode: int = 0):
+    """Algorithmic (bytes, flops) of one launch of `stage` in quantisation
+    `mode` (0 W4A8, 1 W4A16, 2 W8A8): weights are packed E2M1 (0.5 B) or
+    E4M3 (1 B) per element plus one scale byte per 32; the expanded
+    activations are E4M3 (+ a row scale, or a scale byte per 32 in W8A8) or
+    bf16 (W4A16, which has no h-quantisation)."""
     E, k, H, I = cfg.num_experts, cfg.top_k, cfg.hidden, cfg.inter
     R = T * k
-    w1 = 2 * I * H * (0.5 + 1 / 32)
-    w2 = H * I * (0.5 + 1 / 32)
+    wb = 1.0 if mode == 2 else 0.5
+    w1 = 2 * I * H * (wb + 1 / 32)
+    w2 = H * I * (wb + 1 / 32)
+    act = 2.0 if mode == 1 else (1 + 1 / 32) if mode == 2 else 1.0   # bytes per element
+    rs = 0 if mode == 1 else 4                                         # row-scale bytes
     table = {
         "route": (T * E * 4 + R * 8, 0),
         "scan": (R * 0, 0),
         "rank": (R * 12, 0),
-        "quant_scatter": (T * H * 2 + R * H + R * 4, 0),
-        "gemm1": (n_touched * w1 + R * H + R * 4 + R * I * 2, 2.0 * R * H * 2 * I),
-        "hquant": (R * I * 2 + R * I + R * 4, 0),
-        "gemm2": (n_touched * w2 + R * I + R * 4 + R * H * 2, 2.0 * R * I * H),
+        "quant_scatter": (T * H * 2 + R * H * act + R * rs, 0),
+        "gemm1": (n_touched * w1 + R * H * act + R * rs + R * I * 2, 2.0 * R * H * 2 * I),
+        "hquant": (0, 0) if mode == 1 else (R * I * 2 + R * I * act + R * rs, 0),
+        "gemm2": (n_touched * w2 + R * I * act + R * rs + R * H * 2, 2.0 * R * I * H),
         "combine": (R * H * 2 + R * 8 + T * H * 2, 0),
     }
     return table[stage]
+
+
+# Per quantisation mode: the arithmetic the GEMMs compute in, and the
+# weight encoding of the synthetic data.
+MODE_DTYPE = {0: "fp8e4m3 x fp4e2m1 (mxf8f6f4), fp32 accumulate",
+              1: "bf16 x bf16 from fp4e2m1 weights (kind::f16), fp32 accumulate",
+              2: "fp8e4m3 x fp8e4m3 (mxf8f6f4, MX block scales), fp32 accumulate"}
+MODE_WEIGHTS = {0: "MXFP4", 1: "MXFP4", 2: "MXFP8"}
+MODE_NAME = {0: "MXFP4xFP8", 1: "MXFP4xBF16", 2: "MXFP8xMXFP8"}
 
 
 def fused_roofline(cfg, T, n_touched, t_s, pk, mode=0):
@@ -232,8 +248,9 @@ def run_ours(args, dist: Dist):
     T = args.tokens
     K, W = args.steps, args.warmup
     pk, pk_src = peaks()
+    mode = cfg.mode
     case = MI.make_case(cfg, T, device=f"cuda:{dist.local}")
-    moe = P.FusedMoE(case.w1, case.w1_sf, case.w2, case.w2_sf, cfg.top_k)
+    moe = P.FusedMoE(case.w1, case.w1_sf, case.w2, case.w2_sf, cfg.top_k, mode=mode)
     del case.w1, case.w1_sf, case.w2, case.w2_sf
     torch.cuda.synchronize()
     x, logits = case.x, case.logits
@@ -246,7 +263,7 @@ def run_ours(args, dist: Dist):
 
     def fwd(opts=None):
         P.forward(s, x, logits, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, out, ws,
-                  opts=opts)
+                  mode=mode, opts=opts)
 
     base = P.options(tile_variant=args.variant)
     for _ in range(max(W, 3)):
@@ -254,7 +271,7 @@ def run_ours(args, dist: Dist):
     torch.cuda.synchronize()
     if P.read_device_status(ws) != 0:
         raise RuntimeError("device status error after warm-up")
-    lay = P.workspace_layout(s)
+    lay = P.workspace_layout(s, mode)
     counts = ws[lay.counts:lay.counts + 4 * cfg.num_experts].view(torch.int32).cpu().numpy()
     n_touched = int((counts > 0).sum())
 
@@ -278,7 +295,7 @@ def run_ours(args, dist: Dist):
     ms = dist.max(ms_local)
     if P.read_device_status(ws) != 0:
         raise RuntimeError("device status error in timed region")
-    gpu_launches = P._lib.kernels_per_forward(T, 0) * K
+    gpu_launches = P._lib.kernels_per_forward(T, mode) * K
 
     # Kernel timing pass: the same K forwards with CUDA events the library
     # records on its stream before its first kernel and after each kernel.
@@ -300,14 +317,16 @@ def run_ours(args, dist: Dist):
     lh = logits.cpu().pin_memory()
     oh = torch.empty((T, cfg.hidden), dtype=torch.bfloat16).pin_memory()
     for _ in range(2):
-        P.forward_host(s, xh, lh, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, oh, ws, opts=base)
+        P.forward_host(s, xh, lh, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, oh, ws,
+                       mode=mode, opts=base)
     torch.cuda.synchronize()
     dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        P.forward_host(s, xh, lh, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, oh, ws, opts=base)
+        P.forward_host(s, xh, lh, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, oh, ws,
+                       mode=mode, opts=base)
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = dist.max(e0.elapsed_time(e1) / K)
@@ -315,10 +334,10 @@ def run_ours(args, dist: Dist):
 
     # dominant kernel and its roofline
     dom = max(stage_ms, key=stage_ms.get)
-    dbytes, dflops = alg_cost(dom, cfg, T, n_touched)
+    dbytes, dflops = alg_cost(dom, cfg, T, n_touched, mode)
     dsec = stage_ms[dom] / 1e3
     t_mem = dbytes / (pk["hbm_gbs"] * 1e9)
-    tc_peak = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+    tc_peak = pk["bf16_tflops_sustained"] * (1.0 if mode == 1 else FP8_OVER_BF16)
     t_tc = dflops / (tc_peak * 1e12)
     if t_tc > t_mem:
         roof = {"bound": "tensor", "achieved": dflops / dsec / 1e12, "peak": tc_peak,
@@ -333,19 +352,21 @@ def run_ours(args, dist: Dist):
                  "tensor_frac": (dflops / dsec / 1e12) / tc_peak if dflops else 0.0,
                  "hbm_frac": dbytes / dsec / 1e9 / pk["hbm_gbs"]})
 
-    fr = fused_roofline(cfg, T, n_touched, ms / 1e3, pk)
+    fr = fused_roofline(cfg, T, n_touched, ms / 1e3, pk, mode)
+    wbytes = (1.0 if mode == 2 else 0.5) + 1 / 32
     result = {
         "metric": METRIC, "value": dist.world * T / (ms / 1e3), "unit": UNIT,
         "n_gpus": dist.world, "steps": K, "warmup": W, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8e4m3 x fp4e2m1 (mxf8f6f4), fp32 accumulate",
-        "data": "synthetic (seeded N(0,1) activations/logits, N(0,0.02) weights as MXFP4)",
+        "dtype": MODE_DTYPE[mode],
+        "data": "synthetic (seeded N(0,1) activations/logits, N(0,0.02) weights as "
+                f"{MODE_WEIGHTS[mode]})" + (f", Zipf({cfg.zipf}) routing skew" if cfg.zipf else ""),
         "config": {"workload": f"DeepSeek-V3-shaped MoE layer E={cfg.num_experts} top-{cfg.top_k} "
-                               f"H={cfg.hidden} I={cfg.inter} SwiGLU, T={T}, MXFP4xFP8",
+                               f"H={cfg.hidden} I={cfg.inter} SwiGLU, T={T}, {MODE_NAME[mode]}",
                    "num_tokens": T, "num_experts": cfg.num_experts, "top_k": cfg.top_k,
                    "hidden": cfg.hidden, "inter": cfg.inter, "parallelism": f"replicas x{dist.world}",
                    "l2": "no flush: the touched expert weights per step "
-                         f"({n_touched * 3 * cfg.inter * cfg.hidden * 0.53125 / 1e9:.2f} GB) "
+                         f"({n_touched * 3 * cfg.inter * cfg.hidden * wbytes / 1e9:.2f} GB) "
                          "exceed the 129 MB L2",
                    "tile_variant": args.variant},
         "tflops": fr["flops"] / (ms / 1e3) / 1e12,
@@ -366,7 +387,7 @@ def run_ours(args, dist: Dist):
     if not args.no_sweep:
         result["sweep"] = sweep(args, cfg, moe, x, logits, dist, pk)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(cfg, T, x, logits, 6)
+        result["cpu_baseline"] = cpu_baseline(cfg, T, x, logits, 6 if mode != 2 else 3)
     if not args.no_other_modes:
         del moe, ws, out, case
         torch.cuda.empty_cache()
@@ -459,11 +480,12 @@ def sweep(args, cfg, moe, x_all, lg_all, dist, pk):
 
         def fwd(i):
             xs, ls = sets[i % nsets]
-            P.forward(s, xs, ls, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, out, ws, opts=o)
+            P.forward(s, xs, ls, moe.w1_p, moe.w1_sf_p, moe.w2_p, moe.w2_sf_p, out, ws,
+                      mode=cfg.mode, opts=o)
         for i in range(5):
             fwd(i)
         torch.cuda.synchronize()
-        lay = P.workspace_layout(s)
+        lay = P.workspace_layout(s, cfg.mode)
         touched = []
         for i in range(nsets):
             fwd(i)
@@ -480,7 +502,7 @@ def sweep(args, cfg, moe, x_all, lg_all, dist, pk):
         torch.cuda.synchronize()
         ms = dist.max(a.elapsed_time(b) / args.sweep_steps)
         n_t = sum(touched) / len(touched)
-        fr = fused_roofline(cfg, T, n_t, ms / 1e3, pk)
+        fr = fused_roofline(cfg, T, n_t, ms / 1e3, pk, cfg.mode)
         res.append({"T": T, "ms": ms, "tokens_s": dist.world * T / (ms / 1e3),
                     "tflops": fr["flops"] / (ms / 1e3) / 1e12, "experts_touched": n_t,
                     "roofline_frac": fr["frac"], "bound": fr["bound"],
@@ -517,8 +539,9 @@ def oracle_sample(cfg, T, x, logits, n_tok):
         def __getitem__(self, e):
             return w[int(e)][self.j]
     H, I, E = cfg.hidden, cfg.inter, cfg.num_experts
-    W = M.Weights(Lazy(0, (E, 2 * I, H // 2)), Lazy(1, (E, 2 * I, H // 32)),
-                  Lazy(2, (E, H, I // 2)), Lazy(3, (E, H, I // 32)))
+    kd = 1 if cfg.mode == MI.QUANT_W8A8 else 2   # weight bytes hold 1 or 2 elements
+    W = M.Weights(Lazy(0, (E, 2 * I, H // kd)), Lazy(1, (E, 2 * I, H // 32)),
+                  Lazy(2, (E, H, I // kd)), Lazy(3, (E, H, I // 32)), mode=cfg.mode)
     return xb, lg, W, toks, experts
 
 
@@ -527,7 +550,7 @@ def cpu_baseline(cfg, T, x, logits, n_tok):
     from oracle import moe as M
     xb, lg, W, toks, experts = oracle_sample(cfg, T, x, logits, n_tok)
     t = time.perf_counter()
-    M.forward(xb, lg, W, cfg.top_k)
+    M.forward(xb, lg, W, cfg.top_k, mode=cfg.mode)
     dt = time.perf_counter() - t
     return {"value": n_tok / dt, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
@@ -548,10 +571,10 @@ def run_reference(args, dist: Dist):
     from oracle import moe as M
     xb, lg, W, toks, experts = oracle_sample(cfg, T, x, logits, 1)
     for _ in range(args.warmup):
-        M.forward(xb, lg, W, cfg.top_k)
+        M.forward(xb, lg, W, cfg.top_k, mode=cfg.mode)
     t = time.perf_counter()
     for _ in range(args.steps):
-        M.forward(xb, lg, W, cfg.top_k)
+        M.forward(xb, lg, W, cfg.top_k, mode=cfg.mode)
     dt = time.perf_counter() - t
     v = args.steps / dt
     sample = (f"1 of the {T} tokens per step ({len(experts)} experts decoded and applied); "
