@@ -16,6 +16,7 @@
 // rank (one warp per chunk: stable expert-major row of every (token, slot))
 // -> quant_scatter (one CTA per token: FP8 codes written to each of the
 // token's k expanded rows).  Nothing returns to the host.
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cfloat>
@@ -162,11 +163,14 @@ __device__ int2 plan_tiles(int e, int E, int c, int off, int bn, bool write,
   return make_int2(toff, tsz);
 }
 
-// One CTA (blockDim >= E): per-expert counts, offsets, per-chunk bases
-// (stable ranks start there), and the GEMM tile list.  A tile is a run of
-// at most `bn` consecutive rows of one expert; an expert with c rows gets
-// ceil(c / tsz) tiles of tsz = roundup16(ceil(c / ceil(c / bn))) rows, so
-// its tiles are balanced and every MMA-N is a multiple of 16.
+// One CTA of P groups of Ep = roundup32(E) threads (P = blockDim / Ep >= 1):
+// per-expert counts, offsets, per-chunk bases (stable ranks start there),
+// and the GEMM tile list.  Group g sums, for its expert, the chunk counts of
+// its share of the chunks; the groups' partial sums give each expert's total
+// and each group's starting row.  A tile is a run of at most `bn`
+// consecutive rows of one expert; an expert with c rows gets ceil(c / tsz)
+// tiles of tsz = roundup16(ceil(c / ceil(c / bn))) rows, so its tiles are
+// balanced and every MMA-N is a multiple of 16.
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ chunk_counts,
                                                     int num_chunks, int E, int bn,
                                                     int32_t* __restrict__ counts,
@@ -175,33 +179,56 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
                                                     int4* __restrict__ tiles,
                                                     int32_t* __restrict__ num_tiles,
                                                     int2* __restrict__ tile_plan) {
+  __shared__ int32_t part[1024];   // group g's sum for expert e at g * Ep + e
+  __shared__ int32_t eoffs[1024];  // expert offsets, for every group
   griddep_wait();
   griddep_launch_dependents();
-  const int e = threadIdx.x;
+  const int Ep = (E + 31) & ~31, P = static_cast<int>(blockDim.x) / Ep;
+  const int g = static_cast<int>(threadIdx.x) / Ep, e = static_cast<int>(threadIdx.x) % Ep;
+  const bool active = g < P && e < E;
+  const int ch0 = active ? g * num_chunks / P : 0, ch1 = active ? (g + 1) * num_chunks / P : 0;
   int c = 0;
-  if (e < E)
-    for (int ch = 0; ch < num_chunks; ++ch) c += chunk_counts[static_cast<size_t>(ch) * E + e];
+#pragma unroll 4
+  for (int ch = ch0; ch < ch1; ++ch) c += chunk_counts[static_cast<size_t>(ch) * E + e];
+  part[threadIdx.x] = c;
+  __syncthreads();
+  int total = 0, gstart = 0;
+  if (active)
+    for (int h = 0; h < P; ++h) {
+      const int v = part[h * Ep + e];
+      if (h < g) gstart += v;
+      total += v;
+    }
+  // expert offsets: the first group's threads are the experts in order
   int total_rows;
-  const int off = block_exclusive_scan(e < E ? c : 0, &total_rows);
-  if (e < E) {
-    counts[e] = c;
+  const int off = block_exclusive_scan(g == 0 && e < E ? total : 0, &total_rows);
+  if (g == 0) eoffs[e] = off;
+  __syncthreads();
+  if (g == 0 && e < E) {
+    counts[e] = total;
     offsets[e] = off;
-    int run = off;
-    for (int ch = 0; ch < num_chunks; ++ch) {
+  }
+  if (threadIdx.x == 0) offsets[E] = total_rows;
+  if (active) {
+    int run = eoffs[e] + gstart;
+#pragma unroll 4
+    for (int ch = ch0; ch < ch1; ++ch) {
       const size_t i = static_cast<size_t>(ch) * E + e;
       const int cc = chunk_counts[i];
       chunk_base[i] = run;
       run += cc;
     }
   }
-  if (e == 0) offsets[E] = total_rows;
-  plan_tiles(e, E, e < E ? c : 0, off, bn, true, tiles, num_tiles, tile_plan);
+  // tile plan from the first group (others plan nothing: "expert" E, 0 rows)
+  plan_tiles(g == 0 ? e : E, E, g == 0 && e < E ? total : 0, g == 0 ? off : 0, bn, true, tiles,
+             num_tiles, tile_plan);
 }
 
-// One warp per chunk of kRouteChunk tokens: the warp walks the chunk's
-// tokens in order and hands out rows from the chunk's per-expert bases (a
-// token's k experts are distinct, so the k lanes never collide), which makes
-// each expert's rows ascend in token order.
+// One warp per chunk of kRouteChunk tokens: the warp stages the chunk's
+// routed experts and per-expert bases in shared memory, then walks the
+// chunk's tokens in order and hands out rows from the bases (a token's k
+// experts are distinct, so the k lanes never collide), which makes each
+// expert's rows ascend in token order.
 __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ ids,
                                                    const int32_t* __restrict__ chunk_base,
                                                    int T, int E, int k, int num_chunks,
@@ -213,16 +240,16 @@ __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ i
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * (blockDim.x >> 5) + warp;
   if (chunk >= num_chunks) return;
-  int32_t* base = sm + warp * E;
+  int32_t* base = sm + warp * (E + kRouteChunk * k);
+  int32_t* cid = base + E;
+  const int t0 = chunk * kRouteChunk, nt = min(kRouteChunk, T - t0);
   for (int i = lane; i < E; i += 32) base[i] = chunk_base[static_cast<size_t>(chunk) * E + i];
+  for (int i = lane; i < nt * k; i += 32) cid[i] = ids[static_cast<size_t>(t0) * k + i];
   __syncwarp();
-  const int t0 = chunk * kRouteChunk;
-  for (int tt = 0; tt < kRouteChunk; ++tt) {
-    const int t = t0 + tt;
-    if (t >= T) break;
+  for (int tt = 0; tt < nt; ++tt) {
     if (lane < k) {
-      const size_t ts = static_cast<size_t>(t) * k + lane;
-      const int e = ids[ts];
+      const size_t ts = static_cast<size_t>(t0 + tt) * k + lane;
+      const int e = cid[tt * k + lane];
       const int r = base[e];
       base[e] = r + 1;
       row_of[ts] = r;
@@ -589,7 +616,8 @@ cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, 
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
                         int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
                         int32_t* num_tiles, int2* tile_plan, cudaStream_t s) {
-  const int threads = ((E + 31) / 32) * 32;
+  const int ep = ((E + 31) / 32) * 32;    // one group of threads per expert set
+  const int threads = (1024 / ep) * ep;   // as many groups as fit 1024 threads
   return launch_pdl(scan_kernel, dim3(1), dim3(threads), 0, s, chunk_counts, num_chunks, E, bn,
                     counts, offsets, chunk_base, tiles, num_tiles, tile_plan);
 }
@@ -597,8 +625,10 @@ cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int 
 cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,
                         int32_t* row_of, int32_t* token_slot, cudaStream_t s) {
   const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
-  const int warps = 8;
-  const size_t smem = static_cast<size_t>(warps) * E * sizeof(int32_t);
+  // per warp: the chunk's per-expert bases and its routed experts
+  const size_t per_warp = static_cast<size_t>(E + kRouteChunk * k) * sizeof(int32_t);
+  const int warps = static_cast<int>(std::min<size_t>(8, 49152 / per_warp));
+  const size_t smem = static_cast<size_t>(warps) * per_warp;
   return launch_pdl(rank_kernel, dim3((chunks + warps - 1) / warps), dim3(32 * warps), smem, s,
                     ids, chunk_base, T, E, k, chunks, row_of, token_slot);
 }
