@@ -24,10 +24,10 @@
 // Roles: warp 0 = TMA producers (lane s < S: weight half-box + scales into
 // raw slot s; lane S + s: activation atom into activation slot s); warps
 // 1..NI = MMA issuers (warp-uniform, one elected lane issues; issuer i takes
-// the sub-stages g = i mod NI into its own accumulator); the next 8 warps =
-// transform, two per TMEM lane quarter (warp w handles the rows of its
-// quarter, warp % 4, of the sub-stages g = w' mod 2, w' = its rank among
-// the transform warps / 4); the last 8 warps = epilogue.
+// the sub-stages g = i mod NI into its own accumulator); the next 16 warps
+// = transform, four groups of four (group p converts the sub-stages
+// g = p mod 4, warp w of the group the rows of TMEM lane quarter w % 4); the
+// last 4 warps = epilogue, one per lane quarter.
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -38,7 +38,13 @@ namespace moe {
 
 namespace {
 
-constexpr int kTransformWarps = 8;   // two per TMEM lane quarter
+// Transform warps: four groups of four (group g % 4 converts sub-stage g,
+// warp w of the group the rows of TMEM lane quarter w % 4), so each group
+// has four sub-stages of time per conversion.
+constexpr int kXfGroups = 4;
+constexpr int kTransformWarps = 4 * kXfGroups;
+// The W4A16 tiles hold at most 64 tokens: one epilogue warp per quarter.
+constexpr int kBf16EpiWarps = 4;
 constexpr int kBf16Issuers = 2;
 
 template <int BN, int S, int QA>
@@ -48,8 +54,9 @@ struct Bf16Cfg {
   // slot s (raw, activation) and TMEM slot a always belong to one issuer and
   // one transform pair, so each barrier is waited on in phase order by the
   // same threads
-  static_assert(S % kBf16Issuers == 0 && QA % kBf16Issuers == 0 && S % 2 == 0 && QA % 2 == 0,
-                "slots must map to single issuers and transform pairs");
+  static_assert(S % kBf16Issuers == 0 && QA % kBf16Issuers == 0 && S % kXfGroups == 0 &&
+                    QA % kXfGroups == 0,
+                "slots must map to single issuers and transform groups");
   static constexpr int kRawBytes = kTileM * 32;      // packed E2M1, 64 K per row
   static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes (128 K)
   static constexpr int kBBytes = BN * 128;           // 64 bf16 of K per token row
@@ -66,7 +73,7 @@ struct Bf16Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
   static constexpr int kFirstXfWarp = 1 + kBf16Issuers;
   static constexpr int kFirstEpiWarp = kFirstXfWarp + kTransformWarps;
-  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+  static constexpr int kThreads = 32 * (kFirstEpiWarp + kBf16EpiWarps);
   // TMEM: 2 accumulator buffers x NI partials x BN columns, then QA slots of
   // converted weights, 32 columns each (128 rows x 64 bf16)
   static constexpr int kColA = 2 * kBf16Issuers * BN;
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(raw_full + s, 1);
-      mbar_init(raw_empty + s, 4);   // the four quarter warps of its transform pair
+      mbar_init(raw_empty + s, 4);   // the four quarter warps of its transform group
       mbar_init(b_full + s, 1);
       mbar_init(b_empty + s, 1);
     }
@@ -177,7 +184,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull + a, NI);                     // every issuer commits its share
-      mbar_init(tempty + a, kEpiWarps);
+      mbar_init(tempty + a, kBf16EpiWarps);
     }
     for (int i = 0; i < NI; ++i) mbar_init(drain + i, 1);
     *abort_flag = 0;
@@ -295,20 +302,20 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
     mbar_wait_warp(drain + i, 0, timeout_ns, status, kDevTimeout, &none);
   } else if (warp < C::kFirstEpiWarp) {
     // ------------------------------------------------------------ transform
-    // Transform warp w (quarter q = warp % 4, pair p) converts, for the
-    // sub-stages g = p, p + 2, ..., the 32 rows r = 32 q + lane: lane l reads
+    // Transform warp w (quarter q = warp % 4, group p) converts, for the
+    // sub-stages g = p, p + 4, ..., the 32 rows r = 32 q + lane: lane l reads
     // its row's 32 code bytes and two scale bytes, turns each code byte into
     // a bf16 pair through the shared table (this lane's bank copy: no
     // conflicts), applies the 32-K block's scale with one exact bf16x2
     // multiply, and stores the row's 64 values into 32 columns of its TMEM
     // lane in TMEM slot g % QA.
-    const int q = warp & 3, p = (warp - C::kFirstXfWarp) >> 2;
+    const int q = warp & 3, p = (warp - C::kFirstXfWarp) >> 2;   // quarter, group
     const int r = 32 * q + lane;
     const __nv_bfloat162* lut = reinterpret_cast<const __nv_bfloat162*>(smem + C::kOffLut);
     const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
     int total = 0;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) total += KH;
-    for (int g = p; g < total; g += 2) {
+    for (int g = p; g < total; g += kXfGroups) {
       const int s = g % S, a = g % QA;
       if (!mbar_wait_warp(raw_full + s, static_cast<uint32_t>((g / S) & 1), timeout_ns, status,
                           kDevTimeout, abort_flag))
@@ -343,8 +350,9 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const EpiSched sch{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), MT, 1, 0, 0u};
-    epilogue_loop<BN, NI, 2, SWIGLU>(C::kFirstEpiWarp, NI, tiles, num_items, sch, tfull, tempty,
-                                     tmem, nullptr, out, out_ld, timeout_ns, status, abort_flag);
+    epilogue_loop<BN, NI, 2, SWIGLU, kBf16EpiWarps>(C::kFirstEpiWarp, NI, tiles, num_items, sch,
+                                                    tfull, tempty, tmem, nullptr, out, out_ld,
+                                                    timeout_ns, status, abort_flag);
   }
 
   tc_fence_before();

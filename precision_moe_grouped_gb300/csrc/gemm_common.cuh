@@ -62,7 +62,9 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
-template <int BN, int NI, int NB, bool SWIGLU>
+// EW = epilogue warps: 8 (two per lane quarter, splitting the chunks) or 4
+// (one per quarter).
+template <int BN, int NI, int NB, bool SWIGLU, int EW = kEpiWarps>
 __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4* __restrict__ tiles,
                                               int num_items, EpiSched sch, uint64_t* tfull,
                                               uint64_t* tempty, uint32_t tmem,
@@ -72,7 +74,8 @@ __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4
                                               volatile int32_t* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;
-  const int half = (warp - first_warp) >> 2;
+  static_assert(EW == 4 || EW == 8, "one or two epilogue warps per TMEM lane quarter");
+  const int half = EW == 8 ? (warp - first_warp) >> 2 : 0;
   int acc = 0;
   uint32_t acc_phase = 0;
   for (int item = sch.item0; item < num_items; item += sch.item_step) {
@@ -80,7 +83,7 @@ __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4
     const int mt = (item % sch.items_per_tile) * sch.mt_mul + sch.mt_add;
     const int4 td = tiles[tile];
     const int row0 = td.y, ntok = td.z, nchunks = (td.z + 15) >> 4;
-    const int split = (nchunks + 1) >> 1;
+    const int split = EW == 8 ? (nchunks + 1) >> 1 : nchunks;
     const int ch_begin = half == 0 ? 0 : split, ch_end = half == 0 ? split : nchunks;
     if (!mbar_wait(tfull + acc, acc_phase, timeout_ns, status, kDevTimeout, abort_flag)) break;
     tc_fence_after();
