@@ -21,9 +21,9 @@
 // list, swap-AB orientation, persistent static striding, epilogue) is the
 // FP8 GEMM's.
 //
-// Roles: warp 0 = TMA producers (lane s < S: weight half-box + scales into
-// raw slot s; lane S + s: activation atom into activation slot s); warps
-// 1..NI = MMA issuers (warp-uniform, one elected lane issues; issuer i takes
+// Roles: warps 0..2 = TMA producers (slot s in warp s % 3: one lane for the
+// weight half-box + scales into raw slot s, one for the activation atom
+// into activation slot s); the next NI warps = MMA issuers (warp-uniform, one elected lane issues; issuer i takes
 // the sub-stages g = i mod NI into its own accumulator); the next 16 warps
 // = transform, four groups of four (group p converts the sub-stages
 // g = p mod 4, warp w of the group the rows of TMEM lane quarter w % 4); the
@@ -45,12 +45,16 @@ constexpr int kXfGroups = 4;
 constexpr int kTransformWarps = 4 * kXfGroups;
 // The W4A16 tiles hold at most 64 tokens: one epilogue warp per quarter.
 constexpr int kBf16EpiWarps = 4;
+// Producer warps: slot s is served by warp s % 3 (lanes of one warp waiting
+// on different slots' barriers serialise), two lanes per slot.
+constexpr int kBf16ProdWarps = 3;
 constexpr int kBf16Issuers = 2;
 
 template <int BN, int S, int QA>
 struct Bf16Cfg {
   static_assert(BN % 16 == 0 && BN <= 128, "token tile of the W4A16 GEMM: 16..128 rows");
-  static_assert(2 * S <= 32, "producer lanes must fit one warp");
+  static_assert(2 * ((S + kBf16ProdWarps - 1) / kBf16ProdWarps) <= 32,
+                "producer lanes must fit the producer warps");
   // slot s (raw, activation) and TMEM slot a always belong to one issuer and
   // one transform pair, so each barrier is waited on in phase order by the
   // same threads
@@ -71,7 +75,8 @@ struct Bf16Cfg {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-  static constexpr int kFirstXfWarp = 1 + kBf16Issuers;
+  static constexpr int kFirstIssuer = kBf16ProdWarps;   // owns TMEM
+  static constexpr int kFirstXfWarp = kFirstIssuer + kBf16Issuers;
   static constexpr int kFirstEpiWarp = kFirstXfWarp + kTransformWarps;
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kBf16EpiWarps);
   // TMEM: 2 accumulator buffers x NI partials x BN columns, then QA slots of
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
     prefetch_tmap(&tmap_sf);
     for (int i = 0; i < kNumXMaps; ++i) prefetch_tmap(&tmap_x.m[i]);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (warp == C::kFirstIssuer) tmem_alloc(tmem_slot, C::kTmemCols);
   // Code byte -> the bf16 pair (low nibble = even k) of its two E2M1 values,
   // replicated per bank.
   for (int w = threadIdx.x; w < 256 * 32; w += blockDim.x) {
@@ -209,14 +214,15 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
   griddep_launch_dependents();
   const int num_items = *num_tiles_p * MT;
 
-  if (warp == 0) {
+  if (warp < kBf16ProdWarps) {
     // ------------------------------------------------------------ producer
-    // Lane s < S fills raw slot s for this CTA's sub-stages g = s, s + S, ...
-    // (sub-stage g = 64-K half (g % KH) % 2 of the 128-K box (g % KH) / 2 of
-    // the CTA's (g / KH)-th item); lane S + s fills activation slot s.
-    if (lane < 2 * S) {
-      const bool is_w = lane < S;
-      const int s = is_w ? lane : lane - S;
+    // Slot s belongs to warp s % 3: its lane 2 (s / 3) fills raw slot s for
+    // this CTA's sub-stages g = s, s + S, ... (sub-stage g = 64-K half
+    // (g % KH) % 2 of the 128-K box (g % KH) / 2 of the CTA's (g / KH)-th
+    // item) and the next lane fills activation slot s.
+    const int s = warp + kBf16ProdWarps * (lane >> 1);
+    if (s < S) {
+      const bool is_w = (lane & 1) == 0;
       uint32_t phase = 0;
       bool issued = false;
       int kh = s % KH, item = blockIdx.x + (s / KH) * gridDim.x;
@@ -253,9 +259,9 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
         mbar_wait(full, phase ^ 1u, timeout_ns, status, kDevTimeout, &none);
       }
     }
-  } else if (warp <= NI) {
+  } else if (warp < C::kFirstXfWarp) {
     // ------------------------------------------------------------ MMA issuers
-    const int i = warp - 1;
+    const int i = warp - C::kFirstIssuer;
     const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
     int g = i, kh = i, it = 0;
     bool new_item = true;
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == C::kFirstIssuer) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
