@@ -67,6 +67,21 @@ constexpr uint32_t kWeightBoxTxBytes = 128u * 128u / 2u;
 // T=4096: 1797 us with a distance of 8, 1800 us without).
 int default_prefetch(int) { return 0; }
 
+// Persistent-GEMM grid.  A tile holds at least one row, so a GEMM has at
+// most T * k * m_tiles work items; with few rows per expert (T * k <= E / 4)
+// tokens rarely share an expert and the bound is (nearly) the count -- exact
+// at T = 1, whose k experts are distinct.  The grid is then the fewest CTAs
+// that give every CTA the same number of rounds (DSV3 T=1 GEMM1: 256 items on
+// 128 CTAs x 2 instead of 104 CTAs with 2 and 48 with 1), so no round runs on
+// part of the GPU while the rest waits.  Otherwise one CTA per SM.
+int gemm_grid(int num_sms, int64_t T, int k, int E, int m_tiles) {
+  const int64_t rows = T * k;
+  if (4 * rows > E) return num_sms;
+  const int64_t items = rows * m_tiles;
+  const int64_t rounds = (items + num_sms - 1) / num_sms;
+  return static_cast<int>((items + rounds - 1) / rounds);
+}
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -381,7 +396,8 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   // W4A8: the per-row token scale is applied in the epilogues; MXFP8: the
   // block scales ride with the operands into the MMA
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
-                   mx ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, dev.num_sms,
+                   mx ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx,
+                   gemm_grid(dev.num_sms, T, k, E, 2 * I / moe::kTileM),
                    prefetch, mx, sfb1, static_cast<const uint8_t*>(w1), pair ? tm_xp : nullptr};
   MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(true, g1, st) : moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
@@ -394,7 +410,8 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
     MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
   MOE_CUDA(mark());
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
-                   mx ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, dev.num_sms,
+                   mx ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx,
+                   gemm_grid(dev.num_sms, T, k, E, H / moe::kTileM),
                    prefetch, mx, sfb2, static_cast<const uint8_t*>(w2), pair ? tm_hp : nullptr};
   MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(false, g2, st)
                  : moe::launch_gemm(false, variant, g2, st));
