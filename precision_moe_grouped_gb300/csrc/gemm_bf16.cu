@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
     // lane in TMEM slot g % QA.
     const int q = warp & 3, p = (warp - C::kFirstXfWarp) >> 2;   // quarter, group
     const int r = 32 * q + lane;
-    const __nv_bfloat162* lut = reinterpret_cast<const __nv_bfloat162*>(smem + C::kOffLut);
+    const __nv_bfloat162* lutl = reinterpret_cast<const __nv_bfloat162*>(smem + C::kOffLut) + lane;
     const uint32_t tlane = static_cast<uint32_t>(32 * q) << 16;
     int total = 0;
     for (int item = blockIdx.x; item < num_items; item += gridDim.x) total += KH;
@@ -344,8 +344,10 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
       uint32_t v[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {   // code byte c = K elements 2c, 2c + 1
-        const uint32_t byte = (cw[c >> 2] >> (8 * (c & 3))) & 0xFFu;
-        const __nv_bfloat162 pr = __hmul2(lut[(byte << 5) + lane], c < 16 ? s0 : s1);
+        // byte c & 3 of the word moved to the low byte (one byte permute);
+        // this lane's table copy is lutl[32 * byte]
+        const uint32_t byte = __byte_perm(cw[c >> 2], 0u, 0x4440u + static_cast<uint32_t>(c & 3));
+        const __nv_bfloat162 pr = __hmul2(lutl[byte << 5], c < 16 ? s0 : s1);
         v[c] = *reinterpret_cast<const uint32_t*>(&pr);
       }
       tmem_st_32x32b_x32(tmem + tlane + static_cast<uint32_t>(C::kColA + 32 * a), v);
