@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
       tc_fence_after();
       const uint8_t* raw = smem + C::kOffRaw + s * C::kRawBytes + 32 * r;
       const uint8_t* sf = smem + C::kOffSF + s * C::kSFBytes;
-      const int half = (g % KH) & 1;   // the 64-K half of the 128-K box
+      const int half = g & 1;   // the 64-K half of the 128-K box ((g % KH) & 1: KH is even)
       const uint4 c0 = *reinterpret_cast<const uint4*>(raw);
       const uint4 c1 = *reinterpret_cast<const uint4*>(raw + 16);
       const int sfo = 16 * (r & 31) + 4 * (r >> 5) + 2 * half;
