@@ -55,11 +55,14 @@ typedef enum {
   MOE_ERR_MISALIGNED = -3,         /* pointer alignment or shape divisibility */
   MOE_ERR_WORKSPACE_TOO_SMALL = -4,
   MOE_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed       */
-  MOE_ERR_DEVICE_TIMEOUT = -6      /* a device-side bounded wait ran out      */
+  MOE_ERR_DEVICE_TIMEOUT = -6,     /* a device-side bounded wait ran out      */
+  MOE_ERR_DEVICE_CHECK = -7        /* checked builds (libmoe_checked.so, built
+                                      with MOE_CHECKS) only: a device-side
+                                      bounds check of the work map failed    */
 } moe_status;
 
-/* Quantisation modes (the pages' W4A8 / W4A16 / MXFP8 paths).  This build
- * implements MOE_W4A8_MXFP4_FP8; the others return MOE_ERR_UNSUPPORTED. */
+/* Quantisation modes (the pages' W4A8 / W4A16 / MXFP8 paths); all three are
+ * implemented. */
 typedef enum {
   MOE_W4A8_MXFP4_FP8 = 0,    /* MXFP4 weights, runtime per-token FP8 E4M3 acts */
   MOE_W4A16_MXFP4_BF16 = 1,  /* MXFP4 weights, bf16 activations               */
@@ -116,7 +119,7 @@ typedef struct {
 
 /* Byte offsets of the intermediate tensors inside the workspace, for tests
  * and diagnostics (R = num_tokens * top_k expanded rows).  Layouts:
- *   status      int32[4]      device status word, tile count, 2 spare
+ *   status      int32[4]      status word, tile count, R and E (checked builds; else spare)
  *   ids         int32[T,k]    routed expert of (token, slot), descending logit
  *   weights     float[T,k]    renormalised softmax routing weights
  *   row_of      int32[T,k]    expanded row of (token, slot)

@@ -10,7 +10,9 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libmoe.so")
+# MOE_CHECKED=1 selects the bounds-checked debug build (build(checks=True))
+CHECKED = os.environ.get("MOE_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(PKG, "libmoe_checked.so" if CHECKED else "libmoe.so")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = -1
@@ -19,6 +21,7 @@ MOE_ERR_MISALIGNED = -3
 MOE_ERR_WORKSPACE_TOO_SMALL = -4
 MOE_ERR_CUDA = -5
 MOE_ERR_DEVICE_TIMEOUT = -6
+MOE_ERR_DEVICE_CHECK = -7
 
 MOE_W4A8_MXFP4_FP8 = 0
 MOE_W4A16_MXFP4_BF16 = 1

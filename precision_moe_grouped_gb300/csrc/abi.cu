@@ -448,6 +448,7 @@ const char* moe_status_string(int32_t status) {
     case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side bounds check failed (checked build)";
     default: return "unknown status";
   }
 }

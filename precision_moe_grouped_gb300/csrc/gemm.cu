@@ -184,7 +184,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
   // the activations are that kernel's (or an earlier one's) output.
   griddep_wait();
   griddep_launch_dependents();
-  const int num_items = *num_tiles_p * MT;   // < 2^31: tiles <= R/16 + E + 1
+  const WorkLimits lim = work_limits(status);
+  // < 2^31: tiles <= R/16 + E + 1
+  const int num_items = checked_num_tiles(num_tiles_p, status, lim) * MT;
 
   if (warp < C::kProdWarps) {
     // ------------------------------------------------------------ producer
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
       while (item < num_items) {
         if (item != cur_item) {
           cur_item = item;
-          td = tiles[item / MT];
+          td = checked_tile(tiles, item / MT, BN, status, lim);
           // prepared weights: one contiguous 128 x 128 box per (expert,
           // M-tile, K stage); box row = ((e * MT + mt) * KS + ks) * 128
           blk0 = (static_cast<int64_t>(td.x) * MT + item % MT) * KS;
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
         bool ok = true;
         for (int item = blockIdx.x, it = 0; ok && item < num_items;
              item += static_cast<int>(gridDim.x), ++it) {
-          const int4 td = tiles[item / MT];
+          const int4 td = checked_tile(tiles, item / MT, BN, status, lim);
           const int nmma = (td.z + 15) & ~15;
           const uint32_t id0 = idesc_mx(MX8 ? 0 : 5, 0, static_cast<uint32_t>(nmma), 0, 0);
           const int acc = it % NB;
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
       while (blockIdx.x + it * static_cast<int>(gridDim.x) < num_items) {
         if (new_item) {
           const int item = blockIdx.x + it * gridDim.x;
-          const int4 td = tiles[item / MT];
+          const int4 td = checked_tile(tiles, item / MT, BN, status, lim);
           nmma = (td.z + 15) & ~15;
           // A = weights: E2M1, or E4M3 in MXFP8; B = activations: E4M3
           id0 = idesc_mx(MX8 ? 0 : 5, 0, static_cast<uint32_t>(nmma), 0, 0);
@@ -408,7 +410,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
       while (g < total) {
         const int p = *progress;
         if (g <= p + prefetch_stages) {
-          const int64_t bp = (static_cast<int64_t>(tiles[itp / MT].x) * MT + itp % MT) * KS + kp;
+          const int64_t bp =
+              (static_cast<int64_t>(checked_tile(tiles, itp / MT, BN, status, lim).x) * MT +
+               itp % MT) * KS + kp;
           const uint8_t* box = w_base + bp * a_tx_bytes;
           for (uint32_t off = static_cast<uint32_t>(lane) * 128u; off < a_tx_bytes;
                off += 32u * 128u)

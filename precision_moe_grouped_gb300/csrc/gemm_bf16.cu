@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   griddep_wait();
   griddep_launch_dependents();
-  const int num_items = *num_tiles_p * MT;
+  const WorkLimits lim = work_limits(status);
+  const int num_items = checked_num_tiles(num_tiles_p, status, lim) * MT;
 
   if (warp < kBf16ProdWarps) {
     // ------------------------------------------------------------ producer
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
       uint64_t* empty = is_w ? raw_empty + s : b_empty + s;
       while (item < num_items) {
         const int mt = item % MT;
-        const int4 td = tiles[item / MT];
+        const int4 td = checked_tile(tiles, item / MT, BN, status, lim);
         if (!mbar_wait(empty, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag)) break;
         if (is_w) {
           const int64_t blk = (static_cast<int64_t>(td.x) * MT + mt) * KS + (kh >> 1);
@@ -270,7 +271,8 @@ __global__ void __launch_bounds__(Bf16Cfg<BN, S, QA>::kThreads, 1)
     while (blockIdx.x + it * static_cast<int>(gridDim.x) < num_items) {
       if (new_item) {
         const int item = blockIdx.x + it * gridDim.x;
-        id = idesc_bf16(static_cast<uint32_t>((tiles[item / MT].z + 15) & ~15));
+        id = idesc_bf16(
+            static_cast<uint32_t>((checked_tile(tiles, item / MT, BN, status, lim).z + 15) & ~15));
         acc = it & 1;
         if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it >> 1) & 1) ^ 1u, timeout_ns,
                             status, kDevTimeout, abort_flag))

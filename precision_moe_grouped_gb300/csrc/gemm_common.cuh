@@ -31,6 +31,52 @@ __device__ __forceinline__ int x_map_for(int rows) {
 // Number of epilogue warps: two per TMEM lane quarter.
 constexpr int kEpiWarps = 8;
 
+// ------------------------------------------------------- checked builds
+// The work-map limits a checked build validates against: R expanded rows and
+// E experts, recorded by the forward's first kernel (zeros otherwise).
+struct WorkLimits {
+  int R, E;
+};
+
+__device__ __forceinline__ WorkLimits work_limits(const int32_t* status) {
+  if constexpr (kChecks) return WorkLimits{status[2], status[3]};
+  return WorkLimits{0, 0};
+}
+
+// The tile count; a checked build records MOE_ERR_DEVICE_CHECK and runs no
+// tiles when it exceeds the largest list the expansion can build.
+__device__ __forceinline__ int checked_num_tiles(const int32_t* num_tiles_p, int32_t* status,
+                                                 WorkLimits lim) {
+  const int n = *num_tiles_p;
+  if constexpr (kChecks) {
+    const int max_tiles = lim.R / 16 + min(lim.E, lim.R) + 1;
+    if (n < 0 || n > max_tiles) {
+      atomicCAS(status, 0, kDevCheckFailed);
+      return 0;
+    }
+  }
+  return n;
+}
+
+// Tile entry i (expert, first row, rows, 0).  A checked build replaces an
+// entry out of range (expert >= E, rows outside [0, R), more than bn rows)
+// by a harmless 16-row tile of expert 0 marked w = 1, whose outputs the
+// epilogue does not store, and records MOE_ERR_DEVICE_CHECK.  Every role of
+// a GEMM reads the entry through this function, so all agree.
+__device__ __forceinline__ int4 checked_tile(const int4* __restrict__ tiles, int i, int bn,
+                                             int32_t* status, WorkLimits lim) {
+  int4 td = tiles[i];
+  if constexpr (kChecks) {
+    const bool ok = td.x >= 0 && td.x < lim.E && td.y >= 0 && td.z >= 1 && td.z <= bn &&
+                    td.y + td.z <= lim.R && td.w == 0;
+    if (!ok) {
+      atomicCAS(status, 0, kDevCheckFailed);
+      td = make_int4(0, 0, 16, 1);
+    }
+  }
+  return td;
+}
+
 // The epilogue of a persistent grouped GEMM whose TMEM holds, per
 // accumulator buffer a, NI partial accumulators of BN fp32 columns (issuer
 // i's at column (a * NI + i) * BN; ni of them in use), row m = weight row
@@ -78,11 +124,13 @@ __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4
   const int half = EW == 8 ? (warp - first_warp) >> 2 : 0;
   int acc = 0;
   uint32_t acc_phase = 0;
+  const WorkLimits lim = work_limits(status);
   for (int item = sch.item0; item < num_items; item += sch.item_step) {
     const int tile = item / sch.items_per_tile;
     const int mt = (item % sch.items_per_tile) * sch.mt_mul + sch.mt_add;
-    const int4 td = tiles[tile];
-    const int row0 = td.y, ntok = td.z, nchunks = (td.z + 15) >> 4;
+    const int4 td = checked_tile(tiles, tile, BN, status, lim);
+    const int row0 = td.y, ntok = (kChecks && td.w) ? 0 : td.z;   // a replaced tile stores nothing
+    const int nchunks = (ntok + 15) >> 4;
     const int split = EW == 8 ? (nchunks + 1) >> 1 : nchunks;
     const int ch_begin = half == 0 ? 0 : split, ch_end = half == 0 ? split : nchunks;
     if (!mbar_wait(tfull + acc, acc_phase, timeout_ns, status, kDevTimeout, abort_flag)) break;

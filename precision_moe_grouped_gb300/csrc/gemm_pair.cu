@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(PairCfg<BN, STAGES, NB>::kThreads, 1)
   tc_fence_after();
   griddep_wait();
   griddep_launch_dependents();
-  const int num_items = *num_tiles_p * MTP;
+  const WorkLimits lim = work_limits(status);
+  const int num_items = checked_num_tiles(num_tiles_p, status, lim) * MTP;
   const uint32_t full0 = cluster_addr(full, 0);   // rank 0's full barriers
 
   if (warp < C::kProdWarps) {
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(PairCfg<BN, STAGES, NB>::kThreads, 1)
       int ks = s % KS, item = cid + (s / KS) * ncl;
       const uint32_t bar = full0 + static_cast<uint32_t>(8 * s);
       while (item < num_items) {
-        const int4 td = tiles[item / MTP];
+        const int4 td = checked_tile(tiles, item / MTP, BN, status, lim);
         const int mt = 2 * (item % MTP) + static_cast<int>(rank);
         const int64_t blk = (static_cast<int64_t>(td.x) * MT + mt) * KS + ks;
         if (!mbar_wait(empty + s, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag)) break;
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(PairCfg<BN, STAGES, NB>::kThreads, 1)
       int acc = 0;
       while (cid + it * ncl < num_items) {
         if (new_item) {
-          const int4 td = tiles[(cid + it * ncl) / MTP];
+          const int4 td = checked_tile(tiles, (cid + it * ncl) / MTP, BN, status, lim);
           const uint32_t nmma = static_cast<uint32_t>((td.z + 31) & ~31);
           id0 = idesc_mx_pair(5, 0, nmma);   // A = E2M1 weights, B = E4M3 tokens
           acc = it % NB;

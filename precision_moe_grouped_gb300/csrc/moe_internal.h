@@ -15,6 +15,17 @@ namespace moe {
 
 // Device status codes written to the workspace status word (match moe_status).
 constexpr int32_t kDevTimeout = -6;
+constexpr int32_t kDevCheckFailed = -7;   // MOE_ERR_DEVICE_CHECK
+
+// Checked builds (-DMOE_CHECKS, libmoe_checked.so) validate the device-built
+// work map where the GEMMs consume it; release builds compile the checks
+// away.  The first kernel of a forward records the expanded row count R and
+// the expert count E in status[2] and status[3] for them.
+#ifdef MOE_CHECKS
+constexpr bool kChecks = true;
+#else
+constexpr bool kChecks = false;
+#endif
 
 // Launches `kern` with programmatic stream serialisation (PDL): the kernel may
 // begin while its stream predecessor finishes; every kernel of this library

@@ -45,7 +45,13 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   griddep_wait();
   griddep_launch_dependents();
   // the forward's first kernel clears the device status word
-  if (status && blockIdx.x == 0 && threadIdx.x == 0) status[0] = 0;
+  if (status && blockIdx.x == 0 && threadIdx.x == 0) {
+    status[0] = 0;
+    if (kChecks) {   // the work-map limits checked builds validate against
+      status[2] = T * k;
+      status[3] = E;
+    }
+  }
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
@@ -491,7 +497,13 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
   griddep_wait();
   griddep_launch_dependents();
   const int t = blockIdx.x;
-  if (t == 0 && threadIdx.x == 0) status[0] = 0;   // first kernel of the forward
+  if (t == 0 && threadIdx.x == 0) {   // first kernel of the forward
+    status[0] = 0;
+    if (kChecks) {
+      status[2] = T * k;
+      status[3] = E;
+    }
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   {   // L2 prefetch of token t's row (2H bytes), 128-byte lines
     const char* base = reinterpret_cast<const char*>(x + static_cast<size_t>(t) * H);
