@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
     // from a loop that only lane 0 runs, independent of N up to 128), so with
     // small token tiles one issuing warp cannot keep pace with the weight
     // stream.
-    // Issuer i (warp 1 + i) takes fills f = i, i + ni, i + 2 ni, ... -- i.e.
+    // Issuer i (warp kIssuer0 + i) takes fills f = i, i + ni, i + 2 ni, ... -- i.e.
     // the stages s with s % ni == i -- and accumulates its K stages of an item
     // into its own TMEM accumulator; the epilogue sums the ni partials.
     // Every descriptor is precomputed: stage s and K sub-step kk only add
@@ -340,46 +340,46 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
           if (ok) tc_commit_warp(tfull + acc);   // the item's accumulator is final
         }
       } else {
-      int stage = i % STAGES, ks = i % KS, it = i / KS;   // ni <= KS, so it == 0
-      int nmma = 16, fidx = i;
-      uint32_t phase = (i / STAGES) & 1;
-      bool new_item = true;
-      uint32_t d_tmem = 0, id0 = 0;
-      int acc = 0;
-      while (blockIdx.x + it * static_cast<int>(gridDim.x) < num_items) {
-        if (new_item) {
-          const int item = blockIdx.x + it * gridDim.x;
-          const int4 td = checked_tile(tiles, item / MT, BN, status, lim);
-          nmma = (td.z + 15) & ~15;
-          // A = weights: E2M1, or E4M3 in MXFP8; B = activations: E4M3
-          id0 = idesc_mx(MX8 ? 0 : 5, 0, static_cast<uint32_t>(nmma), 0, 0);
-          acc = it % NB;
-          if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
-                              status, kDevTimeout, abort_flag))
+        int stage = i % STAGES, ks = i % KS, it = i / KS;   // ni <= KS, so it == 0
+        int nmma = 16, fidx = i;
+        uint32_t phase = (i / STAGES) & 1;
+        bool new_item = true;
+        uint32_t d_tmem = 0, id0 = 0;
+        int acc = 0;
+        while (blockIdx.x + it * static_cast<int>(gridDim.x) < num_items) {
+          if (new_item) {
+            const int item = blockIdx.x + it * gridDim.x;
+            const int4 td = checked_tile(tiles, item / MT, BN, status, lim);
+            nmma = (td.z + 15) & ~15;
+            // A = weights: E2M1, or E4M3 in MXFP8; B = activations: E4M3
+            id0 = idesc_mx(MX8 ? 0 : 5, 0, static_cast<uint32_t>(nmma), 0, 0);
+            acc = it % NB;
+            if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
+                                status, kDevTimeout, abort_flag))
+              break;
+            tc_fence_after();
+            d_tmem = tmem + static_cast<uint32_t>((acc * NI + i) * BN);
+          }
+          if (!mbar_wait_warp(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag))
             break;
           tc_fence_after();
-          d_tmem = tmem + static_cast<uint32_t>((acc * NI + i) * BN);
+          issue_stage(stage, d_tmem, id0, nmma, new_item);
+          if (i == 0 && lane == 0) *progress = fidx;
+          fidx += ni;
+          stage += ni;
+          if (stage >= STAGES) {
+            stage -= STAGES;
+            phase ^= 1u;
+          }
+          ks += ni;
+          new_item = false;
+          while (ks >= KS) {
+            ks -= KS;
+            ++it;
+            new_item = true;
+          }
+          if (new_item) tc_commit_warp(tfull + acc);   // this issuer's share of the item is queued
         }
-        if (!mbar_wait_warp(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag))
-          break;
-        tc_fence_after();
-        issue_stage(stage, d_tmem, id0, nmma, new_item);
-        if (i == 0 && lane == 0) *progress = fidx;
-        fidx += ni;
-        stage += ni;
-        if (stage >= STAGES) {
-          stage -= STAGES;
-          phase ^= 1u;
-        }
-        ks += ni;
-        new_item = false;
-        while (ks >= KS) {
-          ks -= KS;
-          ++it;
-          new_item = true;
-        }
-        if (new_item) tc_commit_warp(tfull + acc);   // this issuer's share of the item is queued
-      }
       }
       // No MMA or TMEM copy may still be running when TMEM is freed.
       tc_commit_warp(drain + i);
@@ -449,13 +449,9 @@ template <int BN, int STAGES, int NI, int NB, bool SWIGLU, bool MX8>
 cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
   using C = GemmCfg<BN, STAGES, NI, NB, MX8>;
   auto kern = grouped_gemm_kernel<BN, STAGES, NI, NB, SWIGLU, MX8>;
-  static bool attr_set = false;  // per instantiation; set before first launch
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceOnce smem_set;   // per instantiation and device
+  const cudaError_t e = set_smem_limit_once(kern, C::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   XMaps xm;
   for (int i = 0; i < kNumXMaps; ++i) xm.m[i] = a.tmap_x[i];
   return launch_pdl(kern, dim3(a.num_sms), dim3(C::kThreads), C::kSmemBytes, s, *a.tmap_w, xm,

@@ -377,13 +377,9 @@ template <int BN, int S, int QA, bool SWIGLU>
 cudaError_t launch_bf16_variant(const GemmArgs& a, cudaStream_t s) {
   using C = Bf16Cfg<BN, S, QA>;
   auto kern = grouped_gemm_bf16_kernel<BN, S, QA, SWIGLU>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceOnce smem_set;   // per instantiation and device
+  const cudaError_t e = set_smem_limit_once(kern, C::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   XMaps xm;
   for (int i = 0; i < kNumXMaps; ++i) xm.m[i] = a.tmap_x[i];
   return launch_pdl(kern, dim3(a.num_sms), dim3(C::kThreads), C::kSmemBytes, s, *a.tmap_w, xm,

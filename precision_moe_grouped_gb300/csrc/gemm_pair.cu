@@ -371,7 +371,8 @@ template <int BN, int STAGES, int NB, bool SWIGLU>
 cudaError_t launch_pair(const GemmArgs& a, cudaStream_t s) {
   using C = PairCfg<BN, STAGES, NB>;
   auto kern = pair_gemm_kernel<BN, STAGES, NB, SWIGLU>;
-  static int max_clusters = 0;   // per instantiation; queried before the first launch
+  // per instantiation and device: resident clusters, queried before the first launch
+  static DeviceOnce max_clusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.num_sms & ~1));
   cfg.blockDim = dim3(C::kThreads);
@@ -386,21 +387,22 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+  cudaError_t e;
+  std::atomic<int>* mc = device_entry(max_clusters, &e);
+  if (!mc) return e;
+  int n = mc->load(std::memory_order_acquire);
+  if (n == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t q = cfg;
     q.attrs = attr + 1;   // the cluster shape alone
     q.numAttrs = 1;
-    int n = 0;
     if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &q)) != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
-    max_clusters = n;
+    mc->store(n, std::memory_order_release);
   }
   // persistent: no more pairs than can be resident at once
-  if (static_cast<int>(cfg.gridDim.x / 2) > max_clusters)
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * max_clusters));
+  if (static_cast<int>(cfg.gridDim.x / 2) > n) cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
   XMaps xm;
   for (int i = 0; i < kNumXMaps; ++i) xm.m[i] = a.tmap_x_pair[i];
   return cudaLaunchKernelEx(&cfg, kern, *a.tmap_w, xm, *a.tmap_sf, a.tiles, a.num_tiles,

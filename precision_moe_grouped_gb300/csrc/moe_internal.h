@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/moe.h"
@@ -26,6 +27,39 @@ constexpr bool kChecks = true;
 #else
 constexpr bool kChecks = false;
 #endif
+
+// One-time, per-device setup of a kernel: function attributes such as the
+// dynamic shared-memory limit belong to the kernel as loaded on one device,
+// so a process that drives several GPUs sets them on each.  A launcher keeps
+// one table per kernel instantiation (static storage, zero-initialised);
+// the entry for the current device holds 0 until the setup has succeeded.
+constexpr int kMaxDevices = 64;
+using DeviceOnce = std::atomic<int>[kMaxDevices];
+
+// Current device's entry of `table` (null when the ordinal is out of range).
+inline std::atomic<int>* device_entry(DeviceOnce& table, cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  return &table[dev];
+}
+
+// Raises the dynamic shared-memory limit of `kern` to `bytes` on the current
+// device, once per device.
+template <typename... KArgs>
+cudaError_t set_smem_limit_once(void (*kern)(KArgs...), int bytes, DeviceOnce& table) {
+  cudaError_t e;
+  std::atomic<int>* done = device_entry(table, &e);
+  if (!done) return e;
+  if (done->load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done->store(1, std::memory_order_release);
+  return e;
+}
 
 // Launches `kern` with programmatic stream serialisation (PDL): the kernel may
 // begin while its stream predecessor finishes; every kernel of this library
