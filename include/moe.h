@@ -226,7 +226,7 @@ int32_t moe_selftest_timeout(void* workspace, int32_t timeout_us, void* stream);
  * server that is handed only its input and output buffers and has no
  * allocator of its own, or a latency-critical path that must not call
  * cudaMalloc after start-up (it can synchronise the device and take
- * unbounded time).  The paper has no counterpart to this entry point.
+ * unbounded time).  The flashinfer PRs have no counterpart to it.
  *   router_logits  float [T, E] (device)      input
  *   ids            int32 [T, k] (device)      output: experts, descending logit
  *   weights        float [T, k] (device)      output: renormalised weights

@@ -165,6 +165,79 @@ def workspace_layout(s: MoeShape, mode: int = MOE_W4A8_MXFP4_FP8) -> WsLayout:
     return L
 
 
+# ------------------------------------------------------------ tensor checks
+# The C ABI takes raw pointers and cannot tell a host buffer, a wrong dtype or
+# a strided view from a valid device tensor; a wrong one would be read as
+# device memory.  The binding therefore checks every tensor it marshals
+# (placement, device, dtype, contiguity, shape or size) and raises
+# MoeError(MOE_ERR_INVALID_ARG) before any library call.
+
+def _bad(msg: str):
+    raise MoeError(MOE_ERR_INVALID_ARG, msg)
+
+
+def _check_tensor(t, name: str, *, cuda: bool, dtype=None, itemsize: int | None = None,
+                  shape=None, numel: int | None = None, device: int | None = None) -> None:
+    if t is None:
+        _bad(f"{name} is None")
+    if bool(t.is_cuda) != cuda:
+        _bad(f"{name} must be a {'CUDA' if cuda else 'host (CPU)'} tensor, got {t.device}")
+    if cuda and device is not None and t.device.index != device:
+        _bad(f"{name} is on {t.device}, the current device is cuda:{device}")
+    if dtype is not None and t.dtype != dtype:
+        _bad(f"{name} must be {dtype}, got {t.dtype}")
+    if itemsize is not None and t.element_size() != itemsize:
+        _bad(f"{name} must have {itemsize}-byte elements, got {t.dtype}")
+    if not t.is_contiguous():
+        _bad(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        _bad(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if numel is not None and t.numel() != numel:
+        _bad(f"{name} must hold {numel} elements, got {t.numel()}")
+
+
+def weight_numels(s: MoeShape, mode: int) -> tuple:
+    """Elements (bytes) of w1, w1_sf, w2, w2_sf: MXFP4 codes two per byte
+    (MXFP8: one E4M3 byte each) and one E8M0 byte per 32 K."""
+    E, H, I = s.num_experts, s.hidden, s.inter
+    per = 1 if mode == MOE_W8A8_MXFP8 else 2
+    return (E * 2 * I * H // per, E * 2 * I * H // 32, E * H * I // per, E * H * I // 32)
+
+
+def _check_mode(mode: int) -> None:
+    if mode not in (MOE_W4A8_MXFP4_FP8, MOE_W4A16_MXFP4_BF16, MOE_W8A8_MXFP8):
+        _bad(f"quant_mode {mode} unknown")
+
+
+def _check_weights(s: MoeShape, mode: int, tensors, names, device) -> None:
+    for t, name, n in zip(tensors, names, weight_numels(s, mode)):
+        _check_tensor(t, name, cuda=True, itemsize=1, numel=n, device=device)
+
+
+def validate_forward(s: MoeShape, mode: int, x, logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out,
+                     workspace, host: bool = False, device: int | None = None) -> None:
+    """Checks the tensors of forward() (host=False) or forward_host()
+    (host=True: x, logits and out on the host).  `device`: the current CUDA
+    device index every device tensor must live on."""
+    import torch
+    _check_mode(mode)
+    T, E, H = s.num_tokens, s.num_experts, s.hidden
+    dev = not host
+    _check_tensor(x, "x", cuda=dev, dtype=torch.bfloat16, shape=(T, H), device=device)
+    _check_tensor(logits, "logits", cuda=dev, dtype=torch.float32, shape=(T, E), device=device)
+    _check_tensor(out, "out", cuda=dev, dtype=torch.bfloat16, shape=(T, H), device=device)
+    _check_weights(s, mode, (w1_p, w1_sf_p, w2_p, w2_sf_p), ("w1", "w1_sf", "w2", "w2_sf"),
+                   device)
+    _check_tensor(workspace, "workspace", cuda=True, device=device)
+
+
+def _current_device() -> int | None:
+    """Index of the current CUDA device (None without one: every tensor then
+    fails the placement check)."""
+    import torch
+    return torch.cuda.current_device() if torch.cuda.is_available() else None
+
+
 def _stream(stream) -> int:
     if stream is not None:
         return int(stream)
@@ -178,14 +251,25 @@ def _ptr(t) -> int:
 
 def prepare_weights(s: MoeShape, w1, w1_sf, w2, w2_sf, w1_p, w1_sf_p, w2_p, w2_sf_p,
                     mode: int = MOE_W4A8_MXFP4_FP8, stream=None) -> None:
+    _check_mode(mode)
+    dev = _current_device()
+    names = ("w1", "w1_sf", "w2", "w2_sf")
+    _check_weights(s, mode, (w1, w1_sf, w2, w2_sf), names, dev)
+    _check_weights(s, mode, (w1_p, w1_sf_p, w2_p, w2_sf_p), [n + "_p" for n in names], dev)
     check(load().moe_prepare_weights(ctypes.byref(s), mode, *(_ptr(t) for t in (
         w1, w1_sf, w2, w2_sf, w1_p, w1_sf_p, w2_p, w2_sf_p)), _stream(stream)))
 
 
 def forward(s: MoeShape, x, logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out, workspace,
-            mode: int = MOE_W4A8_MXFP4_FP8, opts: MoeOptions | None = None, stream=None) -> None:
+            mode: int = MOE_W4A8_MXFP4_FP8, opts: MoeOptions | None = None, stream=None,
+            validate: bool = True) -> None:
+    """validate=False skips the tensor checks (a few microseconds of host time)
+    for a caller that reuses tensors it has already passed once with checks."""
     lib = load()
-    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if validate:
+        validate_forward(s, mode, x, logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out, workspace,
+                         device=_current_device())
+    nbytes = workspace.numel() * workspace.element_size()
     args = [ctypes.byref(s), mode, _ptr(x), _ptr(logits), _ptr(w1_p), _ptr(w1_sf_p), _ptr(w2_p),
             _ptr(w2_sf_p), _ptr(out), _ptr(workspace), nbytes, _stream(stream)]
     if opts is None:
@@ -196,7 +280,10 @@ def forward(s: MoeShape, x, logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out, workspace
 
 def forward_host(s: MoeShape, x_host, logits_host, w1_p, w1_sf_p, w2_p, w2_sf_p, out_host,
                  workspace, mode: int = MOE_W4A8_MXFP4_FP8, opts: MoeOptions | None = None,
-                 stream=None) -> None:
+                 stream=None, validate: bool = True) -> None:
+    if validate:
+        validate_forward(s, mode, x_host, logits_host, w1_p, w1_sf_p, w2_p, w2_sf_p, out_host,
+                         workspace, host=True, device=_current_device())
     nbytes = workspace.numel() * workspace.element_size()
     check(load().moe_forward_host(ctypes.byref(s), mode, _ptr(x_host), _ptr(logits_host),
                                   _ptr(w1_p), _ptr(w1_sf_p), _ptr(w2_p), _ptr(w2_sf_p),
@@ -205,12 +292,14 @@ def forward_host(s: MoeShape, x_host, logits_host, w1_p, w1_sf_p, w2_p, w2_sf_p,
 
 
 def read_device_status(workspace, stream=None) -> int:
+    _check_tensor(workspace, "workspace", cuda=True, device=_current_device())
     v = ctypes.c_int32(0)
     check(load().moe_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(v)))
     return int(v.value)
 
 
 def selftest_timeout(workspace, timeout_us: int, stream=None) -> None:
+    _check_tensor(workspace, "workspace", cuda=True, device=_current_device())
     check(load().moe_selftest_timeout(_ptr(workspace), timeout_us, _stream(stream)))
 
 
@@ -218,5 +307,13 @@ def route_noalloc(s: MoeShape, logits, ids, weights, offsets, row_of, stream=Non
     """Routing front end (ids, weights, offsets, row map) using the library's
     static device scratch instead of a workspace; see moe_route_noalloc in
     include/moe.h for the size limit and the no-overlap rule."""
+    import torch
+    dev = _current_device()
+    T, E, k = s.num_tokens, s.num_experts, s.top_k
+    _check_tensor(logits, "logits", cuda=True, dtype=torch.float32, shape=(T, E), device=dev)
+    for t, name, dt, shp in ((ids, "ids", torch.int32, (T, k)), (weights, "weights", torch.float32,
+                              (T, k)), (offsets, "offsets", torch.int32, (E + 1,)),
+                             (row_of, "row_of", torch.int32, (T, k))):
+        _check_tensor(t, name, cuda=True, dtype=dt, shape=shp, device=dev)
     check(load().moe_route_noalloc(ctypes.byref(s), _ptr(logits), _ptr(ids), _ptr(weights),
                                    _ptr(offsets), _ptr(row_of), _stream(stream)))

@@ -242,16 +242,25 @@ def test_device_timeout_status_and_recovery():
 
 
 def test_invalid_args_on_device():
-    cfg = MI.custom_config(8, 2, 256, 128)
+    """Well-formed tensors with a short workspace: the library's own check
+    fires; malformed tensors are stopped by the binding before the call."""
     s = P.shape(4, 8, 2, 256, 128)
-    ws = torch.zeros(P.workspace_size(s) - 256, dtype=torch.uint8, device="cuda:0")
-    t = torch.zeros(4096, dtype=torch.uint8, device="cuda:0")
+    dev = "cuda:0"
+    ws = torch.zeros(P.workspace_size(s) - 256, dtype=torch.uint8, device=dev)
+    x = torch.zeros((4, 256), dtype=torch.bfloat16, device=dev)
+    lg = torch.zeros((4, 8), dtype=torch.float32, device=dev)
+    out = torch.empty((4, 256), dtype=torch.bfloat16, device=dev)
+    w = [torch.zeros(n, dtype=torch.uint8, device=dev) for n in P._lib.weight_numels(s, 0)]
     with pytest.raises(P.MoeError) as ei:
-        P.forward(s, t, t.view(torch.float32), t, t, t, t, t, ws)
+        P.forward(s, x, lg, *w, out, ws)
     assert ei.value.code == P._lib.MOE_ERR_WORKSPACE_TOO_SMALL
-    with pytest.raises(P.MoeError) as ei:
-        P.forward(s, t, t.view(torch.float32), t, t, t, t, t, ws, mode=7)
-    assert ei.value.code == P._lib.MOE_ERR_INVALID_ARG
+    for bad in (dict(mode=7), dict(x=x.float()), dict(x=x.cpu()), dict(lg=lg[:2]),
+                dict(out=out.t().contiguous().t())):
+        a = dict(x=x, lg=lg, out=out, mode=0)
+        a.update(bad)
+        with pytest.raises(P.MoeError) as ei:
+            P.forward(s, a["x"], a["lg"], *w, a["out"], ws, mode=a["mode"])
+        assert ei.value.code == P._lib.MOE_ERR_INVALID_ARG
 
 
 # ------------------------------------------------------------------ full sizes
