@@ -31,10 +31,12 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- routing
-// One warp per token (32 warps = one chunk per CTA).  Lane l holds logits of experts l, l+32, ... (NV per
-// lane).  k rounds of a warp argmax pick the experts in descending logit
-// order, equal logits resolved toward the lower expert index.  Weights are
-// the softmax over the k selected logits (renormalised top-k softmax).
+// One warp per token (32 warps = one chunk per CTA).  Lane l holds logits of
+// experts l, l+32, ... (NV per lane).  k rounds of a warp argmax pick the
+// experts in descending logit order, equal logits resolved toward the lower
+// expert index.  Weights are the softmax over the k selected logits
+// (renormalised top-k softmax).  A NaN logit is read as -inf, so every round
+// finds an expert index below E whatever the input holds.
 template <int NV>
 __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T,
                                                     int E, int k, int32_t* __restrict__ ids,
@@ -65,6 +67,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       v[i] = e < E ? row[e] : -FLT_MAX;
+      if (v[i] != v[i]) v[i] = -INFINITY;   // NaN ranks with -inf: k experts are always found
     }
     uint32_t taken = 0;
     float my_v = 0.f;
@@ -519,6 +522,7 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       v[i] = e < E ? row[e] : -FLT_MAX;
+      if (v[i] != v[i]) v[i] = -INFINITY;   // NaN ranks with -inf: k experts are always found
     }
     uint32_t taken = 0;
     float my_v = 0.f;
