@@ -22,6 +22,20 @@ bf16).  Structure, for E = 2 experts, H = 64, I = 32:
             = (448 m)^2 * S_e[c],  S_e[c] = sum_j [rho_j > 0] sigma_j tau[c][j].
   combine: out[t][c] = bf16(sum_{e in top-k(t)} w_te * y_e[c]), with w = 1
      for k = 1 and w = 1/2 exactly for k = 2 with equal logits.
+The same case in the other two quantisation modes:
+  W4A16 (bf16 activations, MXFP4 weights, h fed to GEMM2 as bf16): x = 448
+     enters unquantised and h = (448 m)^2 sigma_j is exact in bf16
+     ((448 m)^2 = 49 * 2^(12 + 2 log2 m)), so y and out equal the W4A8 values.
+  W8A8 (MXFP8 x MXFP8, OCP MX blocks of 32): the same weight values as E4M3
+     codes (+-1 = 0x38/0xB8, +-2 = 0x40/0xC0) with the same scale bytes.  x's
+     block holding 448 has amax 448 = 1.75 * 2^8, so X = 2^(8 - 8) = 1 and the
+     code is 0x7E; all-zero blocks get byte 127 and zero codes.  GEMM1 and
+     SwiGLU are as above.  The h row (I = 32, one block) has amax (448 m)^2 =
+     392 * 2^(9 + 2 log2 m), so X = 2^(9 + 2 log2 m) (scale byte 136 for
+     m = 1, 138 for m = 2) and each nonzero h / X = +-392, which E4M3 cannot
+     hold: round-to-nearest gives +-384 (code 0x7C / 0xFC; the neighbours are
+     384 and 416).  Hence y_e[c] = 384 * X * S_e[c] = 196608 m^2 S_e[c] and
+     out[t][c] = bf16(sum w_te * 196608 m^2 S_e[c]).
 Run: python tests/golden/make_exact_swiglu_case.py
 """
 import json
@@ -31,6 +45,11 @@ import numpy as np
 import torch
 
 E, H, I = 2, 64, 32
+
+
+def _bf16(v) -> list:
+    """float64 values (exact integers here) rounded to bf16, as floats."""
+    return torch.tensor(v, dtype=torch.float32).to(torch.bfloat16).to(torch.float32).tolist()
 
 
 def main():
@@ -46,6 +65,7 @@ def main():
     cases = []
     for k, logits in [(1, [[1.0, 0.0], [0.0, 1.0]]), (2, [[0.5, 0.5], [-1.0, -1.0]])]:
         out = np.zeros((2, H), dtype=np.float64)
+        out_w8a8 = np.zeros((2, H), dtype=np.float64)
         for t in range(2):
             m = 1 if t == 0 else 2
             chosen = [int(np.argmax(logits[t]))] if k == 1 else [0, 1]
@@ -53,8 +73,9 @@ def main():
             for e in chosen:
                 S = ((rho[e] > 0) * sigma[e] * tau[e]).sum(axis=1)   # integer [H]
                 out[t] += w * (448 * m) ** 2 * S
-        out_bf16 = torch.tensor(out, dtype=torch.float32).to(torch.bfloat16).to(torch.float32)
-        cases.append({"top_k": k, "logits": logits, "expected_out": out_bf16.tolist()})
+                out_w8a8[t] += w * 196608 * m * m * S
+        cases.append({"top_k": k, "logits": logits, "expected_out": _bf16(out),
+                      "expected_out_w4a16": _bf16(out), "expected_out_w8a8": _bf16(out_w8a8)})
     doc = {
         "source": "closed-form case; derivation in make_exact_swiglu_case.py. Steps follow "
                   "flashinfer PR #3738 'perf: optimize MXFP4xBF16 & INT4xFP8 and add MXFP4xFP8 "
@@ -63,6 +84,7 @@ def main():
                   "CuTe DSL dispatch to be dtype agnostic' (SwiGLU activation, finalize).",
         "E": E, "H": H, "I": I, "x_positions": [0, 33], "w1_block_scale_bytes": [127, 128],
         "rho": rho.tolist(), "sigma": sigma.tolist(), "tau": tau.tolist(), "cases": cases,
+        "w8a8_h_code_magnitude": 0x7C, "w8a8_h_scale_bytes": [136, 138],
     }
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "exact_swiglu_case.json")
     with open(path, "w") as f:

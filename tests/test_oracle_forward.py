@@ -73,6 +73,78 @@ def test_exact_swiglu_golden_case():
                 assert fw.h_scale[r] == 1.0 and np.all(fw.hq[r] == 0)
 
 
+_VAL2E4M3 = {0: 0x00, 1: 0x38, -1: 0xB8, 2: 0x40, -2: 0xC0}
+
+
+def _exact_case_w8a8_weights(doc):
+    """The golden case's weight values as MXFP8 (E4M3 codes, same scale bytes)."""
+    E, H, I = doc["E"], doc["H"], doc["I"]
+    rho, sigma, tau = (np.array(doc[k]) for k in ("rho", "sigma", "tau"))
+    c1 = np.zeros((E, 2 * I, H), dtype=np.uint8)
+    for e in range(E):
+        for n in range(I):
+            for p in doc["x_positions"]:
+                c1[e, n, p] = _VAL2E4M3[int(rho[e, n])]
+                c1[e, I + n, p] = _VAL2E4M3[int(sigma[e, n])]
+    sf1 = np.full((E, 2 * I, H // 32), 127, dtype=np.uint8)
+    sf1[:, :, 1] = doc["w1_block_scale_bytes"][1]
+    c2 = np.vectorize(lambda v: _VAL2E4M3[int(v)])(tau).astype(np.uint8)
+    sf2 = np.full((E, H, I // 32), 127, dtype=np.uint8)
+    return M.Weights(c1, sf1, c2, sf2, mode=M.QUANT_W8A8)
+
+
+def test_exact_golden_case_w4a16():
+    """bf16 activations and bf16 h: the same exact outputs as W4A8."""
+    with open(os.path.join(GOLDEN, "exact_swiglu_case.json")) as f:
+        doc = json.load(f)
+    xbits, W = _exact_case_inputs(doc)
+    W = M.Weights(W.w1, W.w1_sf, W.w2, W.w2_sf, mode=M.QUANT_W4A16)
+    I = doc["I"]
+    rho, sigma = np.array(doc["rho"]), np.array(doc["sigma"])
+    for case in doc["cases"]:
+        fw = M.forward(xbits, np.array(case["logits"], np.float32), W, case["top_k"],
+                       mode=M.QUANT_W4A16)
+        np.testing.assert_array_equal(fw.out, np.array(case["expected_out_w4a16"], np.float32))
+        assert fw.xq is None and fw.hq is None
+        rt = fw.routing
+        for r in range(len(rt.token_of_row)):
+            t, e = rt.token_of_row[r], rt.expert_of_row[r]
+            m = 1 if t == 0 else 2
+            np.testing.assert_array_equal(fw.g[r, :I], 448.0 * m * rho[e])
+            np.testing.assert_array_equal(fw.h[r], np.where(rho[e] > 0,
+                                                            (448.0 * m) ** 2 * sigma[e], 0.0))
+
+
+def test_exact_golden_case_w8a8():
+    """MXFP8 blocks: x's block scale 1 with code 0x7E; h/X = +-392 rounds to
+    +-384 (code 0x7C/0xFC) under the block scale 2^(9 + 2 log2 m)."""
+    with open(os.path.join(GOLDEN, "exact_swiglu_case.json")) as f:
+        doc = json.load(f)
+    xbits, _ = _exact_case_inputs(doc)
+    W = _exact_case_w8a8_weights(doc)
+    I = doc["I"]
+    rho = np.array(doc["rho"])
+    mag, hbytes = doc["w8a8_h_code_magnitude"], doc["w8a8_h_scale_bytes"]
+    for case in doc["cases"]:
+        fw = M.forward(xbits, np.array(case["logits"], np.float32), W, case["top_k"],
+                       mode=M.QUANT_W8A8)
+        np.testing.assert_array_equal(fw.out, np.array(case["expected_out_w8a8"], np.float32))
+        rt = fw.routing
+        for r in range(len(rt.token_of_row)):
+            t, e = rt.token_of_row[r], rt.expert_of_row[r]
+            m = 1 if t == 0 else 2
+            p = doc["x_positions"][t]
+            assert fw.xq[r, p] == 0x7E and np.all(fw.x_scale[r] == 127)
+            assert np.count_nonzero(fw.xq[r] & 0x7F) == 1
+            np.testing.assert_array_equal(fw.g[r, :I], 448.0 * m * rho[e])
+            if np.any(rho[e] > 0):
+                assert fw.h_scale[r, 0] == hbytes[t]
+                np.testing.assert_array_equal(fw.hq[r][rho[e] > 0] & 0x7F, mag)
+                assert np.all(fw.hq[r][rho[e] < 0] & 0x7F == 0)
+            else:
+                assert fw.h_scale[r, 0] == 127 and np.all(fw.hq[r] & 0x7F == 0)
+
+
 def _to_np(case):
     xbits = case.x.view(torch.int16).numpy().view(np.uint16)
     W = M.Weights(case.w1.numpy(), case.w1_sf.numpy(), case.w2.numpy(), case.w2_sf.numpy(),

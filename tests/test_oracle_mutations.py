@@ -123,6 +123,24 @@ def _pins_forward_w16():
 def test_mode_pins_pass_unmutated():
     _pins_forward_mx()
     _pins_forward_w16()
+    TW.test_exact_golden_case_w8a8()
+    TW.test_exact_golden_case_w4a16()
+
+
+def test_mxfp8_round_up_instead_of_nearest_is_caught(monkeypatch):
+    """E4M3 rounding of the MXFP8 quotient taken upward in magnitude: the
+    golden case's h / X = 392 must give 384, not 416."""
+    orig = F.e4m3_encode
+
+    def bad(v):
+        v = np.asarray(v, dtype=np.float64)
+        codes = orig(v)
+        dec = F.e4m3_decode(codes)
+        up = np.abs(dec) < np.abs(v)                 # rounded down in magnitude
+        bumped = np.where(up & ((codes & 0x7F) < 0x7E), codes + 1, codes)
+        return bumped.astype(np.uint8)
+    monkeypatch.setattr(F, "e4m3_encode", bad)
+    _expect_caught(TW.test_exact_golden_case_w8a8)
 
 
 def test_mxfp8_exponent_off_by_one_is_caught(monkeypatch):
@@ -138,6 +156,7 @@ def test_mxfp8_exponent_off_by_one_is_caught(monkeypatch):
         return codes.reshape(v.shape).astype(np.uint8), (e1 + 127).astype(np.uint8)
     monkeypatch.setattr(M, "quantize_rows_mxfp8", bad)
     _expect_caught(_pins_forward_mx)
+    _expect_caught(TW.test_exact_golden_case_w8a8)
 
 
 def test_mxfp8_dropped_activation_scale_is_caught(monkeypatch):
@@ -149,6 +168,7 @@ def test_mxfp8_dropped_activation_scale_is_caught(monkeypatch):
         return codes, np.full_like(sc, 127)
     monkeypatch.setattr(M, "quantize_rows_mxfp8", bad)
     _expect_caught(_pins_forward_mx)
+    _expect_caught(TW.test_exact_golden_case_w8a8)
 
 
 def test_w4a16_h_not_rounded_to_bf16_is_caught(monkeypatch):
@@ -158,3 +178,4 @@ def test_w4a16_h_not_rounded_to_bf16_is_caught(monkeypatch):
         return (M.silu_f32(g[:, :I]) * g[:, I:]).astype(np.float32) * np.float32(1.0 + 2.0 ** -7)
     monkeypatch.setattr(M, "swiglu_bf16", bad)
     _expect_caught(_pins_forward_w16)
+    _expect_caught(TW.test_exact_golden_case_w4a16)
