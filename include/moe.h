@@ -166,6 +166,8 @@ int32_t moe_workspace_layout(const moe_shape* shape, int32_t quant_mode,
  *   w1    [E, 2I, H/2]  E2M1 codes, two per byte, low nibble = even k
  *   w1_sf [E, 2I, H/32] E8M0 scale per 32 consecutive k
  *   w2    [E, H, I/2],  w2_sf [E, H, I/32]
+ * User layout (W8A8, MXFP8 [P3614]): w1 [E, 2I, H] and w2 [E, H, I] hold one
+ * E4M3 code per byte; w1_sf and w2_sf are as above.
  * Outputs have the same byte sizes and must not alias the inputs.  Pointers
  * must be 256-byte aligned.  Asynchronous on `stream`. */
 int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode,
@@ -178,7 +180,8 @@ int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode,
  * epilogue -> per-row FP8 quantisation of h -> GEMM2 -> top-k weighted
  * combine.
  *   x              bf16  [T, H]  (16-byte aligned)
- *   router_logits  float [T, E]  finite values
+ *   router_logits  float [T, E]  finite values (a NaN is ranked as -inf, so
+ *                                 routing stays in range; its weight is 0)
  *   w1_p .. w2_sf_p              prepared weights (moe_prepare_weights)
  *   out            bf16  [T, H]  written in full (16-byte aligned)
  *   workspace      >= moe_workspace_size() bytes, 256-byte aligned
