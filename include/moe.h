@@ -181,7 +181,9 @@ int32_t moe_prepare_weights(const moe_shape* shape, int32_t quant_mode,
  * combine.
  *   x              bf16  [T, H]  (16-byte aligned)
  *   router_logits  float [T, E]  finite values (a NaN is ranked as -inf, so
- *                                 routing stays in range; its weight is 0)
+ *                                 the routed ids stay in range; it gets
+ *                                 weight 0 unless the whole row is NaN or
+ *                                 -inf, which gives NaN weights)
  *   w1_p .. w2_sf_p              prepared weights (moe_prepare_weights)
  *   out            bf16  [T, H]  written in full (16-byte aligned)
  *   workspace      >= moe_workspace_size() bytes, 256-byte aligned
