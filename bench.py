@@ -51,7 +51,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-modes", action="store_true",
                     help="skip the W4A16 and MXFP8 workloads")
-    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 decode, 2 prefill tiles")
+    ap.add_argument("--variant", type=int, default=0,
+                    help="GEMM tile variant (moe_options.tile_variant): 0 auto, 1-6 forced")
     return ap.parse_args()
 
 
@@ -199,7 +200,7 @@ def alg_cost(stage: str, cfg, T: int, n_touched: int, mode: int = 0):
     rs = 0 if mode == 1 else 4                                         # row-scale bytes
     table = {
         "route": (T * E * 4 + R * 8, 0),
-        "scan": (R * 0, 0),
+        "scan": (2 * 4 * E * -(-T // 32), 0),     # per-chunk counts in, chunk bases out
         "rank": (R * 12, 0),
         "quant_scatter": (T * H * 2 + R * H * act + R * rs, 0),
         "gemm1": (n_touched * w1 + R * H * act + R * rs + R * I * 2, 2.0 * R * H * 2 * I),
