@@ -220,6 +220,22 @@ MODE_WEIGHTS = {0: "MXFP4", 1: "MXFP4", 2: "MXFP8"}
 MODE_NAME = {0: "MXFP4xFP8", 1: "MXFP4xBF16", 2: "MXFP8xMXFP8"}
 
 
+# model whose MoE layer shape a configuration copies (H, I, E, k)
+SHAPE_NAMES = {(7168, 2048, 256, 8): "DeepSeek-V3-shaped ", (7168, 3072, 384, 6):
+               "DeepSeek-V4-Pro-shaped "}
+
+
+def workload_config(cfg, T: int) -> dict:
+    """The `config` keys both arms report for the same workload."""
+    mode = cfg.mode
+    model = SHAPE_NAMES.get((cfg.hidden, cfg.inter, cfg.num_experts, cfg.top_k), "")
+    return {"workload": f"{model}MoE layer E={cfg.num_experts} top-{cfg.top_k} "
+                        f"H={cfg.hidden} I={cfg.inter} SwiGLU, T={T}, {MODE_NAME[mode]}"
+                        + (f", Zipf({cfg.zipf}) routing" if cfg.zipf else ""),
+            "num_tokens": T, "num_experts": cfg.num_experts, "top_k": cfg.top_k,
+            "hidden": cfg.hidden, "inter": cfg.inter}
+
+
 def fused_roofline(cfg, T, n_touched, t_s, pk, mode=0):
     """Roofline of the whole forward: max(touched weight+scale + activation
     bytes / HBM, FLOPs / tensor peak of the MMA kind the mode runs: FP8 for
@@ -368,10 +384,7 @@ def run_ours(args, dist: Dist):
         "dtype": MODE_DTYPE[mode],
         "data": "synthetic (seeded N(0,1) activations/logits, N(0,0.02) weights as "
                 f"{MODE_WEIGHTS[mode]})" + (f", Zipf({cfg.zipf}) routing skew" if cfg.zipf else ""),
-        "config": {"workload": f"DeepSeek-V3-shaped MoE layer E={cfg.num_experts} top-{cfg.top_k} "
-                               f"H={cfg.hidden} I={cfg.inter} SwiGLU, T={T}, {MODE_NAME[mode]}",
-                   "num_tokens": T, "num_experts": cfg.num_experts, "top_k": cfg.top_k,
-                   "hidden": cfg.hidden, "inter": cfg.inter, "parallelism": f"replicas x{dist.world}",
+        "config": {**workload_config(cfg, T), "parallelism": f"replicas x{dist.world}",
                    "l2": "no flush: the touched expert weights per step "
                          f"({n_touched * 3 * cfg.inter * cfg.hidden * wbytes / 1e9:.2f} GB) "
                          "exceed the 129 MB L2",
@@ -597,10 +610,7 @@ def run_reference(args, dist: Dist):
     return {"metric": METRIC, "value": v, "unit": UNIT, "impl": "reference", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32",
-            "data": "synthetic", "config": {"workload": f"DeepSeek-V3-shaped MoE layer "
-                                                        f"E={cfg.num_experts} top-{cfg.top_k} "
-                                                        f"H={cfg.hidden} I={cfg.inter}, T={T}",
-                                            "num_tokens": T},
+            "data": "synthetic", "config": {**workload_config(cfg, T), "parallelism": "replicas x1"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -50,3 +50,23 @@ def test_roofline_helpers():
     pk = dict(bench.FALLBACK)
     fr = bench.fused_roofline(cfg, 4096, 256, 1e-3, pk)
     assert fr["bound"] == "hbm" and 0 < fr["frac"] < 1
+
+
+def test_reference_arm_line_matches_ours():
+    """The reference arm (the oracle on the host) reports the same metric,
+    unit, direction and workload configuration as the GPU arm, with its own
+    cpu_baseline and an e2e entry of its own value."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import moe_inputs as MI
+    args = type("A", (), {"config": "tiny", "tokens": 16, "warmup": 0, "steps": 1})()
+    res = bench.run_reference(args, bench.Dist())
+    cfg = MI.CONFIGS["tiny"]
+    assert res["impl"] == "reference"
+    assert (res["metric"], res["unit"], res["higher_is_better"]) == (bench.METRIC, bench.UNIT,
+                                                                     True)
+    for key, val in bench.workload_config(cfg, 16).items():
+        assert res["config"][key] == val
+    assert res["cpu_baseline"]["kind"] == "oracle" and res["cpu_baseline"]["value"] == res["value"]
+    assert res["e2e"] == {"value": res["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
