@@ -72,7 +72,9 @@ typedef enum {
 /* Problem shape.  Activation SwiGLU and softmax-top-k-renormalised routing
  * are fixed.  Limits: num_tokens >= 0; 1 <= num_experts <= 1024;
  * 1 <= top_k <= min(num_experts, 32); hidden and inter positive multiples of
- * 128; num_tokens * top_k < 2^31. */
+ * 128; num_tokens * top_k < 2^31; num_experts * 2 * inter * hidden / 128 <
+ * 2^31 (the GEMMs' 32-bit weight-box coordinates; MOE_ERR_UNSUPPORTED
+ * otherwise). */
 typedef struct {
   int32_t num_tokens;   /* T */
   int32_t num_experts;  /* E */

@@ -103,6 +103,14 @@ int32_t check_shape(const moe_shape* s, int32_t mode) {
   if (static_cast<int64_t>(s->num_experts) * 2 * s->inter >= (int64_t(1) << 31) ||
       static_cast<int64_t>(s->num_experts) * s->hidden >= (int64_t(1) << 31))
     return fail(MOE_ERR_INVALID_ARG, "num_experts * rows must be < 2^31");
+  // The GEMMs address a weight box by its first row in one tensor map over
+  // all experts' boxes, a 32-bit TMA coordinate: E * 2I * H / 128 rows for w1
+  // (w2 has half as many).
+  if (static_cast<int64_t>(s->num_experts) * 2 * s->inter * (s->hidden / 128) >=
+      (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "num_experts * 2 * inter * hidden / 128 must be < 2^31 (32-bit weight-box "
+                "row coordinates)");
   return MOE_OK;
 }
 

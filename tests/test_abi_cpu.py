@@ -88,12 +88,26 @@ def test_workspace_layout_mxfp8(lib):
 
 
 @pytest.mark.parametrize("bad", [dict(T=-1), dict(E=0), dict(k=0), dict(k=9, E=8), dict(k=33, E=64),
-                                 dict(H=100), dict(I=96), dict(E=2000)])
+                                 dict(H=100), dict(I=96), dict(E=2000),
+                                 dict(E=1024, I=8192, H=16384)])
 def test_workspace_size_rejects_bad_shapes(lib, bad):
     kw = dict(T=16, E=8, k=2, H=256, I=128)
     kw.update(bad)
     assert P.workspace_size(_shape(**kw)) == 0
     assert P.workspace_size(_shape(), 7) == 0
+
+
+def test_weight_box_coordinates_stay_32_bit(lib):
+    """E * 2I * H / 128 weight-box rows must fit a 32-bit TMA coordinate:
+    the largest shape just below the limit is accepted, the next one not."""
+    ok = _shape(T=1, E=1023, k=1, H=16384, I=8192)       # 1023 * 2^14 * 2^7 < 2^31
+    assert P.workspace_size(ok) > 0
+    bad = _shape(T=1, E=1024, k=1, H=16384, I=8192)      # exactly 2^31
+    assert P.workspace_size(bad) == 0
+    L_ = L.WsLayout()
+    assert lib.moe_workspace_layout(ctypes.byref(bad), 0, ctypes.byref(L_)) == \
+        L.MOE_ERR_UNSUPPORTED
+    assert b"32-bit" in lib.moe_last_error()
 
 
 def _fwd(lib, s, ptrs, nbytes, mode=0, opts=None):
