@@ -73,8 +73,9 @@ typedef enum {
  * are fixed.  Limits: num_tokens >= 0; 1 <= num_experts <= 1024;
  * 1 <= top_k <= min(num_experts, 32); hidden and inter positive multiples of
  * 128; num_tokens * top_k < 2^31; num_experts * 2 * inter * hidden / 128 <
- * 2^31 (the GEMMs' 32-bit weight-box coordinates; MOE_ERR_UNSUPPORTED
- * otherwise). */
+ * 2^31 (the GEMMs' 32-bit weight-box coordinates) and
+ * (T*k/16 + min(E, T*k) + 1) * max(2*inter, hidden) / 128 < 2^31 (their
+ * work-item counters); MOE_ERR_UNSUPPORTED otherwise. */
 typedef struct {
   int32_t num_tokens;   /* T */
   int32_t num_experts;  /* E */

@@ -111,6 +111,15 @@ int32_t check_shape(const moe_shape* s, int32_t mode) {
     return fail(MOE_ERR_UNSUPPORTED,
                 "num_experts * 2 * inter * hidden / 128 must be < 2^31 (32-bit weight-box "
                 "row coordinates)");
+  // A GEMM's work items (tiles x M-tiles) are counted in 32 bits: at most
+  // (R / 16 + min(E, R) + 1) tiles times max(2I, H) / 128 M-tiles.
+  {
+    const int64_t R = static_cast<int64_t>(s->num_tokens) * s->top_k;
+    const int64_t tiles = R / 16 + (s->num_experts < R ? s->num_experts : R) + 1;
+    const int64_t mtiles = (2 * s->inter > s->hidden ? 2 * s->inter : s->hidden) / 128;
+    if (tiles * mtiles >= (int64_t(1) << 31))
+      return fail(MOE_ERR_UNSUPPORTED, "too many GEMM work items for 32-bit counters");
+  }
   return MOE_OK;
 }
 

@@ -108,6 +108,9 @@ def test_weight_box_coordinates_stay_32_bit(lib):
     assert lib.moe_workspace_layout(ctypes.byref(bad), 0, ctypes.byref(L_)) == \
         L.MOE_ERR_UNSUPPORTED
     assert b"32-bit" in lib.moe_last_error()
+    # work items: (R/16 + E + 1) * 2I/128 with R = 2^31 - 1 expanded rows
+    many = _shape(T=(1 << 31) - 1, E=8, k=1, H=256, I=1 << 14)
+    assert P.workspace_size(many) == 0 and b"work items" in lib.moe_last_error()
 
 
 def _fwd(lib, s, ptrs, nbytes, mode=0, opts=None):
