@@ -164,3 +164,21 @@ def test_prepare_and_misc_validation_without_gpu(lib):
     st = ctypes.c_int32(0)
     assert lib.moe_read_device_status(None, None, ctypes.byref(st)) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_status_string(-6) == b"device-side wait timed out"
+
+
+def test_no_device_gives_cuda_error(lib):
+    """Valid arguments on a machine without a GPU: the first CUDA call fails
+    and every entry point that reaches one returns MOE_ERR_CUDA with a
+    message, before any memory is touched.  Skipped where a GPU exists (the
+    pointers here are not device memory)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: these pointers must not reach it")
+    s = _shape()
+    good = [0x100000 * (i + 1) for i in range(8)]
+    assert _fwd(lib, s, good, P.workspace_size(s)) == L.MOE_ERR_CUDA
+    assert lib.moe_last_error()
+    assert lib.moe_prepare_weights(ctypes.byref(s), 0, *good, None) == L.MOE_ERR_CUDA
+    assert lib.moe_selftest_timeout(0x100000, 10, None) == L.MOE_ERR_CUDA
+    st = ctypes.c_int32(0)
+    assert lib.moe_read_device_status(0x100000, None, ctypes.byref(st)) == L.MOE_ERR_CUDA
