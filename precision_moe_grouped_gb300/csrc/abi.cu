@@ -115,7 +115,7 @@ int32_t check_shape(const moe_shape* s, int32_t mode) {
   // (R / 16 + min(E, R) + 1) tiles times max(2I, H) / 128 M-tiles.
   {
     const int64_t R = static_cast<int64_t>(s->num_tokens) * s->top_k;
-    const int64_t tiles = R / 16 + (s->num_experts < R ? s->num_experts : R) + 1;
+    const int64_t tiles = moe::max_work_tiles(R, s->num_experts, moe::kTinyBN);
     const int64_t mtiles = (2 * s->inter > s->hidden ? 2 * s->inter : s->hidden) / 128;
     if (tiles * mtiles >= (int64_t(1) << 31))
       return fail(MOE_ERR_UNSUPPORTED, "too many GEMM work items for 32-bit counters");
@@ -129,7 +129,7 @@ void compute_layout(const moe_shape* s, int32_t mode, moe_ws_layout* L) {
                 I = s->inter;
   const int64_t R = T * k;
   const int64_t chunks = (T + moe::kRouteChunk - 1) / moe::kRouteChunk;
-  const int64_t max_tiles = R / moe::kTinyBN + (E < R ? E : R) + 1;
+  const int64_t max_tiles = moe::max_work_tiles(R, E, moe::kTinyBN);   // smallest tiles
   size_t off = 0;
   auto take = [&](int64_t bytes) {
     off = align_up(off, kAlign);

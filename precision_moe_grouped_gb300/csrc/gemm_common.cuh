@@ -49,8 +49,7 @@ __device__ __forceinline__ int checked_num_tiles(const int32_t* num_tiles_p, int
                                                  WorkLimits lim) {
   const int n = *num_tiles_p;
   if constexpr (kChecks) {
-    const int max_tiles = lim.R / 16 + min(lim.E, lim.R) + 1;
-    if (n < 0 || n > max_tiles) {
+    if (n < 0 || n > max_work_tiles(lim.R, lim.E, kTinyBN)) {
       atomicCAS(status, 0, kDevCheckFailed);
       return 0;
     }
@@ -67,9 +66,7 @@ __device__ __forceinline__ int4 checked_tile(const int4* __restrict__ tiles, int
                                              int32_t* status, WorkLimits lim) {
   int4 td = tiles[i];
   if constexpr (kChecks) {
-    const bool ok = td.x >= 0 && td.x < lim.E && td.y >= 0 && td.z >= 1 && td.z <= bn &&
-                    td.y + td.z <= lim.R && td.w == 0;
-    if (!ok) {
+    if (!tile_entry_ok(td.x, td.y, td.z, td.w, bn, lim.R, lim.E)) {
       atomicCAS(status, 0, kDevCheckFailed);
       td = make_int4(0, 0, 16, 1);
     }

@@ -111,6 +111,34 @@ constexpr int kPairBN = 160;
 constexpr int kPairStages = 8;
 __host__ __device__ constexpr int kPairBoxRowsAt(int i) { return 16 * (i + 1); }
 
+// ---------------------------------------------------------------- work map
+// Tile plan of one expert with c > 0 rows and token tiles of at most bn rows
+// (bn a multiple of 16): nt = ceil(c / tsz) tiles of tsz =
+// roundup16(ceil(c / ceil(c / bn))) rows, so the tiles are balanced, every
+// MMA-N is a multiple of 16 and tsz <= bn.  Returns (nt, tsz); (0, 1) for
+// c <= 0.
+__host__ __device__ inline int2 expert_tile_plan(int c, int bn) {
+  if (c <= 0) return make_int2(0, 1);
+  const int n0 = (c + bn - 1) / bn;
+  const int tsz = (((c + n0 - 1) / n0) + 15) & ~15;
+  return make_int2((c + tsz - 1) / tsz, tsz);
+}
+
+// Largest tile list the plan above gives R expanded rows over E experts with
+// tiles of at most bn >= 16 rows: an expert with c rows gets at most
+// ceil(c / bn) <= c / bn + 1 tiles, so R / bn + min(E, R) + 1 entries.
+__host__ __device__ inline int64_t max_work_tiles(int64_t R, int64_t E, int64_t bn) {
+  return R / bn + (E < R ? E : R) + 1;
+}
+
+// Whether entry (x = expert, y = first row, z = rows, w) of a work map is
+// one a GEMM with token tiles of at most bn rows can run: an expert below E,
+// 1..bn rows inside the R expanded rows, w == 0.  Written so that no sum can
+// overflow, whatever the entry holds.
+__host__ __device__ inline bool tile_entry_ok(int x, int y, int z, int w, int bn, int R, int E) {
+  return x >= 0 && x < E && z >= 1 && z <= bn && y >= 0 && y <= R - z && w == 0;
+}
+
 // MXFP8 mode: the activation (B operand) scale bytes are written by the
 // quantisers straight into the GEMM's per-tile layout.  For tile t of the
 // GEMM tile list and K stage ks there is one kSfbTileBytes block at

@@ -43,7 +43,7 @@ struct Carve {
 Carve carve(int64_t T, int64_t E, int64_t k) {
   const int64_t R = T * k;
   const int64_t chunks = (T + moe::kRouteChunk - 1) / moe::kRouteChunk;
-  const int64_t max_tiles = R / moe::kDecodeBN + (E < R ? E : R) + 1;
+  const int64_t max_tiles = moe::max_work_tiles(R, E, moe::kDecodeBN);
   Carve c{};
   size_t off = 0;
   c.chunk_counts = off;

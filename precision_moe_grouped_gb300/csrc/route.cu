@@ -145,20 +145,16 @@ __device__ int block_exclusive_scan(int v, int* total) {
 
 // Tile plan of one expert (thread e of a block with blockDim >= E; every
 // thread of the block must call it): a tile is a run of at most `bn`
-// consecutive rows of one expert; an expert with c rows gets ceil(c / tsz)
-// tiles of tsz = roundup16(ceil(c / ceil(c / bn))) rows, so its tiles are
-// balanced and every MMA-N is a multiple of 16.  Returns (first tile, tsz);
-// with `write` the block also stores the tile list, the tile count and (if
-// tile_plan is not null) the per-expert plan.
+// consecutive rows of one expert, as many and as large as expert_tile_plan
+// gives for its c rows; the block's scan places the experts' tiles in expert
+// order.  Returns (first tile, tsz); with `write` the block also stores the
+// tile list, the tile count and (if tile_plan is not null) the per-expert
+// plan.
 __device__ int2 plan_tiles(int e, int E, int c, int off, int bn, bool write,
                            int4* __restrict__ tiles, int32_t* __restrict__ num_tiles,
                            int2* __restrict__ tile_plan) {
-  int nt = 0, tsz = 1;
-  if (e < E && c > 0) {
-    const int n0 = (c + bn - 1) / bn;
-    tsz = (((c + n0 - 1) / n0) + 15) & ~15;
-    nt = (c + tsz - 1) / tsz;
-  }
+  const int2 plan = expert_tile_plan(e < E ? c : 0, bn);
+  const int nt = plan.x, tsz = plan.y;
   int total_tiles;
   const int toff = block_exclusive_scan(nt, &total_tiles);
   if (write) {
