@@ -179,3 +179,41 @@ def test_w4a16_h_not_rounded_to_bf16_is_caught(monkeypatch):
     monkeypatch.setattr(M, "swiglu_bf16", bad)
     _expect_caught(_pins_forward_w16)
     _expect_caught(TW.test_exact_golden_case_w4a16)
+
+
+def _pin_route_and_quantize():
+    for x, lg, k in TR._front_cases():
+        TR.check_route_and_quantize(M.route_and_quantize, x, lg, k)
+
+
+def test_route_and_quantize_pins_pass_unmutated():
+    _pin_route_and_quantize()
+
+
+@pytest.mark.parametrize("slip", ["bits_as_values", "negated_logits", "scale_reciprocal",
+                                  "unstable_rows"])
+def test_route_and_quantize_slips_are_caught(monkeypatch, slip):
+    """Slips in the three steps route_and_quantize chains (the full-size GPU
+    tests' bit-exact reference): quantising the raw bf16 bit patterns instead
+    of their values, routing on negated logits, returning 448/amax as the
+    scale, and an expansion that is not stable in token order."""
+    orig_q, orig_route, orig_expand = M.quantize_rows_fp8, M.route, M.expand
+
+    def bad(x_bits, logits, k):
+        x = F.bf16_bits_to_f32(x_bits)
+        if slip == "bits_as_values":
+            x = np.asarray(x_bits, np.float32)
+        lg = -np.asarray(logits, np.float32) if slip == "negated_logits" else logits
+        ids, w = orig_route(np.asarray(lg, np.float32), k)
+        rt = orig_expand(ids, w, logits.shape[1])
+        if slip == "unstable_rows":
+            for e in range(len(rt.counts)):
+                a, b = rt.offsets[e], rt.offsets[e + 1]
+                seg = slice(a, b)
+                rt.token_of_row[seg] = rt.token_of_row[seg][::-1].copy()
+        tq, ts = orig_q(x)
+        if slip == "scale_reciprocal":
+            ts = (np.float32(1.0) / ts).astype(np.float32)
+        return rt, tq, ts
+    _expect_caught(lambda: [TR.check_route_and_quantize(bad, x, lg, k)
+                            for x, lg, k in TR._front_cases()])

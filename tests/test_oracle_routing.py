@@ -106,3 +106,78 @@ def test_mxfp8_quant_bounds():
     ok = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * X) * (1 + 1e-9)
     assert np.all(err[~sat] <= ok[~sat])
     assert np.all(sc[np.abs(x).reshape(8, 8, 32).max(-1) > 0] > 0)
+
+
+def _independent_front(x_bf16: torch.Tensor, logits: torch.Tensor, k: int):
+    """Steps 1-3 written with torch primitives only (no oracle routine):
+    torch.topk + softmax routing (distinct logits), a stable argsort of the
+    flattened expert ids for the expert-major order (ascending token inside
+    an expert, since a token's k experts are distinct), and the per-token
+    E4M3 codes by torch's float8 cast of x * fl32(448 / amax) clamped to 448."""
+    T, E = logits.shape
+    _, ids = torch.topk(logits.double(), k, dim=1, sorted=True)
+    sel = logits.double().gather(1, ids)
+    w = torch.softmax(sel, dim=1)
+    flat = ids.reshape(-1)
+    order = torch.sort(flat, stable=True).indices          # row r <- flat (t, j)
+    row_of = torch.empty_like(order)
+    row_of[order] = torch.arange(T * k)
+    counts = torch.bincount(flat, minlength=E)
+    x = x_bf16.float()
+    amax = x.abs().amax(dim=1)
+    nz = amax > 0
+    safe = torch.where(nz, amax, torch.ones_like(amax))
+    inv = torch.tensor(448.0, dtype=torch.float32) / safe
+    s = torch.where(nz, safe / torch.tensor(448.0, dtype=torch.float32), torch.ones_like(amax))
+    prod = (x * inv[:, None]).clamp(-448.0, 448.0)
+    codes = prod.to(torch.float8_e4m3fn).view(torch.uint8)
+    codes[~nz] = 0
+    return (ids.int().numpy(), w.float().numpy(), counts.int().numpy(),
+            row_of.reshape(T, k).int().numpy(), (order // k).int().numpy(), codes.numpy(),
+            s.numpy())
+
+
+def check_route_and_quantize(fn, x_bf16: torch.Tensor, logits: torch.Tensor, k: int):
+    """route_and_quantize (the reference the full-size GPU tests take their
+    bit-exact front end from) against the independent torch formulation and
+    against forward()'s own routing and expanded codes."""
+    bits = x_bf16.view(torch.int16).numpy().view(np.uint16)
+    lg = logits.numpy()
+    rt, tq, ts = fn(bits, lg, k)
+    ids, w, counts, row_of, tok_of_row, codes, s = _independent_front(x_bf16, logits, k)
+    np.testing.assert_array_equal(rt.ids, ids)
+    np.testing.assert_allclose(rt.weights, w, rtol=3e-7, atol=0)
+    np.testing.assert_array_equal(rt.counts, counts)
+    np.testing.assert_array_equal(rt.row_of, row_of)
+    np.testing.assert_array_equal(rt.token_of_row, tok_of_row)
+    np.testing.assert_array_equal(tq, codes)
+    np.testing.assert_array_equal(ts, s)
+    # the same rows forward() quantises and feeds to GEMM1 (W4A8 mode)
+    E, H = logits.shape[1], x_bf16.shape[1]
+    W = M.Weights(np.zeros((E, 256, H // 2), np.uint8), np.full((E, 256, H // 32), 127, np.uint8),
+                  np.zeros((E, H, 64), np.uint8), np.full((E, H, 4), 127, np.uint8))
+    fw = M.forward(bits, lg, W, k)
+    np.testing.assert_array_equal(tq[rt.token_of_row], fw.xq)
+    np.testing.assert_array_equal(ts[rt.token_of_row], fw.x_scale)
+    np.testing.assert_array_equal(rt.row_of, fw.routing.row_of)
+
+
+def _front_cases():
+    g = torch.Generator().manual_seed(23)
+    # the tiny workload shape: E=8, top-2, H=256, T=16
+    x1 = torch.randn(16, 256, generator=g).to(torch.bfloat16)
+    l1 = torch.randn(16, 8, generator=g)
+    # skewed routing (Zipf(1.2) bias over 64 experts, many empty), rows of
+    # widely different magnitude and an all-zero row
+    x2 = (torch.randn(40, 512, generator=g) *
+          torch.exp(torch.empty(40, 1).uniform_(-8, 8, generator=g))).to(torch.bfloat16)
+    x2[7] = 0
+    ranks = torch.randperm(64, generator=g).float() + 1
+    l2 = torch.randn(40, 64, generator=g) - 1.2 * torch.log(ranks)[None, :]
+    return [(x1, l1, 2), (x2, l2, 6)]
+
+
+@pytest.mark.parametrize("case", [0, 1])
+def test_route_and_quantize_matches_independent_front(case):
+    x, lg, k = _front_cases()[case]
+    check_route_and_quantize(M.route_and_quantize, x, lg, k)
