@@ -55,3 +55,39 @@ def test_touched_experts_scale_the_weight_bytes():
     cfg = MI.CONFIGS["dsv3"]
     one = bench.fused_roofline(cfg, 1, 8, 1e-3, PEAKS)["bytes"]
     assert one == pytest.approx(8 * 3 * I * H * (0.5 + 1 / 32) + H * 2 + E * 4 + H * 2)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_oracle_cost_parts_reproduce_forward(mode):
+    """The timed parts of the CPU baseline run the oracle's own steps: the
+    token-linear part and every expert's part together reproduce forward()'s
+    routing and y rows bit for bit, so timing them times the forward."""
+    import numpy as np
+    import torch
+
+    from oracle import moe as M
+    cfg = MI.custom_config(8, 2, 256, 128, mode=mode)
+    case = MI.make_case(cfg, 24, seed=5)
+    xb = case.x.view(torch.int16).numpy().view(np.uint16)
+    lg = case.logits.numpy()
+    W = M.Weights(case.w1.numpy(), case.w1_sf.numpy(), case.w2.numpy(), case.w2_sf.numpy(),
+                  mode=mode)
+    fw = M.forward(xb, lg, W, cfg.top_k, mode=mode)
+    rt, a1, xs, _ = bench.oracle_token_part(xb, lg, cfg.top_k, cfg.num_experts, mode)
+    np.testing.assert_array_equal(rt.row_of, fw.routing.row_of)
+    for e in range(cfg.num_experts):
+        r0, r1 = int(rt.offsets[e]), int(rt.offsets[e + 1])
+        if r1 == r0:
+            continue
+        y = bench.oracle_expert_part(W, e, a1[r0:r1], None if xs is None else xs[r0:r1], mode)
+        np.testing.assert_array_equal(y, fw.y[r0:r1])
+
+
+def test_cpu_baseline_extrapolates_from_timed_parts():
+    """t(T) = T * t_token + n_touched * t_expert, reported as extrapolated."""
+    cfg = MI.CONFIGS["tiny"]
+    case = MI.make_case(cfg, 16)
+    res = bench.cpu_baseline(cfg, 16, case.x, case.logits, n_tok=8, n_exp=2)
+    assert res["extrapolated"] and res["kind"] == "oracle"
+    assert res["value"] == pytest.approx(16 / res["t_forward_s"])
+    assert "extrapolated" in res["sample"]
