@@ -244,13 +244,17 @@ int32_t moe_selftest_timeout(void* workspace, int32_t timeout_us, void* stream);
  * which every GPU that loads this library holds until the process exits.
  * Shapes needing more (about (T/32)*E*4 + T*k*4.5 + E*20 bytes) are rejected
  * with MOE_ERR_WORKSPACE_TOO_SMALL and a message in moe_last_error().  The
- * first call on each device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  All
+ * first call in each CUDA context looks up the array's device address (with
+ * that context current) and caches it under the context's process-unique
+ * id; make that first call before any stream capture.  All
  * calls share the one array, which keeps the last call's contents (every
  * word a call reads is written earlier in the same call): calls that overlap
  * on the GPU -- on different streams or from different host threads -- race
  * on it and must be serialised.  Allocates nothing (no cudaMalloc/cudaFree).
- * num_tokens == 0 returns MOE_OK and launches nothing. */
+ * Runs on sm_103a devices only (MOE_ERR_UNSUPPORTED elsewhere, as
+ * moe_forward).  num_tokens == 0 returns MOE_OK, launches nothing and leaves
+ * every output untouched (the offsets of an empty batch are all zero; a
+ * caller that reads them must write those zeros itself). */
 int32_t moe_route_noalloc(const moe_shape* shape, const float* router_logits, int32_t* ids,
                           float* weights, int32_t* offsets, int32_t* row_of, void* stream);
 

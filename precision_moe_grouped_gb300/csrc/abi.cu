@@ -442,6 +442,13 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
 
 namespace moe {
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
+int32_t check_device(int* num_sms) {
+  DeviceInfo dev;
+  const int32_t rc = device_info(&dev);
+  if (rc == MOE_OK && num_sms) *num_sms = dev.num_sms;
+  return rc;
+}
 }  // namespace moe
 
 extern "C" {

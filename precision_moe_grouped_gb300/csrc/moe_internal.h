@@ -242,6 +242,10 @@ cudaError_t launch_prepare(const uint8_t* w, const uint8_t* sf, uint8_t* w_p, ui
                            int E, int M, int K, int swiglu_I, bool fp8, cudaStream_t s);
 // Sets the message moe_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
+// The current device's check every entry point that launches kernels makes:
+// MOE_OK on an sm_103a device (its SM count in *num_sms when not null), else
+// MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA with the message set.
+int32_t check_device(int* num_sms);
 
 cudaError_t launch_timeout_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 

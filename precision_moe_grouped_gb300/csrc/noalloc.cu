@@ -7,6 +7,7 @@
 // in one file-scope device array instead of a caller workspace.  The array
 // is part of the library image: every GPU that loads the library holds it
 // until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -20,7 +21,8 @@ namespace {
 
 __device__ __align__(256) uint8_t g_route_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+// Contexts whose scratch address is cached (further ones replace entries).
+constexpr int kMaxContexts = 64;
 
 // Records the message where moe_last_error() reads it and returns `code`.
 int32_t noalloc_fail(int32_t code, const char* fmt, ...) {
@@ -60,28 +62,78 @@ Carve carve(int64_t T, int64_t E, int64_t k) {
   return c;
 }
 
-// Device address of g_route_scratch on the current device, looked up once
-// per device with that device current.  In host code the symbol's name is
-// only a host-side handle, never a device pointer.
+// Driver entry points for the current context and its process-unique id,
+// looked up once through the runtime (the library links only cudart).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+// Process-unique id of the calling thread's current context (0 if none).
+int32_t current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  });
+  if (!get_current || !get_id)
+    return noalloc_fail(MOE_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId entry points unavailable");
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS)
+    return noalloc_fail(MOE_ERR_CUDA, "cuCtxGetCurrent failed");
+  *id = 0;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS)
+    return noalloc_fail(MOE_ERR_CUDA, "cuCtxGetId failed");
+  return MOE_OK;
+}
+
+// Device address of g_route_scratch in the calling thread's current CUDA
+// context, looked up once per context with that context current and cached
+// under the context's process-unique id (so a context made after a device
+// reset, or a second context on the same device, gets its own lookup).  In
+// host code the symbol's name is only a host-side handle, never a device
+// pointer.
 int32_t scratch_address(uint8_t** out) {
   static std::mutex mu;
-  static uint8_t* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess)
-    return noalloc_fail(MOE_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices)
-    return noalloc_fail(MOE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  struct Entry {
+    unsigned long long ctx_id;
+    uint8_t* addr;
+  };
+  static Entry cache[kMaxContexts] = {};
+  static int used = 0;
+  unsigned long long id = 0;
+  int32_t rc = current_context_id(&id);
+  if (rc != MOE_OK) return rc;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_route_scratch);
-    if (e != cudaSuccess || !p)
-      return noalloc_fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(g_route_scratch) failed: %s",
-                          cudaGetErrorString(e));
-    addr[dev] = static_cast<uint8_t*>(p);
+  if (id != 0)
+    for (int i = 0; i < used; ++i)
+      if (cache[i].ctx_id == id) {
+        *out = cache[i].addr;
+        return MOE_OK;
+      }
+  // first call in this context (the lookup also makes the device's primary
+  // context current if the thread has none yet)
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+  if (e != cudaSuccess || !p)
+    return noalloc_fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(g_route_scratch) failed: %s",
+                        cudaGetErrorString(e));
+  if (id == 0 && (rc = current_context_id(&id)) != MOE_OK) return rc;
+  if (id != 0) {
+    const int slot = used < kMaxContexts ? used++ : static_cast<int>(id % kMaxContexts);
+    cache[slot] = Entry{id, static_cast<uint8_t*>(p)};
   }
-  *out = addr[dev];
+  *out = static_cast<uint8_t*>(p);
   return MOE_OK;
 }
 
@@ -110,9 +162,11 @@ extern "C" int32_t moe_route_noalloc(const moe_shape* shape, const float* router
   for (const void* p : ptrs)
     if (reinterpret_cast<uintptr_t>(p) % 4 != 0)
       return noalloc_fail(MOE_ERR_MISALIGNED, "logits and outputs must be 4-byte aligned");
-  uint8_t* base = nullptr;
-  int32_t rc = scratch_address(&base);
+  // the same device check as moe_forward: sm_103a only, a clear error otherwise
+  int32_t rc = moe::check_device(nullptr);
   if (rc != MOE_OK) return rc;
+  uint8_t* base = nullptr;
+  if ((rc = scratch_address(&base)) != MOE_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* chunk = reinterpret_cast<int32_t*>(base + c.chunk_counts);
   // Every scratch word read below is written earlier in the same call (the

@@ -176,11 +176,15 @@ __device__ int2 plan_tiles(int e, int E, int c, int off, int bn, bool write,
 // consecutive rows of one expert; an expert with c rows gets ceil(c / tsz)
 // tiles of tsz = roundup16(ceil(c / ceil(c / bn))) rows, so its tiles are
 // balanced and every MMA-N is a multiple of 16.
-__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ chunk_counts,
+// chunk_counts and chunk_base may be the same buffer (the forward turns the
+// histogram into the bases in place): each element is read, by the thread
+// that owns it, before that thread overwrites it, so neither pointer is
+// declared __restrict__.
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* chunk_counts,
                                                     int num_chunks, int E, int bn,
                                                     int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets,
-                                                    int32_t* __restrict__ chunk_base,
+                                                    int32_t* chunk_base,
                                                     int4* __restrict__ tiles,
                                                     int32_t* __restrict__ num_tiles,
                                                     int2* __restrict__ tile_plan) {
