@@ -75,6 +75,11 @@ def mx_parity(case, variant=0, name="mx"):
     try:
         check_front_mx(run, fw.routing, *M.quantize_rows_mxfp8(
             np.asarray(case.x.float().cpu().numpy(), np.float32)))
+        # GEMM2's MXFP8 operand: the oracle's block quantiser applied to the
+        # GPU's own h gives the same codes and scale bytes bit for bit
+        hq_ref, hsf_ref = M.quantize_rows_mxfp8(run.h.astype(np.float32))
+        np.testing.assert_array_equal(run.hq, hq_ref)
+        np.testing.assert_array_equal(run.h_sf, hsf_ref)
         for label, got, ref in (("h", run.h, fw.h), ("y", run.y, fw.y),
                                 ("out", run.out_np(), fw.out)):
             ok, st = max_err_ok(got, ref)

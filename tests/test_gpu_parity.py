@@ -64,6 +64,12 @@ def full_parity(case, variant=0, name="case"):
         np.asarray(case.x.float().cpu().numpy(), np.float32))
     try:
         check_front(run, fw.routing, tq, ts)
+        # GEMM2's FP8 operand: the oracle's quantiser applied to the GPU's
+        # own h gives the same codes and scales bit for bit (h itself is a
+        # tolerance item, so the codes are compared against its quantisation)
+        hq_ref, hs_ref = M.quantize_rows_fp8(run.h.astype(np.float32))
+        np.testing.assert_array_equal(run.hq, hq_ref)
+        np.testing.assert_array_equal(run.h_scale, hs_ref)
         ok_h, st_h = max_err_ok(run.h, fw.h)
         ok_y, st_y = max_err_ok(run.y, fw.y)
         ok_o, st_o = max_err_ok(run.out_np(), fw.out)
