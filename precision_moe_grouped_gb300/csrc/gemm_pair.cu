@@ -255,20 +255,31 @@ __global__ void __launch_bounds__(PairCfg<BN, STAGES, NB>::kThreads, 1)
     if (s < STAGES) {
       uint32_t phase = 0;
       bool issued = false;
+      // fill f = s + j * STAGES: K stage ks of the pair's it-th item; the
+      // counters advance without divisions and the item's tile entry and
+      // first weight box are re-read only when the item changes
       int ks = s % KS, item = cid + (s / KS) * ncl;
+      int cur_item = -1;
+      int4 td = make_int4(0, 0, 0, 0);
+      int64_t blk0 = 0;
+      int halfn = 16, xm = 0;
       const uint32_t bar = full0 + static_cast<uint32_t>(8 * s);
       while (item < num_items) {
-        const int4 td = checked_tile(tiles, item / MTP, BN, status, lim);
-        const int mt = 2 * (item % MTP) + static_cast<int>(rank);
-        const int64_t blk = (static_cast<int64_t>(td.x) * MT + mt) * KS + ks;
+        if (item != cur_item) {
+          cur_item = item;
+          td = checked_tile(tiles, item / MTP, BN, status, lim);
+          const int mt = 2 * (item % MTP) + static_cast<int>(rank);
+          blk0 = (static_cast<int64_t>(td.x) * MT + mt) * KS;
+          halfn = ((td.z + 31) & ~31) >> 1;   // N / 2, a multiple of 16
+          xm = (halfn >> 4) - 1;               // box of exactly N / 2 rows
+        }
+        const int64_t blk = blk0 + ks;
         if (!mbar_wait(empty + s, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag)) break;
         if (role == 0) {
           if (rank == 0) mbar_arrive_expect_tx(full + s, 2u * a_tx_bytes);
           tma_load_2d_pair(smem + C::kOffA + s * C::kABytes, &tmap_w, 0,
                            static_cast<int32_t>(blk * kTileM), bar);
         } else if (role == 1) {
-          const int halfn = ((td.z + 31) & ~31) >> 1;   // N / 2, a multiple of 16
-          const int xm = (halfn >> 4) - 1;               // box of exactly N / 2 rows
           const uint32_t bx = static_cast<uint32_t>(kPairBoxRowsAt(xm)) * 128u;
           if (rank == 0) mbar_arrive_expect_tx(full + s, 2u * bx);
           tma_load_2d_pair(smem + C::kOffB + s * C::kBBytes, &tmap_xh.m[xm], ks * kTileK,
@@ -300,47 +311,44 @@ __global__ void __launch_bounds__(PairCfg<BN, STAGES, NB>::kThreads, 1)
       const uint64_t adesc0 = smem_desc(smem_u32(smem + C::kOffA), 0, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
       const uint64_t sdesc0 = smem_desc(smem_u32(smem + C::kOffSF), 0, 128, 0);
-      int stage = 0, ks = 0, it = 0;
-      uint32_t phase = 0, d_tmem = 0, id0 = 0;
-      bool new_item = true;
-      int acc = 0;
-      while (cid + it * ncl < num_items) {
-        if (new_item) {
-          const int4 td = checked_tile(tiles, (cid + it * ncl) / MTP, BN, status, lim);
-          const uint32_t nmma = static_cast<uint32_t>((td.z + 31) & ~31);
-          id0 = idesc_mx_pair(5, 0, nmma);   // A = E2M1 weights, B = E4M3 tokens
-          acc = it % NB;
-          // both epilogues released this buffer (cluster-scope arrivals)
-          if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
-                              status, kDevTimeout, abort_flag))
-            break;
-          asm volatile("fence.acq_rel.cluster;" ::: "memory");
-          tc_fence_after();
-          d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-        }
-        if (!mbar_wait_warp(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag))
+      // Items in order, an item's K stages in order; the inner loop carries
+      // only the stage and phase counters (as the one-CTA kernel's single
+      // issuer).
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int item = cid, it = 0; ok && item < num_items; item += ncl, ++it) {
+        const int4 td = checked_tile(tiles, item / MTP, BN, status, lim);
+        const uint32_t nmma = static_cast<uint32_t>((td.z + 31) & ~31);
+        const uint32_t id0 = idesc_mx_pair(5, 0, nmma);   // A = E2M1 weights, B = E4M3 tokens
+        const int acc = it % NB;
+        // both epilogues released this buffer (cluster-scope arrivals)
+        if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
+                            status, kDevTimeout, abort_flag))
           break;
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
         tc_fence_after();
-        const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
-        tc2_cp_32x128b_x4_warp(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
-        const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
-        const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+        for (int ks = 0; ks < KS; ++ks) {
+          if (!mbar_wait_warp(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
+          tc2_cp_32x128b_x4_warp(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
+          const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
 #pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)
-          tc2_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
-                          tmem + C::kColSFB, (!new_item || kk > 0) ? 1u : 0u);
-        tc2_commit_both_warp(empty + stage);   // both CTAs' slot s is free again
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+          for (uint32_t kk = 0; kk < 4; ++kk)
+            tc2_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
+                            tmem + C::kColSFB, (ks > 0 || kk > 0) ? 1u : 0u);
+          tc2_commit_both_warp(empty + stage);   // both CTAs' slot is free again
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        new_item = false;
-        if (++ks == KS) {
-          ks = 0;
-          ++it;
-          new_item = true;
-          tc2_commit_both_warp(tfull + acc);   // both halves of the accumulator are final
-        }
+        if (ok) tc2_commit_both_warp(tfull + acc);   // both halves of the accumulator are final
       }
       // No MMA or TMEM copy may still be running when TMEM is freed.
       tc2_commit_local_warp(drain);
