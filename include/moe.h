@@ -86,9 +86,11 @@ typedef struct {
 
 /* Kernels one forward launches, in stream order: route, scan, rank,
  * quant_scatter, gemm1, hquant, gemm2, combine (moe_stage_name() names them).
- * For num_tokens <= MOE_SMALL_BATCH_TOKENS the expansion (scan, rank,
- * quant_scatter) runs as one kernel, timed as stage "scan"; the "rank" and
- * "quant_scatter" stages are then empty and the forward launches 6 kernels.
+ * The scatter kernel ranks the expanded rows itself, so the "rank" stage is
+ * empty and a large batch launches 7 kernels.  For num_tokens <=
+ * MOE_SMALL_BATCH_TOKENS the expansion (scan, rank, quant_scatter) runs as
+ * one kernel, timed as stage "scan"; the "quant_scatter" stage is then empty
+ * too and the forward launches 6 kernels.
  * For num_tokens <= MOE_TINY_BATCH_TOKENS in the W4A8 mode routing and
  * expansion run as one kernel, timed as stage "route" (5 kernels).  The
  * W4A16 mode has no hquant kernel (its stage is empty).

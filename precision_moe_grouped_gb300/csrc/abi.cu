@@ -377,6 +377,8 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   auto mark = [&]() -> cudaError_t {
     return ev ? cudaEventRecord(ev[stage++], st) : cudaSuccess;
   };
+  const int grid1 = gemm_grid(dev.num_sms, T, k, E, 2 * I / moe::kTileM);
+  const int grid2 = gemm_grid(dev.num_sms, T, k, E, H / moe::kTileM);
   // the first kernel clears the status word; tiny batches (W4A8) route,
   // expand and quantise in one kernel, small batches expand in one kernel
   const moe::QuantOut qx{xq, x_scale, mx, x_sf, sfb1, w4a16};
@@ -405,17 +407,17 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
     MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts), offsets,
                               chunk, tiles, num_tiles, tile_plan, st));
     MOE_CUDA(mark());
-    MOE_CUDA(moe::launch_rank(ids, chunk, T, E, k, row_of, token_slot, st));
-    MOE_CUDA(mark());
-    MOE_CUDA(moe::launch_quant_scatter(x, row_of, ids, offsets, tile_plan, T, k, H, qx, st));
+    MOE_CUDA(mark());   // the scatter kernel ranks the rows itself (no rank kernel)
+    MOE_CUDA(moe::launch_quant_scatter(x, chunk, ids, offsets, tile_plan, T, E, k, H, row_of,
+                                       token_slot, qx, st));
     MOE_CUDA(mark());
   }
   // W4A8: the per-row token scale is applied in the epilogues; MXFP8: the
   // block scales ride with the operands into the MMA
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
-                   mx ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx,
-                   gemm_grid(dev.num_sms, T, k, E, 2 * I / moe::kTileM),
-                   prefetch, mx, sfb1, static_cast<const uint8_t*>(w1), pair ? tm_xp : nullptr};
+                   mx ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, grid1,
+                   prefetch, mx, sfb1, static_cast<const uint8_t*>(w1), pair ? tm_xp : nullptr,
+                   L.max_tiles};
   MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(true, g1, st) : moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
   if (w4a16) {
@@ -427,9 +429,9 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
     MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
   MOE_CUDA(mark());
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
-                   mx ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx,
-                   gemm_grid(dev.num_sms, T, k, E, H / moe::kTileM),
-                   prefetch, mx, sfb2, static_cast<const uint8_t*>(w2), pair ? tm_hp : nullptr};
+                   mx ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, grid2,
+                   prefetch, mx, sfb2, static_cast<const uint8_t*>(w2), pair ? tm_hp : nullptr,
+                   L.max_tiles};
   MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(false, g2, st)
                  : moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());

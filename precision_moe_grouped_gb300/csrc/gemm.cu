@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
                         int m_per_expert, int K, int out_ld, int32_t* __restrict__ status,
                         uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages,
                         const uint8_t* __restrict__ sfb_tiled,
-                        const uint8_t* __restrict__ w_base) {
+                        const uint8_t* __restrict__ w_base, int max_tiles) {
   using C = GemmCfg<BN, STAGES, NI, NB, MX8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -182,25 +182,50 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
   tc_fence_after();
   // Everything above overlaps the previous kernel's tail; the tile list and
   // the activations are that kernel's (or an earlier one's) output.
-  griddep_wait();
-  griddep_launch_dependents();
+  // GEMM2's weight and scale copies need only the tile list, which the
+  // expansion kernel wrote before GEMM1 started its work; this grid starts
+  // after GEMM1 has passed that point (each kernel signals its dependents
+  // only after its own wait).  So the weight and scale lanes of the
+  // producer warps issue their stage's first fill, reading the list through
+  // L2, before the producer warps wait for the h quantisation with the rest
+  // of the CTA: the ring fills while the previous kernels finish.
+  constexpr int LPS = C::kLanesPerStage;
+  const bool preissue = !SWIGLU && !kChecks && LPS == 3;
+  const bool early = preissue && warp < C::kProdWarps;
+  if (!early) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   const WorkLimits lim = work_limits(status);
+  // (producer warps of GEMM2 read the list before their wait: through L2)
+  auto tile_at = [&](int i, bool before_wait) -> int4 {
+    return before_wait ? __ldcg(tiles + i) : checked_tile(tiles, i, BN, status, lim);
+  };
+  // The CTA's first tile entry is read together with the tile count (both
+  // come from the expansion kernel, and the entry lies inside the list's
+  // allocation), so the first copies wait for one round trip, not two.
+  const int first_tile = static_cast<int>(blockIdx.x) / MT;
+  const int4 first_td = kChecks || first_tile >= max_tiles ? make_int4(0, 0, 0, 0)
+                        : early                            ? __ldcg(tiles + first_tile)
+                                                           : tiles[first_tile];
   // < 2^31: tiles <= R/16 + E + 1
-  const int num_items = checked_num_tiles(num_tiles_p, status, lim) * MT;
+  const int num_items =
+      (early ? __ldcg(num_tiles_p) : checked_num_tiles(num_tiles_p, status, lim)) * MT;
 
-  if (warp < C::kProdWarps) {
-    // ------------------------------------------------------------ producer
-    // Stage s belongs to producer warp s % kProdWarps; its LPS = 3 lanes
-    // (from lane LPS * (s / kProdWarps)) copy the weight box, the activation
-    // box and the scale block (with LPS = 2 the activation lane also copies
-    // the scale block).  Each lane arrives on the stage's full barrier with
-    // its own byte count, for this CTA's fills f = s, s + STAGES, ... (fill
-    // f = K stage f % KS of the CTA's (f / KS)-th item).  Spreading the
-    // copies over threads and warps keeps their issue off any single
-    // thread's critical path.
-    constexpr int LPS = C::kLanesPerStage;
-    const int s = warp + C::kProdWarps * (lane / LPS), role = lane % LPS;
-    if (s < STAGES) {
+  // ------------------------------------------------------------ producer
+  // Stage s belongs to producer warp s % kProdWarps; its LPS = 3 lanes (from
+  // lane LPS * (s / kProdWarps)) copy the weight box, the activation box and
+  // the scale block (with LPS = 2 the activation lane also copies the scale
+  // block).  Each lane arrives on the stage's full barrier with its own byte
+  // count, for this CTA's fills f = s, s + STAGES, ... (fill f = K stage
+  // f % KS of the CTA's (f / KS)-th item).  Spreading the copies over
+  // threads and warps keeps their issue off any single thread's critical
+  // path.
+  // first_only: issue the stage's first fill only (before the wait) and
+  // return whether it did; skip_first: that fill was issued already.
+  auto produce = [&](const int s, const int role, const bool first_only,
+                     const bool skip_first) -> bool {
+    {
       uint32_t phase = 0;
       bool issued = false;
       // fill f = s + j * STAGES: K stage ks of the CTA's it-th item (KS >= STAGES
@@ -214,14 +239,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
       while (item < num_items) {
         if (item != cur_item) {
           cur_item = item;
-          td = checked_tile(tiles, item / MT, BN, status, lim);
+          td = !kChecks && item / MT == first_tile ? first_td : tile_at(item / MT, first_only);
           // prepared weights: one contiguous 128 x 128 box per (expert,
           // M-tile, K stage); box row = ((e * MT + mt) * KS + ks) * 128
           blk0 = (static_cast<int64_t>(td.x) * MT + item % MT) * KS;
         }
         const int64_t blk = blk0 + ks;
-        if (!mbar_wait(empty + s, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag)) break;
-        if (role == 0) {
+        const bool skip = skip_first && !issued;
+        if (!skip && !mbar_wait(empty + s, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag))
+          break;
+        if (skip) {
+          // issued before the wait
+        } else if (role == 0) {
           mbar_arrive_expect_tx(full + s, a_tx_bytes);
           tma_load_2d(smem + C::kOffA + s * C::kABytes, &tmap_w, 0,
                       static_cast<int32_t>(blk * kTileM), full + s);
@@ -248,6 +277,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
           tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0, static_cast<int32_t>(blk),
                       full + s);
         }
+        if (first_only) return true;
         issued = true;
         phase ^= 1u;
         ks += STAGES;
@@ -256,6 +286,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
           item += gridDim.x;
         }
       }
+      if (first_only) return false;
       // Every issued copy must land before the CTA may exit: wait for this
       // stage's last fill (ignores the abort flag, still bounded).
       if (issued) {
@@ -263,6 +294,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
         mbar_wait(full + s, phase ^ 1u, timeout_ns, status, kDevTimeout, &none);
       }
     }
+    return false;
+  };
+
+  if (warp < C::kProdWarps) {
+    const int s = warp + C::kProdWarps * (lane / LPS), role = lane % LPS;
+    bool pre = false;
+    if (early) {
+      if (s < STAGES && role != 1) pre = produce(s, role, true, false);
+      __syncwarp();
+      griddep_wait();
+      griddep_launch_dependents();
+    }
+    if (s < STAGES) produce(s, role, false, pre);
   } else if (warp < C::kIssuer0 + NI) {
     // ------------------------------------------------------------ MMA issuers
     // Each tcgen05 instruction occupies its issuing warp (measured ~310
@@ -457,7 +501,8 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
   return launch_pdl(kern, dim3(a.num_sms), dim3(C::kThreads), C::kSmemBytes, s, *a.tmap_w, xm,
                     *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
                     static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status,
-                    a.timeout_ns, a.a_tx_bytes, a.prefetch_stages, a.sfb_tiled, a.w_base);
+                    a.timeout_ns, a.a_tx_bytes, a.prefetch_stages, a.sfb_tiled, a.w_base,
+                    a.max_tiles);
 }
 
 }  // namespace

@@ -177,6 +177,7 @@ struct GemmArgs {
   const uint8_t* sfb_tiled;    // MXFP8: activation scales in the per-tile layout
   const uint8_t* w_base;       // prepared weight boxes (for the optional L2 prefetcher)
   const CUtensorMap* tmap_x_pair;  // kNumXMaps maps, box heights kPairBoxRowsAt (or null)
+  int32_t max_tiles;           // entries the tile list's allocation holds
 };
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
@@ -208,9 +209,13 @@ cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int 
                         int32_t* num_tiles, int2* tile_plan, cudaStream_t s);
 cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,
                         int32_t* row_of, int32_t* token_slot, cudaStream_t s);
-cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, const int32_t* ids,
-                                 const int32_t* offsets, const int2* tile_plan, int T, int k,
-                                 int H, const QuantOut& q, cudaStream_t s);
+// One CTA per token: the rows of its slots (from the per-chunk bases the
+// scan leaves in chunk_base) into row_of / token_slot, and the token's
+// quantised activations into them.
+cudaError_t launch_quant_scatter(const void* x, const int32_t* chunk_base, const int32_t* ids,
+                                 const int32_t* offsets, const int2* tile_plan, int T, int E,
+                                 int k, int H, int32_t* row_of, int32_t* token_slot,
+                                 const QuantOut& q, cudaStream_t s);
 cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_scale,
                           cudaStream_t s);
 // MXFP8 quantisation of h: codes, row-major scale bytes [R, I/32] and the

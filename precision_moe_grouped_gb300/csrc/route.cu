@@ -13,9 +13,10 @@
 //
 // Kernel chain: route (one warp per token; per-chunk expert histogram) ->
 // scan (one CTA: counts, offsets, per-chunk bases, GEMM tile list) ->
-// rank (one warp per chunk: stable expert-major row of every (token, slot))
-// -> quant_scatter (one CTA per token: FP8 codes written to each of the
-// token's k expanded rows).  Nothing returns to the host.
+// quant_scatter (one CTA per token: the stable expert-major rows of its k
+// slots, and its FP8 codes written to each of them).  Nothing returns to
+// the host.  rank (one warp per chunk: the rows of every (token, slot)) is
+// the routing-only front end's last kernel (moe_route_noalloc).
 #include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -31,12 +32,72 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- routing
-// One warp per token (32 warps = one chunk per CTA).  Lane l holds logits of
-// experts l, l+32, ... (NV per lane).  k rounds of a warp argmax pick the
-// experts in descending logit order, equal logits resolved toward the lower
-// expert index.  Weights are the softmax over the k selected logits
-// (renormalised top-k softmax).  A NaN logit is read as -inf, so every round
-// finds an expert index below E whatever the input holds.
+// Order-preserving map of a float (not NaN) to an unsigned key: a < b as
+// floats exactly when key(a) < key(b) as integers; key(-inf) = 0x007FFFFF.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_order_key(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Routing of one token by one warp.  Lane l holds the logits of experts l,
+// l + 32, ... (NV per lane).  k rounds of a warp argmax pick the experts in
+// descending logit order, equal logits resolved toward the lower expert
+// index: each round every lane offers its largest remaining logit (its
+// lowest expert index among equal ones), one warp max-reduction over the
+// order-preserving keys finds the round's logit and one min-reduction the
+// lowest expert index offering it.  The weights are the softmax over the k
+// selected logits (renormalised top-k softmax).  A NaN logit is read as
+// -inf, so every round finds an expert index below E whatever the row holds.
+// Lane j < k returns the j-th expert in *id and its weight in *w.
+template <int NV>
+__device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k,
+                                                 int lane, int* id, float* w) {
+  float v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? row[e] : -FLT_MAX;
+    if (v[i] != v[i]) v[i] = -INFINITY;   // NaN ranks with -inf: k experts are always found
+  }
+  uint32_t taken = 0;
+  float my_v = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float best = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
+        best = v[i];
+        bi = e;
+      }
+    }
+    // a lane with nothing left to offer takes no part (key 0 is below -inf)
+    const uint32_t key = bi != INT_MAX ? order_key(best) : 0u;
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const uint32_t win = __reduce_min_sync(
+        0xffffffffu, key == kmax ? static_cast<uint32_t>(bi) : 0xFFFFFFFFu);
+    if (static_cast<int>(win & 31u) == lane) taken |= 1u << (win >> 5);
+    if (lane == j) {
+      my_v = from_order_key(kmax);
+      my_id = static_cast<int>(win);
+    }
+  }
+  const float lmax = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - lmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  *id = my_id;
+  *w = ex / sum;
+}
+
+// One warp per token (32 warps = one chunk per CTA): route_token_warp, then
+// the chunk's per-expert histogram.
 template <int NV>
 __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T,
                                                     int E, int k, int32_t* __restrict__ ids,
@@ -61,51 +122,12 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   for (int tt = warp; tt < kRouteChunk; tt += nwarps) {
     const int t = t0 + tt;
     if (t >= T) break;
-    const float* row = logits + static_cast<size_t>(t) * E;
-    float v[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < E ? row[e] : -FLT_MAX;
-      if (v[i] != v[i]) v[i] = -INFINITY;   // NaN ranks with -inf: k experts are always found
-    }
-    uint32_t taken = 0;
-    float my_v = 0.f;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      float best = -INFINITY;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
-          best = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ob > best || (ob == best && oi < bi)) {
-          best = ob;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        my_v = best;
-        my_id = bi;
-      }
-    }
-    const float lmax = __shfl_sync(0xffffffffu, my_v, 0);
-    float ex = lane < k ? expf(my_v - lmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    int my_id;
+    float my_w;
+    route_token_warp<NV>(logits + static_cast<size_t>(t) * E, E, k, lane, &my_id, &my_w);
     if (lane < k) {
       ids[static_cast<size_t>(t) * k + lane] = my_id;
-      wts[static_cast<size_t>(t) * k + lane] = ex / sum;
+      wts[static_cast<size_t>(t) * k + lane] = my_w;
       atomicAdd(&hist[my_id], 1);
     }
   }
@@ -114,58 +136,73 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     chunk_counts[static_cast<size_t>(blockIdx.x) * E + i] = hist[i];
 }
 
-// Exclusive scan of one int per thread over a block of up to 1024 threads.
-__device__ int block_exclusive_scan(int v, int* total) {
-  __shared__ int warp_sums[32];
+// Exclusive scan of a pair of non-negative ints per thread over a block of up
+// to 1024 threads, as one 64-bit scan of (b << 32) | a: each half's sum
+// stays below 2^31, so no carry crosses between them.  Returns the
+// exclusive prefixes (a, b); *total gets the block's sums.
+__device__ int2 block_exclusive_scan2(int a, int b, int2* total) {
+  __shared__ unsigned long long warp_sums[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  const unsigned long long v =
+      (static_cast<unsigned long long>(static_cast<uint32_t>(b)) << 32) | static_cast<uint32_t>(a);
+  unsigned long long x = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, off);
     if (lane >= off) x += y;
   }
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
     const int nw = (blockDim.x + 31) >> 5;
-    int s = lane < nw ? warp_sums[lane] : 0;
+    unsigned long long sw = lane < nw ? warp_sums[lane] : 0ull;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, off);
-      if (lane >= off) s += y;
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, sw, off);
+      if (lane >= off) sw += y;
     }
-    warp_sums[lane] = s;  // inclusive prefix of warp totals
+    warp_sums[lane] = sw;  // inclusive prefix of warp totals
   }
   __syncthreads();
-  const int base = warp > 0 ? warp_sums[warp - 1] : 0;
-  *total = warp_sums[((blockDim.x + 31) >> 5) - 1];
+  const unsigned long long base = warp > 0 ? warp_sums[warp - 1] : 0ull;
+  const unsigned long long tot = warp_sums[((blockDim.x + 31) >> 5) - 1];
   __syncthreads();
-  return base + x - v;
+  const unsigned long long ex = base + x - v;
+  *total = make_int2(static_cast<int>(tot & 0xFFFFFFFFull), static_cast<int>(tot >> 32));
+  return make_int2(static_cast<int>(ex & 0xFFFFFFFFull), static_cast<int>(ex >> 32));
 }
 
-// Tile plan of one expert (thread e of a block with blockDim >= E; every
-// thread of the block must call it): a tile is a run of at most `bn`
-// consecutive rows of one expert, as many and as large as expert_tile_plan
-// gives for its c rows; the block's scan places the experts' tiles in expert
-// order.  Returns (first tile, tsz); with `write` the block also stores the
-// tile list, the tile count and (if tile_plan is not null) the per-expert
-// plan.
-__device__ int2 plan_tiles(int e, int E, int c, int off, int bn, bool write,
-                           int4* __restrict__ tiles, int32_t* __restrict__ num_tiles,
-                           int2* __restrict__ tile_plan) {
+// Row offsets and tile plan of the experts (thread e of a block with
+// blockDim >= E; every thread of the block must call it; c = expert e's
+// rows, 0 for e >= E).  A tile is a run of at most `bn` consecutive rows of
+// one expert, as many and as large as expert_tile_plan gives for its c
+// rows; one block scan of (rows, tiles) places the experts' rows and tiles
+// in expert order.  With `write` the block also stores the tile list, the
+// tile count and (if tile_plan is not null) the per-expert plan.
+struct ExpertPlan {
+  int off;          // expert e's first expanded row
+  int total_rows;   // rows of all experts
+  int toff;         // expert e's first tile
+  int tsz;          // rows per tile
+  int nt;           // tiles of expert e
+};
+
+__device__ ExpertPlan plan_experts(int e, int E, int c, int bn, bool write,
+                                   int4* __restrict__ tiles, int32_t* __restrict__ num_tiles,
+                                   int2* __restrict__ tile_plan) {
   const int2 plan = expert_tile_plan(e < E ? c : 0, bn);
   const int nt = plan.x, tsz = plan.y;
-  int total_tiles;
-  const int toff = block_exclusive_scan(nt, &total_tiles);
+  int2 tot;
+  const int2 ex = block_exclusive_scan2(e < E ? c : 0, nt, &tot);
   if (write) {
     for (int i = 0; i < nt; ++i) {
       const int r0 = i * tsz;
-      tiles[toff + i] = make_int4(e, off + r0, min(tsz, c - r0), 0);
+      tiles[ex.y + i] = make_int4(e, ex.x + r0, min(tsz, c - r0), 0);
     }
-    if (tile_plan && e < E) tile_plan[e] = make_int2(toff, tsz);
-    if (threadIdx.x == 0) *num_tiles = total_tiles;
+    if (tile_plan && e < E) tile_plan[e] = make_int2(ex.y, tsz);
+    if (threadIdx.x == 0) *num_tiles = tot.y;
   }
-  return make_int2(toff, tsz);
+  return ExpertPlan{ex.x, tot.x, ex.y, tsz, nt};
 }
 
 // One CTA of P groups of Ep = roundup32(E) threads (P = blockDim / Ep >= 1):
@@ -208,16 +245,18 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* chunk_counts,
       if (h < g) gstart += v;
       total += v;
     }
-  // expert offsets: the first group's threads are the experts in order
-  int total_rows;
-  const int off = block_exclusive_scan(g == 0 && e < E ? total : 0, &total_rows);
+  // expert offsets and the tile plan: the first group's threads are the
+  // experts in order (the other groups plan nothing: "expert" E, 0 rows)
+  const ExpertPlan pl = plan_experts(g == 0 ? e : E, E, g == 0 && e < E ? total : 0, bn, true,
+                                     tiles, num_tiles, tile_plan);
+  const int off = pl.off;
   if (g == 0) eoffs[e] = off;
   __syncthreads();
   if (g == 0 && e < E) {
     counts[e] = total;
     offsets[e] = off;
   }
-  if (threadIdx.x == 0) offsets[E] = total_rows;
+  if (threadIdx.x == 0) offsets[E] = pl.total_rows;
   if (active) {
     int run = eoffs[e] + gstart;
 #pragma unroll 4
@@ -228,9 +267,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* chunk_counts,
       run += cc;
     }
   }
-  // tile plan from the first group (others plan nothing: "expert" E, 0 rows)
-  plan_tiles(g == 0 ? e : E, E, g == 0 && e < E ? total : 0, g == 0 ? off : 0, bn, true, tiles,
-             num_tiles, tile_plan);
 }
 
 // One warp per chunk of kRouteChunk tokens: the warp stages the chunk's
@@ -272,14 +308,36 @@ __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ i
 // the codes to the k expanded rows rows[0..k): amax -> s = amax/448, inv =
 // 448/amax (IEEE divisions) -> E4M3 codes of x*inv (round to nearest even,
 // satfinite); an all-zero row gets s = 1 and zero codes.  `warp_max` holds
-// one float per warp of the block.
+// one float per warp of the block.  A thread keeps its first KEEP 16-element
+// vectors in registers between the amax pass and the conversion (the row is
+// read once when H <= 16 * KEEP * blockDim).
+
+__device__ __forceinline__ uint4 fp8_codes16(const uint4 (&q)[2], float inv) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f0 = __bfloat1622float2(b[2 * j]);
+    const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv)), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)), __NV_SATFINITE, __NV_E4M3);
+    w[j] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int KEEP>
 __device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
                                const int32_t* rows, float* warp_max, uint8_t* __restrict__ xq,
                                float* __restrict__ x_scale) {
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
   const int nvec = H / 16;  // 16 elements (two 16-byte loads) per thread step
+  uint4 keep[KEEP][2];
   float amax = 0.f;
-  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+  int it = 0;
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x, ++it) {
     uint4 q[2] = {__ldg(xr + 2 * i), __ldg(xr + 2 * i + 1)};
     const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
 #pragma unroll
@@ -287,6 +345,12 @@ __device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k
       const float2 f = __bfloat1622float2(b[j]);
       amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
     }
+#pragma unroll
+    for (int c = 0; c < KEEP; ++c)
+      if (c == it) {
+        keep[c][0] = q[0];
+        keep[c][1] = q[1];
+      }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -297,23 +361,23 @@ __device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k
   const bool nz = amax > 0.f;
   const float s = nz ? amax / 448.0f : 1.0f;
   const float inv = nz ? 448.0f / amax : 0.0f;
-  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+  it = 0;
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x, ++it) {
     uint4 out = make_uint4(0, 0, 0, 0);
     if (nz) {
-      uint4 q[2] = {__ldg(xr + 2 * i), __ldg(xr + 2 * i + 1)};
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
-      uint32_t w[4];
+      uint4 q[2];
+      if (it < KEEP) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f0 = __bfloat1622float2(b[2 * j]);
-        const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
-        const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv)), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)), __NV_SATFINITE, __NV_E4M3);
-        w[j] = (lo & 0xFFFFu) | (hi << 16);
+        for (int c = 0; c < KEEP; ++c)
+          if (c == it) {
+            q[0] = keep[c][0];
+            q[1] = keep[c][1];
+          }
+      } else {
+        q[0] = __ldg(xr + 2 * i);
+        q[1] = __ldg(xr + 2 * i + 1);
       }
-      out = make_uint4(w[0], w[1], w[2], w[3]);
+      out = fp8_codes16(q, inv);
     }
     for (int j = 0; j < k; ++j)
       reinterpret_cast<uint4*>(xq + static_cast<size_t>(rows[j]) * H)[i] = out;
@@ -365,28 +429,49 @@ __device__ void copy_token(const __nv_bfloat16* __restrict__ x, int t, int k, in
   }
 }
 
-// One CTA per token: FP8 quantisation of the token into its k rows
-// (MX: MXFP8; COPY: the bf16 copy of the W4A16 mode).
+// One CTA per token t: the rows of its k slots, then the FP8 quantisation
+// of the token into them (MX: MXFP8; COPY: the bf16 copy of the W4A16
+// mode).  Slot j's row is the chunk's base row for its expert e (from the
+// scan) plus the number of the chunk's earlier tokens routed to e -- the
+// stable, ascending-token order inside each expert (a token's k experts are
+// distinct).  The CTA writes row_of and token_slot for its slots.
 template <bool MX, bool COPY = false>
-__global__ void __launch_bounds__(128) quant_scatter_kernel(
-    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of,
+__global__ void __launch_bounds__(256) quant_scatter_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ chunk_base,
     const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets,
-    const int2* __restrict__ tile_plan, int k, int H, uint8_t* __restrict__ xq,
-    float* __restrict__ x_scale, uint8_t* __restrict__ x_sf, uint8_t* __restrict__ sfb) {
+    const int2* __restrict__ tile_plan, int E, int k, int H, int32_t* __restrict__ row_of,
+    int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq, float* __restrict__ x_scale,
+    uint8_t* __restrict__ x_sf, uint8_t* __restrict__ sfb) {
   __shared__ int32_t rows[32];
+  __shared__ int32_t my_e[32];
+  __shared__ int32_t before[32];
   __shared__ int64_t sfb_base[32];
   __shared__ float warp_max[32];
   griddep_wait();
   griddep_launch_dependents();
   const int t = blockIdx.x;
+  const int chunk = t / kRouteChunk, t0 = chunk * kRouteChunk;
   if (static_cast<int>(threadIdx.x) < k) {
-    const size_t ts = static_cast<size_t>(t) * k + threadIdx.x;
-    const int r = row_of[ts];
-    rows[threadIdx.x] = r;
-    if (MX) {
-      const int e = ids[ts];
-      sfb_base[threadIdx.x] = sfb_row_base(r, offsets[e], tile_plan[e], H / kTileK);
-    }
+    my_e[threadIdx.x] = ids[static_cast<size_t>(t) * k + threadIdx.x];
+    before[threadIdx.x] = 0;
+  }
+  __syncthreads();
+  // the chunk's earlier (token, slot) entries routed to each of t's experts
+  for (int i = threadIdx.x; i < (t - t0) * k; i += blockDim.x) {
+    const int ei = ids[static_cast<size_t>(t0) * k + i];
+    for (int j = 0; j < k; ++j)
+      if (my_e[j] == ei) atomicAdd(&before[j], 1);
+  }
+  __syncthreads();
+  if (static_cast<int>(threadIdx.x) < k) {
+    const int j = threadIdx.x;
+    const size_t ts = static_cast<size_t>(t) * k + j;
+    const int e = my_e[j];
+    const int r = chunk_base[static_cast<size_t>(chunk) * E + e] + before[j];
+    rows[j] = r;
+    row_of[ts] = r;
+    token_slot[r] = static_cast<int32_t>(ts);
+    if (MX) sfb_base[j] = sfb_row_base(r, offsets[e], tile_plan[e], H / kTileK);
   }
   __syncthreads();
   if (COPY)
@@ -394,7 +479,7 @@ __global__ void __launch_bounds__(128) quant_scatter_kernel(
   else if (MX)
     quantize_token_mx(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
   else
-    quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
+    quantize_token<2>(x, t, k, H, rows, warp_max, xq, x_scale);   // 256 threads
 }
 
 // Small batches (T <= kSmallT): one kernel replaces scan + rank +
@@ -438,11 +523,13 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
         if (my_e[j] == ei) atomicAdd(&my_rank[j], 1);
   }
   __syncthreads();
-  int total_rows;
   const int c = e < E ? cnt[e] : 0;
-  const int off = block_exclusive_scan(c, &total_rows);
-  __syncthreads();
+  // every CTA plans the rows and tiles (its rows' positions); CTA 0 writes
+  // the tile list
+  const ExpertPlan pl = plan_experts(e, E, c, bn, t == 0, tiles, num_tiles, tile_plan);
+  const int off = pl.off, total_rows = pl.total_rows;
   if (e < E) cnt[e] = off;     // cnt now holds the offsets
+  if (MX && e < E) plan[e] = make_int2(pl.toff, pl.tsz);
   __syncthreads();
   if (e < k) {
     const size_t ts = static_cast<size_t>(t) * k + e;
@@ -458,9 +545,6 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
     }
     if (e == 0) offsets_out[E] = total_rows;
   }
-  // every CTA plans the tiles (its rows' tile positions); CTA 0 writes them
-  const int2 pl = plan_tiles(e, E, c, off, bn, t == 0, tiles, num_tiles, tile_plan);
-  if (MX && e < E) plan[e] = pl;
   __syncthreads();
   if (COPY) {
     copy_token(x, t, k, H, rows, reinterpret_cast<__nv_bfloat16*>(xq));
@@ -469,7 +553,7 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
     __syncthreads();
     quantize_token_mx(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
   } else {
-    quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
+    quantize_token<1>(x, t, k, H, rows, warp_max, xq, x_scale);   // 1024 threads
   }
 }
 
@@ -516,74 +600,32 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
   for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
   if (warp < T) {
-    const float* row = logits + static_cast<size_t>(warp) * E;
-    float v[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < E ? row[e] : -FLT_MAX;
-      if (v[i] != v[i]) v[i] = -INFINITY;   // NaN ranks with -inf: k experts are always found
-    }
-    uint32_t taken = 0;
-    float my_v = 0.f;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      float best = -INFINITY;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < bi))) {
-          best = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ob > best || (ob == best && oi < bi)) {
-          best = ob;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        my_v = best;
-        my_id = bi;
-      }
-    }
-    const float lmax = __shfl_sync(0xffffffffu, my_v, 0);
-    float ex = lane < k ? expf(my_v - lmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    int my_id;
+    float my_w;
+    route_token_warp<NV>(logits + static_cast<size_t>(warp) * E, E, k, lane, &my_id, &my_w);
     if (lane < k) {
       if (warp == t) {
         const size_t ts = static_cast<size_t>(warp) * k + lane;
         ids[ts] = my_id;
-        wts[ts] = ex / sum;
+        wts[ts] = my_w;
       }
       sid[warp * 32 + lane] = my_id;
       atomicAdd(&cnt[my_id], 1);
     }
   }
   __syncthreads();
-  // counts -> offsets; the tile list
+  // counts -> offsets and the tile list (one block scan)
   const int e = threadIdx.x;
   const int c = e < E ? cnt[e] : 0;
-  int total_rows;
-  const int off = block_exclusive_scan(c, &total_rows);
-  __syncthreads();
-  if (e < E) cnt[e] = off;
+  const ExpertPlan pl = plan_experts(e, E, c, bn, t == 0, tiles, num_tiles, tile_plan);
+  if (e < E) cnt[e] = pl.off;
   if (t == 0) {
     if (e < E) {
       counts_out[e] = c;
-      offsets_out[e] = off;
+      offsets_out[e] = pl.off;
     }
-    if (e == 0) offsets_out[E] = total_rows;
+    if (e == 0) offsets_out[E] = pl.total_rows;
   }
-  plan_tiles(e, E, c, off, bn, t == 0, tiles, num_tiles, tile_plan);
   __syncthreads();
   // token t's rows: stable rank among earlier tokens routed to the same expert
   if (threadIdx.x < k) {
@@ -598,7 +640,7 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
     token_slot[r] = t * k + j;
   }
   __syncthreads();
-  quantize_token(x, t, k, H, rows, warp_max, xq, x_scale);
+  quantize_token<1>(x, t, k, H, rows, warp_max, xq, x_scale);   // 1024 threads
 }
 
 }  // namespace
@@ -649,14 +691,16 @@ cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, in
                     ids, chunk_base, T, E, k, chunks, row_of, token_slot);
 }
 
-cudaError_t launch_quant_scatter(const void* x, const int32_t* row_of, const int32_t* ids,
-                                 const int32_t* offsets, const int2* tile_plan, int T, int k,
-                                 int H, const QuantOut& q, cudaStream_t s) {
+cudaError_t launch_quant_scatter(const void* x, const int32_t* chunk_base, const int32_t* ids,
+                                 const int32_t* offsets, const int2* tile_plan, int T, int E,
+                                 int k, int H, int32_t* row_of, int32_t* token_slot,
+                                 const QuantOut& q, cudaStream_t s) {
   auto kern = q.bf16_copy ? quant_scatter_kernel<false, true>
               : q.mx8     ? quant_scatter_kernel<true>
                           : quant_scatter_kernel<false>;
-  return launch_pdl(kern, dim3(T), dim3(128), 0, s, static_cast<const __nv_bfloat16*>(x), row_of,
-                    ids, offsets, tile_plan, k, H, q.xq, q.x_scale, q.x_sf, q.sfb);
+  return launch_pdl(kern, dim3(T), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(x),
+                    chunk_base, ids, offsets, tile_plan, E, k, H, row_of, token_slot, q.xq,
+                    q.x_scale, q.x_sf, q.sfb);
 }
 
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,

@@ -23,12 +23,15 @@ namespace {
 
 // One warp per expanded row of h (bf16 [R, I]): amax, s2 = amax/448,
 // codes = E4M3_rne_satfinite(h * (448/amax)); an all-zero row gets s2 = 1 and
-// zero codes.  The row is read twice; the second pass hits L1/L2.
+// zero codes.  The row is read twice; the second pass hits L1/L2.  GEMM2 may
+// launch as soon as these blocks have started: it streams its weights while
+// this kernel waits for GEMM1 and quantises, and waits for this kernel's
+// results itself.
 __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __restrict__ h, int R,
                                                      int I, uint8_t* __restrict__ hq,
                                                      float* __restrict__ h_scale) {
-  griddep_wait();
   griddep_launch_dependents();
+  griddep_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= R) return;
@@ -81,8 +84,8 @@ __global__ void __launch_bounds__(256) hquant_mx_kernel(
     const int32_t* __restrict__ token_slot, const int32_t* __restrict__ offsets,
     const int2* __restrict__ tile_plan, uint8_t* __restrict__ hq, uint8_t* __restrict__ h_sf,
     uint8_t* __restrict__ sfb) {
+  griddep_launch_dependents();   // as hquant_kernel: GEMM2 may start streaming weights
   griddep_wait();
-  griddep_launch_dependents();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= R) return;
