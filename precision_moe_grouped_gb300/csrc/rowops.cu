@@ -1,6 +1,6 @@
 // rowops.cu -- the memory-bound row kernels between and after the GEMMs:
 // per-row FP8 quantisation of h (GEMM2's input), the top-k weighted combine,
-// and the bounded-wait self test.
+// and the bounded-wait self test (their per-row arithmetic: rowops.cuh).
 //
 // Pages cited (title and section):
 //   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add
@@ -16,63 +16,24 @@
 #include "moe_internal.h"
 #include "mxfp8.cuh"
 #include "ptx.cuh"
+#include "rowops.cuh"
 
 namespace moe {
 
 namespace {
 
-// One warp per expanded row of h (bf16 [R, I]): amax, s2 = amax/448,
-// codes = E4M3_rne_satfinite(h * (448/amax)); an all-zero row gets s2 = 1 and
-// zero codes.  The row is read twice; the second pass hits L1/L2.  GEMM2 may
-// launch as soon as these blocks have started: it streams its weights while
-// this kernel waits for GEMM1 and quantises, and waits for this kernel's
-// results itself.
+// One warp per expanded row of h (bf16 [R, I]): hquant_row_warp.  GEMM2
+// may launch as soon as these blocks have started: it streams its weights
+// while this kernel waits for GEMM1 and quantises, and waits for this
+// kernel's results itself.
 __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __restrict__ h, int R,
                                                      int I, uint8_t* __restrict__ hq,
                                                      float* __restrict__ h_scale) {
   griddep_launch_dependents();
   griddep_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   if (warp >= R) return;
-  const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(warp) * I);
-  const int nvec = I / 16;
-  float amax = 0.f;
-  for (int i = lane; i < nvec; i += 32) {
-    uint4 q[2] = {__ldg(hr + 2 * i), __ldg(hr + 2 * i + 1)};
-    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float2 f = __bfloat1622float2(b[j]);
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const bool nz = amax > 0.f;
-  const float inv = nz ? 448.0f / amax : 0.0f;
-  uint4* dst = reinterpret_cast<uint4*>(hq + static_cast<size_t>(warp) * I);
-  for (int i = lane; i < nvec; i += 32) {
-    uint4 out = make_uint4(0, 0, 0, 0);
-    if (nz) {
-      uint4 q[2] = {__ldg(hr + 2 * i), __ldg(hr + 2 * i + 1)};
-      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
-      uint32_t w[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f0 = __bfloat1622float2(b[2 * j]);
-        const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
-        const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv)), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)), __NV_SATFINITE, __NV_E4M3);
-        w[j] = (lo & 0xFFFFu) | (hi << 16);
-      }
-      out = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    dst[i] = out;
-  }
-  if (lane == 0) h_scale[warp] = nz ? amax / 448.0f : 1.0f;
+  hquant_row_warp(h, warp, I, hq, h_scale, threadIdx.x & 31);
 }
 
 // MXFP8 (the W8A8 mode) quantisation of h: one warp per expanded row r,
@@ -109,8 +70,7 @@ __global__ void __launch_bounds__(256) hquant_mx_kernel(
 }
 
 // Grid (T, ceil(H / 1024)): CTA (t, b) computes out[t, 1024 b .. 1024 b + 1023]
-// = bf16( sum_j w[t,j] * y[row_of[t,j]] ), float32 accumulation in slot order,
-// 8 bf16 (16 bytes) per thread.
+// with combine_vec, 8 bf16 (16 bytes) per thread.
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ y,
                                                       const float* __restrict__ wts,
                                                       const int32_t* __restrict__ row_of,
@@ -128,24 +88,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
   __syncthreads();
   const int i = blockIdx.y * blockDim.x + threadIdx.x;   // 16-byte vector index
   if (i >= H / 8) return;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < k; ++j) {
-    const uint4 q =
-        __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(rows[j]) * H) + i);
-    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&q);
-    const float wj = w[j];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const float2 f = __bfloat1622float2(b[p]);
-      acc[2 * p] = fmaf(wj, f.x, acc[2 * p]);
-      acc[2 * p + 1] = fmaf(wj, f.y, acc[2 * p + 1]);
-    }
-  }
-  uint4 r;
-  __nv_bfloat162* rb = reinterpret_cast<__nv_bfloat162*>(&r);
-#pragma unroll
-  for (int p = 0; p < 4; ++p) rb[p] = __floats2bfloat162_rn(acc[2 * p], acc[2 * p + 1]);
-  reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[i] = r;
+  combine_vec(y, w, rows, k, H, t, i, out);
 }
 
 // Waits on a barrier that nothing ever completes, with a bounded wait.
