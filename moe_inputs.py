@@ -53,6 +53,9 @@ CONFIGS = {
     # same ~128 rows as the full layer at T=4096, in 0.75 GB of weights (used
     # for profiler captures that must stay small)
     "dsv3_e32": MoeConfig("dsv3_e32", 5, 32, 8, 7168, 2048, (512,)),
+    # the MXFP8 Zipf workload's shape with 32 experts, for the same purpose
+    "mxfp8_e32": MoeConfig("mxfp8_e32", 6, 32, 8, 7168, 2048, (512,), mode=QUANT_W8A8,
+                           zipf=1.2),
 }
 
 
