@@ -405,7 +405,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
     MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
     MOE_CUDA(mark());
     MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts), offsets,
-                              chunk, tiles, num_tiles, tile_plan, st));
+                              chunk, tiles, num_tiles, tile_plan, status, st));
     MOE_CUDA(mark());
     MOE_CUDA(mark());   // the scatter kernel ranks the rows itself (no rank kernel)
     MOE_CUDA(moe::launch_quant_scatter(x, chunk, ids, offsets, tile_plan, T, E, k, H, row_of,

@@ -204,9 +204,11 @@ cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E,
                                 int32_t* num_tiles, int2* tile_plan, int32_t* row_of,
                                 int32_t* token_slot, const QuantOut& q, cudaStream_t s);
 // tile_plan (nullable): per expert (first tile, rows per tile).
+// status (nullable): where a timed-out wait of the scan's bulk copies is
+// recorded.
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
                         int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
-                        int32_t* num_tiles, int2* tile_plan, cudaStream_t s);
+                        int32_t* num_tiles, int2* tile_plan, int32_t* status, cudaStream_t s);
 cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,
                         int32_t* row_of, int32_t* token_slot, cudaStream_t s);
 // One CTA per token: the rows of its slots (from the per-chunk bases the

@@ -179,7 +179,7 @@ extern "C" int32_t moe_route_noalloc(const moe_shape* shape, const float* router
                          static_cast<int>(E), moe::kDecodeBN,
                          reinterpret_cast<int32_t*>(base + c.counts), offsets, chunk,
                          reinterpret_cast<int4*>(base + c.tiles),
-                         reinterpret_cast<int32_t*>(base + c.num_tiles), nullptr, s);
+                         reinterpret_cast<int32_t*>(base + c.num_tiles), nullptr, nullptr, s);
   if (e == cudaSuccess)
     e = moe::launch_rank(ids, chunk, static_cast<int>(T), static_cast<int>(E),
                          static_cast<int>(k), row_of,

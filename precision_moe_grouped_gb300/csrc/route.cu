@@ -205,6 +205,15 @@ __device__ ExpertPlan plan_experts(int e, int E, int c, int bn, bool write,
   return ExpertPlan{ex.x, tot.x, ex.y, tsz, nt};
 }
 
+// Shared memory the scan stages chunk counts in (whole chunks of E counts).
+constexpr int kScanSmemBytes = 192 * 1024;
+
+// Chunks the scan stages at a time: a multiple of 4, so that every batch
+// starts on a 16-byte boundary of the count matrix.
+__host__ __device__ inline int scan_batch_chunks(int E) {
+  return (kScanSmemBytes / (4 * E)) & ~3;
+}
+
 // One CTA of P groups of Ep = roundup32(E) threads (P = blockDim / Ep >= 1):
 // per-expert counts, offsets, per-chunk bases (stable ranks start there),
 // and the GEMM tile list.  Group g sums, for its expert, the chunk counts of
@@ -213,10 +222,13 @@ __device__ ExpertPlan plan_experts(int e, int E, int c, int bn, bool write,
 // consecutive rows of one expert; an expert with c rows gets ceil(c / tsz)
 // tiles of tsz = roundup16(ceil(c / ceil(c / bn))) rows, so its tiles are
 // balanced and every MMA-N is a multiple of 16.
+// The count matrix [num_chunks, E] comes into shared memory by bulk copies
+// of up to kScanSmemBytes (one round trip per batch instead of one per
+// count a thread reads); with a single batch the second pass reuses it.
 // chunk_counts and chunk_base may be the same buffer (the forward turns the
-// histogram into the bases in place): each element is read, by the thread
-// that owns it, before that thread overwrites it, so neither pointer is
-// declared __restrict__.
+// histogram into the bases in place): every count is read before the bases
+// of its chunk are written, so neither pointer is declared __restrict__.
+// The copy wait is bounded (status, when not null, records a timeout).
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* chunk_counts,
                                                     int num_chunks, int E, int bn,
                                                     int32_t* __restrict__ counts,
@@ -224,18 +236,54 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* chunk_counts,
                                                     int32_t* chunk_base,
                                                     int4* __restrict__ tiles,
                                                     int32_t* __restrict__ num_tiles,
-                                                    int2* __restrict__ tile_plan) {
+                                                    int2* __restrict__ tile_plan,
+                                                    int32_t* __restrict__ status) {
+  extern __shared__ __align__(16) int32_t staged[];   // [chunks of a batch, E]
   __shared__ int32_t part[1024];   // group g's sum for expert e at g * Ep + e
   __shared__ int32_t eoffs[1024];  // expert offsets, for every group
+  __shared__ __align__(8) uint64_t bar;
   griddep_wait();
   griddep_launch_dependents();
   const int Ep = (E + 31) & ~31, P = static_cast<int>(blockDim.x) / Ep;
   const int g = static_cast<int>(threadIdx.x) / Ep, e = static_cast<int>(threadIdx.x) % Ep;
   const bool active = g < P && e < E;
   const int ch0 = active ? g * num_chunks / P : 0, ch1 = active ? (g + 1) * num_chunks / P : 0;
+  const int sb = scan_batch_chunks(E), nb = (num_chunks + sb - 1) / sb;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  // batch b of chunks into shared memory (every thread calls it)
+  auto stage_batch = [&](int b) {
+    fence_proxy_async_smem();   // earlier reads of the buffer before the copy's writes
+    __syncthreads();
+    const int c0 = b * sb, nc = min(sb, num_chunks - c0);
+    if (threadIdx.x == 0) {
+      // whole 16-byte units: a few bytes past the matrix stay inside its
+      // 256-byte-padded region
+      const uint32_t bytes = (static_cast<uint32_t>(nc) * E * 4u + 15u) & ~15u;
+      mbar_arrive_expect_tx(&bar, bytes);
+      bulk_load(staged, chunk_counts + static_cast<size_t>(c0) * E, bytes, &bar);
+    }
+    const uint32_t a = smem_u32(&bar);
+    if (!mbar_try_wait(a, phase)) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait_suspend(a, phase, kSuspendNs))
+        if (globaltimer_ns() - t0 > 1000000000ull) {
+          if (status) atomicCAS(status, 0, kDevTimeout);
+          break;
+        }
+    }
+    phase ^= 1u;
+  };
   int c = 0;
-#pragma unroll 4
-  for (int ch = ch0; ch < ch1; ++ch) c += chunk_counts[static_cast<size_t>(ch) * E + e];
+  for (int b = 0; b < nb; ++b) {
+    stage_batch(b);
+    const int c0 = b * sb, c1 = min(num_chunks, c0 + sb);
+    for (int ch = max(ch0, c0); ch < min(ch1, c1); ++ch) c += staged[(ch - c0) * E + e];
+  }
   part[threadIdx.x] = c;
   __syncthreads();
   int total = 0, gstart = 0;
@@ -257,13 +305,13 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* chunk_counts,
     offsets[e] = off;
   }
   if (threadIdx.x == 0) offsets[E] = pl.total_rows;
-  if (active) {
-    int run = eoffs[e] + gstart;
-#pragma unroll 4
-    for (int ch = ch0; ch < ch1; ++ch) {
-      const size_t i = static_cast<size_t>(ch) * E + e;
-      const int cc = chunk_counts[i];
-      chunk_base[i] = run;
+  int run = active ? eoffs[e] + gstart : 0;
+  for (int b = 0; b < nb; ++b) {
+    if (nb > 1) stage_batch(b);   // a single batch is still staged
+    const int c0 = b * sb, c1 = min(num_chunks, c0 + sb);
+    for (int ch = max(ch0, c0); ch < min(ch1, c1); ++ch) {
+      const int cc = staged[(ch - c0) * E + e];
+      chunk_base[static_cast<size_t>(ch) * E + e] = run;
       run += cc;
     }
   }
@@ -673,11 +721,17 @@ cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, 
 
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
                         int32_t* counts, int32_t* offsets, int32_t* chunk_base, int4* tiles,
-                        int32_t* num_tiles, int2* tile_plan, cudaStream_t s) {
+                        int32_t* num_tiles, int2* tile_plan, int32_t* status, cudaStream_t s) {
   const int ep = ((E + 31) / 32) * 32;    // one group of threads per expert set
   const int threads = (1024 / ep) * ep;   // as many groups as fit 1024 threads
-  return launch_pdl(scan_kernel, dim3(1), dim3(threads), 0, s, chunk_counts, num_chunks, E, bn,
-                    counts, offsets, chunk_base, tiles, num_tiles, tile_plan);
+  static DeviceOnce smem_set;
+  cudaError_t e = set_smem_limit_once(scan_kernel, kScanSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  const int sb = scan_batch_chunks(E);
+  const size_t smem =
+      (static_cast<size_t>(std::min(num_chunks, sb)) * E * 4 + 15) / 16 * 16;
+  return launch_pdl(scan_kernel, dim3(1), dim3(threads), smem, s, chunk_counts, num_chunks, E,
+                    bn, counts, offsets, chunk_base, tiles, num_tiles, tile_plan, status);
 }
 
 cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, int E, int k,

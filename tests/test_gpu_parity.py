@@ -335,3 +335,13 @@ def test_nan_logits_route_in_range(T, E):
     fw = M.forward(x_bits(case), lg, oracle_weights(case), k, tokens=finite)
     ok, st = max_err_ok(run.out_np()[finite], fw.out)
     assert ok, st
+
+
+def test_scan_stages_counts_in_several_batches():
+    """The large-batch scan stages the per-chunk expert counts in shared
+    memory batches; with 1024 experts a batch holds 48 chunks, so T = 2000
+    tokens (63 chunks) take two batches.  Offsets, row maps and codes stay
+    bit-exact."""
+    cfg = MI.custom_config(1024, 2, 128, 128)
+    run, _ = full_parity(MI.make_case(cfg, 2000, seed=97), name="scan_batches")
+    check_tiles(run, 160)
