@@ -97,7 +97,7 @@ typedef struct {
  * Kernels are launched with programmatic dependent launch: each may start
  * while its predecessor finishes and waits for the predecessor's results. */
 #define MOE_NUM_STAGES 8
-#define MOE_SMALL_BATCH_TOKENS 1024
+#define MOE_SMALL_BATCH_TOKENS 256
 #define MOE_TINY_BATCH_TOKENS 32
 
 /* Optional per-call settings (moe_forward_ex); zero-initialise for defaults. */

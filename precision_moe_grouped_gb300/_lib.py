@@ -36,7 +36,7 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_prepare_weights", 
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 MOE_NUM_STAGES = 8
-MOE_SMALL_BATCH_TOKENS = 1024
+MOE_SMALL_BATCH_TOKENS = 256
 
 
 MOE_TINY_BATCH_TOKENS = 32
@@ -44,7 +44,7 @@ MOE_TINY_BATCH_TOKENS = 32
 
 def kernels_per_forward(num_tokens: int, mode: int = 0) -> int:
     """Kernels one forward launches (0 for an empty batch): W4A8 batches of
-    <= 32 tokens route and expand in one kernel, batches of <= 1024 tokens in
+    <= 32 tokens route and expand in one kernel, batches of <= 256 tokens in
     two, larger ones in three (routing, scan, scatter); W4A16 has no h
     quantisation kernel."""
     if num_tokens == 0:

@@ -81,7 +81,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // Largest token count that uses the one-kernel small-batch expansion
-// (expand_small_kernel) instead of scan + rank + quant_scatter.
+// (expand_small_kernel) instead of scan + quant_scatter.  Each of its T
+// blocks recounts all T * k routed ids, so its cost grows with T^2: above
+// 256 tokens the three-kernel path is cheaper (DSV3 T=512: 26.8 us in the
+// one kernel).
 constexpr int kSmallT = MOE_SMALL_BATCH_TOKENS;
 
 // Largest token count that routes, expands and quantises in one single-CTA

@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     quantize_token<2>(x, t, k, H, rows, warp_max, xq, x_scale);   // 256 threads
 }
 
-// Small batches (T <= kSmallT): one kernel replaces scan + rank +
+// Small batches (T <= kSmallT = 256): one kernel replaces scan +
 // quant_scatter.  CTA t (1024 threads, one expert per thread) rebuilds the
 // per-expert counts and offsets from all T*k routed ids in shared memory,
 // ranks its own token's k slots (rank of (t, e) = number of earlier tokens

@@ -3,7 +3,7 @@ stack replays one graph per step): the captured launches -- programmatic
 dependent launches included -- replay to exactly the eager result, and a
 replay after new inputs are copied into the captured buffers matches an
 eager run on those inputs.  One case per front-end path: the one-kernel
-tiny batch (T <= 32), the small-batch expansion (T <= 1024) and the
+tiny batch (T <= 32), the small-batch expansion (T <= 256) and the
 multi-kernel expansion."""
 import pytest
 import torch

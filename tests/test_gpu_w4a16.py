@@ -86,7 +86,7 @@ def test_w16_config_full():
 
 
 def test_w16_large_batch_expansion():
-    """T > 1024: the bf16 rows are copied by the multi-kernel expansion
-    (scan, rank, scatter) instead of the one-kernel small-batch path."""
+    """T > 256: the bf16 rows are copied by the multi-kernel expansion
+    (scan, scatter) instead of the one-kernel small-batch path."""
     run, _ = w16_parity(MI.make_case(_cfg(8, 2, 256, 128), 1500, seed=5), name="w16_large")
     assert run.T > P._lib.MOE_SMALL_BATCH_TOKENS
