@@ -158,6 +158,44 @@ def quantize_rows_mxfp8(rows_f32: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return codes.reshape(shp).astype(np.uint8), (e + 127).astype(np.uint8)
 
 
+def split_rows_mxfp8x2(rows_f32: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """The W4A16 mode's device encoding of bf16 activations as two MXFP8
+    terms, so that block-scaled FP8 tensor cores can take them.  This is the
+    library's own encoding, not a step the pages define: the W4A16 forward
+    stays the exact product of the bf16 activations (forward() below), and
+    this function exists only to check the device's codes bit for bit.
+
+    Per 32-element block v of a row (K elements):
+      hi: Xh = 2^clamp(floor(log2 amax) - 7, -127, 127), codes E4M3_rne(v / Xh);
+      lo: r = v - dec(hi) * Xh (exact), Xl = 2^clamp(floor(log2 max|r|) - 7,
+          -127, 127), codes E4M3_rne(r / Xl);
+    an all-zero block (or residual) gets scale byte 0x7F.  Both quotients
+    stay below 256 (their codes at most 256), so no code saturates.  For a bf16 block, dec(hi) * Xh +
+    dec(lo) * Xl equals v for every element of magnitude >= 2^(E - 13)
+    (E = floor(log2 amax)) and is within 2^(E - 21) of v for the rest.
+
+    Returns codes uint8 [..., 2K] (hi blocks in columns [0, K), lo blocks in
+    [K, 2K)) and scale bytes uint8 [..., 2K/32] in the same order."""
+    v = np.asarray(rows_f32, dtype=np.float32).astype(np.float64)
+    shp = v.shape
+    blk = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
+
+    def term(b):
+        amax = np.abs(b).max(axis=-1)
+        nz = amax > 0
+        _, e2 = np.frexp(np.where(nz, amax, 1.0))
+        e = np.where(nz, np.clip(e2 - 1 - 7, -127, 127), 0)
+        scale = np.ldexp(1.0, e)[..., None]
+        codes = F.e4m3_encode(b / scale)
+        return codes, (e + 127).astype(np.uint8), F.e4m3_decode(codes) * scale
+
+    hc, hs, hval = term(blk)
+    lc, ls, _ = term(blk - hval)
+    codes = np.concatenate([hc.reshape(shp), lc.reshape(shp)], axis=-1).astype(np.uint8)
+    scales = np.concatenate([hs, ls], axis=-1).astype(np.uint8)
+    return codes, scales
+
+
 @dataclass
 class Weights:
     """Expert weights in the user layout of the C ABI.

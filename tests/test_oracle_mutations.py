@@ -10,6 +10,7 @@ sys.path.insert(0, os.path.dirname(__file__))
 import test_oracle_formats as TF  # noqa: E402
 import test_oracle_forward as TW  # noqa: E402
 import test_oracle_routing as TR  # noqa: E402
+import test_oracle_split as TS  # noqa: E402
 from oracle import formats as F
 from oracle import moe as M
 
@@ -217,3 +218,43 @@ def test_route_and_quantize_slips_are_caught(monkeypatch, slip):
         return rt, tq, ts
     _expect_caught(lambda: [TR.check_route_and_quantize(bad, x, lg, k)
                             for x, lg, k in TR._front_cases()])
+
+
+def _split_variant(emax_off=7, residual=True, keep_lo=True):
+    """A copy of the two-term split with one step changed."""
+    def split(rows):
+        v = np.asarray(rows, dtype=np.float32).astype(np.float64)
+        shp = v.shape
+        blk = v.reshape(shp[:-1] + (shp[-1] // 32, 32))
+
+        def term(b):
+            amax = np.abs(b).max(axis=-1)
+            nz = amax > 0
+            _, e2 = np.frexp(np.where(nz, amax, 1.0))
+            e = np.where(nz, np.clip(e2 - 1 - emax_off, -127, 127), 0)
+            sc = np.ldexp(1.0, e)[..., None]
+            c = F.e4m3_encode(b / sc)
+            return c, (e + 127).astype(np.uint8), F.e4m3_decode(c) * sc
+
+        hc, hs, hv = term(blk)
+        lc, ls, _ = term(blk - hv if residual else blk)
+        if not keep_lo:
+            lc = np.zeros_like(lc)
+        return (np.concatenate([hc.reshape(shp), lc.reshape(shp)], -1).astype(np.uint8),
+                np.concatenate([hs, ls], -1).astype(np.uint8))
+    return split
+
+
+def _pin_split():
+    TS.test_split_hand_worked_block()
+    TS.test_split_exact_over_every_bf16_value_of_14_binades()
+    TS.test_split_error_bound_and_no_saturation()
+
+
+@pytest.mark.parametrize("slip", [dict(emax_off=8), dict(emax_off=6), dict(residual=False),
+                                  dict(keep_lo=False)],
+                         ids=["ocp_emax", "one_binade_low", "lo_from_value", "dropped_lo"])
+def test_split_slips_are_caught(monkeypatch, slip):
+    _pin_split()
+    monkeypatch.setattr(M, "split_rows_mxfp8x2", _split_variant(**slip))
+    _expect_caught(_pin_split)
