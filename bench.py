@@ -189,22 +189,23 @@ def alg_cost(stage: str, cfg, T: int, n_touched: int, mode: int = 0):
     """Algorithmic (bytes, flops) of one launch of `stage` in quantisation
     `mode` (0 W4A8, 1 W4A16, 2 W8A8): weights are packed E2M1 (0.5 B) or
     E4M3 (1 B) per element plus one scale byte per 32; the expanded
-    activations are E4M3 (+ a row scale, or a scale byte per 32 in W8A8) or
-    bf16 (W4A16, which has no h-quantisation)."""
+    activations and h are E4M3 (+ a row scale, or a scale byte per 32 in
+    W8A8), or in W4A16 two E4M3 terms with a scale byte per 32 each (the
+    bf16 values split for the FP8 tensor cores)."""
     E, k, H, I = cfg.num_experts, cfg.top_k, cfg.hidden, cfg.inter
     R = T * k
     wb = 1.0 if mode == 2 else 0.5
     w1 = 2 * I * H * (wb + 1 / 32)
     w2 = H * I * (wb + 1 / 32)
-    act = 2.0 if mode == 1 else (1 + 1 / 32) if mode == 2 else 1.0   # bytes per element
-    rs = 0 if mode == 1 else 4                                         # row-scale bytes
+    act = {0: 1.0, 1: 2 * (1 + 1 / 32), 2: 1 + 1 / 32}[mode]   # bytes per element
+    rs = 4 if mode == 0 else 0                                  # row-scale bytes
     table = {
         "route": (T * E * 4 + R * 8, 0),
         "scan": (2 * 4 * E * -(-T // 32), 0),     # per-chunk counts in, chunk bases out
         "rank": (R * 12, 0),
         "quant_scatter": (T * H * 2 + R * H * act + R * rs, 0),
         "gemm1": (n_touched * w1 + R * H * act + R * rs + R * I * 2, 2.0 * R * H * 2 * I),
-        "hquant": (0, 0) if mode == 1 else (R * I * 2 + R * I * act + R * rs, 0),
+        "hquant": (R * I * 2 + R * I * act + R * rs, 0),
         "gemm2": (n_touched * w2 + R * I * act + R * rs + R * H * 2, 2.0 * R * I * H),
         "combine": (R * H * 2 + R * 8 + T * H * 2, 0),
     }
@@ -214,7 +215,8 @@ def alg_cost(stage: str, cfg, T: int, n_touched: int, mode: int = 0):
 # Per quantisation mode: the arithmetic the GEMMs compute in, and the
 # weight encoding of the synthetic data.
 MODE_DTYPE = {0: "fp8e4m3 x fp4e2m1 (mxf8f6f4), fp32 accumulate",
-              1: "bf16 x bf16 from fp4e2m1 weights (kind::f16), fp32 accumulate",
+              1: "bf16 activations as two fp8e4m3 terms x fp4e2m1 (mxf8f6f4, MX block "
+                 "scales), fp32 accumulate",
               2: "fp8e4m3 x fp8e4m3 (mxf8f6f4, MX block scales), fp32 accumulate"}
 MODE_WEIGHTS = {0: "MXFP4", 1: "MXFP4", 2: "MXFP8"}
 MODE_NAME = {0: "MXFP4xFP8", 1: "MXFP4xBF16", 2: "MXFP8xMXFP8"}
@@ -238,8 +240,9 @@ def workload_config(cfg, T: int) -> dict:
 
 def fused_roofline(cfg, T, n_touched, t_s, pk, mode=0):
     """Roofline of the whole forward: max(touched weight+scale + activation
-    bytes / HBM, FLOPs / tensor peak of the MMA kind the mode runs: FP8 for
-    W4A8 (mxf8f6f4) and W8A8, bf16 for W4A16 (kind::f16))."""
+    bytes / HBM, FLOPs / tensor peak): the FP8 peak for W4A8 and W8A8, the
+    bf16 peak for W4A16 (a bf16 product; run as two FP8 MMAs, it takes the
+    same tensor time)."""
     E, k, H, I = cfg.num_experts, cfg.top_k, cfg.hidden, cfg.inter
     w_bytes = 1.0 if mode == 2 else 0.5          # E4M3 or packed E2M1 per weight
     bytes_ = n_touched * 3 * I * H * (w_bytes + 1 / 32) + T * H * 2 + T * E * 4 + T * H * 2

@@ -65,7 +65,10 @@ typedef enum {
  * implemented. */
 typedef enum {
   MOE_W4A8_MXFP4_FP8 = 0,    /* MXFP4 weights, runtime per-token FP8 E4M3 acts */
-  MOE_W4A16_MXFP4_BF16 = 1,  /* MXFP4 weights, bf16 activations               */
+  MOE_W4A16_MXFP4_BF16 = 1,  /* MXFP4 weights, bf16 activations (computed on
+                                the FP8 tensor cores as two MXFP8 terms per
+                                activation: exact for every element within
+                                2^13 of its 32-block's maximum)           */
   MOE_W8A8_MXFP8 = 2         /* MXFP8 weights and MXFP8 activations           */
 } moe_quant_mode;
 
@@ -92,8 +95,7 @@ typedef struct {
  * one kernel, timed as stage "scan"; the "quant_scatter" stage is then empty
  * too and the forward launches 6 kernels.
  * For num_tokens <= MOE_TINY_BATCH_TOKENS in the W4A8 mode routing and
- * expansion run as one kernel, timed as stage "route" (5 kernels).  The
- * W4A16 mode has no hquant kernel (its stage is empty).
+ * expansion run as one kernel, timed as stage "route" (5 kernels).
  * Kernels are launched with programmatic dependent launch: each may start
  * while its predecessor finishes and waits for the predecessor's results. */
 #define MOE_NUM_STAGES 8
@@ -133,16 +135,21 @@ typedef struct {
  *   token_slot  int32[R]      token*top_k + slot of each expanded row
  *   tiles       int32[4*max]  GEMM work map: (expert, first row, rows, 0)
  *   xq          uint8[R,H]    FP8 E4M3 codes of the expanded activations
+ *                             (W4A16: uint8[R,2H], the hi terms in columns
+ *                             0..H-1, the lo terms -- hi's exact residual
+ *                             -- in H..2H-1)
  *   x_scale     float[R]      per-row (per-token) activation scale
  *   h           bf16[R,I]     SwiGLU output
- *   hq          uint8[R,I]    FP8 E4M3 codes of h
+ *   hq          uint8[R,I]    FP8 E4M3 codes of h (W4A16: uint8[R,2I], hi | lo)
  *   h_scale     float[R]      per-row scale of hq
  *   y           bf16[R,H]     GEMM2 output (scaled)
  *   x_stage, logits_stage, out_stage: device staging used by moe_forward_host
  *   tile_plan   int32[E,2]    per expert: first GEMM tile, rows per tile
- * MXFP8 (W8A8) only (0 bytes otherwise; x_scale / h_scale unused):
- *   x_sf        uint8[R,H/32] E8M0 block scales of xq, row-major
- *   h_sf        uint8[R,I/32] E8M0 block scales of hq, row-major
+ * MXFP8 (W8A8) and W4A16 only (0 bytes otherwise; x_scale / h_scale unused):
+ *   x_sf        uint8[R,H/32] E8M0 block scales of xq, row-major (W4A16:
+ *                             [R,2H/32], the hi blocks then the lo blocks)
+ *   h_sf        uint8[R,I/32] E8M0 block scales of hq, row-major (W4A16:
+ *                             [R,2I/32])
  *   x_sf_tiled, h_sf_tiled    the same scales in the GEMMs' per-tile layout:
  *                             1024 bytes per (tile, 128-K stage) */
 typedef struct {

@@ -45,15 +45,13 @@ MOE_TINY_BATCH_TOKENS = 32
 def kernels_per_forward(num_tokens: int, mode: int = 0) -> int:
     """Kernels one forward launches (0 for an empty batch): W4A8 batches of
     <= 32 tokens route and expand in one kernel, batches of <= 256 tokens in
-    two, larger ones in three (routing, scan, scatter); W4A16 has no h
-    quantisation kernel."""
+    two, larger ones in three (routing, scan, scatter); then GEMM1, the h
+    quantisation, GEMM2 and the combine."""
     if num_tokens == 0:
         return 0
     if mode == 0 and num_tokens <= MOE_TINY_BATCH_TOKENS:
-        n = 5
-    else:
-        n = 6 if num_tokens <= MOE_SMALL_BATCH_TOKENS else 7
-    return n - 1 if mode == 1 else n
+        return 5
+    return 6 if num_tokens <= MOE_SMALL_BATCH_TOKENS else 7
 
 
 class MoeShape(ctypes.Structure):

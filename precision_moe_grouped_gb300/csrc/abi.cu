@@ -123,6 +123,15 @@ int32_t check_shape(const moe_shape* s, int32_t mode) {
   return MOE_OK;
 }
 
+// The activation encoding of a quantisation mode: per-row FP8 (W4A8),
+// MXFP8 (W8A8), or the two-term MXFP8 split of the bf16 activations
+// (W4A16).
+int act_of(int32_t mode) {
+  return mode == MOE_W8A8_MXFP8 ? moe::kActMxfp8
+         : mode == MOE_W4A16_MXFP4_BF16 ? moe::kActSplit
+                                         : moe::kActFp8Row;
+}
+
 void compute_layout(const moe_shape* s, int32_t mode, moe_ws_layout* L) {
   std::memset(L, 0, sizeof(*L));
   const int64_t T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden,
@@ -146,22 +155,28 @@ void compute_layout(const moe_shape* s, int32_t mode, moe_ws_layout* L) {
   L->chunk_counts = take(chunks * E * 4);
   L->token_slot = take(R * 4);
   L->tiles = take(max_tiles * 16);
-  L->xq = take(R * H * (mode == MOE_W4A16_MXFP4_BF16 ? 2 : 1));   // bf16 copy in W4A16
+  // W4A16: two FP8 terms per element (the split activations)
+  const int act = act_of(mode);
+  const int64_t terms = act == moe::kActSplit ? 2 : 1;
+  L->xq = take(R * H * terms);
   L->x_scale = take(R * 4);
   L->h = take(R * I * 2);
-  L->hq = take(R * I);
+  L->hq = take(R * I * terms);
   L->h_scale = take(R * 4);
   L->y = take(R * H * 2);
   L->x_stage = take(T * H * 2);
   L->logits_stage = take(T * E * 4);
   L->out_stage = take(T * H * 2);
   L->tile_plan = take(E * 8);
-  // MXFP8 activation scales: row-major bytes and the GEMMs' per-tile layout
-  const bool mx = mode == MOE_W8A8_MXFP8;
-  L->x_sf = take(mx ? R * (H / 32) : 0);
-  L->h_sf = take(mx ? R * (I / 32) : 0);
-  L->x_sf_tiled = take(mx ? max_tiles * (H / 128) * moe::kSfbTileBytes : 0);
-  L->h_sf_tiled = take(mx ? max_tiles * (I / 128) * moe::kSfbTileBytes : 0);
+  // MXFP8 / split activation scales: row-major bytes and the GEMMs' per-tile
+  // layout
+  const bool mx = act != moe::kActFp8Row;
+  L->x_sf = take(mx ? R * (H / 32) * terms : 0);
+  L->h_sf = take(mx ? R * (I / 32) * terms : 0);
+  L->x_sf_tiled =
+      take(mx ? max_tiles * moe::act_k_stages(act, static_cast<int>(H)) * moe::kSfbTileBytes : 0);
+  L->h_sf_tiled =
+      take(mx ? max_tiles * moe::act_k_stages(act, static_cast<int>(I)) * moe::kSfbTileBytes : 0);
   L->total = align_up(off, kAlign);
   L->max_tiles = static_cast<int32_t>(max_tiles);
   L->num_chunks = static_cast<int32_t>(chunks);
@@ -210,7 +225,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-enum class MapKind { kFp4Weights, kBytes, kScaleBlocks, kPackedBytes, kBf16 };
+enum class MapKind { kFp4Weights, kBytes, kScaleBlocks };
 
 // 2-D tensor map over a row-major [rows, cols] matrix of `kind` elements;
 // box = box_cols x box_rows elements.
@@ -218,27 +233,23 @@ enum class MapKind { kFp4Weights, kBytes, kScaleBlocks, kPackedBytes, kBf16 };
 //                 lands as 16 bytes in shared memory), 128-byte swizzle
 //   kBytes:       uint8 (FP8 codes), 128-byte swizzle
 //   kScaleBlocks: uint32 words, no swizzle
-//   kPackedBytes: uint8, no swizzle (packed E2M1 rows copied as they are)
-//   kBf16:        bf16 activations, 128-byte swizzle (64-element boxes)
 int32_t make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, MapKind kind,
                   uint32_t box_cols, uint32_t box_rows) {
   if (!base) return fail(MOE_ERR_INVALID_ARG, "refusing to encode a tensor map for NULL");
   auto fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const bool fp4 = kind == MapKind::kFp4Weights, words = kind == MapKind::kScaleBlocks;
-  const bool bf16 = kind == MapKind::kBf16, plain = words || kind == MapKind::kPackedBytes;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {fp4 ? cols / 2 : words ? cols * 4 : bf16 ? cols * 2 : cols};
+  const cuuint64_t strides[1] = {fp4 ? cols / 2 : words ? cols * 4 : cols};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m,
                   fp4     ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
                   : words ? CU_TENSOR_MAP_DATA_TYPE_UINT32
-                  : bf16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                           : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                   2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  plain ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  words ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) rows=%llu cols=%llu kind=%d",
@@ -306,12 +317,14 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   if (rc != MOE_OK) return rc;
   moe_ws_layout L;
   compute_layout(s, mode, &L);
-  const bool mx = mode == MOE_W8A8_MXFP8;
+  const int act = act_of(mode);
+  const bool fp8w = act == moe::kActMxfp8;       // E4M3 weights (else E2M1)
+  const bool tiled = act != moe::kActFp8Row;     // per-32 activation scales
   const int T = s->num_tokens, E = s->num_experts, k = s->top_k, H = s->hidden, I = s->inter;
   const int R = T * k;
-  const bool w4a16 = mode == MOE_W4A16_MXFP4_BF16;
+  const int terms = act == moe::kActSplit ? 2 : 1;
   const int variant = pick_variant(s, opts);
-  const int bn = w4a16 ? moe::kW4A16BN : moe::gemm_tile_tokens(variant);
+  const int bn = moe::gemm_tile_tokens(variant, act);
   const int prefetch = !opts || opts->prefetch_stages == 0 ? default_prefetch(variant)
                        : opts->prefetch_stages < 0 ? 0 : opts->prefetch_stages;
   const uint64_t timeout_ns =
@@ -330,10 +343,10 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   float* h_scale = at<float>(ws, L.h_scale);
   void* y = at<void>(ws, L.y);
   int2* tile_plan = at<int2>(ws, L.tile_plan);
-  uint8_t* x_sf = mx ? at<uint8_t>(ws, L.x_sf) : nullptr;
-  uint8_t* h_sf = mx ? at<uint8_t>(ws, L.h_sf) : nullptr;
-  uint8_t* sfb1 = mx ? at<uint8_t>(ws, L.x_sf_tiled) : nullptr;
-  uint8_t* sfb2 = mx ? at<uint8_t>(ws, L.h_sf_tiled) : nullptr;
+  uint8_t* x_sf = tiled ? at<uint8_t>(ws, L.x_sf) : nullptr;
+  uint8_t* h_sf = tiled ? at<uint8_t>(ws, L.h_sf) : nullptr;
+  uint8_t* sfb1 = tiled ? at<uint8_t>(ws, L.x_sf_tiled) : nullptr;
+  uint8_t* sfb2 = tiled ? at<uint8_t>(ws, L.h_sf_tiled) : nullptr;
 
   CUtensorMap tm_w1, tm_w2, tm_sf1, tm_sf2, tm_x[moe::kNumXMaps], tm_h[moe::kNumXMaps];
   CUtensorMap tm_xp[moe::kNumXMaps], tm_hp[moe::kNumXMaps];   // CTA-pair half boxes
@@ -342,25 +355,20 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   // scales: one 512-byte block per box
   const uint64_t w1_boxes = static_cast<uint64_t>(E) * (2 * I / 128) * (H / 128);
   const uint64_t w2_boxes = static_cast<uint64_t>(E) * (H / 128) * (I / 128);
-  // W4A16: packed code rows (64 bytes) as they are, for the in-kernel
-  // conversion to bf16
-  const MapKind wkind = mx ? MapKind::kBytes : w4a16 ? MapKind::kPackedBytes : MapKind::kFp4Weights;
-  // (W4A16 copies half a box row -- 64 K, 32 bytes -- per sub-stage)
-  const uint32_t wcols = w4a16 ? 64 : 128, wbox = w4a16 ? 32 : 128;
-  const uint32_t w_tx = mx ? 128u * 128u : kWeightBoxTxBytes;
-  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, wcols, wkind, wbox, 128)) != MOE_OK ||
-      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, wcols, wkind, wbox, 128)) != MOE_OK ||
+  const MapKind wkind = fp8w ? MapKind::kBytes : MapKind::kFp4Weights;
+  const uint32_t w_tx = fp8w ? 128u * 128u : kWeightBoxTxBytes;
+  if ((rc = make_tmap(&tm_w1, w1, w1_boxes * 128, 128, wkind, 128, 128)) != MOE_OK ||
+      (rc = make_tmap(&tm_w2, w2, w2_boxes * 128, 128, wkind, 128, 128)) != MOE_OK ||
       (rc = make_tmap(&tm_sf1, w1_sf, w1_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK ||
       (rc = make_tmap(&tm_sf2, w2_sf, w2_boxes, 128, MapKind::kScaleBlocks, 128, 1)) != MOE_OK)
     return rc;
   for (int i = 0; i < moe::kNumXMaps; ++i) {
     const uint32_t rows = static_cast<uint32_t>(moe::kXBoxRowsAt(i));
-    // W4A16: bf16 activations (the expanded copy of x, and h itself) in
-    // 64-element (128-byte) boxes
-    if ((rc = w4a16 ? make_tmap(&tm_x[i], xq, R, H, MapKind::kBf16, 64, rows)
-                    : make_tmap(&tm_x[i], xq, R, H, MapKind::kBytes, 128, rows)) != MOE_OK ||
-        (rc = w4a16 ? make_tmap(&tm_h[i], h, R, I, MapKind::kBf16, 64, rows)
-                    : make_tmap(&tm_h[i], hq, R, I, MapKind::kBytes, 128, rows)) != MOE_OK)
+    // split activations: rows of 2K codes (hi terms, then lo terms)
+    if ((rc = make_tmap(&tm_x[i], xq, R, static_cast<uint64_t>(terms) * H, MapKind::kBytes, 128,
+                        rows)) != MOE_OK ||
+        (rc = make_tmap(&tm_h[i], hq, R, static_cast<uint64_t>(terms) * I, MapKind::kBytes, 128,
+                        rows)) != MOE_OK)
       return rc;
   }
   const bool pair = variant == 6 && mode == MOE_W4A8_MXFP4_FP8;
@@ -381,7 +389,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   const int grid2 = gemm_grid(dev.num_sms, T, k, E, H / moe::kTileM);
   // the first kernel clears the status word; tiny batches (W4A8) route,
   // expand and quantise in one kernel, small batches expand in one kernel
-  const moe::QuantOut qx{xq, x_scale, mx, x_sf, sfb1, w4a16};
+  const moe::QuantOut qx{xq, x_scale, act, x_sf, sfb1};
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* token_slot = at<int32_t>(ws, L.token_slot);
   MOE_CUDA(mark());
@@ -412,28 +420,25 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
                                        token_slot, qx, st));
     MOE_CUDA(mark());
   }
-  // W4A8: the per-row token scale is applied in the epilogues; MXFP8: the
-  // block scales ride with the operands into the MMA
+  // W4A8: the per-row token scale is applied in the epilogues; MXFP8 and
+  // split: the block scales ride with the operands into the MMA
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
-                   mx ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, grid1,
-                   prefetch, mx, sfb1, static_cast<const uint8_t*>(w1), pair ? tm_xp : nullptr,
+                   tiled ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, grid1,
+                   prefetch, act, sfb1, static_cast<const uint8_t*>(w1), pair ? tm_xp : nullptr,
                    L.max_tiles};
-  MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(true, g1, st) : moe::launch_gemm(true, variant, g1, st));
+  MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
-  if (w4a16) {
-    // GEMM2 reads h (bf16) directly: nothing to quantise
-  } else if (mx)
-    MOE_CUDA(moe::launch_hquant_mx(h, R, I, ids, token_slot, offsets, tile_plan, hq, h_sf, sfb2,
-                                   st));
+  if (tiled)
+    MOE_CUDA(moe::launch_hquant_mx(act, h, R, I, ids, token_slot, offsets, tile_plan, hq, h_sf,
+                                   sfb2, st));
   else
     MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
   MOE_CUDA(mark());
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
-                   mx ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, grid2,
-                   prefetch, mx, sfb2, static_cast<const uint8_t*>(w2), pair ? tm_hp : nullptr,
+                   tiled ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, grid2,
+                   prefetch, act, sfb2, static_cast<const uint8_t*>(w2), pair ? tm_hp : nullptr,
                    L.max_tiles};
-  MOE_CUDA(w4a16 ? moe::launch_gemm_bf16(false, g2, st)
-                 : moe::launch_gemm(false, variant, g2, st));
+  MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));
   MOE_CUDA(mark());

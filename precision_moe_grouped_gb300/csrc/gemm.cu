@@ -21,6 +21,14 @@
 // .kind::mxf8f6f4 (TMA expands each 16-element group to 16 bytes in shared
 // memory).
 //
+// Operands by activation encoding (ACT): W4A8 -- A = E2M1 weights, B = E4M3
+// activations with constant unit block scales (the per-row token scale is
+// applied in the epilogue); W8A8 -- A = E4M3 weights, B = E4M3 activations
+// with their per-32 block scales; W4A16 -- A = E2M1 weights and B = the two
+// MXFP8 terms of the bf16 activations (hi, lo): each stage holds both terms'
+// boxes and scale blocks, and its MMAs accumulate A x hi and A x lo into
+// one accumulator, so the bf16 product runs on the FP8 tensor pipe.
+//
 // Orientation ("swap-AB"): the MMA's M = 128 rows are WEIGHT rows (output
 // features) and its N columns are TOKENS (expanded rows of one expert), so a
 // tile's token count only needs to be a multiple of 16: decode batches of 1-32
@@ -53,10 +61,13 @@ namespace moe {
 
 namespace {
 
-template <int BN, int STAGES, int NI, int NB, bool MX8>
+template <int BN, int STAGES, int NI, int NB, int ACT>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN <= kXBoxRowsAt(kNumXMaps - 1),
                 "token tile must be a multiple of 16 rows and fit the largest box");
+  static constexpr bool kTiledSfb = ACT != kActFp8Row;   // per-tile activation scales
+  static constexpr bool kSplit = ACT == kActSplit;       // two activation terms per stage
+  static_assert(!kSplit || BN <= 128, "a split stage holds one 512-byte scale block per term");
   // Producer warps: stage s is served by warp s % kProdWarps (lanes of one
   // warp spinning on different stages' barriers serialise; three warps
   // measured 9% less time per stage than one in a producer-only benchmark),
@@ -68,17 +79,19 @@ struct GemmCfg {
   static_assert(kLanesPerStage * kStagesPerWarp <= 32, "producer lanes must fit a warp");
   static_assert(STAGES % NI == 0, "each stage must belong to one MMA issuer");
   static constexpr int kABytes = kTileM * 128;       // FP4 expanded to 1 byte/element in smem
-  static constexpr int kBBytes = BN * 128;           // FP8 tokens x 128 K
+  static constexpr int kTermBytes = BN * 128;        // FP8 tokens x 128 K
+  static constexpr int kBBytes = (kSplit ? 2 : 1) * kTermBytes;
   static constexpr int kSFBytes = 512;               // 128 rows x 4 E8M0 bytes
-  // MXFP8: the activation scales of a stage, 512 bytes per 128 tile rows
-  static constexpr int kSFBSlot = MX8 ? 512 * ((BN + 127) / 128) : 0;
+  // MXFP8 / split: the activation scales of a stage, 512 bytes per 128 tile
+  // rows (per term)
+  static constexpr int kSFBSlot = kTiledSfb ? 512 * ((BN + 127) / 128) * (kSplit ? 2 : 1) : 0;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kABytes;
   static constexpr int kOffSF = kOffB + STAGES * kBBytes;
   static constexpr int kOffSFBs = kOffSF + STAGES * kSFBytes;
   static constexpr int kOffSFB = kOffSFBs + STAGES * kSFBSlot;   // constant scales (W4A8)
   static constexpr int kNumBars = 2 * STAGES + 2 * NB + 1 + NI;
-  static constexpr int kOffBar = kOffSFB + (MX8 ? 0 : 512);
+  static constexpr int kOffBar = kOffSFB + (kTiledSfb ? 0 : 512);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
@@ -86,13 +99,13 @@ struct GemmCfg {
   // accumulator of BN columns per MMA issuer (buffer a, issuer i at column
   // (a * NI + i) * BN); 4 columns of weight scales per stage; activation
   // scales: 8 columns of constants (W4A8, up to 256 tokens) or 8 columns per
-  // stage (MXFP8).
+  // stage (MXFP8: rows 0-127 and 128-255; split: the hi and the lo term).
   // producer, issuers, epilogue, L2 prefetcher
   static constexpr int kIssuer0 = kProdWarps;   // first issuer warp; owns TMEM
   static constexpr int kThreads = 32 * (kProdWarps + NI + kEpiWarps + 1);
   static constexpr int kColSFA = NB * NI * BN;
   static constexpr int kColSFB = kColSFA + 4 * STAGES;
-  static constexpr int kColsUsed = kColSFB + (MX8 ? 8 * STAGES : 8);
+  static constexpr int kColsUsed = kColSFB + (kTiledSfb ? 8 * STAGES : 8);
   static constexpr int kTmemCols = kColsUsed <= 32    ? 32
                                    : kColsUsed <= 64  ? 64
                                    : kColsUsed <= 128 ? 128
@@ -101,8 +114,8 @@ struct GemmCfg {
   static_assert(kColsUsed <= 512, "TMEM budget exceeded");
 };
 
-template <int BN, int STAGES, int NI, int NB, bool SWIGLU, bool MX8>
-__global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
+template <int BN, int STAGES, int NI, int NB, bool SWIGLU, int ACT>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ XMaps tmap_x,
                         const __grid_constant__ CUtensorMap tmap_sf,
@@ -113,7 +126,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
                         uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages,
                         const uint8_t* __restrict__ sfb_tiled,
                         const uint8_t* __restrict__ w_base, int max_tiles) {
-  using C = GemmCfg<BN, STAGES, NI, NB, MX8>;
+  using C = GemmCfg<BN, STAGES, NI, NB, ACT>;
+  // A = E2M1 weights, or E4M3 in MXFP8; B = activations: E4M3
+  constexpr uint32_t kAFmt = ACT == kActMxfp8 ? 0u : 5u;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -159,7 +174,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
   if (warp == C::kIssuer0) tmem_alloc(tmem_slot, C::kTmemCols);
   // W4A8: activation (B) scales are all 1.0 (E8M0 byte 127 everywhere); the
   // per-token scale is applied in the epilogue.
-  if (!MX8)
+  if (!C::kTiledSfb)
     for (int i = threadIdx.x; i < 128; i += blockDim.x)
       reinterpret_cast<uint32_t*>(smem + C::kOffSFB)[i] = 0x7F7F7F7Fu;
   fence_proxy_async_smem();
@@ -169,7 +184,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // Constant activation scales into TMEM once, finished before any issuer
   // (each a different thread) runs an MMA that reads them.
-  if (!MX8 && warp == C::kIssuer0 && lane == 0) {
+  if (!C::kTiledSfb && warp == C::kIssuer0 && lane == 0) {
     const uint64_t sfb_desc = smem_desc(smem_u32(smem + C::kOffSFB), 0, 128, 0);
     tc_cp_32x128b_x4(tmem + C::kColSFB, sfb_desc);
     tc_cp_32x128b_x4(tmem + C::kColSFB + 4, sfb_desc);
@@ -259,16 +274,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
           const int nmma = (td.z + 15) & ~15;
           const int xm = x_map_for(nmma);
           const uint32_t bx = static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u;
-          // MXFP8: the tile's activation scales for this K stage (one 512-byte
-          // block per 128 rows of the MMA-N)
-          const uint32_t sfb_bytes = MX8 ? (nmma > 128 ? 1024u : 512u) : 0u;
-          mbar_arrive_expect_tx(full + s, (LPS == 2 ? bx + 512u : bx) + sfb_bytes);
-          tma_load_2d(smem + C::kOffB + s * C::kBBytes, &tmap_x.m[xm], ks * kTileK, td.y,
-                      full + s);
-          if (MX8)
-            bulk_load(smem + C::kOffSFBs + s * C::kSFBSlot,
-                      sfb_tiled + (static_cast<int64_t>(item / MT) * KS + ks) * kSfbTileBytes,
-                      sfb_bytes, full + s);
+          if constexpr (C::kSplit) {
+            // both terms' boxes (hi at K column 128 ks, lo at K + 128 ks of
+            // the 2K-wide code rows) and scale blocks (tile stages ks and
+            // KS + ks)
+            mbar_arrive_expect_tx(full + s, (LPS == 2 ? 2 * bx + 512u : 2 * bx) + 1024u);
+            uint8_t* b = smem + C::kOffB + s * C::kBBytes;
+            tma_load_2d(b, &tmap_x.m[xm], ks * kTileK, td.y, full + s);
+            tma_load_2d(b + C::kTermBytes, &tmap_x.m[xm], (KS + ks) * kTileK, td.y, full + s);
+            const uint8_t* sb =
+                sfb_tiled + (static_cast<int64_t>(item / MT) * 2 * KS + ks) * kSfbTileBytes;
+            uint8_t* sd = smem + C::kOffSFBs + s * C::kSFBSlot;
+            bulk_load(sd, sb, 512u, full + s);
+            bulk_load(sd + 512, sb + static_cast<int64_t>(KS) * kSfbTileBytes, 512u, full + s);
+          } else {
+            // MXFP8: the tile's activation scales for this K stage (one
+            // 512-byte block per 128 rows of the MMA-N)
+            const uint32_t sfb_bytes = C::kTiledSfb ? (nmma > 128 ? 1024u : 512u) : 0u;
+            mbar_arrive_expect_tx(full + s, (LPS == 2 ? bx + 512u : bx) + sfb_bytes);
+            tma_load_2d(smem + C::kOffB + s * C::kBBytes, &tmap_x.m[xm], ks * kTileK, td.y,
+                        full + s);
+            if (C::kTiledSfb)
+              bulk_load(smem + C::kOffSFBs + s * C::kSFBSlot,
+                        sfb_tiled + (static_cast<int64_t>(item / MT) * KS + ks) * kSfbTileBytes,
+                        sfb_bytes, full + s);
+          }
           if (LPS == 2)
             tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0,
                         static_cast<int32_t>(blk), full + s);
@@ -328,17 +358,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
       const uint64_t sdesc0 = smem_desc(smem_u32(smem + C::kOffSF), 0, 128, 0);
       const uint64_t sbdesc0 = smem_desc(smem_u32(smem + C::kOffSFBs), 0, 128, 0);
       // One stage: weight scales into TMEM, the 4 MMAs of its 128 K (the
-      // first of an item's first stage overwrites the accumulator), and the
-      // commit that frees the slot when they complete.
+      // first of an item's first stage overwrites the accumulator; split:
+      // then the lo term's 4 MMAs into the same accumulator), and the commit
+      // that frees the slot when they complete.
       auto issue_stage = [&](int stage, uint32_t d_tmem, uint32_t id0, int nmma, bool first) {
         const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
         tc_cp_32x128b_x4_warp(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
         uint32_t sfb = tmem + C::kColSFB;
-        if (MX8) {
+        if (C::kTiledSfb) {
           sfb += static_cast<uint32_t>(8 * stage);
           const uint64_t sbd = sbdesc0 + static_cast<uint64_t>(stage * (C::kSFBSlot >> 4));
           tc_cp_32x128b_x4_warp(sfb, sbd);
-          if (nmma > 128) tc_cp_32x128b_x4_warp(sfb + 4, sbd + (512 >> 4));
+          if (C::kSplit || nmma > 128) tc_cp_32x128b_x4_warp(sfb + 4, sbd + (512 >> 4));
         }
         const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
         const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
@@ -346,6 +377,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
         for (uint32_t kk = 0; kk < 4; ++kk)
           tc_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
                          sfb, (!first || kk > 0) ? 1u : 0u);
+        if constexpr (C::kSplit) {
+          const uint64_t bl = bd + static_cast<uint64_t>(C::kTermBytes >> 4);
+#pragma unroll
+          for (uint32_t kk = 0; kk < 4; ++kk)
+            tc_mma_mx_warp(d_tmem, ad + 2 * kk, bl + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
+                           sfb + 4, 1u);
+        }
         tc_commit_warp(empty + stage);
       };
       if constexpr (NI == 1) {
@@ -360,7 +398,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
              item += static_cast<int>(gridDim.x), ++it) {
           const int4 td = checked_tile(tiles, item / MT, BN, status, lim);
           const int nmma = (td.z + 15) & ~15;
-          const uint32_t id0 = idesc_mx(MX8 ? 0 : 5, 0, static_cast<uint32_t>(nmma), 0, 0);
+          const uint32_t id0 = idesc_mx(kAFmt, 0, static_cast<uint32_t>(nmma), 0, 0);
           const int acc = it % NB;
           if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
                               status, kDevTimeout, abort_flag))
@@ -395,8 +433,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
             const int item = blockIdx.x + it * gridDim.x;
             const int4 td = checked_tile(tiles, item / MT, BN, status, lim);
             nmma = (td.z + 15) & ~15;
-            // A = weights: E2M1, or E4M3 in MXFP8; B = activations: E4M3
-            id0 = idesc_mx(MX8 ? 0 : 5, 0, static_cast<uint32_t>(nmma), 0, 0);
+            id0 = idesc_mx(kAFmt, 0, static_cast<uint32_t>(nmma), 0, 0);
             acc = it % NB;
             if (!mbar_wait_warp(tempty + acc, static_cast<uint32_t>((it / NB) & 1) ^ 1u, timeout_ns,
                                 status, kDevTimeout, abort_flag))
@@ -489,10 +526,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, MX8>::kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, int NI, int NB, bool SWIGLU, bool MX8>
+template <int BN, int STAGES, int NI, int NB, bool SWIGLU, int ACT>
 cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
-  using C = GemmCfg<BN, STAGES, NI, NB, MX8>;
-  auto kern = grouped_gemm_kernel<BN, STAGES, NI, NB, SWIGLU, MX8>;
+  using C = GemmCfg<BN, STAGES, NI, NB, ACT>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, NI, NB, SWIGLU, ACT>;
   static DeviceOnce smem_set;   // per instantiation and device
   const cudaError_t e = set_smem_limit_once(kern, C::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -526,7 +563,30 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
   X(4, kPrefillBN, 4, 2, 1, 4, 2)     \
   X(5, kMidBN, 6, 1, 2, 6, 1)
 
-int gemm_tile_tokens(int variant) {
+// The split activations (W4A16) carry two terms per stage, so their tiles
+// stop at kW4A16BN tokens: variants 1 and 3 keep their tile size with
+// <BN, stages, issuers, buffers> below; 2, 4, 5 and 6 run the 64-token tile.
+#define MOE_SPLIT_VARIANTS(X)  \
+  X(3, kTinyBN, 10, 5, 2)      \
+  X(1, kDecodeBN, 8, 4, 2)     \
+  X(5, kW4A16BN, 6, 3, 2)
+
+namespace {
+int split_variant(int variant) { return variant == 1 || variant == 3 ? variant : 5; }
+}  // namespace
+
+int gemm_tile_tokens(int variant, int act) {
+  if (act == kActSplit) {
+    switch (split_variant(variant)) {
+#define MOE_S(v, bn, st, ni, nb) \
+  case v:                        \
+    return bn;
+      MOE_SPLIT_VARIANTS(MOE_S)
+#undef MOE_S
+      default:
+        return kW4A16BN;
+    }
+  }
   if (variant == 6) return kPairBN;
   switch (variant) {
 #define MOE_X(v, bn, st, ni, nb, st8, ni8) \
@@ -540,22 +600,34 @@ int gemm_tile_tokens(int variant) {
 }
 
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s) {
+  if (a.act == kActSplit) {
+    switch (split_variant(variant)) {
+#define MOE_S(v, bn, st, ni, nb)                                              \
+  case v:                                                                     \
+    return swiglu ? launch_variant<bn, st, ni, nb, true, kActSplit>(a, s)     \
+                  : launch_variant<bn, st, ni, nb, false, kActSplit>(a, s);
+      MOE_SPLIT_VARIANTS(MOE_S)
+#undef MOE_S
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   // Variant 6: CTA pairs where the operands allow (W4A8, an even number of
   // M-tiles), else the one-CTA kernel with the same 160-token tiles.
   static_assert(kPairBN == kMidBN, "variant 6 falls back to variant 5's tile size");
   if (variant == 6) {
-    if (gemm_pair_supported(a.m_per_expert, a.mx8) && a.tmap_x_pair && a.num_sms >= 2)
+    if (gemm_pair_supported(a.m_per_expert, a.act) && a.tmap_x_pair && a.num_sms >= 2)
       return launch_gemm_pair(swiglu, a, s);
     variant = 5;
   }
   switch (variant) {
 #define MOE_X(v, bn, st, ni, nb, st8, ni8)                                        \
   case v:                                                                         \
-    if (a.mx8)                                                                    \
-      return swiglu ? launch_variant<bn, st8, ni8, nb, true, true>(a, s)          \
-                    : launch_variant<bn, st8, ni8, nb, false, true>(a, s);        \
-    return swiglu ? launch_variant<bn, st, ni, nb, true, false>(a, s)             \
-                  : launch_variant<bn, st, ni, nb, false, false>(a, s);
+    if (a.act == kActMxfp8)                                                       \
+      return swiglu ? launch_variant<bn, st8, ni8, nb, true, kActMxfp8>(a, s)     \
+                    : launch_variant<bn, st8, ni8, nb, false, kActMxfp8>(a, s);   \
+    return swiglu ? launch_variant<bn, st, ni, nb, true, kActFp8Row>(a, s)        \
+                  : launch_variant<bn, st, ni, nb, false, kActFp8Row>(a, s);
     MOE_GEMM_VARIANTS(MOE_X)
 #undef MOE_X
     default:

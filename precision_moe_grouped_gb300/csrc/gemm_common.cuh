@@ -1,6 +1,6 @@
-// gemm_common.cuh -- pieces shared by the grouped GEMM kernels (gemm.cu:
-// block-scaled FP8 operands; gemm_bf16.cu: the W4A16 mode): the activation
-// tensor-map set and the TMEM -> registers -> global epilogue.
+// gemm_common.cuh -- pieces shared by the grouped GEMM kernels (gemm.cu: one
+// CTA per tile; gemm_pair.cu: CTA pairs): the activation tensor-map set and
+// the TMEM -> registers -> global epilogue.
 //
 // Pages cited (title and section):
 //   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add

@@ -420,12 +420,12 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-bool gemm_pair_supported(int m_per_expert, bool mx8) {
-  return !mx8 && m_per_expert % (2 * kTileM) == 0;
+bool gemm_pair_supported(int m_per_expert, int act) {
+  return act == kActFp8Row && m_per_expert % (2 * kTileM) == 0;
 }
 
 cudaError_t launch_gemm_pair(bool swiglu, const GemmArgs& a, cudaStream_t s) {
-  if (!gemm_pair_supported(a.m_per_expert, a.mx8) || a.num_sms < 2 || !a.tmap_x_pair)
+  if (!gemm_pair_supported(a.m_per_expert, a.act) || a.num_sms < 2 || !a.tmap_x_pair)
     return cudaErrorInvalidValue;
   return swiglu ? launch_pair<kPairBN, kPairStages, 2, true>(a, s)
                 : launch_pair<kPairBN, kPairStages, 2, false>(a, s);

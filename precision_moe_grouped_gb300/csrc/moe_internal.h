@@ -102,7 +102,7 @@ constexpr int kDecodeBN = 32;        // max tokens per tile, decode variant
 constexpr int kTinyBN = 16;          // max tokens per tile, 16-token decode variant
 constexpr int kPrefillBN = 224;      // max tokens per tile, prefill variant
 constexpr int kMidBN = 160;          // max tokens per tile, 6-stage prefill variant
-constexpr int kW4A16BN = 64;         // max tokens per tile of the W4A16 GEMM
+constexpr int kW4A16BN = 64;         // max tokens per tile of the split (W4A16) GEMM
 
 // Activation box heights (rows) of the GEMM's activation tensor maps:
 // 16, 32, 64, 96, ..., 224.
@@ -142,7 +142,23 @@ __host__ __device__ inline bool tile_entry_ok(int x, int y, int z, int w, int bn
   return x >= 0 && x < E && z >= 1 && z <= bn && y >= 0 && y <= R - z && w == 0;
 }
 
-// MXFP8 mode: the activation (B operand) scale bytes are written by the
+// Activation encodings written by the expansion and h-quantisation kernels
+// and read by the GEMMs:
+//   kActFp8Row: E4M3 codes, one float scale per row (W4A8; the GEMM's weights
+//               are E2M1);
+//   kActMxfp8:  E4M3 codes, one E8M0 byte per 32 elements (W8A8; E4M3
+//               weights);
+//   kActSplit:  two MXFP8 terms per element -- hi, then the residual lo --
+//               in rows of 2K codes (W4A16: bf16 activations on the FP8
+//               tensor cores; E2M1 weights).
+enum ActQuant : int { kActFp8Row = 0, kActMxfp8 = 1, kActSplit = 2 };
+// K stages (of kTileK) that one row's codes span in the per-tile scale
+// layout below: K / kTileK, twice that for the split.
+__host__ __device__ constexpr int act_k_stages(int act, int K) {
+  return (act == kActSplit ? 2 : 1) * (K / kTileK);
+}
+
+// MXFP8 and split activations: the (B operand) scale bytes are written by the
 // quantisers straight into the GEMM's per-tile layout.  For tile t of the
 // GEMM tile list and K stage ks there is one kSfbTileBytes block at
 // (t * KS + ks) * kSfbTileBytes; tile row n's four scale bytes (K blocks
@@ -176,8 +192,8 @@ struct GemmArgs {
   uint32_t a_tx_bytes;         // transaction bytes one weight TMA box counts
   int32_t num_sms;
   int32_t prefetch_stages;     // L2 prefetch distance of weight tiles, in K stages
-  bool mx8;                    // MXFP8 operands: E4M3 weights, per-32 activation scales
-  const uint8_t* sfb_tiled;    // MXFP8: activation scales in the per-tile layout
+  int32_t act;                 // ActQuant of the activations (and so the weights' type)
+  const uint8_t* sfb_tiled;    // MXFP8 / split: activation scales in the per-tile layout
   const uint8_t* w_base;       // prepared weight boxes (for the optional L2 prefetcher)
   const CUtensorMap* tmap_x_pair;  // kNumXMaps maps, box heights kPairBoxRowsAt (or null)
   int32_t max_tiles;           // entries the tile list's allocation holds
@@ -185,17 +201,16 @@ struct GemmArgs {
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
                          int32_t* chunk_counts, int32_t* status, cudaStream_t s);
-// Activation outputs of the expansion kernels, by mode.  W4A8: FP8 codes
-// xq and x_scale (per-row float).  MXFP8 (mx8): codes, x_sf (row-major scale
-// bytes [R, H/32]) and sfb (per-tile layout above).  W4A16 (bf16_copy): xq
-// receives the rows' bf16 values unchanged (2 bytes per element).
+// Activation outputs of the expansion kernels, by encoding.  kActFp8Row:
+// FP8 codes xq [R, H] and x_scale (per-row float).  kActMxfp8: codes, x_sf
+// (row-major scale bytes [R, H/32]) and sfb (per-tile layout above).
+// kActSplit: codes [R, 2H], x_sf [R, 2H/32] and sfb.
 struct QuantOut {
   uint8_t* xq;
   float* x_scale;
-  bool mx8;
+  int act;
   uint8_t* x_sf;
   uint8_t* sfb;
-  bool bf16_copy;
 };
 cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, int E, int k,
                                      int H, int bn, int32_t* ids, float* wts, int32_t* counts,
@@ -223,28 +238,24 @@ cudaError_t launch_quant_scatter(const void* x, const int32_t* chunk_base, const
                                  const QuantOut& q, cudaStream_t s);
 cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_scale,
                           cudaStream_t s);
-// MXFP8 quantisation of h: codes, row-major scale bytes [R, I/32] and the
-// per-tile scale layout of GEMM2.
-cudaError_t launch_hquant_mx(const void* h, int R, int I, const int32_t* ids,
+// MXFP8 quantisation (act kActMxfp8) or two-term split (kActSplit) of h:
+// codes, row-major scale bytes and the per-tile scale layout of GEMM2.
+cudaError_t launch_hquant_mx(int act, const void* h, int R, int I, const int32_t* ids,
                              const int32_t* token_slot, const int32_t* offsets,
                              const int2* tile_plan, uint8_t* hq, uint8_t* h_sf, uint8_t* sfb,
                              cudaStream_t s);
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
                            int H, void* out, cudaStream_t s);
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);
-// The W4A16 GEMM (tiles of <= kW4A16BN tokens; tmap_w over the packed
-// weight boxes as bytes, tmap_x over bf16 activations with 64-element
-// boxes; row_scale, mx8 and sfb_tiled unused).
-cudaError_t launch_gemm_bf16(bool swiglu, const GemmArgs& a, cudaStream_t s);
 // The grouped GEMM on CTA pairs (gemm_pair.cu): W4A8 operands, M-tiles
 // taken two at a time, so m_per_expert must be a multiple of 256; needs
 // tmap_x_pair.
-bool gemm_pair_supported(int m_per_expert, bool mx8);
+bool gemm_pair_supported(int m_per_expert, int act);
 cudaError_t launch_gemm_pair(bool swiglu, const GemmArgs& a, cudaStream_t s);
 // Tile variants 1..kMaxTileVariant; the largest token tile of each (the tile
 // list is built with this bound).
 constexpr int kMaxTileVariant = 6;
-int gemm_tile_tokens(int variant);
+int gemm_tile_tokens(int variant, int act);
 // Re-lays one weight tensor [E, M, K] (E2M1 with K/2 bytes per row, or E4M3
 // with K bytes per row when fp8) and its scales [E, M, K/32] for the GEMM;
 // swiglu_I > 0 applies GEMM1's gate/up row interleave (M = 2 * swiglu_I).

@@ -441,49 +441,53 @@ __device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k
 // go to the k expanded rows; scale bytes to the row-major x_sf [R, H/32] and
 // to the GEMM's per-tile layout at sfb_base[j] + (b / 4) * kSfbTileBytes +
 // b % 4 for block b of row rows[j].
+// SPLIT (the W4A16 mode): the two-term split of each block (split_block),
+// in rows of 2H codes -- hi blocks in columns [0, H), lo blocks in [H, 2H)
+// -- whose scale bytes follow the same order (block H/32 + b is b's lo
+// term), in x_sf [R, 2H/32] and in the per-tile layout of 2H/128 K stages.
+template <bool SPLIT>
 __device__ void quantize_token_mx(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
                                   const int32_t* rows, const int64_t* sfb_base,
                                   uint8_t* __restrict__ xq, uint8_t* __restrict__ x_sf,
                                   uint8_t* __restrict__ sfb) {
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
   const int nblk = H / 32;
+  const int64_t W = SPLIT ? 2 * H : H, nsf = SPLIT ? 2 * nblk : nblk;
   for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
     uint4 q[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) q[i] = __ldg(xr + 4 * b + i);
-    uint8_t sbyte;
-    uint4 codes[2];
-    mx_quant_block(q, &sbyte, codes);
+    uint8_t sbyte, lbyte = 0;
+    uint4 codes[2], lcodes[2];
+    if constexpr (SPLIT)
+      split_block(q, &sbyte, codes, &lbyte, lcodes);
+    else
+      mx_quant_block(q, &sbyte, codes);
     for (int j = 0; j < k; ++j) {
       const int64_t r = rows[j];
-      uint4* dst = reinterpret_cast<uint4*>(xq + r * H + 32 * b);
+      uint4* dst = reinterpret_cast<uint4*>(xq + r * W + 32 * b);
       dst[0] = codes[0];
       dst[1] = codes[1];
-      x_sf[r * nblk + b] = sbyte;
+      x_sf[r * nsf + b] = sbyte;
       sfb[sfb_base[j] + static_cast<int64_t>(b >> 2) * kSfbTileBytes + (b & 3)] = sbyte;
+      if constexpr (SPLIT) {
+        uint4* ldst = reinterpret_cast<uint4*>(xq + r * W + H + 32 * b);
+        ldst[0] = lcodes[0];
+        ldst[1] = lcodes[1];
+        const int lb = nblk + b;
+        x_sf[r * nsf + lb] = lbyte;
+        sfb[sfb_base[j] + static_cast<int64_t>(lb >> 2) * kSfbTileBytes + (lb & 3)] = lbyte;
+      }
     }
   }
 }
 
-// W4A16: the token's bf16 row copied unchanged into its k expanded rows.
-__device__ void copy_token(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
-                           const int32_t* rows, __nv_bfloat16* __restrict__ xb) {
-  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
-  const int nvec = H / 8;
-  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
-    const uint4 v = __ldg(xr + i);
-    for (int j = 0; j < k; ++j)
-      reinterpret_cast<uint4*>(xb + static_cast<size_t>(rows[j]) * H)[i] = v;
-  }
-}
-
-// One CTA per token t: the rows of its k slots, then the FP8 quantisation
-// of the token into them (MX: MXFP8; COPY: the bf16 copy of the W4A16
-// mode).  Slot j's row is the chunk's base row for its expert e (from the
+// One CTA per token t: the rows of its k slots, then the quantisation of
+// the token into them (AQ: per-row FP8, MXFP8 or the two-term split).  Slot j's row is the chunk's base row for its expert e (from the
 // scan) plus the number of the chunk's earlier tokens routed to e -- the
 // stable, ascending-token order inside each expert (a token's k experts are
 // distinct).  The CTA writes row_of and token_slot for its slots.
-template <bool MX, bool COPY = false>
+template <int AQ>
 __global__ void __launch_bounds__(256) quant_scatter_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ chunk_base,
     const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets,
@@ -519,15 +523,14 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     rows[j] = r;
     row_of[ts] = r;
     token_slot[r] = static_cast<int32_t>(ts);
-    if (MX) sfb_base[j] = sfb_row_base(r, offsets[e], tile_plan[e], H / kTileK);
+    if (AQ != kActFp8Row)
+      sfb_base[j] = sfb_row_base(r, offsets[e], tile_plan[e], act_k_stages(AQ, H));
   }
   __syncthreads();
-  if (COPY)
-    copy_token(x, t, k, H, rows, reinterpret_cast<__nv_bfloat16*>(xq));
-  else if (MX)
-    quantize_token_mx(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
-  else
+  if constexpr (AQ == kActFp8Row)
     quantize_token<2>(x, t, k, H, rows, warp_max, xq, x_scale);   // 256 threads
+  else
+    quantize_token_mx<AQ == kActSplit>(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
 }
 
 // Small batches (T <= kSmallT = 256): one kernel replaces scan +
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
 // quantises its token into them.  CTA 0 also writes counts, offsets and the
 // GEMM tile list.  The redundant O(T*k) counting per CTA is cheap at these
 // sizes and removes three launches from the decode path.
-template <bool MX, bool COPY = false>
+template <int AQ>
 __global__ void __launch_bounds__(1024) expand_small_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids, int T, int E, int k,
     int H, int bn, int32_t* __restrict__ counts_out, int32_t* __restrict__ offsets_out,
@@ -577,7 +580,7 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
   const ExpertPlan pl = plan_experts(e, E, c, bn, t == 0, tiles, num_tiles, tile_plan);
   const int off = pl.off, total_rows = pl.total_rows;
   if (e < E) cnt[e] = off;     // cnt now holds the offsets
-  if (MX && e < E) plan[e] = make_int2(pl.toff, pl.tsz);
+  if (AQ != kActFp8Row && e < E) plan[e] = make_int2(pl.toff, pl.tsz);
   __syncthreads();
   if (e < k) {
     const size_t ts = static_cast<size_t>(t) * k + e;
@@ -594,14 +597,13 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
     if (e == 0) offsets_out[E] = total_rows;
   }
   __syncthreads();
-  if (COPY) {
-    copy_token(x, t, k, H, rows, reinterpret_cast<__nv_bfloat16*>(xq));
-  } else if (MX) {
-    if (e < k) sfb_base[e] = sfb_row_base(rows[e], cnt[my_e[e]], plan[my_e[e]], H / kTileK);
-    __syncthreads();
-    quantize_token_mx(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
-  } else {
+  if constexpr (AQ == kActFp8Row) {
     quantize_token<1>(x, t, k, H, rows, warp_max, xq, x_scale);   // 1024 threads
+  } else {
+    if (e < k)
+      sfb_base[e] = sfb_row_base(rows[e], cnt[my_e[e]], plan[my_e[e]], act_k_stages(AQ, H));
+    __syncthreads();
+    quantize_token_mx<AQ == kActSplit>(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
   }
 }
 
@@ -749,9 +751,9 @@ cudaError_t launch_quant_scatter(const void* x, const int32_t* chunk_base, const
                                  const int32_t* offsets, const int2* tile_plan, int T, int E,
                                  int k, int H, int32_t* row_of, int32_t* token_slot,
                                  const QuantOut& q, cudaStream_t s) {
-  auto kern = q.bf16_copy ? quant_scatter_kernel<false, true>
-              : q.mx8     ? quant_scatter_kernel<true>
-                          : quant_scatter_kernel<false>;
+  auto kern = q.act == kActSplit    ? quant_scatter_kernel<kActSplit>
+              : q.act == kActMxfp8 ? quant_scatter_kernel<kActMxfp8>
+                                   : quant_scatter_kernel<kActFp8Row>;
   return launch_pdl(kern, dim3(T), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(x),
                     chunk_base, ids, offsets, tile_plan, E, k, H, row_of, token_slot, q.xq,
                     q.x_scale, q.x_sf, q.sfb);
@@ -763,9 +765,9 @@ cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E,
                                 int32_t* token_slot, const QuantOut& q, cudaStream_t s) {
   // plan int2[E], cnt[E], my_e/my_rank/rows [32] each
   const size_t smem = static_cast<size_t>(3 * E + 96) * sizeof(int32_t);
-  auto kern = q.bf16_copy ? expand_small_kernel<false, true>
-              : q.mx8     ? expand_small_kernel<true>
-                          : expand_small_kernel<false>;
+  auto kern = q.act == kActSplit    ? expand_small_kernel<kActSplit>
+              : q.act == kActMxfp8 ? expand_small_kernel<kActMxfp8>
+                                   : expand_small_kernel<kActFp8Row>;
   return launch_pdl(kern, dim3(T), dim3(1024), smem, s, static_cast<const __nv_bfloat16*>(x),
                     ids, T, E, k, H, bn, counts, offsets, tiles, num_tiles, tile_plan, row_of,
                     token_slot, q.xq, q.x_scale, q.x_sf, q.sfb);

@@ -36,10 +36,14 @@ __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __rest
   hquant_row_warp(h, warp, I, hq, h_scale, threadIdx.x & 31);
 }
 
-// MXFP8 (the W8A8 mode) quantisation of h: one warp per expanded row r,
-// lane l converts the 32-element blocks l, l + 32, ...; codes to hq, scale
-// bytes to the row-major h_sf [R, I/32] and to GEMM2's per-tile layout
-// (row r's expert from its (token, slot), its tile from the expert's plan).
+// MXFP8 (the W8A8 mode) quantisation of h, or (SPLIT, the W4A16 mode) its
+// two-term split: one warp per expanded row r, lane l converts the
+// 32-element blocks l, l + 32, ...; codes to hq (rows of I codes, or 2I
+// with the lo terms in columns [I, 2I)), scale bytes to the row-major h_sf
+// [R, I/32] (or [R, 2I/32], lo blocks after the hi blocks) and to GEMM2's
+// per-tile layout (row r's expert from its (token, slot), its tile from the
+// expert's plan).
+template <bool SPLIT>
 __global__ void __launch_bounds__(256) hquant_mx_kernel(
     const __nv_bfloat16* __restrict__ h, int R, int I, const int32_t* __restrict__ ids,
     const int32_t* __restrict__ token_slot, const int32_t* __restrict__ offsets,
@@ -51,21 +55,34 @@ __global__ void __launch_bounds__(256) hquant_mx_kernel(
   const int lane = threadIdx.x & 31;
   if (r >= R) return;
   const int e = ids[token_slot[r]];
-  const int64_t base = sfb_row_base(r, offsets[e], tile_plan[e], I / kTileK);
+  const int64_t base =
+      sfb_row_base(r, offsets[e], tile_plan[e], act_k_stages(SPLIT ? kActSplit : kActMxfp8, I));
   const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(r) * I);
   const int nblk = I / 32;
+  const int64_t W = SPLIT ? 2 * I : I, nsf = SPLIT ? 2 * nblk : nblk;
   for (int b = lane; b < nblk; b += 32) {
     uint4 q[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = __ldg(hr + 4 * b + i);
-    uint8_t sbyte;
-    uint4 codes[2];
-    mx_quant_block(q, &sbyte, codes);
-    uint4* dst = reinterpret_cast<uint4*>(hq + static_cast<size_t>(r) * I + 32 * b);
+    for (int i = 0; i < 4; ++i) q[i] = __ldcg(hr + 4 * b + i);
+    uint8_t sbyte, lbyte = 0;
+    uint4 codes[2], lcodes[2];
+    if constexpr (SPLIT)
+      split_block(q, &sbyte, codes, &lbyte, lcodes);
+    else
+      mx_quant_block(q, &sbyte, codes);
+    uint4* dst = reinterpret_cast<uint4*>(hq + r * W + 32 * b);
     dst[0] = codes[0];
     dst[1] = codes[1];
-    h_sf[static_cast<size_t>(r) * nblk + b] = sbyte;
+    h_sf[r * nsf + b] = sbyte;
     sfb[base + static_cast<int64_t>(b >> 2) * kSfbTileBytes + (b & 3)] = sbyte;
+    if constexpr (SPLIT) {
+      uint4* ldst = reinterpret_cast<uint4*>(hq + r * W + I + 32 * b);
+      ldst[0] = lcodes[0];
+      ldst[1] = lcodes[1];
+      const int lb = nblk + b;
+      h_sf[r * nsf + lb] = lbyte;
+      sfb[base + static_cast<int64_t>(lb >> 2) * kSfbTileBytes + (lb & 3)] = lbyte;
+    }
   }
 }
 
@@ -115,13 +132,14 @@ cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_sca
                     static_cast<const __nv_bfloat16*>(h), R, I, hq, h_scale);
 }
 
-cudaError_t launch_hquant_mx(const void* h, int R, int I, const int32_t* ids,
+cudaError_t launch_hquant_mx(int act, const void* h, int R, int I, const int32_t* ids,
                              const int32_t* token_slot, const int32_t* offsets,
                              const int2* tile_plan, uint8_t* hq, uint8_t* h_sf, uint8_t* sfb,
                              cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   const int blocks = (R + 7) / 8;
-  return launch_pdl(hquant_mx_kernel, dim3(blocks), dim3(256), 0, s,
+  auto kern = act == kActSplit ? hquant_mx_kernel<true> : hquant_mx_kernel<false>;
+  return launch_pdl(kern, dim3(blocks), dim3(256), 0, s,
                     static_cast<const __nv_bfloat16*>(h), R, I, ids, token_slot, offsets,
                     tile_plan, hq, h_sf, sfb);
 }

@@ -78,6 +78,8 @@ class GpuRun:
         self.status = P.read_device_status(self.ws)
         self.L = P.workspace_layout(s, mode)
         self.T, self.E, self.k, self.H, self.I, self.R = T, E, k, H, I, T * k
+        # W4A16: the activations and h are stored as two FP8 terms (hi | lo)
+        self.terms = 2 if mode == MI.QUANT_W4A16 else 1
 
     def _view(self, off, n, dtype):
         nbytes = n * torch.tensor([], dtype=dtype).element_size()
@@ -115,7 +117,9 @@ class GpuRun:
 
     @property
     def xq(self):
-        return self._view(self.L.xq, self.R * self.H, torch.uint8).numpy().reshape(self.R, self.H)
+        """FP8 codes of the expanded rows, [R, H] (W4A16: [R, 2H], hi | lo)."""
+        w = self.terms * self.H
+        return self._view(self.L.xq, self.R * w, torch.uint8).numpy().reshape(self.R, w)
 
     @property
     def x_scale(self):
@@ -126,13 +130,17 @@ class GpuRun:
 
     @property
     def x_sf(self):
-        """MXFP8 mode: E8M0 block scales of xq, [R, H/32]."""
-        return self.bytes_("x_sf", self.R * self.H // 32).reshape(self.R, self.H // 32)
+        """MXFP8 and W4A16 modes: E8M0 block scales of xq, [R, H/32] (W4A16:
+        [R, 2H/32])."""
+        n = self.terms * self.H // 32
+        return self.bytes_("x_sf", self.R * n).reshape(self.R, n)
 
     @property
     def h_sf(self):
-        """MXFP8 mode: E8M0 block scales of hq, [R, I/32]."""
-        return self.bytes_("h_sf", self.R * self.I // 32).reshape(self.R, self.I // 32)
+        """MXFP8 and W4A16 modes: E8M0 block scales of hq, [R, I/32] (W4A16:
+        [R, 2I/32])."""
+        n = self.terms * self.I // 32
+        return self.bytes_("h_sf", self.R * n).reshape(self.R, n)
 
     @property
     def tile_plan(self):
@@ -145,7 +153,8 @@ class GpuRun:
 
     @property
     def hq(self):
-        return self._view(self.L.hq, self.R * self.I, torch.uint8).numpy().reshape(self.R, self.I)
+        w = self.terms * self.I
+        return self._view(self.L.hq, self.R * w, torch.uint8).numpy().reshape(self.R, w)
 
     @property
     def h_scale(self):

@@ -132,7 +132,8 @@ def test_forward_validation_without_gpu(lib):
     mis[2] += 32                                        # w1 not 256-byte aligned
     assert _fwd(lib, s, mis, need) == L.MOE_ERR_MISALIGNED
     assert _fwd(lib, s, good, need - 1) == L.MOE_ERR_WORKSPACE_TOO_SMALL
-    # W4A16 keeps bf16 expanded rows: the W4A8 workspace is too small for it
+    # W4A16 keeps two FP8 terms per expanded element: the W4A8 workspace is
+    # too small for it
     assert P.workspace_size(s, 1) > need
     assert _fwd(lib, s, good, need, mode=1) == L.MOE_ERR_WORKSPACE_TOO_SMALL
     assert _fwd(lib, s, good, need, mode=2) == L.MOE_ERR_WORKSPACE_TOO_SMALL

@@ -26,12 +26,14 @@ def test_gemm_bytes_per_mode():
     assert f == 2.0 * R * H * 2 * I
     # W8A8: E4M3 weights, activations with one scale byte per 32, no row scale
     b, f = bench.alg_cost("gemm2", cfg, T, E, mode=2)
-    assert b == E * H * I * (1 + 1 / 32) + R * I * (1 + 1 / 32) + R * 4 + R * H * 2
+    assert b == E * H * I * (1 + 1 / 32) + R * I * (1 + 1 / 32) + R * H * 2
     assert f == 2.0 * R * I * H
-    # W4A16: bf16 activations, no h quantisation at all
+    # W4A16: each bf16 activation (and element of h) as two E4M3 terms, each
+    # term with one scale byte per 32; no row scale
     b, _ = bench.alg_cost("gemm1", cfg, T, E, mode=1)
-    assert b == E * 2 * I * H * (0.5 + 1 / 32) + R * H * 2 + R * I * 2
-    assert bench.alg_cost("hquant", cfg, T, E, mode=1) == (0, 0)
+    assert b == E * 2 * I * H * (0.5 + 1 / 32) + R * H * (2 + 2 / 32) + R * I * 2
+    b, _ = bench.alg_cost("hquant", cfg, T, E, mode=1)
+    assert b == R * I * 2 + R * I * (2 + 2 / 32)
 
 
 @pytest.mark.parametrize("mode,w_bytes,peak", [(0, 0.5, 2 * 2000.0), (1, 0.5, 2000.0),

@@ -1,8 +1,11 @@
-"""GPU parity of the W4A16 mode (MXFP4 weights x bf16 activations fed
-unquantised) against the CPU oracle on the same seeded inputs.
+"""GPU parity of the W4A16 mode (MXFP4 weights x bf16 activations) against
+the CPU oracle on the same seeded inputs.  The device carries each bf16
+activation (and each element of h) into the FP8 tensor cores as two MXFP8
+terms; the oracle's forward is the exact bf16 product.
 
-Bit-exact: routing, expansion and the expanded bf16 activation rows (a
-copy).  Floating point (h, y, output): max|err| <= 2e-2 * max|ref| and
+Bit-exact: routing, expansion, and the two-term codes and scale bytes of
+the expanded rows and of h (against the oracle's split of the same bf16
+values).  Floating point (h, y, output): max|err| <= 2e-2 * max|ref| and
 sum|err| / sum|ref| <= 5e-3."""
 import numpy as np
 import pytest
@@ -38,9 +41,14 @@ def w16_parity(case, name="w16"):
         np.testing.assert_array_equal(run.offsets, rt.offsets)
         np.testing.assert_array_equal(run.row_of, rt.row_of)
         np.testing.assert_array_equal(run.token_slot // run.k, rt.token_of_row)
-        # the expanded activations are the tokens' bf16 rows, bit for bit
-        xb = run._view(run.L.xq, run.R * run.H, torch.int16).numpy().reshape(run.R, run.H)
-        np.testing.assert_array_equal(xb.view(np.uint16), x_bits(case)[rt.token_of_row])
+        # the expanded rows: the two-term split of the tokens' bf16 rows
+        xc, xs = M.split_rows_mxfp8x2(case.x.float().cpu().numpy()[rt.token_of_row])
+        np.testing.assert_array_equal(run.xq, xc)
+        np.testing.assert_array_equal(run.x_sf, xs)
+        # GEMM2's operand: the split of the GPU's own h
+        hc, hs = M.split_rows_mxfp8x2(run.h)
+        np.testing.assert_array_equal(run.hq, hc)
+        np.testing.assert_array_equal(run.h_sf, hs)
         for label, got, ref in (("h", run.h, fw.h), ("y", run.y, fw.y),
                                 ("out", run.out_np(), fw.out)):
             ok, st = max_err_ok(got, ref)
@@ -90,3 +98,15 @@ def test_w16_large_batch_expansion():
     (scan, scatter) instead of the one-kernel small-batch path."""
     run, _ = w16_parity(MI.make_case(_cfg(8, 2, 256, 128), 1500, seed=5), name="w16_large")
     assert run.T > P._lib.MOE_SMALL_BATCH_TOKENS
+
+
+def test_w16_wide_dynamic_range():
+    """Rows whose elements span 2^-40 .. 2^8 inside each 32-block, so many
+    fall below the split's exact range (2^-13 of the block maximum): the
+    codes still match the oracle's split bit for bit, and the outputs stay
+    within the tolerance of the exact bf16 product."""
+    case = MI.make_case(_cfg(8, 2, 256, 128), 40, seed=17)
+    g = torch.Generator().manual_seed(3)
+    mag = torch.pow(2.0, torch.randint(-40, 9, case.x.shape, generator=g).float())
+    case.x = (case.x.float() * mag).to(torch.bfloat16)
+    w16_parity(case, name="w16_wide")
