@@ -38,8 +38,9 @@
 // handed out statically (item = CTA + i * grid) from the device-built tile
 // list, so nothing returns to the host.
 //
-// Roles: warps 0..2 = TMA producers (three lanes per stage, stage s in warp
-// s % 3); the next NI warps = MMA issuers (one elected lane each; the first
+// Roles: the first warps = TMA producers (one warp per pipeline stage --
+// three for the MXFP8 prefill tiles -- three lanes per stage); the next NI
+// warps = MMA issuers (one elected lane each; the first
 // also owns the TMEM allocation); the next 8 warps = epilogue (warp w reads
 // TMEM lanes 32*(w%4) .. +31; two warps per lane quarter split the
 // columns); the last warp = optional L2 prefetcher.  Two TMEM accumulator
@@ -68,12 +69,16 @@ struct GemmCfg {
   static constexpr bool kTiledSfb = ACT != kActFp8Row;   // per-tile activation scales
   static constexpr bool kSplit = ACT == kActSplit;       // two activation terms per stage
   static_assert(!kSplit || BN <= 128, "a split stage holds one 512-byte scale block per term");
-  // Producer warps: stage s is served by warp s % kProdWarps (lanes of one
-  // warp spinning on different stages' barriers serialise; three warps
-  // measured 9% less time per stage than one in a producer-only benchmark),
-  // with three lanes per stage (weight, activation and scale copies), or two
-  // (the scale copy rides with the activation) if three do not fit a warp.
-  static constexpr int kProdWarps = STAGES >= 3 ? 3 : STAGES;
+  // Producer warps: stage s is served by warp s % kProdWarps, with three
+  // lanes per stage (weight, activation and scale copies), or two (the scale
+  // copy rides with the activation) if three do not fit a warp.  Lanes of one
+  // warp waiting on different stages' barriers serialise, so each stage gets
+  // its own warp (against three warps sharing the stages: DSV3 T=1 54.5 ->
+  // 51.9 us, T=512 981 -> 941 us, T=4096 1566 -> 1548 us, W4A16 T=256 77.4
+  // -> 73.3 us); the MXFP8 prefill tiles keep three warps (2144 -> 2183 us
+  // with one per stage).
+  static constexpr int kProdWarps =
+      ACT == kActMxfp8 && NI == 1 ? (STAGES >= 3 ? 3 : STAGES) : STAGES;
   static constexpr int kStagesPerWarp = (STAGES + kProdWarps - 1) / kProdWarps;
   static constexpr int kLanesPerStage = 3 * kStagesPerWarp <= 32 ? 3 : 2;
   static_assert(kLanesPerStage * kStagesPerWarp <= 32, "producer lanes must fit a warp");
