@@ -173,10 +173,8 @@ void compute_layout(const moe_shape* s, int32_t mode, moe_ws_layout* L) {
   const bool mx = act != moe::kActFp8Row;
   L->x_sf = take(mx ? R * (H / 32) * terms : 0);
   L->h_sf = take(mx ? R * (I / 32) * terms : 0);
-  L->x_sf_tiled =
-      take(mx ? max_tiles * moe::act_k_stages(act, static_cast<int>(H)) * moe::kSfbTileBytes : 0);
-  L->h_sf_tiled =
-      take(mx ? max_tiles * moe::act_k_stages(act, static_cast<int>(I)) * moe::kSfbTileBytes : 0);
+  L->x_sf_tiled = take(mx ? max_tiles * (H / 128) * moe::kSfbTileBytes : 0);
+  L->h_sf_tiled = take(mx ? max_tiles * (I / 128) * moe::kSfbTileBytes : 0);
   L->total = align_up(off, kAlign);
   L->max_tiles = static_cast<int32_t>(max_tiles);
   L->num_chunks = static_cast<int32_t>(chunks);

@@ -281,17 +281,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
           const uint32_t bx = static_cast<uint32_t>(kXBoxRowsAt(xm)) * 128u;
           if constexpr (C::kSplit) {
             // both terms' boxes (hi at K column 128 ks, lo at K + 128 ks of
-            // the 2K-wide code rows) and scale blocks (tile stages ks and
-            // KS + ks)
+            // the 2K-wide code rows) and the stage's scale block (the hi
+            // term's 512 bytes, then the lo term's)
             mbar_arrive_expect_tx(full + s, (LPS == 2 ? 2 * bx + 512u : 2 * bx) + 1024u);
             uint8_t* b = smem + C::kOffB + s * C::kBBytes;
             tma_load_2d(b, &tmap_x.m[xm], ks * kTileK, td.y, full + s);
             tma_load_2d(b + C::kTermBytes, &tmap_x.m[xm], (KS + ks) * kTileK, td.y, full + s);
-            const uint8_t* sb =
-                sfb_tiled + (static_cast<int64_t>(item / MT) * 2 * KS + ks) * kSfbTileBytes;
-            uint8_t* sd = smem + C::kOffSFBs + s * C::kSFBSlot;
-            bulk_load(sd, sb, 512u, full + s);
-            bulk_load(sd + 512, sb + static_cast<int64_t>(KS) * kSfbTileBytes, 512u, full + s);
+            bulk_load(smem + C::kOffSFBs + s * C::kSFBSlot,
+                      sfb_tiled + (static_cast<int64_t>(item / MT) * KS + ks) * kSfbTileBytes,
+                      1024u, full + s);
           } else {
             // MXFP8: the tile's activation scales for this K stage (one
             // 512-byte block per 128 rows of the MMA-N)

@@ -152,19 +152,17 @@ __host__ __device__ inline bool tile_entry_ok(int x, int y, int z, int w, int bn
 //               in rows of 2K codes (W4A16: bf16 activations on the FP8
 //               tensor cores; E2M1 weights).
 enum ActQuant : int { kActFp8Row = 0, kActMxfp8 = 1, kActSplit = 2 };
-// K stages (of kTileK) that one row's codes span in the per-tile scale
-// layout below: K / kTileK, twice that for the split.
-__host__ __device__ constexpr int act_k_stages(int act, int K) {
-  return (act == kActSplit ? 2 : 1) * (K / kTileK);
-}
 
 // MXFP8 and split activations: the (B operand) scale bytes are written by the
 // quantisers straight into the GEMM's per-tile layout.  For tile t of the
 // GEMM tile list and K stage ks there is one kSfbTileBytes block at
 // (t * KS + ks) * kSfbTileBytes; tile row n's four scale bytes (K blocks
 // 4ks .. 4ks+3) sit at sfb_row_offset(n): the 32-lane x 16-byte shape of the
-// weight scale blocks, one 512-byte half per 128 rows.
+// weight scale blocks, one 512-byte half per 128 rows.  Split activations
+// (tiles of <= 128 rows): the hi term's bytes in the first half, the lo
+// term's at the same offsets + kSfbLoOffset.
 constexpr int kSfbTileBytes = 1024;   // up to 256 tile rows
+constexpr int kSfbLoOffset = 512;     // the split's lo term
 __host__ __device__ inline uint32_t sfb_row_offset(int n) {
   return static_cast<uint32_t>((n >> 7) * 512 + 16 * (n & 31) + 4 * ((n >> 5) & 3));
 }

@@ -102,6 +102,37 @@ __device__ __forceinline__ void mx_term7(const float (&v)[32], uint8_t* sbyte, u
   codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// One MXFP8 term of a 32-element block spread over an aligned group of 8
+// lanes, 4 consecutive elements v[0..3] per lane (call it from all 32 lanes
+// of a warp; the four groups hold four blocks): e = clamp(floor(log2 amax) -
+// emax, -127, 127) over the block (0 when all are zero); returns the lane's
+// four codes E4M3_rne_satfinite(v * 2^-e) (element i in byte i), with the
+// scale byte e + 127 in *sbyte and each code's value times 2^e in dec.
+// Element for element the arithmetic of mx_quant_block (emax 8) and
+// mx_term7 (emax 7).
+__device__ __forceinline__ uint32_t mx_quad_term(const float (&v)[4], int emax, uint8_t* sbyte,
+                                                 float (&dec)[4]) {
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const int e = amax > 0.f ? max(-127, min(127, floor_log2(amax) - emax)) : 0;
+  *sbyte = static_cast<uint8_t>(e + 127);
+  const float inv = exp2i(-e), sc = exp2i(e);
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+      make_float2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv)), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+      make_float2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv)), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t codes = (lo & 0xFFFFu) | (hi << 16);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const __half_raw hr =
+        __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>((codes >> (8 * p)) & 0xFFu),
+                                __NV_E4M3);
+    dec[p] = __fmul_rn(__half2float(__half(hr)), sc);
+  }
+  return codes;
+}
+
 // The two-term split of 32 bf16 values (q[0..3], in K order): hi = the
 // MXFP8 term of the values, lo = the MXFP8 term of the residuals v -
 // dec(hi) (exact in float: both lie on the value's bf16 grid or finer).

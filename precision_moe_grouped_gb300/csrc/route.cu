@@ -443,8 +443,9 @@ __device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k
 // b % 4 for block b of row rows[j].
 // SPLIT (the W4A16 mode): the two-term split of each block (split_block),
 // in rows of 2H codes -- hi blocks in columns [0, H), lo blocks in [H, 2H)
-// -- whose scale bytes follow the same order (block H/32 + b is b's lo
-// term), in x_sf [R, 2H/32] and in the per-tile layout of 2H/128 K stages.
+// -- whose scale bytes follow the same order in x_sf [R, 2H/32] (block H/32
+// + b is b's lo term); in the per-tile layout the lo byte sits kSfbLoOffset
+// after the hi byte.
 template <bool SPLIT>
 __device__ void quantize_token_mx(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
                                   const int32_t* rows, const int64_t* sfb_base,
@@ -474,9 +475,55 @@ __device__ void quantize_token_mx(const __nv_bfloat16* __restrict__ x, int t, in
         uint4* ldst = reinterpret_cast<uint4*>(xq + r * W + H + 32 * b);
         ldst[0] = lcodes[0];
         ldst[1] = lcodes[1];
-        const int lb = nblk + b;
-        x_sf[r * nsf + lb] = lbyte;
-        sfb[sfb_base[j] + static_cast<int64_t>(lb >> 2) * kSfbTileBytes + (lb & 3)] = lbyte;
+        x_sf[r * nsf + nblk + b] = lbyte;
+        sfb[sfb_base[j] + static_cast<int64_t>(b >> 2) * kSfbTileBytes + kSfbLoOffset + (b & 3)] =
+            lbyte;
+      }
+    }
+  }
+}
+
+// quantize_token_mx with 8 lanes per 32-element block (lane l of the warp
+// holds elements 4 (l % 8) .. + 3 of block 4 w' + l / 8, w' the warp's
+// iteration) instead of one thread: few registers per thread, so that two
+// 1024-thread CTAs of the small-batch kernel fit an SM.  The same codes and
+// scale bytes.
+template <bool SPLIT>
+__device__ void quantize_token_mx_lanes(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
+                                        const int32_t* rows, const int64_t* sfb_base,
+                                        uint8_t* __restrict__ xq, uint8_t* __restrict__ x_sf,
+                                        uint8_t* __restrict__ sfb) {
+  const int lane = threadIdx.x & 31, sub = lane & 7;
+  const int nblk = H / 32;   // a multiple of 4
+  const int64_t W = SPLIT ? 2 * H : H, nsf = SPLIT ? 2 * nblk : nblk;
+  for (int b = 4 * (threadIdx.x >> 5) + (lane >> 3); b < nblk; b += 4 * (blockDim.x >> 5)) {
+    const int c0 = 32 * b + 4 * sub;   // the lane's first column
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * H + c0));
+    const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+    const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+    float v[4] = {f01.x, f01.y, f23.x, f23.y}, dec[4];
+    uint8_t sbyte, lbyte = 0;
+    const uint32_t c = mx_quad_term(v, SPLIT ? 7 : 8, &sbyte, dec);
+    uint32_t lc = 0;
+    if constexpr (SPLIT) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __fsub_rn(v[i], dec[i]);
+      lc = mx_quad_term(v, 7, &lbyte, dec);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int64_t r = rows[j];
+      const int64_t sb = sfb_base[j] + static_cast<int64_t>(b >> 2) * kSfbTileBytes + (b & 3);
+      *reinterpret_cast<uint32_t*>(xq + r * W + c0) = c;
+      if (sub == 0) {
+        x_sf[r * nsf + b] = sbyte;
+        sfb[sb] = sbyte;
+      }
+      if constexpr (SPLIT) {
+        *reinterpret_cast<uint32_t*>(xq + r * W + H + c0) = lc;
+        if (sub == 1) {
+          x_sf[r * nsf + nblk + b] = lbyte;
+          sfb[sb + kSfbLoOffset] = lbyte;
+        }
       }
     }
   }
@@ -524,7 +571,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     row_of[ts] = r;
     token_slot[r] = static_cast<int32_t>(ts);
     if (AQ != kActFp8Row)
-      sfb_base[j] = sfb_row_base(r, offsets[e], tile_plan[e], act_k_stages(AQ, H));
+      sfb_base[j] = sfb_row_base(r, offsets[e], tile_plan[e], H / kTileK);
   }
   __syncthreads();
   if constexpr (AQ == kActFp8Row)
@@ -542,7 +589,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
 // GEMM tile list.  The redundant O(T*k) counting per CTA is cheap at these
 // sizes and removes three launches from the decode path.
 template <int AQ>
-__global__ void __launch_bounds__(1024) expand_small_kernel(
+__global__ void __launch_bounds__(1024, 2) expand_small_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids, int T, int E, int k,
     int H, int bn, int32_t* __restrict__ counts_out, int32_t* __restrict__ offsets_out,
     int4* __restrict__ tiles, int32_t* __restrict__ num_tiles, int2* __restrict__ tile_plan,
@@ -601,9 +648,9 @@ __global__ void __launch_bounds__(1024) expand_small_kernel(
     quantize_token<1>(x, t, k, H, rows, warp_max, xq, x_scale);   // 1024 threads
   } else {
     if (e < k)
-      sfb_base[e] = sfb_row_base(rows[e], cnt[my_e[e]], plan[my_e[e]], act_k_stages(AQ, H));
+      sfb_base[e] = sfb_row_base(rows[e], cnt[my_e[e]], plan[my_e[e]], H / kTileK);
     __syncthreads();
-    quantize_token_mx<AQ == kActSplit>(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
+    quantize_token_mx_lanes<AQ == kActSplit>(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
   }
 }
 

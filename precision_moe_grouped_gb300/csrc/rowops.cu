@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __rest
 // with the lo terms in columns [I, 2I)), scale bytes to the row-major h_sf
 // [R, I/32] (or [R, 2I/32], lo blocks after the hi blocks) and to GEMM2's
 // per-tile layout (row r's expert from its (token, slot), its tile from the
-// expert's plan).
+// expert's plan; split: the lo byte kSfbLoOffset after the hi byte).
 template <bool SPLIT>
 __global__ void __launch_bounds__(256) hquant_mx_kernel(
     const __nv_bfloat16* __restrict__ h, int R, int I, const int32_t* __restrict__ ids,
@@ -55,8 +55,7 @@ __global__ void __launch_bounds__(256) hquant_mx_kernel(
   const int lane = threadIdx.x & 31;
   if (r >= R) return;
   const int e = ids[token_slot[r]];
-  const int64_t base =
-      sfb_row_base(r, offsets[e], tile_plan[e], act_k_stages(SPLIT ? kActSplit : kActMxfp8, I));
+  const int64_t base = sfb_row_base(r, offsets[e], tile_plan[e], I / kTileK);
   const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(r) * I);
   const int nblk = I / 32;
   const int64_t W = SPLIT ? 2 * I : I, nsf = SPLIT ? 2 * nblk : nblk;
@@ -79,9 +78,8 @@ __global__ void __launch_bounds__(256) hquant_mx_kernel(
       uint4* ldst = reinterpret_cast<uint4*>(hq + r * W + I + 32 * b);
       ldst[0] = lcodes[0];
       ldst[1] = lcodes[1];
-      const int lb = nblk + b;
-      h_sf[r * nsf + lb] = lbyte;
-      sfb[base + static_cast<int64_t>(lb >> 2) * kSfbTileBytes + (lb & 3)] = lbyte;
+      h_sf[r * nsf + nblk + b] = lbyte;
+      sfb[base + static_cast<int64_t>(b >> 2) * kSfbTileBytes + kSfbLoOffset + (b & 3)] = lbyte;
     }
   }
 }
