@@ -211,11 +211,14 @@ int32_t moe_forward_ex(const moe_shape* shape, int32_t quant_mode, const void* x
                        const void* w2_p, const void* w2_sf_p, void* out, void* workspace,
                        size_t workspace_bytes, void* stream, const moe_options* opts);
 
-/* End-to-end variant with HOST activations: copies x_host (bf16 [T,H]) and
- * logits_host (float [T,E]) into the workspace's staging area, runs the
- * forward, and copies the result back to out_host (bf16 [T,H]) -- all on
- * `stream`.  Host buffers should be pinned for asynchronous copies; they must
- * stay valid until the stream reaches this point. */
+/* End-to-end variant with HOST activations x_host (bf16 [T,H]), logits_host
+ * (float [T,E]) and out_host (bf16 [T,H]), all on `stream`.  A page-locked
+ * host buffer (cudaHostAlloc, cudaMallocHost, cudaHostRegister) is read or
+ * written in place by the kernels, over the host link, so its transfer
+ * overlaps the computation; any other host buffer is copied through the
+ * workspace's staging area (x and logits before the forward, out after it).
+ * Host buffers must stay valid, and out_host unread, until the stream
+ * reaches this point.  The results are the same either way. */
 int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void* x_host,
                          const float* logits_host, const void* w1_p, const void* w1_sf_p,
                          const void* w2_p, const void* w2_sf_p, void* out_host,

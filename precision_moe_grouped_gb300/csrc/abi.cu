@@ -307,6 +307,20 @@ T* at(void* ws, uint64_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+// The address under which this device's kernels reach host buffer p in
+// place: page-locked host memory (cudaHostAlloc, cudaMallocHost,
+// cudaHostRegister), which unified addressing maps into every device --
+// else nullptr (pageable memory, or memory of another device): the caller
+// then stages the buffer with copies.
+const void* host_in_place(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();   // clear the sticky-free error of an unknown pointer
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float* logits,
                     const void* w1, const void* w1_sf, const void* w2, const void* w2_sf,
                     void* out, void* ws, cudaStream_t st, const moe_options* opts) {
@@ -555,20 +569,29 @@ int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void*
     return fail(MOE_ERR_INVALID_ARG, "a required pointer is NULL");
   moe_ws_layout L;
   compute_layout(shape, quant_mode, &L);
-  void* xs = at<void>(workspace, L.x_stage);
-  float* ls = at<float>(workspace, L.logits_stage);
-  void* os = at<void>(workspace, L.out_stage);
-  st = check_forward_args(shape, quant_mode, xs, ls, w1_p, w1_sf_p, w2_p, w2_sf_p, os, workspace,
-                          workspace_bytes, opts);
+  // Page-locked host buffers are read and written in place by the kernels
+  // (over the host link); the others are staged through the workspace.
+  const void* xd = host_in_place(x_host);
+  const float* ld = static_cast<const float*>(host_in_place(logits_host));
+  void* od = const_cast<void*>(host_in_place(out_host));
+  const void* xin = xd ? xd : at<void>(workspace, L.x_stage);
+  const float* lin = ld ? ld : at<float>(workspace, L.logits_stage);
+  void* oout = od ? od : at<void>(workspace, L.out_stage);
+  st = check_forward_args(shape, quant_mode, xin, lin, w1_p, w1_sf_p, w2_p, w2_sf_p, oout,
+                          workspace, workspace_bytes, opts);
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t T = shape->num_tokens, H = shape->hidden, E = shape->num_experts;
-  MOE_CUDA(cudaMemcpyAsync(xs, x_host, T * H * 2, cudaMemcpyHostToDevice, s));
-  MOE_CUDA(cudaMemcpyAsync(ls, logits_host, T * E * 4, cudaMemcpyHostToDevice, s));
-  st = run_forward(shape, quant_mode, xs, ls, w1_p, w1_sf_p, w2_p, w2_sf_p, os, workspace, s,
+  if (!xd)
+    MOE_CUDA(cudaMemcpyAsync(const_cast<void*>(xin), x_host, T * H * 2, cudaMemcpyHostToDevice,
+                             s));
+  if (!ld)
+    MOE_CUDA(cudaMemcpyAsync(const_cast<float*>(lin), logits_host, T * E * 4,
+                             cudaMemcpyHostToDevice, s));
+  st = run_forward(shape, quant_mode, xin, lin, w1_p, w1_sf_p, w2_p, w2_sf_p, oout, workspace, s,
                    opts);
   if (st != MOE_OK) return st;
-  MOE_CUDA(cudaMemcpyAsync(out_host, os, T * H * 2, cudaMemcpyDeviceToHost, s));
+  if (!od) MOE_CUDA(cudaMemcpyAsync(out_host, oout, T * H * 2, cudaMemcpyDeviceToHost, s));
   return MOE_OK;
 }
 

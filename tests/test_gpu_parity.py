@@ -221,18 +221,28 @@ def test_prepare_weights_layout():
                                   relayout(case.w2_sf.numpy(), np.arange(H), H, I))
 
 
-def test_forward_host_matches_device_path():
-    cfg = MI.custom_config(8, 2, 256, 128)
-    case = MI.make_case(cfg, 50, seed=17)
+@pytest.mark.parametrize("mode", [MI.QUANT_W4A8, MI.QUANT_W4A16, MI.QUANT_W8A8])
+@pytest.mark.parametrize("T", [1, 50, 300])
+@pytest.mark.parametrize("pinned", ["all", "none", "x_only"])
+def test_forward_host_matches_device_path(mode, T, pinned):
+    """moe_forward_host reads page-locked host buffers in place (over the host
+    link) and stages the others through the workspace; every combination
+    gives the device-buffer forward's output bit for bit, on the tiny, small
+    and large-batch front ends."""
+    cfg = MI.custom_config(8, 2, 256, 128, mode=mode)
+    case = MI.make_case(cfg, T, seed=17)
     run = GpuRun(case)
-    s = P.shape(50, 8, 2, 256, 128)
-    xh = case.x.clone().pin_memory()
-    lh = case.logits.clone().pin_memory()
-    oh = torch.empty((50, 256), dtype=torch.bfloat16).pin_memory()
-    ws = torch.zeros(P.workspace_size(s), dtype=torch.uint8, device="cuda:0")
+    s = P.shape(T, 8, 2, 256, 128)
+    pin = {"all": (True, True, True), "none": (False, False, False),
+           "x_only": (True, False, False)}[pinned]
+    xh, lh = case.x.clone(), case.logits.clone()
+    oh = torch.empty((T, 256), dtype=torch.bfloat16)
+    xh, lh, oh = [t.pin_memory() if p else t for t, p in zip((xh, lh, oh), pin)]
+    ws = torch.zeros(P.workspace_size(s, mode), dtype=torch.uint8, device="cuda:0")
     P.forward_host(s, xh, lh, run.moe.w1_p, run.moe.w1_sf_p, run.moe.w2_p, run.moe.w2_sf_p, oh,
-                   ws)
+                   ws, mode=mode)
     torch.cuda.synchronize()
+    assert P.read_device_status(ws) == 0
     np.testing.assert_array_equal(oh.float().numpy(), run.out_np())
 
 
