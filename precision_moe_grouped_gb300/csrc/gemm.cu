@@ -360,34 +360,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
       const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffB), 0, 1024, 2);
       const uint64_t sdesc0 = smem_desc(smem_u32(smem + C::kOffSF), 0, 128, 0);
       const uint64_t sbdesc0 = smem_desc(smem_u32(smem + C::kOffSFBs), 0, 128, 0);
-      // One stage: weight scales into TMEM, the 4 MMAs of its 128 K (the
+      // One stage, from one elected lane in one block: weight scales (and
+      // per-stage activation scales) into TMEM, the 4 MMAs of its 128 K (the
       // first of an item's first stage overwrites the accumulator; split:
       // then the lo term's 4 MMAs into the same accumulator), and the commit
-      // that frees the slot when they complete.
+      // that frees the slot when they complete.  Electing once per stage
+      // instead of once per instruction took DSV3 T=4096 from 1557 to 1532
+      // us.
       auto issue_stage = [&](int stage, uint32_t d_tmem, uint32_t id0, int nmma, bool first) {
         const uint32_t sfa = tmem + static_cast<uint32_t>(C::kColSFA + 4 * stage);
-        tc_cp_32x128b_x4_warp(sfa, sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4)));
-        uint32_t sfb = tmem + C::kColSFB;
-        if (C::kTiledSfb) {
-          sfb += static_cast<uint32_t>(8 * stage);
-          const uint64_t sbd = sbdesc0 + static_cast<uint64_t>(stage * (C::kSFBSlot >> 4));
-          tc_cp_32x128b_x4_warp(sfb, sbd);
-          if (C::kSplit || nmma > 128) tc_cp_32x128b_x4_warp(sfb + 4, sbd + (512 >> 4));
-        }
+        const uint64_t sfa_src = sdesc0 + static_cast<uint64_t>(stage * (C::kSFBytes >> 4));
         const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::kABytes >> 4));
         const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::kBBytes >> 4));
-#pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)
-          tc_mma_mx_warp(d_tmem, ad + 2 * kk, bd + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
-                         sfb, (!first || kk > 0) ? 1u : 0u);
-        if constexpr (C::kSplit) {
-          const uint64_t bl = bd + static_cast<uint64_t>(C::kTermBytes >> 4);
-#pragma unroll
-          for (uint32_t kk = 0; kk < 4; ++kk)
-            tc_mma_mx_warp(d_tmem, ad + 2 * kk, bl + 2 * kk, id0 | (kk << 4) | (kk << 29), sfa,
-                           sfb + 4, 1u);
+        const uint32_t acc0 = first ? 0u : 1u, bar = smem_u32(empty + stage);
+        if constexpr (!C::kTiledSfb) {
+          tc_stage_mx4_warp(d_tmem, ad, bd, id0, sfa, sfa_src, tmem + C::kColSFB, acc0, bar);
+        } else {
+          const uint32_t sfb = tmem + static_cast<uint32_t>(C::kColSFB + 8 * stage);
+          const uint64_t sfb_src = sbdesc0 + static_cast<uint64_t>(stage * (C::kSFBSlot >> 4));
+          if constexpr (C::kSplit)
+            tc_stage_split_warp(d_tmem, ad, bd, bd + static_cast<uint64_t>(C::kTermBytes >> 4),
+                                id0, sfa, sfa_src, sfb, sfb_src, acc0, bar);
+          else
+            tc_stage_mx4_sfb_warp(d_tmem, ad, bd, id0, sfa, sfa_src, sfb, sfb_src,
+                                  nmma > 128 ? 1u : 0u, acc0, bar);
         }
-        tc_commit_warp(empty + stage);
       };
       if constexpr (NI == 1) {
         // One issuer (prefill tiles): items in order, an item's K stages in

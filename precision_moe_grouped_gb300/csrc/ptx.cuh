@@ -265,6 +265,124 @@ __device__ __forceinline__ void tc_mma_mx_warp(uint32_t d_tmem, uint64_t adesc, 
       : "memory");
 }
 
+// One 128-K pipeline stage from one elected lane, in a single block so that
+// the warp elects once: the weight scales into TMEM (32x128b.warpx4 from
+// sfa_src), the 4 block-scaled MMAs of K sub-steps 0..3 (A and B advanced
+// 32 bytes per step; scale IDs = the step; the first accumulates only when
+// acc0 != 0), and a commit to the stage's empty barrier.
+__device__ __forceinline__ void tc_stage_mx4_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                  uint32_t id0, uint32_t sfa_tmem,
+                                                  uint64_t sfa_src, uint32_t sfb_tmem,
+                                                  uint32_t acc0, uint32_t empty_bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, q;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "setp.eq.b32 q, %7, %7;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%6], p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %9, %10, %11, [%4], [%6], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %12, %13, %14, [%4], [%6], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %15, %16, %17, [%4], [%6], q;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t}" ::
+          "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(id0), "r"(sfa_tmem), "l"(sfa_src),
+      "r"(sfb_tmem), "r"(acc0), "r"(empty_bar),
+      "l"(adesc + 2), "l"(bdesc + 2), "r"(id0 | (1u << 4) | (1u << 29)),
+      "l"(adesc + 4), "l"(bdesc + 4), "r"(id0 | (2u << 4) | (2u << 29)),
+      "l"(adesc + 6), "l"(bdesc + 6), "r"(id0 | (3u << 4) | (3u << 29))
+      : "memory");
+}
+
+// As tc_stage_mx4_warp, with per-stage activation scales (MXFP8): after the
+// weight scales, the activation scales into TMEM from sfb_src (and the next
+// 512 bytes into sfb_tmem + 4 when sfb2 != 0: MMA-N > 128), then the 4 MMAs
+// and the commit.
+__device__ __forceinline__ void tc_stage_mx4_sfb_warp(uint32_t d_tmem, uint64_t adesc,
+                                                      uint64_t bdesc, uint32_t id0,
+                                                      uint32_t sfa_tmem, uint64_t sfa_src,
+                                                      uint32_t sfb_tmem, uint64_t sfb_src,
+                                                      uint32_t sfb2, uint32_t acc0,
+                                                      uint32_t empty_bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, e2, p, q;\n\t"
+      ".reg .b64 a1, a2, a3, b1, b2, b3, s2;\n\t"
+      ".reg .b32 i1, i2, i3, t2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %9, 0;\n\t"
+      "setp.eq.b32 q, %9, %9;\n\t"
+      "setp.ne.and.b32 e2, %8, 0, e;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "or.b32 i1, %3, 0x20000010;\n\tor.b32 i2, %3, 0x40000020;\n\tor.b32 i3, %3, 0x60000030;\n\t"
+      "add.s64 s2, %7, 32;\n\tadd.u32 t2, %6, 4;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%6], %7;\n\t"
+      "@e2 tcgen05.cp.cta_group::1.32x128b.warpx4 [t2], s2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%6], p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a1, b1, i1, [%4], [%6], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a2, b2, i2, [%4], [%6], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a3, b3, i3, [%4], [%6], q;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}" ::
+          "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(id0), "r"(sfa_tmem), "l"(sfa_src),
+      "r"(sfb_tmem), "l"(sfb_src), "r"(sfb2), "r"(acc0), "r"(empty_bar)
+      : "memory");
+}
+
+// A split-activation stage (W4A16): weight scales, the hi term's scales
+// (sfb_src) and the lo term's (the next 512 bytes, into sfb_tmem + 4), the 4
+// MMAs of the hi box (bdesc; the first accumulates only when acc0 != 0) and
+// the 4 of the lo box (bdesc_lo) into the same accumulator, and the commit.
+__device__ __forceinline__ void tc_stage_split_warp(uint32_t d_tmem, uint64_t adesc,
+                                                    uint64_t bdesc, uint64_t bdesc_lo,
+                                                    uint32_t id0, uint32_t sfa_tmem,
+                                                    uint64_t sfa_src, uint32_t sfb_tmem,
+                                                    uint64_t sfb_src, uint32_t acc0,
+                                                    uint32_t empty_bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, q;\n\t"
+      ".reg .b64 a1, a2, a3, b1, b2, b3, l1, l2, l3, s2;\n\t"
+      ".reg .b32 i1, i2, i3, t2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %9, 0;\n\t"
+      "setp.eq.b32 q, %9, %9;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "add.s64 l1, %3, 2;\n\tadd.s64 l2, %3, 4;\n\tadd.s64 l3, %3, 6;\n\t"
+      "or.b32 i1, %4, 0x20000010;\n\tor.b32 i2, %4, 0x40000020;\n\tor.b32 i3, %4, 0x60000030;\n\t"
+      "add.s64 s2, %8, 32;\n\tadd.u32 t2, %7, 4;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%5], %6;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%7], %8;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [t2], s2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %4, [%5], [%7], p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a1, b1, i1, [%5], [%7], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a2, b2, i2, [%5], [%7], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a3, b3, i3, [%5], [%7], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %3, %4, [%5], [t2], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a1, l1, i1, [%5], [t2], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a2, l2, i2, [%5], [t2], q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], a3, l3, i3, [%5], [t2], q;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}" ::
+          "r"(d_tmem), "l"(adesc), "l"(bdesc), "l"(bdesc_lo), "r"(id0), "r"(sfa_tmem),
+      "l"(sfa_src), "r"(sfb_tmem), "l"(sfb_src), "r"(acc0), "r"(empty_bar)
+      : "memory");
+}
+
 // Instruction descriptor for block-scaled .kind::mxf8f6f4, M = 128, both
 // operands K-major, E8M0 scales.  Formats: 0 = E4M3, 5 = E2M1.
 __host__ __device__ constexpr uint32_t idesc_mx(uint32_t a_fmt, uint32_t b_fmt, uint32_t n,
