@@ -38,12 +38,11 @@
 // handed out statically (item = CTA + i * grid) from the device-built tile
 // list, so nothing returns to the host.
 //
-// Roles: the first warps = TMA producers (one warp per pipeline stage --
-// three for the MXFP8 prefill tiles -- three lanes per stage); the next NI
-// warps = MMA issuers (one elected lane each; the first
-// also owns the TMEM allocation); the next 8 warps = epilogue (warp w reads
-// TMEM lanes 32*(w%4) .. +31; two warps per lane quarter split the
-// columns); the last warp = optional L2 prefetcher.  Two TMEM accumulator
+// Roles: the first warps = TMA producers (one warp per pipeline stage, three
+// lanes per stage); the next NI warps = MMA issuers (one elected lane each;
+// the first also owns the TMEM allocation); the next 8 warps = epilogue
+// (warp w reads TMEM lanes 32*(w%4) .. +31; two warps per lane quarter split
+// the columns); the last warp = optional L2 prefetcher.  Two TMEM accumulator
 // buffers let the epilogue of one item overlap the main loop of the next.
 //
 // Epilogues:
@@ -75,10 +74,9 @@ struct GemmCfg {
   // warp waiting on different stages' barriers serialise, so each stage gets
   // its own warp (against three warps sharing the stages: DSV3 T=1 54.5 ->
   // 51.9 us, T=512 981 -> 941 us, T=4096 1566 -> 1548 us, W4A16 T=256 77.4
-  // -> 73.3 us); the MXFP8 prefill tiles keep three warps (2144 -> 2183 us
-  // with one per stage).
-  static constexpr int kProdWarps =
-      ACT == kActMxfp8 && NI == 1 ? (STAGES >= 3 ? 3 : STAGES) : STAGES;
+  // -> 73.3 us; MXFP8 Zipf T=4096 2021 -> 1965 us once the issuer elects
+  // once per stage).
+  static constexpr int kProdWarps = STAGES;
   static constexpr int kStagesPerWarp = (STAGES + kProdWarps - 1) / kProdWarps;
   static constexpr int kLanesPerStage = 3 * kStagesPerWarp <= 32 ? 3 : 2;
   static_assert(kLanesPerStage * kStagesPerWarp <= 32, "producer lanes must fit a warp");
