@@ -444,7 +444,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
     MOE_CUDA(moe::launch_hquant_mx(act, h, R, I, ids, token_slot, offsets, tile_plan, hq, h_sf,
                                    sfb2, st));
   else
-    MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, st));
+    MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, status, timeout_ns, st));
   MOE_CUDA(mark());
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
                    tiled ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, grid2,

@@ -234,8 +234,10 @@ cudaError_t launch_quant_scatter(const void* x, const int32_t* chunk_base, const
                                  const int32_t* offsets, const int2* tile_plan, int T, int E,
                                  int k, int H, int32_t* row_of, int32_t* token_slot,
                                  const QuantOut& q, cudaStream_t s);
+// Per-row FP8 quantisation of h; status / timeout_ns: the bounded wait of
+// its staged form.
 cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_scale,
-                          cudaStream_t s);
+                          int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 // MXFP8 quantisation (act kActMxfp8) or two-term split (kActSplit) of h:
 // codes, row-major scale bytes and the per-tile scale layout of GEMM2.
 cudaError_t launch_hquant_mx(int act, const void* h, int R, int I, const int32_t* ids,

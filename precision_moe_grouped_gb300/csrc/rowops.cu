@@ -25,7 +25,7 @@ namespace {
 // One warp per expanded row of h (bf16 [R, I]): hquant_row_warp.  GEMM2
 // may launch as soon as these blocks have started: it streams its weights
 // while this kernel waits for GEMM1 and quantises, and waits for this
-// kernel's results itself.
+// kernel's results itself.  (The form for rows too long to stage.)
 __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __restrict__ h, int R,
                                                      int I, uint8_t* __restrict__ hq,
                                                      float* __restrict__ h_scale) {
@@ -34,6 +34,44 @@ __global__ void __launch_bounds__(256) hquant_kernel(const __nv_bfloat16* __rest
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (warp >= R) return;
   hquant_row_warp(h, warp, I, hq, h_scale, threadIdx.x & 31);
+}
+
+// Rows of h one staged block holds, and the longest row staged.
+constexpr int kHqStageRows = 8;
+constexpr int kHqStageMaxI = 4096;   // 8 rows x 8 KB = 64 KB of shared memory
+
+// The same quantisation with the block's kHqStageRows consecutive rows
+// brought into shared memory by one bulk copy (up to 64 KB in flight per
+// block, several blocks per SM), then one warp per row (hquant_row_smem).
+// A timed-out wait for the copy records MOE_ERR_DEVICE_TIMEOUT in status.
+__global__ void __launch_bounds__(256) hquant_staged_kernel(const __nv_bfloat16* __restrict__ h,
+                                                            int R, int I,
+                                                            uint8_t* __restrict__ hq,
+                                                            float* __restrict__ h_scale,
+                                                            int32_t* __restrict__ status,
+                                                            uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t hstage[];
+  __shared__ __align__(8) uint64_t bar;
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  griddep_wait();
+  const int r0 = blockIdx.x * kHqStageRows;
+  const int nr = min(kHqStageRows, R - r0);
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(I) * 2u;
+    mbar_arrive_expect_tx(&bar, bytes);
+    bulk_load(hstage, h + static_cast<size_t>(r0) * I, bytes, &bar);
+  }
+  int32_t none = 0;
+  if (!mbar_wait(&bar, 0, timeout_ns, status, kDevTimeout, &none)) return;
+  const int warp = threadIdx.x >> 5;
+  if (warp < nr)
+    hquant_row_smem(reinterpret_cast<const __nv_bfloat16*>(hstage) + static_cast<size_t>(warp) * I,
+                    r0 + warp, I, hq, h_scale, threadIdx.x & 31);
 }
 
 // MXFP8 (the W8A8 mode) quantisation of h, or (SPLIT, the W4A16 mode) its
@@ -123,8 +161,18 @@ __global__ void timeout_selftest_kernel(int32_t* status, uint64_t timeout_ns) {
 }  // namespace
 
 cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_scale,
-                          cudaStream_t s) {
+                          int32_t* status, uint64_t timeout_ns, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
+  if (I <= kHqStageMaxI) {
+    const size_t smem = static_cast<size_t>(kHqStageRows) * I * 2;
+    static DeviceOnce smem_set;   // the limit for the longest staged row, once
+    const cudaError_t e =
+        set_smem_limit_once(hquant_staged_kernel, kHqStageRows * kHqStageMaxI * 2, smem_set);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(hquant_staged_kernel, dim3((R + kHqStageRows - 1) / kHqStageRows),
+                      dim3(32 * kHqStageRows), smem, s, static_cast<const __nv_bfloat16*>(h), R,
+                      I, hq, h_scale, status, timeout_ns);
+  }
   const int blocks = (R + 7) / 8;
   return launch_pdl(hquant_kernel, dim3(blocks), dim3(256), 0, s,
                     static_cast<const __nv_bfloat16*>(h), R, I, hq, h_scale);

@@ -102,6 +102,51 @@ __device__ __forceinline__ void hquant_row_warp(const __nv_bfloat16* __restrict_
   if (lane == 0) h_scale[r] = nz ? amax / 448.0f : 1.0f;
 }
 
+// hquant_row_warp on a row already staged in shared memory (hs: I bf16):
+// the same arithmetic, both passes reading shared memory.
+__device__ __forceinline__ void hquant_row_smem(const __nv_bfloat16* hs, int r, int I,
+                                                uint8_t* __restrict__ hq,
+                                                float* __restrict__ h_scale, int lane) {
+  const uint4* hr = reinterpret_cast<const uint4*>(hs);
+  const int nvec = I / 16;
+  float amax = 0.f;
+  for (int i = lane; i < nvec; i += 32) {
+    const uint4 q[2] = {hr[2 * i], hr[2 * i + 1]};
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 f = __bfloat1622float2(b[j]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const bool nz = amax > 0.f;
+  const float inv = nz ? 448.0f / amax : 0.0f;
+  uint4* dst = reinterpret_cast<uint4*>(hq + static_cast<size_t>(r) * I);
+  for (int i = lane; i < nvec; i += 32) {
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (nz) {
+      const uint4 q[2] = {hr[2 * i], hr[2 * i + 1]};
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f0 = __bfloat1622float2(b[2 * j]);
+        const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv)), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)), __NV_SATFINITE, __NV_E4M3);
+        w[j] = (lo & 0xFFFFu) | (hi << 16);
+      }
+      out = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    dst[i] = out;
+  }
+  if (lane == 0) h_scale[r] = nz ? amax / 448.0f : 1.0f;
+}
+
 // One 16-byte vector (8 outputs, columns 8i .. 8i + 7) of token t's combine:
 // out[t, c] = bf16( sum_j w[t, j] * y[row_j, c] ), float32 fused
 // multiply-adds from 0 in slot order j = 0 .. k-1.
