@@ -321,9 +321,23 @@ const void* host_in_place(const void* p) {
   return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
+// Whether p is device memory of the current device (cudaMalloc), which
+// bulk copies may read; host-mapped and unregistered pointers are not.
+bool on_device(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  int dev = -1;
+  return a.type == cudaMemoryTypeDevice && cudaGetDevice(&dev) == cudaSuccess && a.device == dev;
+}
+
+// x_on_device: x is device memory (see on_device).
 int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float* logits,
                     const void* w1, const void* w1_sf, const void* w2, const void* w2_sf,
-                    void* out, void* ws, cudaStream_t st, const moe_options* opts) {
+                    void* out, void* ws, cudaStream_t st, const moe_options* opts,
+                    bool x_on_device) {
   DeviceInfo dev;
   int32_t rc = device_info(&dev);
   if (rc != MOE_OK) return rc;
@@ -428,8 +442,8 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
                               chunk, tiles, num_tiles, tile_plan, status, st));
     MOE_CUDA(mark());
     MOE_CUDA(mark());   // the scatter kernel ranks the rows itself (no rank kernel)
-    MOE_CUDA(moe::launch_quant_scatter(x, chunk, ids, offsets, tile_plan, T, E, k, H, row_of,
-                                       token_slot, qx, st));
+    MOE_CUDA(moe::launch_quant_scatter(x, x_on_device, chunk, ids, offsets, tile_plan, T, E, k,
+                                       H, row_of, token_slot, qx, status, st));
     MOE_CUDA(mark());
   }
   // W4A8: the per-row token scale is applied in the epilogues; MXFP8 and
@@ -546,7 +560,7 @@ int32_t moe_forward_ex(const moe_shape* shape, int32_t quant_mode, const void* x
                                   w2_sf_p, out, workspace, workspace_bytes, opts);
   if (st != MOE_OK || shape->num_tokens == 0) return st;
   return run_forward(shape, quant_mode, x, router_logits, w1_p, w1_sf_p, w2_p, w2_sf_p, out,
-                     workspace, static_cast<cudaStream_t>(stream), opts);
+                     workspace, static_cast<cudaStream_t>(stream), opts, on_device(x));
 }
 
 int32_t moe_forward(const moe_shape* shape, int32_t quant_mode, const void* x,
@@ -589,7 +603,7 @@ int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void*
     MOE_CUDA(cudaMemcpyAsync(const_cast<float*>(lin), logits_host, T * E * 4,
                              cudaMemcpyHostToDevice, s));
   st = run_forward(shape, quant_mode, xin, lin, w1_p, w1_sf_p, w2_p, w2_sf_p, oout, workspace, s,
-                   opts);
+                   opts, xd == nullptr);
   if (st != MOE_OK) return st;
   if (!od) MOE_CUDA(cudaMemcpyAsync(out_host, oout, T * H * 2, cudaMemcpyDeviceToHost, s));
   return MOE_OK;

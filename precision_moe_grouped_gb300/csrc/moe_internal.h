@@ -230,10 +230,13 @@ cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, in
 // One CTA per token: the rows of its slots (from the per-chunk bases the
 // scan leaves in chunk_base) into row_of / token_slot, and the token's
 // quantised activations into them.
-cudaError_t launch_quant_scatter(const void* x, const int32_t* chunk_base, const int32_t* ids,
-                                 const int32_t* offsets, const int2* tile_plan, int T, int E,
-                                 int k, int H, int32_t* row_of, int32_t* token_slot,
-                                 const QuantOut& q, cudaStream_t s);
+// x_on_device: x is device memory (else page-locked host memory read in
+// place), which lets the per-row FP8 form stage the row by a bulk copy.
+// status: where a timed-out wait for that copy is recorded.
+cudaError_t launch_quant_scatter(const void* x, bool x_on_device, const int32_t* chunk_base,
+                                 const int32_t* ids, const int32_t* offsets, const int2* tile_plan,
+                                 int T, int E, int k, int H, int32_t* row_of, int32_t* token_slot,
+                                 const QuantOut& q, int32_t* status, cudaStream_t s);
 // Per-row FP8 quantisation of h; status / timeout_ns: the bounded wait of
 // its staged form.
 cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_scale,

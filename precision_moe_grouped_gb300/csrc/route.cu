@@ -433,6 +433,44 @@ __device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k
   if (static_cast<int>(threadIdx.x) < k) x_scale[rows[threadIdx.x]] = s;
 }
 
+// quantize_token on a row already staged in shared memory (xs: H bf16): the
+// same arithmetic, both passes reading shared memory.
+__device__ void quantize_token_staged(const __nv_bfloat16* xs, int k, int H, const int32_t* rows,
+                                      float* warp_max, uint8_t* __restrict__ xq,
+                                      float* __restrict__ x_scale) {
+  const uint4* xr = reinterpret_cast<const uint4*>(xs);
+  const int nvec = H / 16;
+  float amax = 0.f;
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+    const uint4 q[2] = {xr[2 * i], xr[2 * i + 1]};
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(q);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 f = __bfloat1622float2(b[j]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.f;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) amax = fmaxf(amax, warp_max[w]);
+  const bool nz = amax > 0.f;
+  const float s = nz ? amax / 448.0f : 1.0f;
+  const float inv = nz ? 448.0f / amax : 0.0f;
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (nz) {
+      const uint4 q[2] = {xr[2 * i], xr[2 * i + 1]};
+      out = fp8_codes16(q, inv);
+    }
+    for (int j = 0; j < k; ++j)
+      reinterpret_cast<uint4*>(xq + static_cast<size_t>(rows[j]) * H)[i] = out;
+  }
+  if (static_cast<int>(threadIdx.x) < k) x_scale[rows[threadIdx.x]] = s;
+}
+
 // MXFP8 (the W8A8 mode) quantisation of token t's row, per 32-element
 // block: X = 2^clamp(floor(log2 amax) - 8, -127, 127) (8 = E4M3's emax),
 // codes = E4M3_rne_satfinite(x / X), scale byte = exponent + 127; an
@@ -530,7 +568,12 @@ __device__ void quantize_token_mx_lanes(const __nv_bfloat16* __restrict__ x, int
 }
 
 // One CTA per token t: the rows of its k slots, then the quantisation of
-// the token into them (AQ: per-row FP8, MXFP8 or the two-term split).  Slot j's row is the chunk's base row for its expert e (from the
+// the token into them (AQ: per-row FP8, MXFP8 or the two-term split).
+// stage_x (per-row FP8, x in device memory): the token's row comes into
+// shared memory by one bulk copy issued before the grid dependency wait --
+// x is the forward's input, complete before the forward's first kernel
+// passed its own wait, hence before this grid started -- so the copy
+// overlaps the wait and the ranking.  Slot j's row is the chunk's base row for its expert e (from the
 // scan) plus the number of the chunk's earlier tokens routed to e -- the
 // stable, ascending-token order inside each expert (a token's k experts are
 // distinct).  The CTA writes row_of and token_slot for its slots.
@@ -540,15 +583,25 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets,
     const int2* __restrict__ tile_plan, int E, int k, int H, int32_t* __restrict__ row_of,
     int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq, float* __restrict__ x_scale,
-    uint8_t* __restrict__ x_sf, uint8_t* __restrict__ sfb) {
+    uint8_t* __restrict__ x_sf, uint8_t* __restrict__ sfb, int stage_x,
+    int32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t xstage[];
   __shared__ int32_t rows[32];
   __shared__ int32_t my_e[32];
   __shared__ int32_t before[32];
   __shared__ int64_t sfb_base[32];
   __shared__ float warp_max[32];
+  __shared__ __align__(8) uint64_t xbar;
+  const int t = blockIdx.x;
+  const bool staged = AQ == kActFp8Row && stage_x != 0;
+  if (staged && threadIdx.x == 0) {
+    mbar_init(&xbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&xbar, static_cast<uint32_t>(H) * 2u);
+    bulk_load(xstage, x + static_cast<size_t>(t) * H, static_cast<uint32_t>(H) * 2u, &xbar);
+  }
   griddep_wait();
   griddep_launch_dependents();
-  const int t = blockIdx.x;
   const int chunk = t / kRouteChunk, t0 = chunk * kRouteChunk;
   if (static_cast<int>(threadIdx.x) < k) {
     my_e[threadIdx.x] = ids[static_cast<size_t>(t) * k + threadIdx.x];
@@ -574,10 +627,18 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
       sfb_base[j] = sfb_row_base(r, offsets[e], tile_plan[e], H / kTileK);
   }
   __syncthreads();
-  if constexpr (AQ == kActFp8Row)
-    quantize_token<2>(x, t, k, H, rows, warp_max, xq, x_scale);   // 256 threads
-  else
+  if constexpr (AQ == kActFp8Row) {
+    if (staged) {
+      int32_t none = 0;
+      if (!mbar_wait(&xbar, 0, 1000000000ull, status, kDevTimeout, &none)) return;
+      quantize_token_staged(reinterpret_cast<const __nv_bfloat16*>(xstage), k, H, rows,
+                            warp_max, xq, x_scale);
+    } else {
+      quantize_token<2>(x, t, k, H, rows, warp_max, xq, x_scale);   // 256 threads
+    }
+  } else {
     quantize_token_mx<AQ == kActSplit>(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
+  }
 }
 
 // Small batches (T <= kSmallT = 256): one kernel replaces scan +
@@ -794,16 +855,19 @@ cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, in
                     ids, chunk_base, T, E, k, chunks, row_of, token_slot);
 }
 
-cudaError_t launch_quant_scatter(const void* x, const int32_t* chunk_base, const int32_t* ids,
-                                 const int32_t* offsets, const int2* tile_plan, int T, int E,
-                                 int k, int H, int32_t* row_of, int32_t* token_slot,
-                                 const QuantOut& q, cudaStream_t s) {
+cudaError_t launch_quant_scatter(const void* x, bool x_on_device, const int32_t* chunk_base,
+                                 const int32_t* ids, const int32_t* offsets, const int2* tile_plan,
+                                 int T, int E, int k, int H, int32_t* row_of, int32_t* token_slot,
+                                 const QuantOut& q, int32_t* status, cudaStream_t s) {
   auto kern = q.act == kActSplit    ? quant_scatter_kernel<kActSplit>
               : q.act == kActMxfp8 ? quant_scatter_kernel<kActMxfp8>
                                    : quant_scatter_kernel<kActFp8Row>;
-  return launch_pdl(kern, dim3(T), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(x),
-                    chunk_base, ids, offsets, tile_plan, E, k, H, row_of, token_slot, q.xq,
-                    q.x_scale, q.x_sf, q.sfb);
+  // the staged row within the default shared-memory limit (48 KB)
+  const bool stage = q.act == kActFp8Row && x_on_device && H * 2 <= 48 * 1024;
+  return launch_pdl(kern, dim3(T), dim3(256), stage ? static_cast<size_t>(H) * 2 : 0, s,
+                    static_cast<const __nv_bfloat16*>(x), chunk_base, ids, offsets, tile_plan, E,
+                    k, H, row_of, token_slot, q.xq, q.x_scale, q.x_sf, q.sfb, stage ? 1 : 0,
+                    status);
 }
 
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
