@@ -131,13 +131,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
                                                       __nv_bfloat16* __restrict__ out) {
   __shared__ int32_t rows[32];
   __shared__ float w[32];
+  const int t = blockIdx.x;
+  // The row map and the routing weights come from the front end, which
+  // finished before the previous kernel passed its wait (every kernel
+  // signals its dependents only after its own wait), so they are read
+  // before this grid's wait; y, the previous kernel's output, after it.
+  if (static_cast<int>(threadIdx.x) < k) {
+    rows[threadIdx.x] = __ldcg(row_of + static_cast<size_t>(t) * k + threadIdx.x);
+    w[threadIdx.x] = __ldcg(wts + static_cast<size_t>(t) * k + threadIdx.x);
+  }
   griddep_wait();
   griddep_launch_dependents();
-  const int t = blockIdx.x;
-  if (static_cast<int>(threadIdx.x) < k) {
-    rows[threadIdx.x] = row_of[static_cast<size_t>(t) * k + threadIdx.x];
-    w[threadIdx.x] = wts[static_cast<size_t>(t) * k + threadIdx.x];
-  }
   __syncthreads();
   const int i = blockIdx.y * blockDim.x + threadIdx.x;   // 16-byte vector index
   if (i >= H / 8) return;
