@@ -419,6 +419,8 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* token_slot = at<int32_t>(ws, L.token_slot);
   MOE_CUDA(mark());
+  // large batches: the scan writes the tile list, the scatter kernel follows
+  const bool large_front = !(T <= moe::kTinyT && mode == MOE_W4A8_MXFP4_FP8) && T > moe::kSmallT;
   if (T <= moe::kTinyT && mode == MOE_W4A8_MXFP4_FP8) {
     MOE_CUDA(moe::launch_route_expand_tiny(logits, x, T, E, k, H, bn, ids, wts,
                                            at<int32_t>(ws, L.counts), offsets, tiles, num_tiles,
@@ -451,7 +453,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
                    tiled ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, grid1,
                    prefetch, act, sfb1, static_cast<const uint8_t*>(w1), pair ? tm_xp : nullptr,
-                   L.max_tiles};
+                   L.max_tiles, large_front};
   MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
   if (tiled)
@@ -463,7 +465,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
                    tiled ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, grid2,
                    prefetch, act, sfb2, static_cast<const uint8_t*>(w2), pair ? tm_hp : nullptr,
-                   L.max_tiles};
+                   L.max_tiles, true};
   MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());
   MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));

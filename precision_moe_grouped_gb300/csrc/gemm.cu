@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
                         int m_per_expert, int K, int out_ld, int32_t* __restrict__ status,
                         uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages,
                         const uint8_t* __restrict__ sfb_tiled,
-                        const uint8_t* __restrict__ w_base, int max_tiles) {
+                        const uint8_t* __restrict__ w_base, int max_tiles, int early_list) {
   using C = GemmCfg<BN, STAGES, NI, NB, ACT>;
   // A = E2M1 weights, or E4M3 in MXFP8; B = activations: E4M3
   constexpr uint32_t kAFmt = ACT == kActMxfp8 ? 0u : 5u;
@@ -200,15 +200,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
   tc_fence_after();
   // Everything above overlaps the previous kernel's tail; the tile list and
   // the activations are that kernel's (or an earlier one's) output.
-  // GEMM2's weight and scale copies need only the tile list, which the
-  // expansion kernel wrote before GEMM1 started its work; this grid starts
-  // after GEMM1 has passed that point (each kernel signals its dependents
-  // only after its own wait).  So the weight and scale lanes of the
-  // producer warps issue their stage's first fill, reading the list through
-  // L2, before the producer warps wait for the h quantisation with the rest
-  // of the CTA: the ring fills while the previous kernels finish.
+  // The weight and scale copies need only the tile list.  When it was
+  // complete before the previous kernel passed its own wait (early_list:
+  // GEMM2, whose list the expansion wrote before GEMM1 started its work, and
+  // GEMM1 after the large-batch expansion, whose list the scan wrote before
+  // the scatter kernel started) -- each kernel signals its dependents only
+  // after its own wait, so this grid starts after that point -- the weight
+  // and scale lanes of the producer warps issue their stage's first fill,
+  // reading the list through L2, before the producer warps wait with the
+  // rest of the CTA: the ring fills while the previous kernels finish.
   constexpr int LPS = C::kLanesPerStage;
-  const bool preissue = !SWIGLU && !kChecks && LPS == 3;
+  const bool preissue = early_list != 0 && !kChecks && LPS == 3;
   const bool early = preissue && warp < C::kProdWarps;
   if (!early) {
     griddep_wait();
@@ -537,7 +539,7 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
                     *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
                     static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status,
                     a.timeout_ns, a.a_tx_bytes, a.prefetch_stages, a.sfb_tiled, a.w_base,
-                    a.max_tiles);
+                    a.max_tiles, a.early_list ? 1 : 0);
 }
 
 }  // namespace

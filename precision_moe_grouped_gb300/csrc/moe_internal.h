@@ -195,6 +195,9 @@ struct GemmArgs {
   const uint8_t* w_base;       // prepared weight boxes (for the optional L2 prefetcher)
   const CUtensorMap* tmap_x_pair;  // kNumXMaps maps, box heights kPairBoxRowsAt (or null)
   int32_t max_tiles;           // entries the tile list's allocation holds
+  // The tile list was complete before the previous kernel passed its grid
+  // wait, so the weight copies may start before this kernel's wait.
+  bool early_list;
 };
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
