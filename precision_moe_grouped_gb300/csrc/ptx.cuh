@@ -228,43 +228,6 @@ __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
                : "memory");
 }
 
-__device__ __forceinline__ void tc_cp_32x128b_x4_warp(uint32_t taddr, uint64_t sdesc) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
-      "l"(sdesc)
-      : "memory");
-}
-
-// D(tmem) (+)= A(smem) x B(smem)^T with per-32-K E8M0 scale factors read from
-// TMEM, .kind::mxf8f6f4 (operand types come from the instruction descriptor).
-__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
-      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
-}
-
-// Warp-wide form of tc_mma_mx (one elected lane issues).
-__device__ __forceinline__ void tc_mma_mx_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t sfa_tmem,
-                                               uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
-      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
-}
-
 // One 128-K pipeline stage from one elected lane, in a single block so that
 // the warp elects once: the weight scales into TMEM (32x128b.warpx4 from
 // sfa_src), the 4 block-scaled MMAs of K sub-steps 0..3 (A and B advanced

@@ -355,3 +355,14 @@ def test_scan_stages_counts_in_several_batches():
     cfg = MI.custom_config(1024, 2, 128, 128)
     run, _ = full_parity(MI.make_case(cfg, 2000, seed=97), name="scan_batches")
     check_tiles(run, 160)
+
+
+@pytest.mark.parametrize("T", [40, 400])
+def test_long_h_rows_take_the_register_quantisation(T):
+    """I = 4224 (> 4096): the h quantisation keeps its register form instead
+    of staging 8 rows in shared memory; T = 400 also takes the large-batch
+    expansion.  (The scatter kernel's register form, for rows it does not
+    stage, runs in the page-locked host-buffer tests.)  Every code and scale
+    is bit-exact, the outputs within the tolerance."""
+    cfg = MI.custom_config(8, 2, 256, 4224)
+    full_parity(MI.make_case(cfg, T, seed=77 + T), name=f"long_h_{T}")
