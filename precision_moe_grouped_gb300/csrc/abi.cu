@@ -458,7 +458,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   MOE_CUDA(mark());
   if (tiled)
     MOE_CUDA(moe::launch_hquant_mx(act, h, R, I, ids, token_slot, offsets, tile_plan, hq, h_sf,
-                                   sfb2, st));
+                                   sfb2, status, timeout_ns, st));
   else
     MOE_CUDA(moe::launch_hquant(h, R, I, hq, h_scale, status, timeout_ns, st));
   MOE_CUDA(mark());

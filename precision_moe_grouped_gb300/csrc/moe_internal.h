@@ -249,7 +249,7 @@ cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_sca
 cudaError_t launch_hquant_mx(int act, const void* h, int R, int I, const int32_t* ids,
                              const int32_t* token_slot, const int32_t* offsets,
                              const int2* tile_plan, uint8_t* hq, uint8_t* h_sf, uint8_t* sfb,
-                             cudaStream_t s);
+                             int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
                            int H, void* out, cudaStream_t s);
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);

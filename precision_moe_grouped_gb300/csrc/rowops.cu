@@ -80,27 +80,53 @@ __global__ void __launch_bounds__(256) hquant_staged_kernel(const __nv_bfloat16*
 // with the lo terms in columns [I, 2I)), scale bytes to the row-major h_sf
 // [R, I/32] (or [R, 2I/32], lo blocks after the hi blocks) and to GEMM2's
 // per-tile layout (row r's expert from its (token, slot), its tile from the
-// expert's plan; split: the lo byte kSfbLoOffset after the hi byte).
+// expert's plan; split: the lo byte kSfbLoOffset after the hi byte).  With
+// `staged` (rows of at most kHqStageMaxI elements) the block's
+// kHqStageRows rows come into shared memory by one bulk copy first, as in
+// hquant_staged_kernel.
 template <bool SPLIT>
 __global__ void __launch_bounds__(256) hquant_mx_kernel(
     const __nv_bfloat16* __restrict__ h, int R, int I, const int32_t* __restrict__ ids,
     const int32_t* __restrict__ token_slot, const int32_t* __restrict__ offsets,
     const int2* __restrict__ tile_plan, uint8_t* __restrict__ hq, uint8_t* __restrict__ h_sf,
-    uint8_t* __restrict__ sfb) {
+    uint8_t* __restrict__ sfb, int staged, int32_t* __restrict__ status, uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t hstage[];
+  __shared__ __align__(8) uint64_t bar;
   griddep_launch_dependents();   // as hquant_kernel: GEMM2 may start streaming weights
+  const int r0 = blockIdx.x * kHqStageRows;
+  const int nr = min(kHqStageRows, R - r0);
+  if (staged) {
+    // as hquant_staged_kernel: the block's rows by one bulk copy
+    if (threadIdx.x == 0) {
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+  }
   griddep_wait();
-  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= R) return;
+  if (staged) {
+    if (threadIdx.x == 0) {
+      const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(I) * 2u;
+      mbar_arrive_expect_tx(&bar, bytes);
+      bulk_load(hstage, h + static_cast<size_t>(r0) * I, bytes, &bar);
+    }
+    int32_t none = 0;
+    if (!mbar_wait(&bar, 0, timeout_ns, status, kDevTimeout, &none)) return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = r0 + warp;
+  if (warp >= nr) return;
   const int e = ids[token_slot[r]];
   const int64_t base = sfb_row_base(r, offsets[e], tile_plan[e], I / kTileK);
-  const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(r) * I);
+  const uint4* hr = staged
+                        ? reinterpret_cast<const uint4*>(hstage) + static_cast<size_t>(warp) * I / 8
+                        : reinterpret_cast<const uint4*>(h + static_cast<size_t>(r) * I);
   const int nblk = I / 32;
   const int64_t W = SPLIT ? 2 * I : I, nsf = SPLIT ? 2 * nblk : nblk;
   for (int b = lane; b < nblk; b += 32) {
     uint4 q[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = __ldcg(hr + 4 * b + i);
+    for (int i = 0; i < 4; ++i) q[i] = staged ? hr[4 * b + i] : __ldcg(hr + 4 * b + i);
     uint8_t sbyte, lbyte = 0;
     uint4 codes[2], lcodes[2];
     if constexpr (SPLIT)
@@ -185,13 +211,19 @@ cudaError_t launch_hquant(const void* h, int R, int I, uint8_t* hq, float* h_sca
 cudaError_t launch_hquant_mx(int act, const void* h, int R, int I, const int32_t* ids,
                              const int32_t* token_slot, const int32_t* offsets,
                              const int2* tile_plan, uint8_t* hq, uint8_t* h_sf, uint8_t* sfb,
-                             cudaStream_t s) {
+                             int32_t* status, uint64_t timeout_ns, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  const int blocks = (R + 7) / 8;
+  const int blocks = (R + kHqStageRows - 1) / kHqStageRows;
   auto kern = act == kActSplit ? hquant_mx_kernel<true> : hquant_mx_kernel<false>;
-  return launch_pdl(kern, dim3(blocks), dim3(256), 0, s,
+  const bool staged = I <= kHqStageMaxI;
+  static DeviceOnce smem_set[2];   // the limit for the longest staged row, once
+  const cudaError_t e = set_smem_limit_once(kern, kHqStageRows * kHqStageMaxI * 2,
+                                            smem_set[act == kActSplit ? 1 : 0]);
+  if (e != cudaSuccess) return e;
+  const size_t smem = staged ? static_cast<size_t>(kHqStageRows) * I * 2 : 0;
+  return launch_pdl(kern, dim3(blocks), dim3(32 * kHqStageRows), smem, s,
                     static_cast<const __nv_bfloat16*>(h), R, I, ids, token_slot, offsets,
-                    tile_plan, hq, h_sf, sfb);
+                    tile_plan, hq, h_sf, sfb, staged ? 1 : 0, status, timeout_ns);
 }
 
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
