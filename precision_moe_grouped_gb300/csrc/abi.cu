@@ -468,7 +468,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
                    L.max_tiles, true};
   MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());
-  MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, st));
+  MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, status, timeout_ns, st));
   MOE_CUDA(mark());
   return MOE_OK;
 }

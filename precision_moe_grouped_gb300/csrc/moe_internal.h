@@ -250,8 +250,10 @@ cudaError_t launch_hquant_mx(int act, const void* h, int R, int I, const int32_t
                              const int32_t* token_slot, const int32_t* offsets,
                              const int2* tile_plan, uint8_t* hq, uint8_t* h_sf, uint8_t* sfb,
                              int32_t* status, uint64_t timeout_ns, cudaStream_t s);
+// status / timeout_ns: the bounded wait for the combine's staging copies.
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
-                           int H, void* out, cudaStream_t s);
+                           int H, void* out, int32_t* status, uint64_t timeout_ns,
+                           cudaStream_t s);
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);
 // The grouped GEMM on CTA pairs (gemm_pair.cu): W4A8 operands, M-tiles
 // taken two at a time, so m_per_expert must be a multiple of 256; needs

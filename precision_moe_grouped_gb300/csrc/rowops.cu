@@ -1,6 +1,7 @@
 // rowops.cu -- the memory-bound row kernels between and after the GEMMs:
 // per-row FP8 quantisation of h (GEMM2's input), the top-k weighted combine,
-// and the bounded-wait self test (their per-row arithmetic: rowops.cuh).
+// and the bounded-wait self test (the h quantisation's per-row arithmetic:
+// rowops.cuh).
 //
 // Pages cited (title and section):
 //   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add
@@ -148,15 +149,21 @@ __global__ void __launch_bounds__(256) hquant_mx_kernel(
   }
 }
 
-// Grid (T, ceil(H / 1024)): CTA (t, b) computes out[t, 1024 b .. 1024 b + 1023]
-// with combine_vec, 8 bf16 (16 bytes) per thread.
-__global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ y,
-                                                      const float* __restrict__ wts,
-                                                      const int32_t* __restrict__ row_of,
-                                                      int k, int H,
-                                                      __nv_bfloat16* __restrict__ out) {
+// The top-k weighted combine [P4793 walkthrough: finalize fusion]: grid (T,
+// ceil(H / 1024)); block (t, b) computes out[t, 1024 b .. 1024 b + 1023] =
+// bf16( sum_j w[t, j] * y[row(t, j), c] ), float32 fused multiply-adds from 0
+// in slot order j = 0 .. k-1, 8 columns (16 bytes) per thread.  The block's
+// k row chunks (its 1024 columns of each of the token's k rows of y) come
+// into shared memory by k bulk copies issued together, then are summed from
+// there.  A timed-out wait for the copies records MOE_ERR_DEVICE_TIMEOUT.
+__global__ void __launch_bounds__(128) combine_staged_kernel(
+    const __nv_bfloat16* __restrict__ y, const float* __restrict__ wts,
+    const int32_t* __restrict__ row_of, int k, int H, __nv_bfloat16* __restrict__ out,
+    int32_t* __restrict__ status, uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t ystage[];   // [k][1024] bf16
   __shared__ int32_t rows[32];
   __shared__ float w[32];
+  __shared__ __align__(8) uint64_t bar;
   const int t = blockIdx.x;
   // The row map and the routing weights come from the front end, which
   // finished before the previous kernel passed its wait (every kernel
@@ -166,12 +173,44 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
     rows[threadIdx.x] = __ldcg(row_of + static_cast<size_t>(t) * k + threadIdx.x);
     w[threadIdx.x] = __ldcg(wts + static_cast<size_t>(t) * k + threadIdx.x);
   }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
   griddep_wait();
   griddep_launch_dependents();
   __syncthreads();
-  const int i = blockIdx.y * blockDim.x + threadIdx.x;   // 16-byte vector index
-  if (i >= H / 8) return;
-  combine_vec(y, w, rows, k, H, t, i, out);
+  const int c0 = blockIdx.y * 1024;                       // first column
+  const int ncol = min(1024, H - c0);                     // a multiple of 128
+  const uint32_t bytes = static_cast<uint32_t>(ncol) * 2u;
+  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&bar, bytes * static_cast<uint32_t>(k));
+    __syncwarp();
+    if (static_cast<int>(threadIdx.x) < k)
+      bulk_load(ystage + static_cast<size_t>(threadIdx.x) * 2048,
+                y + static_cast<size_t>(rows[threadIdx.x]) * H + c0, bytes, &bar);
+  }
+  int32_t none = 0;
+  if (!mbar_wait(&bar, 0, timeout_ns, status, kDevTimeout, &none)) return;
+  const int i = threadIdx.x;   // the block's 16-byte vector
+  if (8 * i >= ncol) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < k; ++j) {
+    const uint4 q = reinterpret_cast<const uint4*>(ystage + static_cast<size_t>(j) * 2048)[i];
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&q);
+    const float wj = w[j];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 f = __bfloat1622float2(b[p]);
+      acc[2 * p] = fmaf(wj, f.x, acc[2 * p]);
+      acc[2 * p + 1] = fmaf(wj, f.y, acc[2 * p + 1]);
+    }
+  }
+  uint4 r;
+  __nv_bfloat162* rb = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) rb[p] = __floats2bfloat162_rn(acc[2 * p], acc[2 * p + 1]);
+  reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + c0)[i] = r;
 }
 
 // Waits on a barrier that nothing ever completes, with a bounded wait.
@@ -227,11 +266,16 @@ cudaError_t launch_hquant_mx(int act, const void* h, int R, int I, const int32_t
 }
 
 cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_of, int T, int k,
-                           int H, void* out, cudaStream_t s) {
+                           int H, void* out, int32_t* status, uint64_t timeout_ns,
+                           cudaStream_t s) {
   const int nvec = H / 8;
-  return launch_pdl(combine_kernel, dim3(T, (nvec + 127) / 128), dim3(128), 0, s,
+  const size_t smem = static_cast<size_t>(k) * 2048;   // <= 64 KB (k <= 32)
+  static DeviceOnce smem_set;
+  const cudaError_t e = set_smem_limit_once(combine_staged_kernel, 32 * 2048, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(combine_staged_kernel, dim3(T, (nvec + 127) / 128), dim3(128), smem, s,
                     static_cast<const __nv_bfloat16*>(y), wts, row_of, k, H,
-                    static_cast<__nv_bfloat16*>(out));
+                    static_cast<__nv_bfloat16*>(out), status, timeout_ns);
 }
 
 cudaError_t launch_timeout_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t s) {

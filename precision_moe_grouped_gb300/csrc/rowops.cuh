@@ -1,14 +1,11 @@
-// rowops.cuh -- the per-row arithmetic of the h quantisation and of the
-// top-k weighted combine (their kernels are in rowops.cu).
+// rowops.cuh -- the per-row arithmetic of the h quantisation (its kernels
+// are in rowops.cu).
 //
 // Pages cited (title and section):
 //   [P3738] flashinfer PR #3738, "perf: optimize MXFP4xBF16 & INT4xFP8 and add
 //           MXFP4xFP8 CUTLASS MoE backend for SM90": Description (per-token FP8
 //           scales threaded through activation and GEMM1/GEMM2), review
 //           comments (FP8 x MXFP4 quant params carry fc1 and fc2 token scales).
-//   [P4793] flashinfer PR #4793, "Unify MoE CuTe DSL dispatch to be dtype
-//           agnostic": walkthrough (grouped GEMM with finalize fusion: the
-//           top-k weighted un-permute of the expert outputs).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -145,32 +142,6 @@ __device__ __forceinline__ void hquant_row_smem(const __nv_bfloat16* hs, int r, 
     dst[i] = out;
   }
   if (lane == 0) h_scale[r] = nz ? amax / 448.0f : 1.0f;
-}
-
-// One 16-byte vector (8 outputs, columns 8i .. 8i + 7) of token t's combine:
-// out[t, c] = bf16( sum_j w[t, j] * y[row_j, c] ), float32 fused
-// multiply-adds from 0 in slot order j = 0 .. k-1.
-__device__ __forceinline__ void combine_vec(const __nv_bfloat16* __restrict__ y,
-                                            const float* w, const int32_t* rows, int k, int H,
-                                            int t, int i, __nv_bfloat16* __restrict__ out) {
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < k; ++j) {
-    const uint4 q =
-        __ldcg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(rows[j]) * H) + i);
-    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&q);
-    const float wj = w[j];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const float2 f = __bfloat1622float2(b[p]);
-      acc[2 * p] = fmaf(wj, f.x, acc[2 * p]);
-      acc[2 * p + 1] = fmaf(wj, f.y, acc[2 * p + 1]);
-    }
-  }
-  uint4 r;
-  __nv_bfloat162* rb = reinterpret_cast<__nv_bfloat162*>(&r);
-#pragma unroll
-  for (int p = 0; p < 4; ++p) rb[p] = __floats2bfloat162_rn(acc[2 * p], acc[2 * p + 1]);
-  reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[i] = r;
 }
 
 }  // namespace moe
