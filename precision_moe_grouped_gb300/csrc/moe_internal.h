@@ -234,7 +234,7 @@ cudaError_t launch_rank(const int32_t* ids, const int32_t* chunk_base, int T, in
 // scan leaves in chunk_base) into row_of / token_slot, and the token's
 // quantised activations into them.
 // x_on_device: x is device memory (else page-locked host memory read in
-// place), which lets the per-row FP8 form stage the row by a bulk copy.
+// place), which lets the kernel stage each token's row by a bulk copy.
 // status: where a timed-out wait for that copy is recorded.
 cudaError_t launch_quant_scatter(const void* x, bool x_on_device, const int32_t* chunk_base,
                                  const int32_t* ids, const int32_t* offsets, const int2* tile_plan,

@@ -471,7 +471,8 @@ __device__ void quantize_token_staged(const __nv_bfloat16* xs, int k, int H, con
   if (static_cast<int>(threadIdx.x) < k) x_scale[rows[threadIdx.x]] = s;
 }
 
-// MXFP8 (the W8A8 mode) quantisation of token t's row, per 32-element
+// MXFP8 (the W8A8 mode) quantisation of a token's row xrow (global or
+// shared memory), per 32-element
 // block: X = 2^clamp(floor(log2 amax) - 8, -127, 127) (8 = E4M3's emax),
 // codes = E4M3_rne_satfinite(x / X), scale byte = exponent + 127; an
 // all-zero block gets byte 127 (its codes are those of +-0).  Dividing by a
@@ -485,17 +486,16 @@ __device__ void quantize_token_staged(const __nv_bfloat16* xs, int k, int H, con
 // + b is b's lo term); in the per-tile layout the lo byte sits kSfbLoOffset
 // after the hi byte.
 template <bool SPLIT>
-__device__ void quantize_token_mx(const __nv_bfloat16* __restrict__ x, int t, int k, int H,
-                                  const int32_t* rows, const int64_t* sfb_base,
-                                  uint8_t* __restrict__ xq, uint8_t* __restrict__ x_sf,
-                                  uint8_t* __restrict__ sfb) {
-  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+__device__ void quantize_token_mx(const __nv_bfloat16* xrow, int k, int H, const int32_t* rows,
+                                  const int64_t* sfb_base, uint8_t* __restrict__ xq,
+                                  uint8_t* __restrict__ x_sf, uint8_t* __restrict__ sfb) {
+  const uint4* xr = reinterpret_cast<const uint4*>(xrow);   // the token's row (global or shared)
   const int nblk = H / 32;
   const int64_t W = SPLIT ? 2 * H : H, nsf = SPLIT ? 2 * nblk : nblk;
   for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
     uint4 q[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = __ldg(xr + 4 * b + i);
+    for (int i = 0; i < 4; ++i) q[i] = xr[4 * b + i];
     uint8_t sbyte, lbyte = 0;
     uint4 codes[2], lcodes[2];
     if constexpr (SPLIT)
@@ -569,8 +569,8 @@ __device__ void quantize_token_mx_lanes(const __nv_bfloat16* __restrict__ x, int
 
 // One CTA per token t: the rows of its k slots, then the quantisation of
 // the token into them (AQ: per-row FP8, MXFP8 or the two-term split).
-// stage_x (per-row FP8, x in device memory): the token's row comes into
-// shared memory by one bulk copy issued before the grid dependency wait --
+// stage_x (x in device memory): the token's row comes into shared memory by
+// one bulk copy issued before the grid dependency wait --
 // x is the forward's input, complete before the forward's first kernel
 // passed its own wait, hence before this grid started -- so the copy
 // overlaps the wait and the ranking.  Slot j's row is the chunk's base row for its expert e (from the
@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
   __shared__ float warp_max[32];
   __shared__ __align__(8) uint64_t xbar;
   const int t = blockIdx.x;
-  const bool staged = AQ == kActFp8Row && stage_x != 0;
+  const bool staged = stage_x != 0;
   if (staged && threadIdx.x == 0) {
     mbar_init(&xbar, 1);
     fence_mbar_init();
@@ -627,17 +627,19 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
       sfb_base[j] = sfb_row_base(r, offsets[e], tile_plan[e], H / kTileK);
   }
   __syncthreads();
+  const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(xstage);
+  if (staged) {
+    int32_t none = 0;
+    if (!mbar_wait(&xbar, 0, 1000000000ull, status, kDevTimeout, &none)) return;
+  }
   if constexpr (AQ == kActFp8Row) {
-    if (staged) {
-      int32_t none = 0;
-      if (!mbar_wait(&xbar, 0, 1000000000ull, status, kDevTimeout, &none)) return;
-      quantize_token_staged(reinterpret_cast<const __nv_bfloat16*>(xstage), k, H, rows,
-                            warp_max, xq, x_scale);
-    } else {
+    if (staged)
+      quantize_token_staged(xs, k, H, rows, warp_max, xq, x_scale);
+    else
       quantize_token<2>(x, t, k, H, rows, warp_max, xq, x_scale);   // 256 threads
-    }
   } else {
-    quantize_token_mx<AQ == kActSplit>(x, t, k, H, rows, sfb_base, xq, x_sf, sfb);
+    quantize_token_mx<AQ == kActSplit>(staged ? xs : x + static_cast<size_t>(t) * H, k, H, rows,
+                                       sfb_base, xq, x_sf, sfb);
   }
 }
 
@@ -863,7 +865,7 @@ cudaError_t launch_quant_scatter(const void* x, bool x_on_device, const int32_t*
               : q.act == kActMxfp8 ? quant_scatter_kernel<kActMxfp8>
                                    : quant_scatter_kernel<kActFp8Row>;
   // the staged row within the default shared-memory limit (48 KB)
-  const bool stage = q.act == kActFp8Row && x_on_device && H * 2 <= 48 * 1024;
+  const bool stage = x_on_device && H * 2 <= 48 * 1024;
   return launch_pdl(kern, dim3(T), dim3(256), stage ? static_cast<size_t>(H) * 2 : 0, s,
                     static_cast<const __nv_bfloat16*>(x), chunk_base, ids, offsets, tile_plan, E,
                     k, H, row_of, token_slot, q.xq, q.x_scale, q.x_sf, q.sfb, stage ? 1 : 0,
