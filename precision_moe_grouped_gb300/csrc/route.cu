@@ -97,14 +97,32 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, 
 }
 
 // One warp per token (32 warps = one chunk per CTA): route_token_warp, then
-// the chunk's per-expert histogram.
+// the chunk's per-expert histogram.  The logits are the forward's input,
+// complete before the previous kernel on the stream passed its own grid
+// wait (every kernel here signals its dependents only after that wait), so
+// the routing and the shared-memory histogram run before this kernel's
+// wait, overlapping the previous forward's last kernel; every global write
+// (which that kernel's reads of the workspace may still precede) follows
+// the wait.
 template <int NV>
 __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T,
                                                     int E, int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ wts,
                                                     int32_t* __restrict__ chunk_counts,
                                                     int32_t* __restrict__ status) {
+  static_assert(kRouteChunk == 32, "one warp per token of the chunk");
   extern __shared__ int32_t hist[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRouteChunk + warp;
+  int my_id = 0;
+  float my_w = 0.f;
+  if (warp < kRouteChunk && t < T) {
+    route_token_warp<NV>(logits + static_cast<size_t>(t) * E, E, k, lane, &my_id, &my_w);
+    if (lane < k) atomicAdd(&hist[my_id], 1);
+  }
+  __syncthreads();
   griddep_wait();
   griddep_launch_dependents();
   // the forward's first kernel clears the device status word
@@ -115,23 +133,10 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
       status[3] = E;
     }
   }
-  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const int t0 = blockIdx.x * kRouteChunk;
-  for (int tt = warp; tt < kRouteChunk; tt += nwarps) {
-    const int t = t0 + tt;
-    if (t >= T) break;
-    int my_id;
-    float my_w;
-    route_token_warp<NV>(logits + static_cast<size_t>(t) * E, E, k, lane, &my_id, &my_w);
-    if (lane < k) {
-      ids[static_cast<size_t>(t) * k + lane] = my_id;
-      wts[static_cast<size_t>(t) * k + lane] = my_w;
-      atomicAdd(&hist[my_id], 1);
-    }
+  if (warp < kRouteChunk && t < T && lane < k) {
+    ids[static_cast<size_t>(t) * k + lane] = my_id;
+    wts[static_cast<size_t>(t) * k + lane] = my_w;
   }
-  __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     chunk_counts[static_cast<size_t>(blockIdx.x) * E + i] = hist[i];
 }
@@ -723,10 +728,12 @@ __global__ void __launch_bounds__(1024, 2) expand_small_kernel(
 // CTA t:
 //   1. prefetches token t's row into L2; warp w routes token w (every CTA
 //      routes all T tokens -- the same selection and softmax as
-//      route_kernel; the logits are L2-resident after the first CTA);
-//   2. counts (shared atomics), offsets (block scan), the tile plan and the
-//      stable rank of token t's slots (earlier tokens routed to the same
-//      expert); CTA 0 writes counts, offsets and the tile list;
+//      route_kernel; the logits are L2-resident after the first CTA) and
+//      counts its experts (shared atomics) -- all before the grid wait, as
+//      in route_kernel: logits and x are the forward's inputs;
+//   2. after the wait: offsets (block scan), the tile plan and the stable
+//      rank of token t's slots (earlier tokens routed to the same expert);
+//      CTA 0 writes counts, offsets and the tile list;
 //   3. quantises token t into its k rows (quantize_token).
 template <int NV>
 __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
@@ -741,16 +748,7 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
   int32_t* sid = sm + E;                    // [kTinyT * 32] routed experts
   __shared__ int32_t rows[32];
   __shared__ float warp_max[32];
-  griddep_wait();
-  griddep_launch_dependents();
   const int t = blockIdx.x;
-  if (t == 0 && threadIdx.x == 0) {   // first kernel of the forward
-    status[0] = 0;
-    if (kChecks) {
-      status[2] = T * k;
-      status[3] = E;
-    }
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   {   // L2 prefetch of token t's row (2H bytes), 128-byte lines
     const char* base = reinterpret_cast<const char*>(x + static_cast<size_t>(t) * H);
@@ -759,21 +757,30 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
   }
   for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
+  int my_id = 0;
+  float my_w = 0.f;
   if (warp < T) {
-    int my_id;
-    float my_w;
     route_token_warp<NV>(logits + static_cast<size_t>(warp) * E, E, k, lane, &my_id, &my_w);
     if (lane < k) {
-      if (warp == t) {
-        const size_t ts = static_cast<size_t>(warp) * k + lane;
-        ids[ts] = my_id;
-        wts[ts] = my_w;
-      }
       sid[warp * 32 + lane] = my_id;
       atomicAdd(&cnt[my_id], 1);
     }
   }
   __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  if (t == 0 && threadIdx.x == 0) {   // first kernel of the forward
+    status[0] = 0;
+    if (kChecks) {
+      status[2] = T * k;
+      status[3] = E;
+    }
+  }
+  if (warp == t && lane < k) {
+    const size_t ts = static_cast<size_t>(warp) * k + lane;
+    ids[ts] = my_id;
+    wts[ts] = my_w;
+  }
   // counts -> offsets and the tile list (one block scan)
   const int e = threadIdx.x;
   const int c = e < E ? cnt[e] : 0;
