@@ -213,11 +213,26 @@ struct QuantOut {
   uint8_t* x_sf;
   uint8_t* sfb;
 };
+// GEMM1 weights the tiny-batch front end asks L2 for: the first `boxes` K
+// stages (prepared E2M1 boxes of kFp4BoxBytes, and their 512-byte scale
+// blocks) of GEMM1's items 0 .. first_items-1 (the items its CTAs take
+// first), from `ctas` extra CTAs.  Disabled when w is null or ctas == 0.
+constexpr int kFp4BoxBytes = kTileM * kTileK / 2;
+constexpr int kTinyPrefetchTiles = 160;   // tiles a prefetch CTA maps (>= the items of a round)
+struct TinyPrefetch {
+  const uint8_t* w;    // prepared w1 boxes
+  const uint8_t* sf;   // prepared w1 scale blocks
+  int32_t mt, ks;      // GEMM1's M-tiles per expert and K stages
+  int32_t first_items;
+  int32_t boxes;
+  int32_t ctas;
+};
 cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, int E, int k,
                                      int H, int bn, int32_t* ids, float* wts, int32_t* counts,
                                      int32_t* offsets, int4* tiles, int32_t* num_tiles,
                                      int2* tile_plan, int32_t* row_of, int32_t* token_slot,
-                                     uint8_t* xq, float* x_scale, int32_t* status, cudaStream_t s);
+                                     uint8_t* xq, float* x_scale, int32_t* status,
+                                     const TinyPrefetch& pf, cudaStream_t s);
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
                                 int bn, int32_t* counts, int32_t* offsets, int4* tiles,
                                 int32_t* num_tiles, int2* tile_plan, int32_t* row_of,

@@ -190,6 +190,7 @@ struct ExpertPlan {
   int toff;         // expert e's first tile
   int tsz;          // rows per tile
   int nt;           // tiles of expert e
+  int total_tiles;  // tiles of all experts
 };
 
 __device__ ExpertPlan plan_experts(int e, int E, int c, int bn, bool write,
@@ -207,7 +208,7 @@ __device__ ExpertPlan plan_experts(int e, int E, int c, int bn, bool write,
     if (tile_plan && e < E) tile_plan[e] = make_int2(ex.y, tsz);
     if (threadIdx.x == 0) *num_tiles = tot.y;
   }
-  return ExpertPlan{ex.x, tot.x, ex.y, tsz, nt};
+  return ExpertPlan{ex.x, tot.x, ex.y, tsz, nt, tot.y};
 }
 
 // Shared memory the scan stages chunk counts in (whole chunks of E counts).
@@ -742,14 +743,55 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
     int32_t* __restrict__ counts_out, int32_t* __restrict__ offsets_out, int4* __restrict__ tiles,
     int32_t* __restrict__ num_tiles, int2* __restrict__ tile_plan, int32_t* __restrict__ row_of,
     int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq, float* __restrict__ x_scale,
-    int32_t* __restrict__ status) {
+    int32_t* __restrict__ status, const TinyPrefetch pf) {
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;                        // [E] counts, then offsets
   int32_t* sid = sm + E;                    // [kTinyT * 32] routed experts
   __shared__ int32_t rows[32];
   __shared__ float warp_max[32];
+  __shared__ int32_t tile_expert[kTinyPrefetchTiles];
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (t >= T) {
+    // ---------------------------------------------------- prefetch CTAs
+    // Route the T tokens like the CTAs below, plan the tiles without
+    // writing them, and ask L2 for the first weight boxes (and their scale
+    // blocks) of the GEMM1 items that run first: items 0 .. first_items-1,
+    // item i = tile i / MT, M-tile i % MT.  Only inputs are read and
+    // nothing is written, so these CTAs never wait for the previous grid:
+    // the weight stream starts while the front end (and the previous
+    // forward's last kernel) runs.
+    for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    if (warp < T) {
+      int my_id;
+      float my_w;
+      route_token_warp<NV>(logits + static_cast<size_t>(warp) * E, E, k, lane, &my_id, &my_w);
+      if (lane < k) atomicAdd(&cnt[my_id], 1);
+    }
+    __syncthreads();
+    const int e = threadIdx.x;
+    const ExpertPlan pl = plan_experts(e, E, e < E ? cnt[e] : 0, bn, false, nullptr, nullptr,
+                                       nullptr);
+    if (e < E)
+      for (int i = 0; i < pl.nt && pl.toff + i < kTinyPrefetchTiles; ++i)
+        tile_expert[pl.toff + i] = e;
+    __syncthreads();
+    const int ntiles = min(pl.total_tiles, kTinyPrefetchTiles);
+    const int items = min(pf.first_items, ntiles * pf.mt);
+    const int nb = min(pf.boxes, pf.ks);
+    const int p = t - T, np = static_cast<int>(gridDim.x) - T;
+    for (int idx = threadIdx.x; idx < items * nb; idx += blockDim.x) {
+      const int it = p + (idx / nb) * np;   // this CTA's items: p, p + np, ...
+      if (it >= items) continue;
+      const int ks = idx % nb;
+      const int64_t box =
+          (static_cast<int64_t>(tile_expert[it / pf.mt]) * pf.mt + it % pf.mt) * pf.ks + ks;
+      bulk_prefetch_l2(pf.w + box * kFp4BoxBytes, kFp4BoxBytes);
+      bulk_prefetch_l2(pf.sf + box * 512, 512u);
+    }
+    return;
+  }
   {   // L2 prefetch of token t's row (2H bytes), 128-byte lines
     const char* base = reinterpret_cast<const char*>(x + static_cast<size_t>(t) * H);
     for (int i = threadIdx.x; i < (2 * H + 127) / 128; i += blockDim.x)
@@ -827,15 +869,19 @@ cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, 
                                      int H, int bn, int32_t* ids, float* wts, int32_t* counts,
                                      int32_t* offsets, int4* tiles, int32_t* num_tiles,
                                      int2* tile_plan, int32_t* row_of, int32_t* token_slot,
-                                     uint8_t* xq, float* x_scale, int32_t* status, cudaStream_t s) {
+                                     uint8_t* xq, float* x_scale, int32_t* status,
+                                     const TinyPrefetch& pf, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(E + kTinyT * 32) * sizeof(int32_t);
   const int nv = (E + 31) / 32;
   auto kern = nv <= 1 ? route_expand_tiny_kernel<1> : nv <= 2 ? route_expand_tiny_kernel<2>
             : nv <= 4 ? route_expand_tiny_kernel<4> : nv <= 8 ? route_expand_tiny_kernel<8>
             : nv <= 16 ? route_expand_tiny_kernel<16> : route_expand_tiny_kernel<32>;
-  return launch_pdl(kern, dim3(T), dim3(1024), smem, s, logits,
+  const bool on = pf.w && pf.sf && pf.ctas > 0 && pf.boxes > 0 && pf.first_items > 0 &&
+                  pf.mt > 0 && pf.ks > 0;
+  return launch_pdl(kern, dim3(T + (on ? pf.ctas : 0)), dim3(1024), smem, s, logits,
                     static_cast<const __nv_bfloat16*>(x), T, E, k, H, bn, ids, wts, counts,
-                    offsets, tiles, num_tiles, tile_plan, row_of, token_slot, xq, x_scale, status);
+                    offsets, tiles, num_tiles, tile_plan, row_of, token_slot, xq, x_scale, status,
+                    pf);
 }
 
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,
