@@ -225,6 +225,37 @@ int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void*
                          void* workspace, size_t workspace_bytes, void* stream,
                          const moe_options* opts);
 
+/* Workspace bytes moe_forward_host_steps needs: moe_workspace_size plus a
+ * second staging set (x, logits and out of one step).  0 for an invalid
+ * shape or mode. */
+size_t moe_steps_workspace_size(const moe_shape* shape, int32_t quant_mode);
+
+/* n_steps forwards of one shape, step i from host buffers x_host[i] (bf16
+ * [T,H]), logits_host[i] (float [T,E]) into out_host[i] (bf16 [T,H]), with
+ * the host<->device copies overlapped with the computation: two copy
+ * streams of its own move step i+1's inputs into one device staging set and
+ * step i-1's output out of the other while step i computes on `stream`
+ * (double-buffered staging; the first set is the workspace's x_stage /
+ * logits_stage / out_stage, the second follows the moe_workspace_size bytes).
+ * The overlap needs page-locked host buffers (cudaHostAlloc,
+ * cudaMallocHost, cudaHostRegister); others are copied synchronously by the
+ * runtime.  Each step's results equal moe_forward's on the same inputs
+ * [P3738 Description: the fused MoE forward; P4411 Description:
+ * caller-owned workspace].
+ *   workspace: device, 256-byte aligned, >= moe_steps_workspace_size bytes
+ *   opts: as moe_forward_ex; stage_events must be NULL (MOE_ERR_INVALID_ARG)
+ * Asynchronous: returns once everything is queued; `stream` reaches its end
+ * when every out_host[i] is written.  Host buffers must stay valid, and the
+ * outputs unread, until then.  Errors: the argument errors of moe_forward,
+ * n_steps < 0 or a NULL step pointer (MOE_ERR_INVALID_ARG), a workspace
+ * below moe_steps_workspace_size (MOE_ERR_WORKSPACE_TOO_SMALL); a CUDA error
+ * while queueing returns MOE_ERR_CUDA with the steps before it queued. */
+int32_t moe_forward_host_steps(const moe_shape* shape, int32_t quant_mode, int32_t n_steps,
+                               const void* const* x_host, const float* const* logits_host,
+                               const void* w1_p, const void* w1_sf_p, const void* w2_p,
+                               const void* w2_sf_p, void* const* out_host, void* workspace,
+                               size_t workspace_bytes, void* stream, const moe_options* opts);
+
 /* Reads the device status word of `workspace` (synchronises `stream`).
  * *status = MOE_OK or the moe_status of the first device-side error since
  * the workspace was last used by moe_forward (which clears it). */

@@ -10,13 +10,14 @@ from __future__ import annotations
 
 from . import _lib
 from ._lib import (MOE_W4A8_MXFP4_FP8, MOE_W4A16_MXFP4_BF16, MOE_W8A8_MXFP8, MoeError,
-                   MoeOptions, MoeShape, WsLayout, forward, forward_host, load, options,
-                   prepare_weights, read_device_status, selftest_timeout, shape,
-                   workspace_layout, workspace_size)
+                   MoeOptions, MoeShape, WsLayout, forward, forward_host, forward_host_steps,
+                   load, options, prepare_weights, read_device_status, selftest_timeout, shape,
+                   steps_workspace_size, workspace_layout, workspace_size)
 
 __all__ = ["FusedMoE", "MoeError", "MoeOptions", "MoeShape", "WsLayout", "forward",
-           "forward_host", "load", "options", "prepare_weights", "read_device_status",
-           "selftest_timeout", "shape", "workspace_layout", "workspace_size",
+           "forward_host", "forward_host_steps", "load", "options", "prepare_weights",
+           "read_device_status", "selftest_timeout", "shape", "steps_workspace_size",
+           "workspace_layout", "workspace_size",
            "MOE_W4A8_MXFP4_FP8", "MOE_W4A16_MXFP4_BF16", "MOE_W8A8_MXFP8"]
 
 

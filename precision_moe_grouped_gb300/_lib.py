@@ -31,7 +31,8 @@ MOE_W8A8_MXFP8 = 2
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_prepare_weights", "moe_forward",
            "moe_forward_ex", "moe_forward_host", "moe_read_device_status",
            "moe_selftest_timeout", "moe_last_error", "moe_stage_name", "moe_status_string",
-           "moe_version", "moe_route_noalloc")
+           "moe_version", "moe_route_noalloc", "moe_steps_workspace_size",
+           "moe_forward_host_steps")
 
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -105,6 +106,11 @@ def load() -> ctypes.CDLL:
     lib.moe_forward_ex.restype = i32
     lib.moe_forward_host.argtypes = [shp, i32] + [vp] * 8 + [sz, vp, ctypes.POINTER(MoeOptions)]
     lib.moe_forward_host.restype = i32
+    lib.moe_steps_workspace_size.argtypes = [shp, i32]
+    lib.moe_steps_workspace_size.restype = sz
+    lib.moe_forward_host_steps.argtypes = ([shp, i32, i32, vp, vp] + [vp] * 6 +
+                                           [sz, vp, ctypes.POINTER(MoeOptions)])
+    lib.moe_forward_host_steps.restype = i32
     lib.moe_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.moe_read_device_status.restype = i32
     lib.moe_selftest_timeout.argtypes = [vp, i32, vp]
@@ -156,6 +162,11 @@ def stage_event_array(events) -> "ctypes.Array":
 
 def workspace_size(s: MoeShape, mode: int = MOE_W4A8_MXFP4_FP8) -> int:
     return int(load().moe_workspace_size(ctypes.byref(s), mode))
+
+
+def steps_workspace_size(s: MoeShape, mode: int = MOE_W4A8_MXFP4_FP8) -> int:
+    """Workspace bytes of forward_host_steps (moe_steps_workspace_size)."""
+    return int(load().moe_steps_workspace_size(ctypes.byref(s), mode))
 
 
 def workspace_layout(s: MoeShape, mode: int = MOE_W4A8_MXFP4_FP8) -> WsLayout:
@@ -288,6 +299,32 @@ def forward_host(s: MoeShape, x_host, logits_host, w1_p, w1_sf_p, w2_p, w2_sf_p,
                                   _ptr(w1_p), _ptr(w1_sf_p), _ptr(w2_p), _ptr(w2_sf_p),
                                   _ptr(out_host), _ptr(workspace), nbytes, _stream(stream),
                                   ctypes.byref(opts) if opts is not None else None))
+
+
+def forward_host_steps(s: MoeShape, x_hosts, logits_hosts, w1_p, w1_sf_p, w2_p, w2_sf_p,
+                       out_hosts, workspace, mode: int = MOE_W4A8_MXFP4_FP8,
+                       opts: MoeOptions | None = None, stream=None,
+                       validate: bool = True) -> None:
+    """len(x_hosts) forwards, step i from host tensors x_hosts[i],
+    logits_hosts[i] into out_hosts[i], copies overlapped with the computation
+    (moe_forward_host_steps; page-locked host tensors for the overlap).  The
+    workspace holds steps_workspace_size(s, mode) bytes."""
+    n = len(x_hosts)
+    if len(logits_hosts) != n or len(out_hosts) != n:
+        _bad("x_hosts, logits_hosts and out_hosts must have the same length")
+    if validate:
+        dev = _current_device()
+        for i in range(n):
+            validate_forward(s, mode, x_hosts[i], logits_hosts[i], w1_p, w1_sf_p, w2_p, w2_sf_p,
+                             out_hosts[i], workspace, host=True, device=dev)
+    xs = (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in x_hosts])
+    ls = (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in logits_hosts])
+    os_ = (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in out_hosts])
+    nbytes = workspace.numel() * workspace.element_size()
+    check(load().moe_forward_host_steps(ctypes.byref(s), mode, n, xs, ls, _ptr(w1_p),
+                                        _ptr(w1_sf_p), _ptr(w2_p), _ptr(w2_sf_p), os_,
+                                        _ptr(workspace), nbytes, _stream(stream),
+                                        ctypes.byref(opts) if opts is not None else None))
 
 
 def read_device_status(workspace, stream=None) -> int:

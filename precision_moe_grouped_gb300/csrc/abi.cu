@@ -628,6 +628,122 @@ int32_t moe_forward_host(const moe_shape* shape, int32_t quant_mode, const void*
   return MOE_OK;
 }
 
+namespace {
+
+// moe_forward_host_steps: the second staging set, after moe_forward's
+// workspace (the first is the workspace's own x_stage / logits_stage /
+// out_stage).
+struct StepsLayout {
+  uint64_t x, logits, out, end;
+};
+
+StepsLayout steps_layout(const moe_shape* s, const moe_ws_layout& L) {
+  const uint64_t T = static_cast<uint64_t>(s->num_tokens), H = static_cast<uint64_t>(s->hidden),
+                 E = static_cast<uint64_t>(s->num_experts);
+  StepsLayout r;
+  uint64_t off = L.total;
+  r.x = off;
+  off = align_up(off + T * H * 2, kAlign);
+  r.logits = off;
+  off = align_up(off + T * E * 4, kAlign);
+  r.out = off;
+  r.end = align_up(off + T * H * 2, kAlign);
+  return r;
+}
+
+// The copy streams and events of one moe_forward_host_steps call; released
+// when the call returns (the runtime defers the release until the work
+// queued on them has finished).
+struct StepsSync {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, in_ready[2] = {}, consumed[2] = {}, out_free[2] = {};
+  cudaError_t create() {
+    cudaError_t e = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&start, &in_ready[0], &in_ready[1], &consumed[0], &consumed[1],
+                            &out_free[0], &out_free[1]})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    return e;
+  }
+  ~StepsSync() {
+    for (cudaEvent_t ev : {start, in_ready[0], in_ready[1], consumed[0], consumed[1], out_free[0],
+                           out_free[1]})
+      if (ev) cudaEventDestroy(ev);
+    if (h2d) cudaStreamDestroy(h2d);
+    if (d2h) cudaStreamDestroy(d2h);
+  }
+};
+
+}  // namespace
+
+size_t moe_steps_workspace_size(const moe_shape* shape, int32_t quant_mode) {
+  if (check_shape(shape, quant_mode) != MOE_OK) return 0;
+  moe_ws_layout L;
+  compute_layout(shape, quant_mode, &L);
+  return static_cast<size_t>(steps_layout(shape, L).end);
+}
+
+int32_t moe_forward_host_steps(const moe_shape* shape, int32_t quant_mode, int32_t n_steps,
+                               const void* const* x_host, const float* const* logits_host,
+                               const void* w1_p, const void* w1_sf_p, const void* w2_p,
+                               const void* w2_sf_p, void* const* out_host, void* workspace,
+                               size_t workspace_bytes, void* stream, const moe_options* opts) {
+  int32_t st = check_shape(shape, quant_mode);
+  if (st != MOE_OK) return st;
+  if (n_steps < 0) return fail(MOE_ERR_INVALID_ARG, "n_steps < 0");
+  if (opts && opts->stage_events)
+    return fail(MOE_ERR_INVALID_ARG, "stage_events is not supported over several steps");
+  if (shape->num_tokens == 0 || n_steps == 0) return MOE_OK;
+  if (!x_host || !logits_host || !out_host || !workspace)
+    return fail(MOE_ERR_INVALID_ARG, "a required pointer is NULL");
+  for (int32_t i = 0; i < n_steps; ++i)
+    if (!x_host[i] || !logits_host[i] || !out_host[i])
+      return fail(MOE_ERR_INVALID_ARG, "host buffer pointer of step %d is NULL", i);
+  moe_ws_layout L;
+  compute_layout(shape, quant_mode, &L);
+  const StepsLayout S = steps_layout(shape, L);
+  if (workspace_bytes < S.end)
+    return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < required %llu",
+                workspace_bytes, static_cast<unsigned long long>(S.end));
+  void* const xs[2] = {at<void>(workspace, L.x_stage), at<void>(workspace, S.x)};
+  float* const ls[2] = {at<float>(workspace, L.logits_stage), at<float>(workspace, S.logits)};
+  void* const os[2] = {at<void>(workspace, L.out_stage), at<void>(workspace, S.out)};
+  st = check_forward_args(shape, quant_mode, xs[0], ls[0], w1_p, w1_sf_p, w2_p, w2_sf_p, os[0],
+                          workspace, workspace_bytes, opts);
+  if (st != MOE_OK) return st;
+  const size_t T = shape->num_tokens, H = shape->hidden, E = shape->num_experts;
+  const size_t xb = T * H * 2, lb = T * E * 4, ob = T * H * 2;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StepsSync q;
+  MOE_CUDA(q.create());
+  // the copy streams start after the work already queued on `stream`
+  MOE_CUDA(cudaEventRecord(q.start, s));
+  MOE_CUDA(cudaStreamWaitEvent(q.h2d, q.start, 0));
+  MOE_CUDA(cudaStreamWaitEvent(q.d2h, q.start, 0));
+  for (int32_t i = 0; i < n_steps; ++i) {
+    const int b = i & 1;
+    // staging set b: its inputs were consumed by step i - 2 (recorded after
+    // that forward), its output copied out by step i - 2's D2H
+    if (i >= 2) MOE_CUDA(cudaStreamWaitEvent(q.h2d, q.consumed[b], 0));
+    MOE_CUDA(cudaMemcpyAsync(xs[b], x_host[i], xb, cudaMemcpyHostToDevice, q.h2d));
+    MOE_CUDA(cudaMemcpyAsync(ls[b], logits_host[i], lb, cudaMemcpyHostToDevice, q.h2d));
+    MOE_CUDA(cudaEventRecord(q.in_ready[b], q.h2d));
+    MOE_CUDA(cudaStreamWaitEvent(s, q.in_ready[b], 0));
+    if (i >= 2) MOE_CUDA(cudaStreamWaitEvent(s, q.out_free[b], 0));
+    st = run_forward(shape, quant_mode, xs[b], ls[b], w1_p, w1_sf_p, w2_p, w2_sf_p, os[b],
+                     workspace, s, opts, true);
+    if (st != MOE_OK) return st;
+    MOE_CUDA(cudaEventRecord(q.consumed[b], s));
+    MOE_CUDA(cudaStreamWaitEvent(q.d2h, q.consumed[b], 0));
+    MOE_CUDA(cudaMemcpyAsync(out_host[i], os[b], ob, cudaMemcpyDeviceToHost, q.d2h));
+    MOE_CUDA(cudaEventRecord(q.out_free[b], q.d2h));
+  }
+  // `stream` reaches its end once every output has reached the host
+  MOE_CUDA(cudaStreamWaitEvent(s, q.out_free[(n_steps - 1) & 1], 0));
+  if (n_steps >= 2) MOE_CUDA(cudaStreamWaitEvent(s, q.out_free[n_steps & 1], 0));
+  return MOE_OK;
+}
+
 int32_t moe_read_device_status(const void* workspace, void* stream, int32_t* status) {
   if (!workspace || !status) return fail(MOE_ERR_INVALID_ARG, "NULL workspace or status");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -1,7 +1,8 @@
 """The boundary from C: a C99 program compiled against include/moe.h (strict,
 pedantic, warnings as errors) links libmoe.so and calls the host-side entry
-points -- version and status strings, workspace size and layout, and a
-forward with NULL arguments, which must be rejected before any CUDA call."""
+points -- version and status strings, workspace sizes and layout, and a
+forward and a multi-step host forward with NULL arguments, which must be
+rejected before any CUDA call."""
 import os
 import shutil
 import subprocess
@@ -31,6 +32,10 @@ int main(void) {
   rc = moe_forward(&s, MOE_W4A8_MXFP4_FP8, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
                    NULL, 0, NULL);
   if (rc != MOE_ERR_INVALID_ARG) { printf("forward %d\n", (int)rc); return 5; }
+  if (moe_steps_workspace_size(&s, MOE_W4A8_MXFP4_FP8) <= bytes) return 7;
+  rc = moe_forward_host_steps(&s, MOE_W4A8_MXFP4_FP8, 2, NULL, NULL, NULL, NULL, NULL, NULL,
+                              NULL, NULL, 0, NULL, NULL);
+  if (rc != MOE_ERR_INVALID_ARG) { printf("steps %d\n", (int)rc); return 8; }
   s.num_experts = 0;
   if (moe_workspace_size(&s, MOE_W4A8_MXFP4_FP8) != 0) return 6;
   printf("ok %lu\n", (unsigned long)bytes);

@@ -167,6 +167,42 @@ def test_prepare_and_misc_validation_without_gpu(lib):
     assert lib.moe_status_string(-6) == b"device-side wait timed out"
 
 
+def _steps(lib, s, n, ptrs, x, lg, out, nbytes, opts=None):
+    arr = lambda v: (ctypes.c_void_p * len(v))(*v) if v is not None else None
+    return lib.moe_forward_host_steps(ctypes.byref(s), 0, n, arr(x), arr(lg), *ptrs, arr(out),
+                                      0x200000, nbytes, None,
+                                      ctypes.byref(opts) if opts is not None else None)
+
+
+def test_steps_workspace_and_validation_without_gpu(lib):
+    """moe_forward_host_steps: its workspace is moe_forward's plus a second
+    staging set (x, logits, out of one step, each 256-byte aligned); argument
+    errors return before any CUDA call."""
+    T, E, H = 16, 8, 256
+    s = _shape(T, E, 2, H, 128)
+    up = lambda n: (n + 255) // 256 * 256
+    need = P.steps_workspace_size(s)
+    assert need == P.workspace_size(s) + up(T * H * 2) + up(T * E * 4) + up(T * H * 2)
+    assert P.steps_workspace_size(s, 1) > need           # W4A16's larger workspace
+    assert P.steps_workspace_size(_shape(H=200)) == 0
+    w = [0x100000 * (i + 1) for i in range(4)]
+    hx, hl, ho = [0x7000] * 3, [0x8000] * 3, [0x9000] * 3
+    assert _steps(lib, s, -1, w, hx, hl, ho, need) == L.MOE_ERR_INVALID_ARG
+    assert _steps(lib, s, 0, w, None, None, None, 0) == L.MOE_OK
+    assert _steps(lib, _shape(T=0), 3, w, None, None, None, 0) == L.MOE_OK
+    assert _steps(lib, s, 3, w, None, hl, ho, need) == L.MOE_ERR_INVALID_ARG
+    assert _steps(lib, s, 3, w, hx, hl, [0x9000, None, 0x9000], need) == L.MOE_ERR_INVALID_ARG
+    assert _steps(lib, s, 3, w, hx, hl, ho, P.workspace_size(s)) == \
+        L.MOE_ERR_WORKSPACE_TOO_SMALL
+    mis = list(w)
+    mis[1] += 32                                          # w1_sf not 256-byte aligned
+    assert _steps(lib, s, 3, mis, hx, hl, ho, need) == L.MOE_ERR_MISALIGNED
+    ev = (ctypes.c_void_p * 9)(*([0x10] * 9))
+    o = P.options(stage_events=ev)
+    assert _steps(lib, s, 3, w, hx, hl, ho, need, opts=o) == L.MOE_ERR_INVALID_ARG
+    assert b"stage_events" in lib.moe_last_error()
+
+
 def test_no_device_gives_cuda_error(lib):
     """Valid arguments on a machine without a GPU: the first CUDA call fails
     and every entry point that reaches one returns MOE_ERR_CUDA with a
@@ -181,5 +217,8 @@ def test_no_device_gives_cuda_error(lib):
     assert lib.moe_last_error()
     assert lib.moe_prepare_weights(ctypes.byref(s), 0, *good, None) == L.MOE_ERR_CUDA
     assert lib.moe_selftest_timeout(0x100000, 10, None) == L.MOE_ERR_CUDA
+    hx = (ctypes.c_void_p * 2)(0x7000, 0x7000)
+    assert lib.moe_forward_host_steps(ctypes.byref(s), 0, 2, hx, hx, *good[:4], hx, 0x200000,
+                                      P.steps_workspace_size(s), None, None) == L.MOE_ERR_CUDA
     st = ctypes.c_int32(0)
     assert lib.moe_read_device_status(0x100000, None, ctypes.byref(st)) == L.MOE_ERR_CUDA

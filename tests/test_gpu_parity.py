@@ -246,6 +246,55 @@ def test_forward_host_matches_device_path(mode, T, pinned):
     np.testing.assert_array_equal(oh.float().numpy(), run.out_np())
 
 
+@pytest.mark.parametrize("mode", [MI.QUANT_W4A8, MI.QUANT_W4A16, MI.QUANT_W8A8])
+@pytest.mark.parametrize("T,n_steps", [(1, 5), (50, 2), (300, 3), (300, 1)])
+def test_forward_host_steps_match_device_path(mode, T, n_steps):
+    """moe_forward_host_steps: step i's inputs come in, and step i-1's output
+    goes out, on copy streams of their own through two device staging sets
+    while step i computes; every step's output equals the device-buffer
+    forward of its own inputs, bit for bit (distinct inputs per step, so a
+    staging set read by the wrong step shows)."""
+    cfg = MI.custom_config(8, 2, 256, 128, mode=mode)
+    cases = [MI.make_case(cfg, T, seed=31 + i) for i in range(n_steps)]
+    run0 = GpuRun(cases[0])
+    refs = [run0.out_np()] + [GpuRun(c, moe=run0.moe).out_np() for c in cases[1:]]
+    s = P.shape(T, 8, 2, 256, 128)
+    xs = [c.x.clone().pin_memory() for c in cases]
+    ls = [c.logits.clone().pin_memory() for c in cases]
+    outs = [torch.full((T, 256), float("nan"), dtype=torch.bfloat16).pin_memory()
+            for _ in range(n_steps)]
+    assert P.steps_workspace_size(s, mode) > P.workspace_size(s, mode)
+    ws = torch.zeros(P.steps_workspace_size(s, mode), dtype=torch.uint8, device="cuda:0")
+    m = run0.moe
+    P.forward_host_steps(s, xs, ls, m.w1_p, m.w1_sf_p, m.w2_p, m.w2_sf_p, outs, ws, mode=mode)
+    torch.cuda.current_stream().synchronize()
+    assert P.read_device_status(ws) == 0
+    for i in range(n_steps):
+        np.testing.assert_array_equal(outs[i].float().numpy(), refs[i])
+
+
+def test_forward_host_steps_pageable_and_short_workspace():
+    """Pageable host buffers give the same outputs (the copies just do not
+    overlap); the workspace of a single forward is too small."""
+    cfg = MI.custom_config(8, 2, 256, 128)
+    cases = [MI.make_case(cfg, 40, seed=51 + i) for i in range(3)]
+    run0 = GpuRun(cases[0])
+    refs = [run0.out_np()] + [GpuRun(c, moe=run0.moe).out_np() for c in cases[1:]]
+    s = P.shape(40, 8, 2, 256, 128)
+    outs = [torch.empty((40, 256), dtype=torch.bfloat16) for _ in range(3)]
+    m = run0.moe
+    small = torch.zeros(P.workspace_size(s), dtype=torch.uint8, device="cuda:0")
+    with pytest.raises(P.MoeError):
+        P.forward_host_steps(s, [c.x for c in cases], [c.logits for c in cases], m.w1_p,
+                             m.w1_sf_p, m.w2_p, m.w2_sf_p, outs, small)
+    ws = torch.zeros(P.steps_workspace_size(s), dtype=torch.uint8, device="cuda:0")
+    P.forward_host_steps(s, [c.x for c in cases], [c.logits for c in cases], m.w1_p, m.w1_sf_p,
+                         m.w2_p, m.w2_sf_p, outs, ws)
+    torch.cuda.current_stream().synchronize()
+    for o, r in zip(outs, refs):
+        np.testing.assert_array_equal(o.float().numpy(), r)
+
+
 def test_device_timeout_status_and_recovery():
     """A bounded wait that nothing satisfies returns an error status; the
     context stays usable for the next forward."""
