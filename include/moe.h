@@ -121,7 +121,16 @@ typedef struct {
                             kernel i, so event pairs time each kernel      */
   int32_t prefetch_stages; /* L2 prefetch distance of the GEMM weight stream,
                             in K stages: 0 = default (off), < 0 = off   */
-  int32_t reserved[3];   /* must be zero                                     */
+  int32_t gather_x;      /* W4A8 batches of more than MOE_SMALL_BATCH_TOKENS
+                            tokens with x in device memory, tile variants
+                            1-5: 1 = the expansion writes each token's FP8
+                            row once (token-major [T, H] in the xq region;
+                            the x_scale of every expanded row as before)
+                            and GEMM1's producers gather each tile's rows
+                            by token with asynchronous copies; 0 or -1 =
+                            the expanded [R, H] copy (the default: faster
+                            from T = 2048 on).  Ignored elsewhere.       */
+  int32_t reserved[2];   /* must be zero                                     */
 } moe_options;
 
 /* Byte offsets of the intermediate tensors inside the workspace, for tests

@@ -280,7 +280,9 @@ int32_t check_options(const moe_options* o) {
     return fail(MOE_ERR_INVALID_ARG, "tile_variant must be in [0, %d]", moe::kMaxTileVariant);
   if (o->timeout_ms < 0) return fail(MOE_ERR_INVALID_ARG, "timeout_ms < 0");
   if (o->prefetch_stages > 1024) return fail(MOE_ERR_INVALID_ARG, "prefetch_stages > 1024");
-  for (int i = 0; i < 3; ++i)
+  if (o->gather_x < -1 || o->gather_x > 1)
+    return fail(MOE_ERR_INVALID_ARG, "gather_x must be -1, 0 or 1");
+  for (int i = 0; i < 2; ++i)
     if (o->reserved[i] != 0) return fail(MOE_ERR_INVALID_ARG, "reserved option fields must be 0");
   return MOE_OK;
 }
@@ -421,12 +423,17 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   const int grid2 = gemm_grid(dev.num_sms, T, k, E, H / moe::kTileM);
   // the first kernel clears the status word; tiny batches (W4A8) route,
   // expand and quantise in one kernel, small batches expand in one kernel
-  const moe::QuantOut qx{xq, x_scale, act, x_sf, sfb1};
+  // GEMM1 gathers token-major activation rows (W4A8 large batches with x on
+  // the device, staged by the expansion; not on CTA pairs)
+  const bool large = !(T <= moe::kTinyT && mode == MOE_W4A8_MXFP4_FP8) && T > moe::kSmallT;
+  const bool gather = opts && opts->gather_x > 0 && mode == MOE_W4A8_MXFP4_FP8 && large &&
+                      x_on_device && H * 2 <= 48 * 1024 && moe::gemm_gather_supported(variant);
+  const moe::QuantOut qx{xq, x_scale, act, x_sf, sfb1, gather};
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* token_slot = at<int32_t>(ws, L.token_slot);
   MOE_CUDA(mark());
   // large batches: the scan writes the tile list, the scatter kernel follows
-  const bool large_front = !(T <= moe::kTinyT && mode == MOE_W4A8_MXFP4_FP8) && T > moe::kSmallT;
+  const bool large_front = large;
   if (T <= moe::kTinyT && mode == MOE_W4A8_MXFP4_FP8) {
     // extra CTAs of the front end start GEMM1's weight stream into L2: the
     // first kTinyPrefetchBoxes K stages of the items GEMM1's CTAs take
@@ -470,7 +477,8 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   moe::GemmArgs g1{&tm_w1, tm_x, &tm_sf1, tiles, num_tiles,
                    tiled ? nullptr : x_scale, h, 2 * I, H, I, status, timeout_ns, w_tx, grid1,
                    prefetch, act, sfb1, static_cast<const uint8_t*>(w1), pair ? tm_xp : nullptr,
-                   L.max_tiles, large_front};
+                   L.max_tiles, large_front, gather ? token_slot : nullptr, k,
+                   gather ? xq : nullptr};
   MOE_CUDA(moe::launch_gemm(true, variant, g1, st));
   MOE_CUDA(mark());
   if (tiled)

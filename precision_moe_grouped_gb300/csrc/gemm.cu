@@ -45,6 +45,15 @@
 // the columns); the last warp = optional L2 prefetcher.  Two TMEM accumulator
 // buffers let the epilogue of one item overlap the main loop of the next.
 //
+// Gathered activations (W4A8 GEMM1, opt-in): with gather_slot set, the
+// activations are token-major ([T, K]: each token's FP8 row written once by
+// the expansion) and each stage's producer warp copies the tile's rows by
+// token (token = gather_slot[row] / gather_k) with 16-byte asynchronous
+// copies into the slot's 128-byte-swizzled box, arriving on the slot's
+// barrier as they land -- the gather-fused grouped GEMM of [P4793] (file
+// list: blockscaled_contiguous_gather_grouped_gemm_act_fusion), without the
+// expanded [R, K] copy.
+//
 // Epilogues:
 //   GEMM1 (SWIGLU): acc * s_x[row] -> h = silu(gate) * up -> bf16 h[row, f].
 //     Prepared w1 rows put gate feature f in tile row 32q + i and up feature f
@@ -96,7 +105,14 @@ struct GemmCfg {
   static constexpr int kNumBars = 2 * STAGES + 2 * NB + 1 + NI;
   static constexpr int kOffBar = kOffSFB + (kTiledSfb ? 0 : 512);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + base alignment slack
+  // W4A8: each producer warp's token list of its current tile (one int per
+  // tile row) for GEMM1 gathering token-major activations, where it fits
+  static constexpr int kTokBytes = ACT == kActFp8Row ? kProdWarps * BN * 4 : 0;
+  static constexpr bool kGatherFits =
+      kTokBytes > 0 && kOffMisc + 16 + kTokBytes + 1024 <= 232448;
+  static constexpr int kOffTok = kOffMisc + 16;
+  static constexpr int kSmemBytes =
+      kOffMisc + 16 + (kGatherFits ? kTokBytes : 0) + 1024;   // + base alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
   // TMEM columns: for each of the NB accumulator buffers, one fp32
   // accumulator of BN columns per MMA issuer (buffer a, issuer i at column
@@ -128,7 +144,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
                         int m_per_expert, int K, int out_ld, int32_t* __restrict__ status,
                         uint64_t timeout_ns, uint32_t a_tx_bytes, int prefetch_stages,
                         const uint8_t* __restrict__ sfb_tiled,
-                        const uint8_t* __restrict__ w_base, int max_tiles, int early_list) {
+                        const uint8_t* __restrict__ w_base, int max_tiles, int early_list,
+                        const int32_t* __restrict__ gather_slot, int gather_k,
+                        const uint8_t* __restrict__ xg) {
   using C = GemmCfg<BN, STAGES, NI, NB, ACT>;
   // A = E2M1 weights, or E4M3 in MXFP8; B = activations: E4M3
   constexpr uint32_t kAFmt = ACT == kActMxfp8 ? 0u : 5u;
@@ -156,9 +174,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
   int ni = NI < KS ? NI : KS;
   while (STAGES % ni != 0) --ni;
 
+  // GEMM1 of W4A8 with gather_slot: the activations are token-major (xg,
+  // [T, K] codes); each stage's producer warp copies the weights and scales
+  // (lane 0, one arrival) and gathers the tile's rows by token with vector
+  // loads and swizzled shared stores (one more arrival).
+  const bool gather = C::kGatherFits && ACT == kActFp8Row && SWIGLU && gather_slot != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full + s, C::kLanesPerStage);   // each producer lane arrives with its bytes
+      // each producer lane arrives with its bytes (gathering: lane 0 with
+      // the weight bytes, and every lane of the warp once its copies land)
+      mbar_init(full + s, gather ? 1 + 32 : C::kLanesPerStage);
       mbar_init(empty + s, 1);
     }
     for (int a = 0; a < NB; ++a) {
@@ -330,16 +355,94 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
     return false;
   };
 
+  // Gathering producer warp s (the whole warp, warp-uniform): per fill, wait
+  // for the slot; lane 0 copies the weight box and its scales; the 32 lanes
+  // copy the tile's nmma rows (row r = token tok[r], K columns 128 ks ..
+  // +127) into the slot's 128-byte-swizzled activation box by 16-byte
+  // asynchronous copies (row (lane / 8) + 4 i, piece lane % 8), all in
+  // flight at once, each lane arriving on the slot's barrier when its copies
+  // land (the issuer fences the proxies after its wait).  first_only /
+  // skip_first as in produce (the token list is read only after the grid
+  // wait: the previous kernel wrote it).
+  auto produce_gather = [&](const int s, const bool first_only, const bool skip_first) -> bool {
+    if constexpr (C::kGatherFits && ACT == kActFp8Row && SWIGLU) {
+      uint32_t phase = 0;
+      bool issued = false;
+      int ks = s % KS, item = blockIdx.x + (s / KS) * gridDim.x;
+      int cur_item = -1, nmma = 16;
+      int4 td = make_int4(0, 0, 0, 0);
+      int64_t blk0 = 0;
+      int32_t* tok = reinterpret_cast<int32_t*>(smem + C::kOffTok) + s * BN;
+      const int c = lane & 7;
+      while (item < num_items) {
+        if (item != cur_item) {
+          cur_item = item;
+          td = !kChecks && item / MT == first_tile ? first_td : tile_at(item / MT, first_only);
+          blk0 = (static_cast<int64_t>(td.x) * MT + item % MT) * KS;
+          nmma = (td.z + 15) & ~15;
+          if (!first_only) {
+            // rows past the tile's count repeat its last row (their MMA
+            // columns are not stored)
+            const int last = max(td.z, 1) - 1;
+            __syncwarp();
+            for (int r = lane; r < nmma; r += 32)
+              tok[r] = __ldg(gather_slot + td.y + min(r, last)) / gather_k;
+            __syncwarp();
+          }
+        }
+        const int64_t blk = blk0 + ks;
+        const bool skip = skip_first && !issued;
+        if (!skip &&
+            !mbar_wait_warp(empty + s, phase ^ 1u, timeout_ns, status, kDevTimeout, abort_flag))
+          break;
+        if (!skip && lane == 0) {
+          mbar_arrive_expect_tx(full + s, a_tx_bytes + 512u);
+          tma_load_2d(smem + C::kOffA + s * C::kABytes, &tmap_w, 0,
+                      static_cast<int32_t>(blk * kTileM), full + s);
+          tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0, static_cast<int32_t>(blk),
+                      full + s);
+        }
+        if (first_only) return true;
+        uint8_t* b = smem + C::kOffB + s * C::kBBytes;
+        const uint8_t* src = xg + static_cast<int64_t>(ks) * kTileK + 16 * c;
+        for (int row = lane >> 3; row < nmma; row += 4)
+          cp_async_16(b + row * 128 + ((c ^ (row & 7)) << 4),
+                      src + static_cast<int64_t>(tok[row]) * K);
+        cp_async_arrive(full + s);   // each lane, once its copies have landed
+        issued = true;
+        phase ^= 1u;
+        ks += STAGES;
+        while (ks >= KS) {
+          ks -= KS;
+          item += gridDim.x;
+        }
+      }
+      if (first_only) return false;
+      // every issued copy lands before the CTA may exit (bounded)
+      if (issued) {
+        int32_t none = 0;
+        mbar_wait(full + s, phase ^ 1u, timeout_ns, status, kDevTimeout, &none);
+      }
+    }
+    return false;
+  };
+
   if (warp < C::kProdWarps) {
     const int s = warp + C::kProdWarps * (lane / LPS), role = lane % LPS;
     bool pre = false;
     if (early) {
-      if (s < STAGES && role != 1) pre = produce(s, role, true, false);
+      if (gather)
+        pre = produce_gather(warp, true, false);
+      else if (s < STAGES && role != 1)
+        pre = produce(s, role, true, false);
       __syncwarp();
       griddep_wait();
       griddep_launch_dependents();
     }
-    if (s < STAGES) produce(s, role, false, pre);
+    if (gather)
+      produce_gather(warp, false, pre);
+    else if (s < STAGES)
+      produce(s, role, false, pre);
   } else if (warp < C::kIssuer0 + NI) {
     // ------------------------------------------------------------ MMA issuers
     // Each tcgen05 instruction occupies its issuing warp (measured ~310
@@ -411,6 +514,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
               break;
             }
             tc_fence_after();
+            if (gather) fence_proxy_async_smem();   // gathered rows: generic-proxy copies
             issue_stage(static_cast<int>(stage), d_tmem, id0, nmma, ks == 0);
             if (prefetch_stages > 0 && lane == 0) *progress = fidx;
             ++fidx;
@@ -444,6 +548,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
           if (!mbar_wait_warp(full + stage, phase, timeout_ns, status, kDevTimeout, abort_flag))
             break;
           tc_fence_after();
+          if (gather) fence_proxy_async_smem();
           issue_stage(stage, d_tmem, id0, nmma, new_item);
           if (i == 0 && lane == 0) *progress = fidx;
           fidx += ni;
@@ -535,11 +640,12 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   XMaps xm;
   for (int i = 0; i < kNumXMaps; ++i) xm.m[i] = a.tmap_x[i];
+  if (a.gather_slot && !(C::kGatherFits && ACT == kActFp8Row && SWIGLU)) return cudaErrorInvalidValue;
   return launch_pdl(kern, dim3(a.num_sms), dim3(C::kThreads), C::kSmemBytes, s, *a.tmap_w, xm,
                     *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
                     static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status,
                     a.timeout_ns, a.a_tx_bytes, a.prefetch_stages, a.sfb_tiled, a.w_base,
-                    a.max_tiles, a.early_list ? 1 : 0);
+                    a.max_tiles, a.early_list ? 1 : 0, a.gather_slot, a.gather_k, a.gather_x);
 }
 
 }  // namespace
@@ -596,6 +702,18 @@ int gemm_tile_tokens(int variant, int act) {
 #undef MOE_X
     default:
       return kMidBN;
+  }
+}
+
+bool gemm_gather_supported(int variant) {
+  switch (variant) {
+#define MOE_X(v, bn, st, ni, nb, st8, ni8) \
+  case v:                                  \
+    return GemmCfg<bn, st, ni, nb, kActFp8Row>::kGatherFits;
+    MOE_GEMM_VARIANTS(MOE_X)
+#undef MOE_X
+    default:
+      return false;
   }
 }
 

@@ -198,6 +198,12 @@ struct GemmArgs {
   // The tile list was complete before the previous kernel passed its grid
   // wait, so the weight copies may start before this kernel's wait.
   bool early_list;
+  // GEMM1 of W4A8 only, or null: the activations are token-major (gather_x:
+  // [T, K] codes) and the kernel gathers each tile's rows by token (token =
+  // gather_slot[row] / gather_k); see gemm_gather_supported.
+  const int32_t* gather_slot;
+  int32_t gather_k;
+  const uint8_t* gather_x;
 };
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
@@ -212,6 +218,10 @@ struct QuantOut {
   int act;
   uint8_t* x_sf;
   uint8_t* sfb;
+  // kActFp8Row with a staged x only: the codes of token t go to row t of xq
+  // (token-major [T, H], which GEMM1 gathers rows from) instead of the k
+  // expanded rows; x_scale is still written per expanded row.
+  bool token_major;
 };
 // GEMM1 weights the tiny-batch front end asks L2 for: the first `boxes` K
 // stages (prepared E2M1 boxes of kFp4BoxBytes, and their 512-byte scale
@@ -270,6 +280,9 @@ cudaError_t launch_combine(const void* y, const float* wts, const int32_t* row_o
                            int H, void* out, int32_t* status, uint64_t timeout_ns,
                            cudaStream_t s);
 cudaError_t launch_gemm(bool swiglu, int variant, const GemmArgs& a, cudaStream_t s);
+// Whether the W4A8 GEMM of tile variant 1..5 can gather token-major
+// activation rows (its shared memory holds the producers' token lists).
+bool gemm_gather_supported(int variant);
 // The grouped GEMM on CTA pairs (gemm_pair.cu): W4A8 operands, M-tiles
 // taken two at a time, so m_per_expert must be a multiple of 256; needs
 // tmap_x_pair.

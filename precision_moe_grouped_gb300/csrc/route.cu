@@ -440,10 +440,12 @@ __device__ void quantize_token(const __nv_bfloat16* __restrict__ x, int t, int k
 }
 
 // quantize_token on a row already staged in shared memory (xs: H bf16): the
-// same arithmetic, both passes reading shared memory.
+// same arithmetic, both passes reading shared memory.  code_row >= 0: the
+// codes go to that one row of xq only (the token-major copy GEMM1 gathers
+// from); the scale still goes to the k rows.
 __device__ void quantize_token_staged(const __nv_bfloat16* xs, int k, int H, const int32_t* rows,
                                       float* warp_max, uint8_t* __restrict__ xq,
-                                      float* __restrict__ x_scale) {
+                                      float* __restrict__ x_scale, int code_row = -1) {
   const uint4* xr = reinterpret_cast<const uint4*>(xs);
   const int nvec = H / 16;
   float amax = 0.f;
@@ -471,8 +473,11 @@ __device__ void quantize_token_staged(const __nv_bfloat16* xs, int k, int H, con
       const uint4 q[2] = {xr[2 * i], xr[2 * i + 1]};
       out = fp8_codes16(q, inv);
     }
-    for (int j = 0; j < k; ++j)
-      reinterpret_cast<uint4*>(xq + static_cast<size_t>(rows[j]) * H)[i] = out;
+    if (code_row >= 0)
+      reinterpret_cast<uint4*>(xq + static_cast<size_t>(code_row) * H)[i] = out;
+    else
+      for (int j = 0; j < k; ++j)
+        reinterpret_cast<uint4*>(xq + static_cast<size_t>(rows[j]) * H)[i] = out;
   }
   if (static_cast<int>(threadIdx.x) < k) x_scale[rows[threadIdx.x]] = s;
 }
@@ -590,7 +595,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     const int2* __restrict__ tile_plan, int E, int k, int H, int32_t* __restrict__ row_of,
     int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq, float* __restrict__ x_scale,
     uint8_t* __restrict__ x_sf, uint8_t* __restrict__ sfb, int stage_x,
-    int32_t* __restrict__ status) {
+    int32_t* __restrict__ status, int token_major) {
   extern __shared__ __align__(128) uint8_t xstage[];
   __shared__ int32_t rows[32];
   __shared__ int32_t my_e[32];
@@ -640,7 +645,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
   }
   if constexpr (AQ == kActFp8Row) {
     if (staged)
-      quantize_token_staged(xs, k, H, rows, warp_max, xq, x_scale);
+      quantize_token_staged(xs, k, H, rows, warp_max, xq, x_scale, token_major ? t : -1);
     else
       quantize_token<2>(x, t, k, H, rows, warp_max, xq, x_scale);   // 256 threads
   } else {
@@ -919,10 +924,11 @@ cudaError_t launch_quant_scatter(const void* x, bool x_on_device, const int32_t*
                                    : quant_scatter_kernel<kActFp8Row>;
   // the staged row within the default shared-memory limit (48 KB)
   const bool stage = x_on_device && H * 2 <= 48 * 1024;
+  if (q.token_major && (!stage || q.act != kActFp8Row)) return cudaErrorInvalidValue;
   return launch_pdl(kern, dim3(T), dim3(256), stage ? static_cast<size_t>(H) * 2 : 0, s,
                     static_cast<const __nv_bfloat16*>(x), chunk_base, ids, offsets, tile_plan, E,
                     k, H, row_of, token_slot, q.xq, q.x_scale, q.x_sf, q.sfb, stage ? 1 : 0,
-                    status);
+                    status, q.token_major ? 1 : 0);
 }
 
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,

@@ -57,7 +57,8 @@ def x_bits(case: MI.MoeCase) -> np.ndarray:
 class GpuRun:
     """One forward through the C ABI with every intermediate read back."""
 
-    def __init__(self, case: MI.MoeCase, variant: int = 0, moe: P.FusedMoE | None = None):
+    def __init__(self, case: MI.MoeCase, variant: int = 0, moe: P.FusedMoE | None = None,
+                 gather_x: int = 0):
         dev = torch.device("cuda:0")
         cfg = case.cfg
         self.case = case
@@ -71,7 +72,7 @@ class GpuRun:
         self.ws = torch.zeros(max(P.workspace_size(s, mode), 256), dtype=torch.uint8,
                               device=dev)
         self.out = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=dev)
-        opts = P.options(tile_variant=variant)
+        opts = P.options(tile_variant=variant, gather_x=gather_x)
         P.forward(s, x, logits, self.moe.w1_p, self.moe.w1_sf_p, self.moe.w2_p,
                   self.moe.w2_sf_p, self.out, self.ws, mode=mode, opts=opts)
         torch.cuda.synchronize()

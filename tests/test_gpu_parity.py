@@ -295,6 +295,40 @@ def test_forward_host_steps_pageable_and_short_workspace():
         np.testing.assert_array_equal(o.float().numpy(), r)
 
 
+@pytest.mark.parametrize("T", [300, 700])
+def test_gather_x_matches_expanded_copy(T):
+    """gather_x = 1 (W4A8, more than 256 tokens): the expansion writes each
+    token's FP8 row once, token-major in the xq region, and GEMM1 gathers
+    its tiles' rows by token with TMA gather4.  The token rows equal the
+    oracle's per-token quantisation, every expanded row keeps its scale,
+    and h, hq and the output equal the expanded-copy forward's bit for bit
+    (tiles that split an expert, ragged tails of 1..15 padded rows)."""
+    cfg = MI.custom_config(8, 2, 256, 128)
+    case = MI.make_case(cfg, T, seed=71)
+    a = GpuRun(case)
+    b = GpuRun(case, moe=a.moe, gather_x=1)
+    assert b.status == 0
+    tq, ts = M.quantize_rows_fp8(np.asarray(case.x.float().cpu().numpy(), np.float32))
+    np.testing.assert_array_equal(b.xq[:T], tq)
+    np.testing.assert_array_equal(b.x_scale, a.x_scale)
+    np.testing.assert_array_equal(b.row_of, a.row_of)
+    np.testing.assert_array_equal(b.h, a.h)
+    np.testing.assert_array_equal(b.hq, a.hq)
+    np.testing.assert_array_equal(b.out_np(), a.out_np())
+
+
+def test_gather_x_dsv3_T4096_sampled():
+    """The DSV3 layer at T=4096 with gather_x = 1: output tokens on a sample
+    equal the expanded-copy forward's, bit for bit."""
+    case = MI.make_case(MI.CONFIGS["dsv3"], 4096, device="cuda")
+    a = GpuRun(case)
+    b = GpuRun(case, moe=a.moe, gather_x=1)
+    assert b.status == 0
+    rng = np.random.default_rng(3)
+    toks = rng.choice(4096, 64, replace=False)
+    np.testing.assert_array_equal(b.out_np()[toks], a.out_np()[toks])
+
+
 def test_device_timeout_status_and_recovery():
     """A bounded wait that nothing satisfies returns an error status; the
     context stays usable for the next forward."""
