@@ -361,7 +361,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
   // +127) into the slot's 128-byte-swizzled activation box by 16-byte
   // asynchronous copies (row (lane / 8) + 4 i, piece lane % 8), all in
   // flight at once, each lane arriving on the slot's barrier when its copies
-  // land (the issuer fences the proxies after its wait).  first_only /
+  // land (the issuer fences the proxies after its wait).  The token rows are
+  // read by each token's k tiles at different times, so they are kept in L2
+  // (evict-last) while the weight boxes stream past (evict-first).  first_only /
   // skip_first as in produce (the token list is read only after the grid
   // wait: the previous kernel wrote it).
   auto produce_gather = [&](const int s, const bool first_only, const bool skip_first) -> bool {
@@ -374,6 +376,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
       int64_t blk0 = 0;
       int32_t* tok = reinterpret_cast<int32_t*>(smem + C::kOffTok) + s * BN;
       const int c = lane & 7;
+      const uint64_t pol_keep = l2_policy_evict_last(), pol_stream = l2_policy_evict_first();
       while (item < num_items) {
         if (item != cur_item) {
           cur_item = item;
@@ -397,8 +400,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
           break;
         if (!skip && lane == 0) {
           mbar_arrive_expect_tx(full + s, a_tx_bytes + 512u);
-          tma_load_2d(smem + C::kOffA + s * C::kABytes, &tmap_w, 0,
-                      static_cast<int32_t>(blk * kTileM), full + s);
+          tma_load_2d_hint(smem + C::kOffA + s * C::kABytes, &tmap_w, 0,
+                           static_cast<int32_t>(blk * kTileM), full + s, pol_stream);
           tma_load_2d(smem + C::kOffSF + s * C::kSFBytes, &tmap_sf, 0, static_cast<int32_t>(blk),
                       full + s);
         }
@@ -406,8 +409,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
         uint8_t* b = smem + C::kOffB + s * C::kBBytes;
         const uint8_t* src = xg + static_cast<int64_t>(ks) * kTileK + 16 * c;
         for (int row = lane >> 3; row < nmma; row += 4)
-          cp_async_16(b + row * 128 + ((c ^ (row & 7)) << 4),
-                      src + static_cast<int64_t>(tok[row]) * K);
+          cp_async_16_hint(b + row * 128 + ((c ^ (row & 7)) << 4),
+                           src + static_cast<int64_t>(tok[row]) * K, pol_keep);
         cp_async_arrive(full + s);   // each lane, once its copies have landed
         issued = true;
         phase ^= 1u;
