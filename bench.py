@@ -365,7 +365,7 @@ def run_ours(args, dist: Dist):
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = dist.max(e0.elapsed_time(e1) / K)
-    for oh in ohs:
+    for oh in ohs[:min(K, 3)]:   # the output sets the timed steps wrote
         assert torch.equal(oh.to(dev), out), "host-buffer forward disagrees with device forward"
     del ws_steps
 
