@@ -273,6 +273,28 @@ def test_forward_host_steps_match_device_path(mode, T, n_steps):
         np.testing.assert_array_equal(outs[i].float().numpy(), refs[i])
 
 
+def test_forward_host_steps_with_gather():
+    """The multi-step host entry point with gather_x = 1 (T > 256, W4A8): the
+    staged x is on the device, so the expansion writes token-major rows and
+    GEMM1 gathers them; every step equals the expanded-copy device forward."""
+    cfg = MI.custom_config(8, 2, 256, 128)
+    cases = [MI.make_case(cfg, 300, seed=81 + i) for i in range(3)]
+    run0 = GpuRun(cases[0])
+    refs = [run0.out_np()] + [GpuRun(c, moe=run0.moe).out_np() for c in cases[1:]]
+    s = P.shape(300, 8, 2, 256, 128)
+    xs = [c.x.clone().pin_memory() for c in cases]
+    ls = [c.logits.clone().pin_memory() for c in cases]
+    outs = [torch.empty((300, 256), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    ws = torch.zeros(P.steps_workspace_size(s), dtype=torch.uint8, device="cuda:0")
+    m = run0.moe
+    P.forward_host_steps(s, xs, ls, m.w1_p, m.w1_sf_p, m.w2_p, m.w2_sf_p, outs, ws,
+                         opts=P.options(gather_x=1))
+    torch.cuda.current_stream().synchronize()
+    assert P.read_device_status(ws) == 0
+    for o, r in zip(outs, refs):
+        np.testing.assert_array_equal(o.float().numpy(), r)
+
+
 def test_forward_host_steps_pageable_and_short_workspace():
     """Pageable host buffers give the same outputs (the copies just do not
     overlap); the workspace of a single forward is too small."""
