@@ -130,7 +130,16 @@ typedef struct {
                             by token with asynchronous copies; 0 or -1 =
                             the expanded [R, H] copy (the default: faster
                             from T = 2048 on).  Ignored elsewhere.       */
-  int32_t reserved[2];   /* must be zero                                     */
+  int32_t fuse_combine;  /* tile variants 1-5: 1 = GEMM2's epilogue also
+                            forms the weighted top-k combine (the last of a
+                            token's k slots to finish a 32-column segment
+                            sums the k rows of y in slot order, the
+                            combine kernel's arithmetic, and writes out),
+                            no combine kernel; 0 or -1 = the combine
+                            kernel (the default: faster at every size
+                            measured, e.g. DSV3 T=4096 1.50 against
+                            3.50 ms).                                   */
+  int32_t reserved[1];   /* must be zero                                     */
 } moe_options;
 
 /* Byte offsets of the intermediate tensors inside the workspace, for tests
@@ -160,7 +169,9 @@ typedef struct {
  *   h_sf        uint8[R,I/32] E8M0 block scales of hq, row-major (W4A16:
  *                             [R,2I/32])
  *   x_sf_tiled, h_sf_tiled    the same scales in the GEMMs' per-tile layout:
- *                             1024 bytes per (tile, 128-K stage) */
+ *                             1024 bytes per (tile, 128-K stage)
+ * The workspace ends with int32 [T, H/128, 4] arrival counters used by
+ * moe_options.fuse_combine (cleared by the forward's first kernel). */
 typedef struct {
   uint64_t status, ids, weights, row_of, counts, offsets, chunk_counts, token_slot,
       tiles, xq, x_scale, h, hq, h_scale, y, x_stage, logits_stage, out_stage, tile_plan,

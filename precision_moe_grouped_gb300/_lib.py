@@ -63,7 +63,8 @@ class MoeShape(ctypes.Structure):
 class MoeOptions(ctypes.Structure):
     _fields_ = [("tile_variant", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("stage_events", ctypes.c_void_p), ("prefetch_stages", ctypes.c_int32),
-                ("gather_x", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+                ("gather_x", ctypes.c_int32), ("fuse_combine", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 1)]
 
 
 class WsLayout(ctypes.Structure):
@@ -140,12 +141,12 @@ def shape(T: int, E: int, k: int, H: int, I: int) -> MoeShape:
 
 
 def options(tile_variant: int = 0, timeout_ms: int = 0, stage_events=None,
-            prefetch_stages: int = 0, gather_x: int = 0) -> MoeOptions:
+            prefetch_stages: int = 0, gather_x: int = 0, fuse_combine: int = 0) -> MoeOptions:
     """stage_events: None, or a ctypes array of MOE_NUM_STAGES + 1 cudaEvent_t
     handles (e.g. from stage_event_array())."""
     o = MoeOptions()
     o.tile_variant, o.timeout_ms, o.prefetch_stages = tile_variant, timeout_ms, prefetch_stages
-    o.gather_x = gather_x
+    o.gather_x, o.fuse_combine = gather_x, fuse_combine
     o.stage_events = ctypes.cast(stage_events, ctypes.c_void_p) if stage_events is not None else None
     return o
 

@@ -181,9 +181,18 @@ void compute_layout(const moe_shape* s, int32_t mode, moe_ws_layout* L) {
   L->h_sf = take(mx ? R * (I / 32) * terms : 0);
   L->x_sf_tiled = take(mx ? max_tiles * (H / 128) * moe::kSfbTileBytes : 0);
   L->h_sf_tiled = take(mx ? max_tiles * (I / 128) * moe::kSfbTileBytes : 0);
+  // last: the fused combine's arrival counters [T, H/128, 4] (at
+  // combine_cnt_offset)
+  take(T * (H / 128) * 4 * 4);
   L->total = align_up(off, kAlign);
   L->max_tiles = static_cast<int32_t>(max_tiles);
   L->num_chunks = static_cast<int32_t>(chunks);
+}
+
+// The fused combine's counters: the workspace's last region.
+uint64_t combine_cnt_offset(const moe_shape* s, const moe_ws_layout& L) {
+  const uint64_t bytes = static_cast<uint64_t>(s->num_tokens) * (s->hidden / 128) * 16;
+  return L.total - align_up(bytes, kAlign);
 }
 
 // ----------------------------------------------------------- device state
@@ -282,8 +291,9 @@ int32_t check_options(const moe_options* o) {
   if (o->prefetch_stages > 1024) return fail(MOE_ERR_INVALID_ARG, "prefetch_stages > 1024");
   if (o->gather_x < -1 || o->gather_x > 1)
     return fail(MOE_ERR_INVALID_ARG, "gather_x must be -1, 0 or 1");
-  for (int i = 0; i < 2; ++i)
-    if (o->reserved[i] != 0) return fail(MOE_ERR_INVALID_ARG, "reserved option fields must be 0");
+  if (o->fuse_combine < -1 || o->fuse_combine > 1)
+    return fail(MOE_ERR_INVALID_ARG, "fuse_combine must be -1, 0 or 1");
+  if (o->reserved[0] != 0) return fail(MOE_ERR_INVALID_ARG, "reserved option fields must be 0");
   return MOE_OK;
 }
 
@@ -431,6 +441,11 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   const moe::QuantOut qx{xq, x_scale, act, x_sf, sfb1, gather};
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* token_slot = at<int32_t>(ws, L.token_slot);
+  // GEMM2's epilogue forms the combine (one-CTA kernel); the front end
+  // clears its counters
+  const bool fuse_cmb = opts && opts->fuse_combine > 0 && variant != 6;
+  int32_t* cmb_cnt = fuse_cmb ? at<int32_t>(ws, combine_cnt_offset(s, L)) : nullptr;
+  const int64_t cmb_n = static_cast<int64_t>(T) * (H / moe::kTileM) * 4;
   MOE_CUDA(mark());
   // large batches: the scan writes the tile list, the scatter kernel follows
   const bool large_front = large;
@@ -448,13 +463,13 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
     MOE_CUDA(moe::launch_route_expand_tiny(logits, x, T, E, k, H, bn, ids, wts,
                                            at<int32_t>(ws, L.counts), offsets, tiles, num_tiles,
                                            tile_plan, row_of, token_slot, xq, x_scale, status, pf,
-                                           st));
+                                           cmb_cnt, cmb_n, st));
     MOE_CUDA(mark());
     MOE_CUDA(mark());
     MOE_CUDA(mark());
     MOE_CUDA(mark());
   } else if (T <= moe::kSmallT) {
-    MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
+    MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, cmb_cnt, cmb_n, st));
     MOE_CUDA(mark());
     MOE_CUDA(moe::launch_expand_small(x, ids, T, E, k, H, bn, at<int32_t>(ws, L.counts), offsets,
                                       tiles, num_tiles, tile_plan, row_of, token_slot, qx, st));
@@ -462,7 +477,7 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
     MOE_CUDA(mark());
     MOE_CUDA(mark());
   } else {
-    MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, st));
+    MOE_CUDA(moe::launch_route(logits, T, E, k, ids, wts, chunk, status, cmb_cnt, cmb_n, st));
     MOE_CUDA(mark());
     MOE_CUDA(moe::launch_scan(chunk, L.num_chunks, E, bn, at<int32_t>(ws, L.counts), offsets,
                               chunk, tiles, num_tiles, tile_plan, status, st));
@@ -490,10 +505,12 @@ int32_t run_forward(const moe_shape* s, int32_t mode, const void* x, const float
   moe::GemmArgs g2{&tm_w2, tm_h, &tm_sf2, tiles, num_tiles,
                    tiled ? nullptr : h_scale, y, H, I, H, status, timeout_ns, w_tx, grid2,
                    prefetch, act, sfb2, static_cast<const uint8_t*>(w2), pair ? tm_hp : nullptr,
-                   L.max_tiles, true};
+                   L.max_tiles, true, nullptr, 0, nullptr, cmb_cnt, token_slot, row_of, wts,
+                   fuse_cmb ? out : nullptr, k};
   MOE_CUDA(moe::launch_gemm(false, variant, g2, st));
   MOE_CUDA(mark());
-  MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, status, timeout_ns, st));
+  if (!fuse_cmb)
+    MOE_CUDA(moe::launch_combine(y, wts, row_of, T, k, H, out, status, timeout_ns, st));
   MOE_CUDA(mark());
   return MOE_OK;
 }

@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
                         const uint8_t* __restrict__ sfb_tiled,
                         const uint8_t* __restrict__ w_base, int max_tiles, int early_list,
                         const int32_t* __restrict__ gather_slot, int gather_k,
-                        const uint8_t* __restrict__ xg) {
+                        const uint8_t* __restrict__ xg, const CombineArgs cmb) {
   using C = GemmCfg<BN, STAGES, NI, NB, ACT>;
   // A = E2M1 weights, or E4M3 in MXFP8; B = activations: E4M3
   constexpr uint32_t kAFmt = ACT == kActMxfp8 ? 0u : 5u;
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, NI, NB, ACT>::kThreads, 1)
       const EpiSched sch{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), MT, 1, 0, 0u};
       epilogue_loop<BN, NI, NB, SWIGLU>(C::kIssuer0 + NI, ni, tiles, num_items, sch, tfull, tempty,
                                          tmem, row_scale, out, out_ld, timeout_ns, status,
-                                         abort_flag);
+                                         abort_flag, SWIGLU ? CombineArgs{} : cmb);
     } else if (prefetch_stages > 0) {
       // ---------------------------------------------------------- prefetcher
       // Optional: asks L2 for the weight box of fill g while the first issuer
@@ -648,7 +648,10 @@ cudaError_t launch_variant(const GemmArgs& a, cudaStream_t s) {
                     *a.tmap_sf, a.tiles, a.num_tiles, a.row_scale,
                     static_cast<__nv_bfloat16*>(a.out), a.m_per_expert, a.k, a.out_ld, a.status,
                     a.timeout_ns, a.a_tx_bytes, a.prefetch_stages, a.sfb_tiled, a.w_base,
-                    a.max_tiles, a.early_list ? 1 : 0, a.gather_slot, a.gather_k, a.gather_x);
+                    a.max_tiles, a.early_list ? 1 : 0, a.gather_slot, a.gather_k, a.gather_x,
+                    CombineArgs{a.cmb_cnt, a.cmb_slot, a.cmb_row_of, a.cmb_wts,
+                                static_cast<__nv_bfloat16*>(a.cmb_out), a.cmb_k,
+                                a.m_per_expert / kTileM});
 }
 
 }  // namespace

@@ -105,6 +105,24 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Top-k combine formed in GEMM2's epilogue (moe_options.fuse_combine; null
+// cnt = off).  After a warp has stored its 32 columns of y for a chunk of
+// tokens, it counts, per token t of the chunk, one arrival on
+// cnt[(t * MT + mt) * 4 + q] (q = its lane quarter); the warp whose arrival
+// is the k-th combines that 32-column segment of t: out[t, c] = bf16(sum over
+// slots j in order of fmaf(w[t, j], y[row_of[t, j], c], acc)) -- the combine
+// kernel's arithmetic -- and clears the counter.  Release: every lane fences
+// its y stores before the arrivals; acquire: a fence before reading the
+// other rows (written by other CTAs) through L2.
+struct CombineArgs {
+  int32_t* cnt;             // [T, MT, 4], zero when the kernel starts
+  const int32_t* slot;      // token_slot [R]: token = slot / k
+  const int32_t* row_of;    // [T, k]
+  const float* wts;         // [T, k]
+  __nv_bfloat16* out;       // [T, out_ld]
+  int k, MT;
+};
+
 // EW = epilogue warps: 8 (two per lane quarter, splitting the chunks) or 4
 // (one per quarter).
 template <int BN, int NI, int NB, bool SWIGLU, int EW = kEpiWarps>
@@ -114,7 +132,8 @@ __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4
                                               const float* __restrict__ row_scale,
                                               __nv_bfloat16* __restrict__ out, int out_ld,
                                               uint64_t timeout_ns, int32_t* status,
-                                              volatile int32_t* abort_flag) {
+                                              volatile int32_t* abort_flag,
+                                              const CombineArgs cmb = CombineArgs{}) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;
   static_assert(EW == 4 || EW == 8, "one or two epilogue warps per TMEM lane quarter");
@@ -174,6 +193,34 @@ __device__ __forceinline__ void epilogue_loop(int first_warp, int ni, const int4
         for (int j = 0; j < 16; ++j) {
           const int n = c0 + j;
           if (n < ntok) out[static_cast<int64_t>(row0 + n) * out_ld + c] = __float2bfloat16_rn(v[j]);
+        }
+        if (cmb.cnt) {
+          __threadfence();
+          __syncwarp();
+          int tt = 0;
+          bool last = false;
+          if (lane < 16 && c0 + lane < ntok) {
+            tt = __ldg(cmb.slot + row0 + c0 + lane) / cmb.k;
+            last = atomicAdd(cmb.cnt + (static_cast<int64_t>(tt) * cmb.MT + mt) * 4 + q, 1) ==
+                   cmb.k - 1;
+          }
+          unsigned pend = __ballot_sync(0xffffffffu, last);
+          if (pend) __threadfence();
+          while (pend) {
+            const int src = __ffs(pend) - 1;
+            pend &= pend - 1;
+            const int t = __shfl_sync(0xffffffffu, tt, src);
+            const int64_t tk = static_cast<int64_t>(t) * cmb.k;
+            float acc = 0.f;
+            for (int j = 0; j < cmb.k; ++j) {
+              const int64_t r = __ldg(cmb.row_of + tk + j);
+              const unsigned short yb =
+                  __ldcg(reinterpret_cast<const unsigned short*>(out + r * out_ld + c));
+              acc = fmaf(__ldg(cmb.wts + tk + j), __bfloat162float(__ushort_as_bfloat16(yb)), acc);
+            }
+            cmb.out[static_cast<int64_t>(t) * out_ld + c] = __float2bfloat16_rn(acc);
+            if (lane == 0) cmb.cnt[(static_cast<int64_t>(t) * cmb.MT + mt) * 4 + q] = 0;
+          }
         }
       }
     }

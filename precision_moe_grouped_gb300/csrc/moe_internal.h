@@ -204,10 +204,21 @@ struct GemmArgs {
   const int32_t* gather_slot;
   int32_t gather_k;
   const uint8_t* gather_x;
+  // GEMM2 only, or null: the epilogue also forms the top-k combine (see
+  // CombineArgs in gemm_common.cuh).
+  int32_t* cmb_cnt;            // [T, m_per_expert / 128, 4] arrival counters, zero on entry
+  const int32_t* cmb_slot;     // token_slot [R]
+  const int32_t* cmb_row_of;   // row_of [T, k]
+  const float* cmb_wts;        // routing weights [T, k]
+  void* cmb_out;               // bf16 out [T, m_per_expert]
+  int32_t cmb_k;
 };
 
+// zero / nzero (nullable): int32 words the kernel clears after its grid
+// wait (the fused combine's counters).
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
-                         int32_t* chunk_counts, int32_t* status, cudaStream_t s);
+                         int32_t* chunk_counts, int32_t* status, int32_t* zero, int64_t nzero,
+                         cudaStream_t s);
 // Activation outputs of the expansion kernels, by encoding.  kActFp8Row:
 // FP8 codes xq [R, H] and x_scale (per-row float).  kActMxfp8: codes, x_sf
 // (row-major scale bytes [R, H/32]) and sfb (per-tile layout above).
@@ -242,7 +253,8 @@ cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, 
                                      int32_t* offsets, int4* tiles, int32_t* num_tiles,
                                      int2* tile_plan, int32_t* row_of, int32_t* token_slot,
                                      uint8_t* xq, float* x_scale, int32_t* status,
-                                     const TinyPrefetch& pf, cudaStream_t s);
+                                     const TinyPrefetch& pf, int32_t* zero, int64_t nzero,
+                                     cudaStream_t s);
 cudaError_t launch_expand_small(const void* x, const int32_t* ids, int T, int E, int k, int H,
                                 int bn, int32_t* counts, int32_t* offsets, int4* tiles,
                                 int32_t* num_tiles, int2* tile_plan, int32_t* row_of,

@@ -173,7 +173,8 @@ extern "C" int32_t moe_route_noalloc(const moe_shape* shape, const float* router
   // route kernel writes the whole histogram, the scan kernel every count,
   // base and tile), so nothing needs clearing between calls.
   cudaError_t e = moe::launch_route(router_logits, static_cast<int>(T), static_cast<int>(E),
-                                    static_cast<int>(k), ids, weights, chunk, nullptr, s);
+                                    static_cast<int>(k), ids, weights, chunk, nullptr, nullptr, 0,
+                                    s);
   if (e == cudaSuccess)
     e = moe::launch_scan(chunk, static_cast<int>((T + moe::kRouteChunk - 1) / moe::kRouteChunk),
                          static_cast<int>(E), moe::kDecodeBN,

@@ -109,7 +109,8 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
                                                     int E, int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ wts,
                                                     int32_t* __restrict__ chunk_counts,
-                                                    int32_t* __restrict__ status) {
+                                                    int32_t* __restrict__ status,
+                                                    int32_t* __restrict__ zero, int64_t nzero) {
   static_assert(kRouteChunk == 32, "one warp per token of the chunk");
   extern __shared__ int32_t hist[];
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
@@ -137,6 +138,9 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
     ids[static_cast<size_t>(t) * k + lane] = my_id;
     wts[static_cast<size_t>(t) * k + lane] = my_w;
   }
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nzero;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    zero[i] = 0;
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     chunk_counts[static_cast<size_t>(blockIdx.x) * E + i] = hist[i];
 }
@@ -748,7 +752,8 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
     int32_t* __restrict__ counts_out, int32_t* __restrict__ offsets_out, int4* __restrict__ tiles,
     int32_t* __restrict__ num_tiles, int2* __restrict__ tile_plan, int32_t* __restrict__ row_of,
     int32_t* __restrict__ token_slot, uint8_t* __restrict__ xq, float* __restrict__ x_scale,
-    int32_t* __restrict__ status, const TinyPrefetch pf) {
+    int32_t* __restrict__ status, const TinyPrefetch pf, int32_t* __restrict__ zero,
+    int64_t nzero) {
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;                        // [E] counts, then offsets
   int32_t* sid = sm + E;                    // [kTinyT * 32] routed experts
@@ -828,6 +833,9 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
     ids[ts] = my_id;
     wts[ts] = my_w;
   }
+  for (int64_t i = static_cast<int64_t>(t) * blockDim.x + threadIdx.x; i < nzero;
+       i += static_cast<int64_t>(T) * blockDim.x)
+    zero[i] = 0;
   // counts -> offsets and the tile list (one block scan)
   const int e = threadIdx.x;
   const int c = e < E ? cnt[e] : 0;
@@ -860,14 +868,15 @@ __global__ void __launch_bounds__(1024) route_expand_tiny_kernel(
 }  // namespace
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* wts,
-                         int32_t* chunk_counts, int32_t* status, cudaStream_t s) {
+                         int32_t* chunk_counts, int32_t* status, int32_t* zero, int64_t nzero,
+                         cudaStream_t s) {
   const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
   const size_t smem = static_cast<size_t>(E) * sizeof(int32_t);
   const int nv = (E + 31) / 32;
   auto kern = nv <= 1 ? route_kernel<1> : nv <= 2 ? route_kernel<2> : nv <= 4 ? route_kernel<4>
             : nv <= 8 ? route_kernel<8> : nv <= 16 ? route_kernel<16> : route_kernel<32>;
   return launch_pdl(kern, dim3(chunks), dim3(1024), smem, s, logits, T, E, k, ids, wts,
-                    chunk_counts, status);
+                    chunk_counts, status, zero, zero ? nzero : int64_t{0});
 }
 
 cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, int E, int k,
@@ -875,7 +884,8 @@ cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, 
                                      int32_t* offsets, int4* tiles, int32_t* num_tiles,
                                      int2* tile_plan, int32_t* row_of, int32_t* token_slot,
                                      uint8_t* xq, float* x_scale, int32_t* status,
-                                     const TinyPrefetch& pf, cudaStream_t s) {
+                                     const TinyPrefetch& pf, int32_t* zero, int64_t nzero,
+                                     cudaStream_t s) {
   const size_t smem = static_cast<size_t>(E + kTinyT * 32) * sizeof(int32_t);
   const int nv = (E + 31) / 32;
   auto kern = nv <= 1 ? route_expand_tiny_kernel<1> : nv <= 2 ? route_expand_tiny_kernel<2>
@@ -886,7 +896,7 @@ cudaError_t launch_route_expand_tiny(const float* logits, const void* x, int T, 
   return launch_pdl(kern, dim3(T + (on ? pf.ctas : 0)), dim3(1024), smem, s, logits,
                     static_cast<const __nv_bfloat16*>(x), T, E, k, H, bn, ids, wts, counts,
                     offsets, tiles, num_tiles, tile_plan, row_of, token_slot, xq, x_scale, status,
-                    pf);
+                    pf, zero, zero ? nzero : int64_t{0});
 }
 
 cudaError_t launch_scan(const int32_t* chunk_counts, int num_chunks, int E, int bn,

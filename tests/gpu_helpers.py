@@ -58,7 +58,7 @@ class GpuRun:
     """One forward through the C ABI with every intermediate read back."""
 
     def __init__(self, case: MI.MoeCase, variant: int = 0, moe: P.FusedMoE | None = None,
-                 gather_x: int = 0):
+                 gather_x: int = 0, fuse_combine: int = 0, ws=None):
         dev = torch.device("cuda:0")
         cfg = case.cfg
         self.case = case
@@ -69,10 +69,10 @@ class GpuRun:
         x = case.x.to(dev)
         logits = case.logits.to(dev)
         s = P.shape(T, E, k, H, I)
-        self.ws = torch.zeros(max(P.workspace_size(s, mode), 256), dtype=torch.uint8,
-                              device=dev)
+        self.ws = ws if ws is not None else torch.zeros(max(P.workspace_size(s, mode), 256),
+                                                        dtype=torch.uint8, device=dev)
         self.out = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=dev)
-        opts = P.options(tile_variant=variant, gather_x=gather_x)
+        opts = P.options(tile_variant=variant, gather_x=gather_x, fuse_combine=fuse_combine)
         P.forward(s, x, logits, self.moe.w1_p, self.moe.w1_sf_p, self.moe.w2_p,
                   self.moe.w2_sf_p, self.out, self.ws, mode=mode, opts=opts)
         torch.cuda.synchronize()

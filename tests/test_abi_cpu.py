@@ -142,9 +142,10 @@ def test_forward_validation_without_gpu(lib):
     assert _fwd(lib, s, good, need, opts=P.options(tile_variant=99)) == L.MOE_ERR_INVALID_ARG
     assert _fwd(lib, s, good, need, opts=P.options(tile_variant=-1)) == L.MOE_ERR_INVALID_ARG
     o = P.options()
-    o.reserved[1] = 1
+    o.reserved[0] = 1
     assert _fwd(lib, s, good, need, opts=o) == L.MOE_ERR_INVALID_ARG
     assert _fwd(lib, s, good, need, opts=P.options(gather_x=2)) == L.MOE_ERR_INVALID_ARG
+    assert _fwd(lib, s, good, need, opts=P.options(fuse_combine=3)) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_last_error()                          # a message was recorded
     # zero tokens: a no-op that succeeds without touching the device
     assert _fwd(lib, _shape(T=0), [None] * 8, 0) == L.MOE_OK

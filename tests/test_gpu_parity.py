@@ -351,6 +351,37 @@ def test_gather_x_dsv3_T4096_sampled():
     np.testing.assert_array_equal(b.out_np()[toks], a.out_np()[toks])
 
 
+@pytest.mark.parametrize("mode", [MI.QUANT_W4A8, MI.QUANT_W4A16, MI.QUANT_W8A8])
+@pytest.mark.parametrize("T", [1, 50, 300, 700])
+def test_fused_combine_matches_combine_kernel(mode, T):
+    """fuse_combine = 1: GEMM2's epilogue forms the top-k combine (the last
+    of a token's k slots to finish a 32-column segment sums the k rows of y
+    in slot order) and no combine kernel runs.  The output equals the
+    combine kernel's bit for bit, on a workspace that starts as garbage (the
+    front end clears the counters) and again on the same workspace (every
+    counter was reset by its last arrival)."""
+    cfg = MI.custom_config(8, 2, 256, 128, mode=mode)
+    case = MI.make_case(cfg, T, seed=91)
+    a = GpuRun(case)
+    s = P.shape(T, 8, 2, 256, 128)
+    ws = torch.full((P.workspace_size(s, mode),), 0x5A, dtype=torch.uint8, device="cuda:0")
+    b = GpuRun(case, moe=a.moe, fuse_combine=1, ws=ws)
+    assert b.status == 0
+    np.testing.assert_array_equal(b.out_np(), a.out_np())
+    c = GpuRun(case, moe=a.moe, fuse_combine=1, ws=ws)
+    np.testing.assert_array_equal(c.out_np(), a.out_np())
+
+
+def test_fused_combine_dsv3_T4096():
+    """The DSV3 layer at T=4096 with the combine in GEMM2's epilogue: the whole
+    output equals the combine kernel's, bit for bit."""
+    case = MI.make_case(MI.CONFIGS["dsv3"], 4096, device="cuda")
+    a = GpuRun(case)
+    b = GpuRun(case, moe=a.moe, fuse_combine=1)
+    assert b.status == 0
+    assert torch.equal(a.out, b.out)
+
+
 def test_device_timeout_status_and_recovery():
     """A bounded wait that nothing satisfies returns an error status; the
     context stays usable for the next forward."""
