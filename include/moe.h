@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = -1,        /* null pointer, negative size, bad enum   */
-  MOE_ERR_UNSUPPORTED = -2,        /* mode/shape/device this build cannot run */
+  MOE_ERR_UNSUPPORTED = -2,        /* mode/shape/device the library cannot run */
   MOE_ERR_MISALIGNED = -3,         /* pointer alignment or shape divisibility */
   MOE_ERR_WORKSPACE_TOO_SMALL = -4,
   MOE_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed       */

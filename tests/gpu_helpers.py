@@ -54,7 +54,7 @@ def x_bits(case: MI.MoeCase) -> np.ndarray:
     return case.x.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-class GpuRun:
+class DeviceRun:
     """One forward through the C ABI with every intermediate read back."""
 
     def __init__(self, case: MI.MoeCase, variant: int = 0, moe: P.FusedMoE | None = None,

@@ -58,10 +58,10 @@ def test_limits_recorded_in_checked_build():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import moe_inputs as MI
-    from gpu_helpers import GpuRun
+    from gpu_helpers import DeviceRun
     cfg = MI.CONFIGS["tiny"]
     for T in (1, 37, 300):
-        run = GpuRun(MI.make_case(cfg, T))
+        run = DeviceRun(MI.make_case(cfg, T))
         assert run.status == 0
         assert list(run.ints("status", 4)[2:]) == [T * cfg.top_k, cfg.num_experts]
 

@@ -14,7 +14,7 @@ import moe_inputs as MI
 import precision_moe_grouped_gb300 as P
 from oracle import moe as M
 
-from gpu_helpers import GpuRun, dump, max_err_ok, oracle_weights, x_bits
+from gpu_helpers import DeviceRun, dump, max_err_ok, oracle_weights, x_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +35,7 @@ def _sfb_offset(n: int) -> int:
     return (n >> 7) * 512 + 16 * (n & 31) + 4 * ((n >> 5) & 3)
 
 
-def check_tiled_scales(run: GpuRun, which: str):
+def check_tiled_scales(run: DeviceRun, which: str):
     """The per-tile scale copy holds, for every row of every tile, the same
     bytes as the row-major scales (x: K = H, h: K = I)."""
     K = run.H if which == "x" else run.I
@@ -52,7 +52,7 @@ def check_tiled_scales(run: GpuRun, which: str):
                                               rowmajor[r0 + n, 4 * ks:4 * ks + 4])
 
 
-def check_front_mx(run: GpuRun, rt: M.Routing, tq: np.ndarray, ts: np.ndarray, rows=None):
+def check_front_mx(run: DeviceRun, rt: M.Routing, tq: np.ndarray, ts: np.ndarray, rows=None):
     np.testing.assert_array_equal(run.ids, rt.ids)
     np.testing.assert_array_equal(run.counts, rt.counts)
     np.testing.assert_array_equal(run.offsets, rt.offsets)
@@ -68,7 +68,7 @@ def check_front_mx(run: GpuRun, rt: M.Routing, tq: np.ndarray, ts: np.ndarray, r
 
 def mx_parity(case, variant=0, name="mx"):
     assert case.mode == W8A8
-    run = GpuRun(case, variant=variant)
+    run = DeviceRun(case, variant=variant)
     assert run.status == 0
     fw = M.forward(x_bits(case), case.logits.cpu().numpy(), oracle_weights(case),
                    case.cfg.top_k, mode=M.QUANT_W8A8)
@@ -132,9 +132,9 @@ def test_mx_zipf_skew_with_empty_experts():
 
 def test_mx_variants_agree_bitwise():
     case = MI.make_case(_cfg(8, 2, 256, 128), 96, seed=13)
-    a = GpuRun(case, variant=1)
+    a = DeviceRun(case, variant=1)
     for v in (2, 3, 4, 5):
-        b = GpuRun(case, variant=v, moe=a.moe)
+        b = DeviceRun(case, variant=v, moe=a.moe)
         np.testing.assert_array_equal(a.out_np(), b.out_np())
 
 
@@ -160,7 +160,7 @@ def test_mx_zipf_full_size(T):
     the output on a token sample."""
     cfg = MI.CONFIGS["mxfp8_zipf"]
     case = MI.make_case(cfg, T, device="cuda")
-    run = GpuRun(case)
+    run = DeviceRun(case)
     assert run.status == 0
     x32 = np.asarray(case.x.float().cpu().numpy(), np.float32)
     ids, w = M.route(case.logits.cpu().numpy(), cfg.top_k)

@@ -10,7 +10,7 @@ import torch
 import moe_inputs as MI
 import precision_moe_grouped_gb300 as P
 
-from gpu_helpers import GpuRun
+from gpu_helpers import DeviceRun
 from test_gpu_parity import _sampled_parity, check_tiles, full_parity
 
 pytestmark = pytest.mark.gpu
@@ -68,8 +68,8 @@ def test_pair_matches_one_cta_kernel():
     5) compute the same products; their outputs agree to bf16 rounding."""
     cfg = MI.custom_config(8, 2, 512, 256)
     case = MI.make_case(cfg, 150, seed=17)
-    a = GpuRun(case, variant=5)
-    b = GpuRun(case, variant=PAIR, moe=a.moe)
+    a = DeviceRun(case, variant=5)
+    b = DeviceRun(case, variant=PAIR, moe=a.moe)
     np.testing.assert_array_equal(a.tiles, b.tiles)
     diff = np.abs(a.out_np().astype(np.float64) - b.out_np().astype(np.float64))
     assert diff.max() <= 1e-2 * np.abs(a.out_np().astype(np.float64)).max()
@@ -78,8 +78,8 @@ def test_pair_matches_one_cta_kernel():
 def test_pair_deterministic():
     cfg = MI.custom_config(16, 4, 256, 256)
     case = MI.make_case(cfg, 300, seed=21)
-    a = GpuRun(case, variant=PAIR)
-    b = GpuRun(case, variant=PAIR, moe=a.moe)
+    a = DeviceRun(case, variant=PAIR)
+    b = DeviceRun(case, variant=PAIR, moe=a.moe)
     np.testing.assert_array_equal(a.out_np(), b.out_np())
 
 

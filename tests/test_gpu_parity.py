@@ -13,7 +13,7 @@ import moe_inputs as MI
 import precision_moe_grouped_gb300 as P
 from oracle import moe as M
 
-from gpu_helpers import GpuRun, dump, max_err_ok, oracle_weights, x_bits
+from gpu_helpers import DeviceRun, dump, max_err_ok, oracle_weights, x_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def _gpu():
     P.load()
 
 
-def check_front(run: GpuRun, rt: M.Routing, tq: np.ndarray, ts: np.ndarray, rows=None):
+def check_front(run: DeviceRun, rt: M.Routing, tq: np.ndarray, ts: np.ndarray, rows=None):
     """Bit-exact checks of routing, expansion and FP8 activation quantisation
     (rows: optional subset of expanded rows to compare codes on)."""
     np.testing.assert_array_equal(run.ids, rt.ids)
@@ -42,7 +42,7 @@ def check_front(run: GpuRun, rt: M.Routing, tq: np.ndarray, ts: np.ndarray, rows
     np.testing.assert_array_equal(xq[sel], tq[rt.token_of_row[sel]])
 
 
-def check_tiles(run: GpuRun, bn: int):
+def check_tiles(run: DeviceRun, bn: int):
     """The work map covers every expanded row exactly once, in expert order,
     with tiles of at most bn rows."""
     tiles = run.tiles
@@ -56,7 +56,7 @@ def check_tiles(run: GpuRun, bn: int):
 
 
 def full_parity(case, variant=0, name="case"):
-    run = GpuRun(case, variant=variant)
+    run = DeviceRun(case, variant=variant)
     assert run.status == 0
     fw = M.forward(x_bits(case), case.logits.cpu().numpy(), oracle_weights(case),
                    case.cfg.top_k)
@@ -111,17 +111,17 @@ def test_expert_split_over_tiles_prefill(variant):
 def test_variants_agree_bitwise():
     cfg = MI.custom_config(8, 2, 256, 128)
     case = MI.make_case(cfg, 96, seed=13)
-    a = GpuRun(case, variant=1)
+    a = DeviceRun(case, variant=1)
     for v in (2, 3, 4, 5):
-        b = GpuRun(case, variant=v, moe=a.moe)
+        b = DeviceRun(case, variant=v, moe=a.moe)
         np.testing.assert_array_equal(a.out_np(), b.out_np())
 
 
 def test_deterministic():
     cfg = MI.custom_config(16, 4, 256, 256)
     case = MI.make_case(cfg, 64, seed=21)
-    a = GpuRun(case)
-    b = GpuRun(case, moe=a.moe)
+    a = DeviceRun(case)
+    b = DeviceRun(case, moe=a.moe)
     np.testing.assert_array_equal(a.out_np(), b.out_np())
 
 
@@ -231,7 +231,7 @@ def test_forward_host_matches_device_path(mode, T, pinned):
     and large-batch front ends."""
     cfg = MI.custom_config(8, 2, 256, 128, mode=mode)
     case = MI.make_case(cfg, T, seed=17)
-    run = GpuRun(case)
+    run = DeviceRun(case)
     s = P.shape(T, 8, 2, 256, 128)
     pin = {"all": (True, True, True), "none": (False, False, False),
            "x_only": (True, False, False)}[pinned]
@@ -256,8 +256,8 @@ def test_forward_host_steps_match_device_path(mode, T, n_steps):
     staging set read by the wrong step shows)."""
     cfg = MI.custom_config(8, 2, 256, 128, mode=mode)
     cases = [MI.make_case(cfg, T, seed=31 + i) for i in range(n_steps)]
-    run0 = GpuRun(cases[0])
-    refs = [run0.out_np()] + [GpuRun(c, moe=run0.moe).out_np() for c in cases[1:]]
+    run0 = DeviceRun(cases[0])
+    refs = [run0.out_np()] + [DeviceRun(c, moe=run0.moe).out_np() for c in cases[1:]]
     s = P.shape(T, 8, 2, 256, 128)
     xs = [c.x.clone().pin_memory() for c in cases]
     ls = [c.logits.clone().pin_memory() for c in cases]
@@ -279,8 +279,8 @@ def test_forward_host_steps_with_gather():
     GEMM1 gathers them; every step equals the expanded-copy device forward."""
     cfg = MI.custom_config(8, 2, 256, 128)
     cases = [MI.make_case(cfg, 300, seed=81 + i) for i in range(3)]
-    run0 = GpuRun(cases[0])
-    refs = [run0.out_np()] + [GpuRun(c, moe=run0.moe).out_np() for c in cases[1:]]
+    run0 = DeviceRun(cases[0])
+    refs = [run0.out_np()] + [DeviceRun(c, moe=run0.moe).out_np() for c in cases[1:]]
     s = P.shape(300, 8, 2, 256, 128)
     xs = [c.x.clone().pin_memory() for c in cases]
     ls = [c.logits.clone().pin_memory() for c in cases]
@@ -300,8 +300,8 @@ def test_forward_host_steps_pageable_and_short_workspace():
     overlap); the workspace of a single forward is too small."""
     cfg = MI.custom_config(8, 2, 256, 128)
     cases = [MI.make_case(cfg, 40, seed=51 + i) for i in range(3)]
-    run0 = GpuRun(cases[0])
-    refs = [run0.out_np()] + [GpuRun(c, moe=run0.moe).out_np() for c in cases[1:]]
+    run0 = DeviceRun(cases[0])
+    refs = [run0.out_np()] + [DeviceRun(c, moe=run0.moe).out_np() for c in cases[1:]]
     s = P.shape(40, 8, 2, 256, 128)
     outs = [torch.empty((40, 256), dtype=torch.bfloat16) for _ in range(3)]
     m = run0.moe
@@ -327,8 +327,8 @@ def test_gather_x_matches_expanded_copy(T):
     (tiles that split an expert, ragged tails of 1..15 padded rows)."""
     cfg = MI.custom_config(8, 2, 256, 128)
     case = MI.make_case(cfg, T, seed=71)
-    a = GpuRun(case)
-    b = GpuRun(case, moe=a.moe, gather_x=1)
+    a = DeviceRun(case)
+    b = DeviceRun(case, moe=a.moe, gather_x=1)
     assert b.status == 0
     tq, ts = M.quantize_rows_fp8(np.asarray(case.x.float().cpu().numpy(), np.float32))
     np.testing.assert_array_equal(b.xq[:T], tq)
@@ -343,8 +343,8 @@ def test_gather_x_dsv3_T4096_sampled():
     """The DSV3 layer at T=4096 with gather_x = 1: output tokens on a sample
     equal the expanded-copy forward's, bit for bit."""
     case = MI.make_case(MI.CONFIGS["dsv3"], 4096, device="cuda")
-    a = GpuRun(case)
-    b = GpuRun(case, moe=a.moe, gather_x=1)
+    a = DeviceRun(case)
+    b = DeviceRun(case, moe=a.moe, gather_x=1)
     assert b.status == 0
     rng = np.random.default_rng(3)
     toks = rng.choice(4096, 64, replace=False)
@@ -362,13 +362,13 @@ def test_fused_combine_matches_combine_kernel(mode, T):
     counter was reset by its last arrival)."""
     cfg = MI.custom_config(8, 2, 256, 128, mode=mode)
     case = MI.make_case(cfg, T, seed=91)
-    a = GpuRun(case)
+    a = DeviceRun(case)
     s = P.shape(T, 8, 2, 256, 128)
     ws = torch.full((P.workspace_size(s, mode),), 0x5A, dtype=torch.uint8, device="cuda:0")
-    b = GpuRun(case, moe=a.moe, fuse_combine=1, ws=ws)
+    b = DeviceRun(case, moe=a.moe, fuse_combine=1, ws=ws)
     assert b.status == 0
     np.testing.assert_array_equal(b.out_np(), a.out_np())
-    c = GpuRun(case, moe=a.moe, fuse_combine=1, ws=ws)
+    c = DeviceRun(case, moe=a.moe, fuse_combine=1, ws=ws)
     np.testing.assert_array_equal(c.out_np(), a.out_np())
 
 
@@ -376,8 +376,8 @@ def test_fused_combine_dsv3_T4096():
     """The DSV3 layer at T=4096 with the combine in GEMM2's epilogue: the whole
     output equals the combine kernel's, bit for bit."""
     case = MI.make_case(MI.CONFIGS["dsv3"], 4096, device="cuda")
-    a = GpuRun(case)
-    b = GpuRun(case, moe=a.moe, fuse_combine=1)
+    a = DeviceRun(case)
+    b = DeviceRun(case, moe=a.moe, fuse_combine=1)
     assert b.status == 0
     assert torch.equal(a.out, b.out)
 
@@ -422,7 +422,7 @@ def _sampled_parity(cfg, T, n_sample, variant=0):
     bit-exactly, the output on a seeded token sample (a token's output
     depends only on its own inputs)."""
     case = MI.make_case(cfg, T, device="cuda")
-    run = GpuRun(case, variant=variant)
+    run = DeviceRun(case, variant=variant)
     assert run.status == 0
     rt, tq, ts = M.route_and_quantize(x_bits(case), case.logits.cpu().numpy(), cfg.top_k)
     check_front(run, rt, tq, ts)        # every expanded row's codes, bit for bit
@@ -462,7 +462,7 @@ def test_nan_logits_route_in_range(T, E):
     case.logits[1, 5] = nan
     case.logits[3, ::2] = nan
     case.logits[T - 2] = nan
-    run = GpuRun(case)
+    run = DeviceRun(case)
     assert run.status == 0
     ids = run.ids
     assert ids.min() >= 0 and ids.max() < E

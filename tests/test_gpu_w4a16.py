@@ -15,7 +15,7 @@ import moe_inputs as MI
 import precision_moe_grouped_gb300 as P
 from oracle import moe as M
 
-from gpu_helpers import GpuRun, dump, max_err_ok, oracle_weights, x_bits
+from gpu_helpers import DeviceRun, dump, max_err_ok, oracle_weights, x_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,7 @@ def _gpu():
 
 def w16_parity(case, name="w16"):
     assert case.mode == W4A16
-    run = GpuRun(case)
+    run = DeviceRun(case)
     assert run.status == 0
     fw = M.forward(x_bits(case), case.logits.cpu().numpy(), oracle_weights(case),
                    case.cfg.top_k, mode=M.QUANT_W4A16)

@@ -22,8 +22,8 @@ from precision_moe_grouped_gb300 import _lib as L
 
 def _forward_front(case):
     """ids, weights, offsets, row_of as moe_forward computes them."""
-    from gpu_helpers import GpuRun
-    run = GpuRun(case)
+    from gpu_helpers import DeviceRun
+    run = DeviceRun(case)
     assert run.status == 0
     return run.ids, run.weights, run.offsets, run.row_of
 
