@@ -43,6 +43,7 @@ class FusedMoE:
         prepare_weights(self.shape(0), w1, w1_sf, w2, w2_sf, self.w1_p, self.w1_sf_p, self.w2_p,
                         self.w2_sf_p, mode)
         self._ws = None
+        self._steps_ws = None
 
     def shape(self, T: int) -> MoeShape:
         return shape(T, self.E, self.top_k, self.H, self.I)
@@ -63,3 +64,22 @@ class FusedMoE:
         forward(self.shape(T), x, logits, self.w1_p, self.w1_sf_p, self.w2_p, self.w2_sf_p, out,
                 ws, self.mode, opts)
         return out
+
+    def host_steps(self, xs, logits, outs=None, opts: MoeOptions | None = None):
+        """Forwards of host (CPU) tensors xs[i] [T, H] bf16 and logits[i]
+        [T, E] float32, one per step, with the host<->device copies
+        overlapped with the neighbouring steps' computation
+        (moe_forward_host_steps; page-locked tensors for the overlap).
+        Returns the host outputs, complete when the current stream reaches
+        this point."""
+        import torch
+        T = xs[0].shape[0]
+        if outs is None:
+            outs = [torch.empty((T, self.H), dtype=torch.bfloat16, pin_memory=True)
+                    for _ in xs]
+        need = steps_workspace_size(self.shape(T), self.mode)
+        if self._steps_ws is None or self._steps_ws.numel() < need:
+            self._steps_ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        forward_host_steps(self.shape(T), xs, logits, self.w1_p, self.w1_sf_p, self.w2_p,
+                           self.w2_sf_p, outs, self._steps_ws, self.mode, opts)
+        return outs

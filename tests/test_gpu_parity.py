@@ -295,6 +295,20 @@ def test_forward_host_steps_with_gather():
         np.testing.assert_array_equal(o.float().numpy(), r)
 
 
+def test_fused_moe_host_steps():
+    """FusedMoE.host_steps: the convenience wrapper of the multi-step host
+    entry point returns each step's output equal to FusedMoE.__call__'s."""
+    cfg = MI.custom_config(8, 2, 256, 128)
+    cases = [MI.make_case(cfg, 64, seed=95 + i) for i in range(3)]
+    m = P.FusedMoE(cases[0].w1.cuda(), cases[0].w1_sf.cuda(), cases[0].w2.cuda(),
+                   cases[0].w2_sf.cuda(), 2)
+    refs = [m(c.x.cuda(), c.logits.cuda()).cpu() for c in cases]
+    outs = m.host_steps([c.x.pin_memory() for c in cases], [c.logits.pin_memory() for c in cases])
+    torch.cuda.current_stream().synchronize()
+    for o, r in zip(outs, refs):
+        assert torch.equal(o, r)
+
+
 def test_forward_host_steps_pageable_and_short_workspace():
     """Pageable host buffers give the same outputs (the copies just do not
     overlap); the workspace of a single forward is too small."""
